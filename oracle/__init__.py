@@ -1,0 +1,231 @@
+"""CPU oracle for the block-quantized decode matvec -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, fp64 C++ (``lq_oracle.cpp``) behind a numpy/ctypes wrapper.  It
+shares no code with the CUDA library and the library never imports it; only
+``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it.
+
+What it computes, and the passages it follows, is stated at the top of
+``lq_oracle.cpp``.  ``build()`` compiles it with g++ (no GPU needed).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "lq_oracle.cpp")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(BUILD_DIR, "liblq_oracle.so")
+
+Q4_K, Q6_K, Q8_0 = 1, 2, 3
+ACT_GEGLU_TANH, ACT_SWIGLU = 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """compile the oracle to a shared library (g++, -ffp-contract=off)."""
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+        return LIB
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+           SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def _p(a):
+    return a.ctypes.data_as(C.c_void_p) if a is not None else None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = C.CDLL(LIB)
+        i64, i32, vp, d = C.c_int64, C.c_int, C.c_void_p, C.c_double
+        L.orc_block_bytes.argtypes = [i32]
+        L.orc_block_elems.argtypes = [i32]
+        L.orc_half_to_double.argtypes = [C.c_uint16]
+        L.orc_half_to_double.restype = d
+        L.orc_gelu_tanh.argtypes = [d]
+        L.orc_gelu_tanh.restype = d
+        L.orc_silu.argtypes = [d]
+        L.orc_silu.restype = d
+        L.orc_dequant.argtypes = [i32, vp, i64, i64, vp, i32]
+        L.orc_matvec.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, i32]
+        L.orc_matvec_rows.argtypes = [i32, vp, i64, vp, i64, vp, i32, vp, vp, i32]
+        L.orc_ffn_gate_up.argtypes = [i32, vp, vp, i64, i64, vp, i32, i32, vp, vp, vp, vp, vp, i32]
+        L.orc_moe_route.argtypes = [vp, i32, i64, vp, i32, i32, vp, vp, vp, vp]
+        L.orc_moe_ffn.argtypes = [i32, vp, vp, vp, i64, i64, vp, i32, i32, vp, vp, vp, vp, vp,
+                                  vp, vp, vp, vp, vp, i32]
+        L.orc_abs_matvec.argtypes = [i32, vp, i64, i64, vp, vp, i32]
+        _lib = L
+    return _lib
+
+
+def _u8(W):
+    W = np.ascontiguousarray(W)
+    assert W.dtype == np.uint8
+    return W
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def threads_default() -> int:
+    return os.cpu_count() or 1
+
+
+def block_bytes(fmt: int) -> int:
+    return lib().orc_block_bytes(fmt)
+
+
+def block_elems(fmt: int) -> int:
+    return lib().orc_block_elems(fmt)
+
+
+def half_to_double(bits: int) -> float:
+    return lib().orc_half_to_double(bits)
+
+
+def gelu_tanh(g: float) -> float:
+    return lib().orc_gelu_tanh(g)
+
+
+def silu(g: float) -> float:
+    return lib().orc_silu(g)
+
+
+def dequant(fmt: int, W, rows: int, cols: int, nthreads: int = 1) -> np.ndarray:
+    W = _u8(W)
+    out = np.empty((rows, cols), dtype=np.float32)
+    lib().orc_dequant(fmt, _p(W), rows, cols, _p(out), nthreads)
+    return out
+
+
+def matvec(fmt: int, W, rows: int, cols: int, x, nthreads: int = 1):
+    """y = dequant(W) . x for x [batch][cols]; returns (y, S) each [batch][rows] fp64."""
+    W, x = _u8(W), _f32(x)
+    x2 = x.reshape(-1, cols)
+    batch = x2.shape[0]
+    y = np.empty((batch, rows), dtype=np.float64)
+    S = np.empty((batch, rows), dtype=np.float64)
+    lib().orc_matvec(fmt, _p(W), rows, cols, _p(x2), batch, _p(y), _p(S), nthreads)
+    return y, S
+
+
+def matvec_rows(fmt: int, W, cols: int, row_idx, x, nthreads: int = 1):
+    W, x = _u8(W), _f32(x)
+    idx = np.ascontiguousarray(row_idx, dtype=np.int64)
+    x2 = x.reshape(-1, cols)
+    batch = x2.shape[0]
+    y = np.empty((batch, idx.size), dtype=np.float64)
+    S = np.empty((batch, idx.size), dtype=np.float64)
+    lib().orc_matvec_rows(fmt, _p(W), cols, _p(idx), idx.size, _p(x2), batch, _p(y), _p(S),
+                          nthreads)
+    return y, S
+
+
+def ffn_gate_up(fmt: int, Wg, Wu, inter: int, cols: int, x, act: int, nthreads: int = 1):
+    """returns dict of fp64 [batch][inter] arrays: h, g, u, Sg, Su."""
+    Wg, Wu, x = _u8(Wg), _u8(Wu), _f32(x)
+    x2 = x.reshape(-1, cols)
+    batch = x2.shape[0]
+    out = {k: np.empty((batch, inter), dtype=np.float64) for k in ("h", "g", "u", "Sg", "Su")}
+    lib().orc_ffn_gate_up(fmt, _p(Wg), _p(Wu), inter, cols, _p(x2), batch, act, _p(out["h"]),
+                          _p(out["g"]), _p(out["u"]), _p(out["Sg"]), _p(out["Su"]), nthreads)
+    return out
+
+
+def moe_route(R, X, topk: int):
+    R, X = _f32(R), _f32(X)
+    E, hidden = R.shape
+    ntok = X.shape[0]
+    idx = np.empty((ntok, topk), dtype=np.int32)
+    w = np.empty((ntok, topk), dtype=np.float64)
+    logits = np.empty((ntok, E), dtype=np.float64)
+    labs = np.empty((ntok, E), dtype=np.float64)
+    lib().orc_moe_route(_p(R), E, hidden, _p(X), ntok, topk, _p(idx), _p(w), _p(logits),
+                        _p(labs))
+    return idx, w, logits, labs
+
+
+def moe_ffn(fmt: int, W1, W3, W2, hidden: int, inter: int, X, idx, w, nthreads: int = 1):
+    """expert FFN + weighted combine for a given routing (idx, w)."""
+    W1 = [_u8(a) for a in W1]
+    W3 = [_u8(a) for a in W3]
+    W2 = [_u8(a) for a in W2]
+    E = len(W1)
+    P = C.c_void_p * E
+    p1, p3, p2 = P(*[_p(a) for a in W1]), P(*[_p(a) for a in W3]), P(*[_p(a) for a in W2])
+    X = _f32(X)
+    ntok = X.shape[0]
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    topk = idx.shape[1]
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    nslot = ntok * topk
+    out = {
+        "Y": np.empty((ntok, hidden)),
+        "ye": np.empty((nslot, hidden)),
+        "Sy": np.empty((nslot, hidden)),
+        "h": np.empty((nslot, inter)),
+        "g": np.empty((nslot, inter)),
+        "u": np.empty((nslot, inter)),
+        "Sg": np.empty((nslot, inter)),
+        "Su": np.empty((nslot, inter)),
+    }
+    lib().orc_moe_ffn(fmt, C.cast(p1, C.c_void_p), C.cast(p3, C.c_void_p),
+                      C.cast(p2, C.c_void_p), hidden, inter, _p(X), ntok, topk, _p(idx), _p(w),
+                      _p(out["Y"]), _p(out["ye"]), _p(out["Sy"]), _p(out["h"]), _p(out["g"]),
+                      _p(out["u"]), _p(out["Sg"]), _p(out["Su"]), nthreads)
+    return out
+
+
+def abs_matvec(fmt: int, W, rows: int, cols: int, v, nthreads: int = 1) -> np.ndarray:
+    """sum_j |w_ij| v_j for each row (carries an input bound through a matvec)."""
+    W = _u8(W)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(rows, dtype=np.float64)
+    lib().orc_abs_matvec(fmt, _p(W), rows, cols, _p(v), _p(out), nthreads)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Error bounds the GPU results are held to (functions of oracle quantities).
+# ---------------------------------------------------------------------------
+U32 = 2.0 ** -24
+
+
+def matvec_bound(S):
+    """|y_gpu - y| <= 1e-5 * sum_j |w_ij x_j| + 1e-6 per element."""
+    return 1e-5 * np.asarray(S) + 1e-6
+
+
+def act_abs(g, act: int):
+    g = np.asarray(g, dtype=np.float64)
+    if act == ACT_GEGLU_TANH:
+        k = np.sqrt(2.0 / np.pi)
+        a = 0.5 * g * (1.0 + np.tanh(k * (g + 0.044715 * g ** 3)))
+    else:
+        a = g / (1.0 + np.exp(-g))
+    return np.abs(a)
+
+
+def gate_up_bound(g, u, Sg, Su, act: int):
+    """per-element bound on h = act(g)*u when g and u each carry the matvec
+    bound: 1.2 e_g (|u| + e_u) + |act(g)| e_u + 8 u32 (|act(g)| + 1.2 e_g)(|u| + e_u).
+
+    1.2 bounds |act'| for both GELU-tanh and SiLU; the last term covers the
+    fp32 evaluation of the activation and of the product."""
+    eg, eu = matvec_bound(Sg), matvec_bound(Su)
+    a = act_abs(g, act)
+    au = np.abs(u) + eu
+    return 1.2 * eg * au + a * eu + 8 * U32 * (a + 1.2 * eg) * au
