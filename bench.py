@@ -1,0 +1,363 @@
+"""Benchmark: one Gemma-3-4B-shaped decode layer of block-quantized matvecs.
+
+A step is one decode layer at batch 1, hidden 2560 (the larql Gemma 3 table's
+quantized path): mixed QKV (Q/K Q4_K, V Q6_K) -> O projection (Q4_K
+2560x2048) -> FFN gate+up with GELU-tanh (Q4_K 2 x 10240 x 2560) -> FFN down
+(Q6_K 2560 x 10240).  Each op feeds the next (q -> O, O's output -> gate+up,
+h -> down).  34 layer copies (the model's depth, 2.06 GB of weights) rotate
+step by step, so the weights never sit in the 129 MB L2 between uses.
+
+Headline metric: effective weight GB/s = weight-block bytes of the layer per
+second (60,518,400 B per step), with us/layer = ms_per_step * 1000.  The
+device-timed number replays one CUDA graph per layer with inputs resident;
+`e2e` times the C ABI calls directly with the step's x copied in from pinned
+host memory and the layer output copied back, every step.
+
+--impl reference runs the CPU oracle (fp64, all host cores) on a bounded
+sample of the same layers as the reference arm.
+
+Multi-GPU (torchrun): every rank runs an independent replica (the layer has
+no data-path exchange); timing is max over ranks, value is the sum.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+LAYER_BYTES = 6_574_080 + 2_949_120 + 29_491_200 + 21_504_000   # 60,518,400
+GATEUP_BYTES = 29_491_200
+NLAYERS = 34
+METRIC = "effective weight GB/s per quantized matvec (decode layer, batch 1)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
+    ap.add_argument("--layers", type=int, default=NLAYERS)
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            p = [s.strip() for s in l.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx = float(p[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_layers(n, dev):
+    """n Gemma-3-4B-shaped layers (seeded synthetic blocks), gate/up packed."""
+    import torch
+    import block_quantized_weight_super_gb300 as lq
+    import synth
+    layers = []
+    for i in range(n):
+        L, x = synth.gemma3_layer(seed=i)
+        d = {k: torch.from_numpy(v).to(dev) for k, v in L.items()}
+        rb = lq.lq_row_bytes(lq.LQ_Q4_K, synth.GEMMA3_HIDDEN)
+        wgu = torch.empty(2 * synth.GEMMA3_INTER * rb, dtype=torch.uint8, device=dev)
+        lq.lq_pack_gate_up(lq.LQ_Q4_K, d["wg"], d["wu"], synth.GEMMA3_INTER, synth.GEMMA3_HIDDEN, wgu)
+        d["wgu"] = wgu
+        del d["wg"], d["wu"]
+        layers.append(d)
+        if i == 0:
+            x0 = x
+    torch.cuda.synchronize()
+    return layers, x0
+
+
+class Layer:
+    """buffers and calls of one decode layer through the C ABI."""
+
+    def __init__(self, dev):
+        import torch
+        import synth
+        H, I, NQ, NKV = synth.GEMMA3_HIDDEN, synth.GEMMA3_INTER, synth.GEMMA3_NQ, synth.GEMMA3_NKV
+        f = dict(dtype=torch.float32, device=dev)
+        self.x = torch.zeros((1, H), **f)
+        self.q = torch.empty((1, NQ), **f)
+        self.k = torch.empty((1, NKV), **f)
+        self.v = torch.empty((1, NKV), **f)
+        self.o = torch.empty((1, H), **f)
+        self.h = torch.empty((1, I), **f)
+        self.y = torch.empty((1, H), **f)
+        self.dims = (H, I, NQ, NKV)
+
+    def run(self, w, stream, mark=None):
+        import block_quantized_weight_super_gb300 as lq
+        H, I, NQ, NKV = self.dims
+        lq.lq_qkv_mixed(lq.LQ_Q4_K, w["wq"], NQ, lq.LQ_Q4_K, w["wk"], NKV, lq.LQ_Q6_K, w["wv"], NKV,
+                        H, self.x, self.q, self.k, self.v, 1, stream)
+        lq.lq_matvec(lq.LQ_Q4_K, w["wo"], H, NQ, self.q, self.o, 1, stream)
+        if mark:
+            mark[0].record(stream)
+        lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, self.o, self.h, 1, lq.LQ_ACT_GEGLU_TANH, stream)
+        if mark:
+            mark[1].record(stream)
+        lq.lq_matvec(lq.LQ_Q6_K, w["wd"], H, I, self.h, self.y, 1, stream)
+
+
+def bench_lq(args, ws, rank, local):
+    import torch
+    import block_quantized_weight_super_gb300 as lq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lq.lib()
+    layers, x0 = make_layers(args.layers, dev)
+    st = torch.cuda.Stream(device=dev)
+    lay = Layer(dev)
+    lay.x.copy_(torch.from_numpy(x0))
+    torch.cuda.synchronize()
+    rc, bits = lq.lq_device_status()
+    assert rc == 0
+
+    # one CUDA graph per layer copy
+    graphs = []
+    with torch.cuda.stream(st):
+        for w in layers:        # warm the kernels once outside capture
+            lay.run(w, st)
+        st.synchronize()
+        for w in layers:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                lay.run(w, st)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    n = len(graphs)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % n].replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(st):
+            e0.record(st)
+            for i in range(args.steps):
+                graphs[i % n].replay()
+            e1.record(st)
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_all = ms
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_all = float(t.item())
+    rc, bits = lq.lq_device_status()
+    assert rc == 0, "device status after timed region"
+
+    # dominant kernel (FFN gate+up, 29.5 MB) timed alone with CUDA events on
+    # its stream, rotating the layer copies: one graph of n launches
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        H, I = lay.dims[0], lay.dims[1]
+        for w in layers:
+            lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, lay.o, lay.h, 1, lq.LQ_ACT_GEGLU_TANH, st)
+        st.synchronize()
+        with torch.cuda.graph(gk, stream=st):
+            for w in layers:
+                lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, lay.o, lay.h, 1,
+                                      lq.LQ_ACT_GEGLU_TANH, st)
+        for _ in range(3):
+            gk.replay()
+        st.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, args.steps // n)
+        k0.record(st)
+        for _ in range(reps):
+            gk.replay()
+        k1.record(st)
+        st.synchronize()
+    gate_ms = k0.elapsed_time(k1) / (reps * n)
+
+    # e2e through the C ABI: pinned host x in, layer output out, every step
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x0).pin_memory()
+        yh = torch.empty((1, lay.dims[0]), dtype=torch.float32).pin_memory()
+        with torch.cuda.stream(st):
+            for i in range(min(args.warmup, 5)):
+                lay.x.copy_(xh, non_blocking=True)
+                lay.run(layers[i % n], st)
+                yh.copy_(lay.y, non_blocking=True)
+            st.synchronize()
+            barrier()
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                lay.x.copy_(xh, non_blocking=True)
+                lay.run(layers[i % n], st)
+                yh.copy_(lay.y, non_blocking=True)
+            st.synchronize()
+            t_e2e = (time.perf_counter() - t0) / args.steps
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([t_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": ws * LAYER_BYTES / t_e2e / 1e9, "unit": "GB/s",
+               "us_per_layer": t_e2e * 1e6,
+               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4)}
+    return ms_all, gate_ms, clk.summary(), e2e
+
+
+def cpu_baseline(sample_layers=1, rows_frac=0.25):
+    """the oracle (fp64 C++, all host threads) on a bounded sample: the first
+    rows_frac of every matrix of one layer; reported as weight GB/s."""
+    import oracle
+    import synth
+    L, x = synth.gemma3_layer(seed=0)
+    H, I, NQ = synth.GEMMA3_HIDDEN, synth.GEMMA3_INTER, synth.GEMMA3_NQ
+    nth = os.cpu_count() or 1
+    jobs = [(oracle.Q4_K, L["wq"], H, x), (oracle.Q4_K, L["wk"], H, x), (oracle.Q6_K, L["wv"], H, x),
+            (oracle.Q4_K, L["wo"], NQ, np.zeros((1, NQ), np.float32)),
+            (oracle.Q4_K, L["wg"], H, x), (oracle.Q4_K, L["wu"], H, x),
+            (oracle.Q6_K, L["wd"], I, np.zeros((1, I), np.float32))]
+    nbytes = 0
+    t0 = time.perf_counter()
+    for fmt, W, cols, xin in jobs:
+        r = max(1, int(W.shape[0] * rows_frac))
+        oracle.matvec(fmt, W[:r], r, cols, xin, nth)
+        nbytes += W[:r].nbytes
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+            "sample": f"first {int(rows_frac * 100)}% of the rows of every matrix of one layer "
+                      f"({nbytes} weight bytes), fp64, {nth} threads"}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    peak, peak_src = peaks()
+    base = {"metric": METRIC, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random Q4_K/Q6_K blocks)",
+            "config": {"workload": "Gemma-3-4B-shaped decode layer, batch 1, hidden 2560: QKV "
+                                   "(Q/K Q4_K, V Q6_K), O Q4_K, gate+up Q4_K GEGLU-tanh, down Q6_K",
+                       "layer_weight_bytes": LAYER_BYTES, "layer_copies": args.layers,
+                       "l2": "inputs larger than L2 (34 rotating layer copies, 2.06 GB)",
+                       "parallelism": f"replicas x{ws}"}}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        for _ in range(args.warmup):
+            cpu_baseline(rows_frac=0.02)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            vals.append(cpu_baseline(rows_frac=0.02))
+        dt = (time.perf_counter() - t0) / args.steps
+        cb = vals[-1]
+        v = statistics.median(c["value"] for c in vals)
+        cb["value"] = v
+        line = dict(base, impl="reference", value=v, ms_per_step=dt * 1e3, n_gpus=1,
+                    cpu_baseline=cb, e2e={"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0})
+        print(json.dumps(line))
+        return
+
+    ms, gate_ms, clocks, e2e = bench_lq(args, ws, rank, local)
+    if rank != 0:
+        return
+    value = ws * LAYER_BYTES / (ms * 1e-3) / 1e9
+    achieved = GATEUP_BYTES / (gate_ms * 1e-3) / 1e9
+    cb = cpu_baseline() if ws == 1 else None
+    line = dict(base, value=value, ms_per_step=ms, us_per_layer=ms * 1e3,
+                frac_of_hbm=value / peak,
+                roofline={"bound": "hbm", "kernel": "ffn gate+up GEGLU (Q4_K 2x10240x2560)",
+                          "achieved": achieved, "peak": peak, "peak_source": peak_src,
+                          "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                          "us_per_launch": gate_ms * 1e3},
+                clocks=clocks, e2e=e2e, gpu_launches=4 * args.steps, cpu_baseline=cb)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

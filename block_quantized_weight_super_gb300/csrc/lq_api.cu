@@ -1,0 +1,488 @@
+// lq_api.cu -- the C ABI (include/lq.h): argument validation, launch
+// planning and dispatch to the kernels.  Host code only, apart from the
+// device status word.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/lq.h"
+#include "lq_codec.cuh"
+#include "lq_internal.h"
+
+namespace lq {
+
+// Status word the kernels set when a bounded wait runs out; its device
+// address is passed to kernels (no relocatable device code needed).
+static __device__ unsigned g_status_word = 0;
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(LQ_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool fmt_ok(int fmt) { return fmt == FMT_Q4_K || fmt == FMT_Q6_K || fmt == FMT_Q8_0; }
+
+int64_t rowbytes(int fmt, int64_t cols) { return cols / block_elems_of(fmt) * block_bytes_of(fmt); }
+
+bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Per-device facts and one-time set-up.
+struct DevInfo {
+    bool init = false;
+    int sms = 0;
+    unsigned* status = nullptr;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int dev_info(DevInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(LQ_EUNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.init) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        d.status = static_cast<unsigned*>(p);
+        e = stream_set_smem_limit(227 * 1024);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        d.init = true;
+    }
+    *out = &d;
+    return LQ_OK;
+}
+
+// ---------------------------------------------------------------- planning
+struct Plan {
+    int B = 0, k = 0, R = 0, RT = 0, NT = 0, nstages = 0, stage_bytes = 0;
+    size_t smem = 0;
+};
+
+// Streaming-kernel geometry for batch width B over `cols` with segments of
+// the given formats (their row bytes set the stage size).  False if the
+// kernel cannot take this shape (then the plain-load kernel is used).
+bool plan_stream(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, Plan& p) {
+    if (cols % 64 != 0 || cols <= 0 || cols > (1 << 20)) return false;
+    const int64_t ngroups = cols / 64;
+    const int64_t U = ngroups * B;
+    if (U > 512) return false;
+    int k = 0;
+    for (int kk = 1; U * kk <= 512; ++kk) {
+        if ((U * kk) % 32) continue;
+        k = kk;
+        if (U * kk >= 256) break;
+    }
+    if (k == 0) return false;
+    int64_t rbmax = 0;
+    for (int f : fmts) rbmax = std::max<int64_t>(rbmax, rowbytes(f, cols));
+    // rows per thread per tile: R*B <= 8, stage <= 48 KB, tile rows even for pairs
+    int R = 0;
+    for (int r = 8 / B; r >= 1; --r) {
+        const int64_t RT = (int64_t)k * r;
+        if (pairs && (RT & 1)) continue;
+        if (RT * rbmax <= 48 * 1024) {
+            // prefer tile sizes whose byte offsets stay 16-aligned for every format
+            bool aligned = true;
+            for (int f : fmts) {
+                const int64_t unit = pairs ? RT / 2 : RT;
+                if ((unit * rowbytes(f, cols)) % 16) aligned = false;
+            }
+            if (aligned || R == 0) R = r;
+            if (aligned) break;
+        }
+    }
+    if (R == 0) {   // a single tile row set is larger than 48 KB: smallest legal tile
+        R = (pairs && (k & 1)) ? 2 : 1;
+        if ((int64_t)k * R * rbmax > 200 * 1024) return false;
+    }
+    p.B = B;
+    p.k = k;
+    p.R = R;
+    p.RT = k * R;
+    p.NT = (int)(U * k);
+    p.stage_bytes = (int)(((int64_t)p.RT * rbmax + 15) / 16 * 16 + 16);
+    const size_t red = (size_t)2 * p.RT * B * U * sizeof(float);
+    const size_t budget = 200 * 1024;
+    int S = (int)((budget - red - 64) / p.stage_bytes);
+    if (S > 4) S = 4;
+    if (S < 2) S = 2;
+    p.nstages = S;
+    p.smem = (size_t)S * p.stage_bytes + red + 8 * S;
+    if (p.smem > 227 * 1024) return false;
+    return true;
+}
+
+cudaError_t launch_stream_plan(const StreamParams& P, const Plan& pl, int sms, cudaStream_t st) {
+    int per_sm = 0;
+    cudaError_t e = stream_occupancy(pl.B, pl.NT, pl.smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int grid = sms * per_sm;
+    if (grid > P.ntiles) grid = P.ntiles;
+    if (grid < 1) grid = 1;
+    return stream_launch(pl.B, P, grid, pl.NT, pl.smem, st);
+}
+
+// Run the segments (all sharing cols and the batch width B) with the
+// streaming kernel when it can take the shape, else the plain-load kernel.
+int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    std::vector<int> fmts;
+    bool pairs = false;
+    for (auto& s : segs) {
+        fmts.push_back(s.fmt);
+        pairs = pairs || s.mode != MODE_PLAIN;
+    }
+    Plan pl;
+    if (!plan_stream(B, cols, fmts, pairs, pl)) {
+        for (auto& s : segs) {
+            if (s.nout <= 0) continue;
+            cudaError_t e = launch_direct(s, cols, B, st);
+            if (e != cudaSuccess) return cuda_fail(e, "direct matvec launch");
+        }
+        return LQ_OK;
+    }
+    for (size_t s0 = 0; s0 < segs.size(); s0 += MAX_SEG) {
+        StreamParams P;
+        memset(&P, 0, sizeof P);
+        int t = 0, n = 0;
+        for (size_t i = s0; i < segs.size() && i < s0 + MAX_SEG; ++i) {
+            Seg s = segs[i];
+            if (s.nout <= 0) continue;
+            const int opt = s.mode == MODE_PLAIN ? pl.RT : pl.RT / 2;
+            s.tile0 = t;
+            s.ntiles = (s.nout + opt - 1) / opt;
+            t += s.ntiles;
+            P.seg[n++] = s;
+        }
+        if (n == 0) continue;
+        P.nseg = n;
+        P.ntiles = t;
+        P.cols = (int32_t)cols;
+        P.ngroups = (int32_t)(cols / 64);
+        P.RT = pl.RT;
+        P.k = pl.k;
+        P.nstages = pl.nstages;
+        P.stage_bytes = pl.stage_bytes;
+        P.timeout_ns = g_timeout_ns.load();
+        P.status = dev->status;
+        cudaError_t e = launch_stream_plan(P, pl, dev->sms, st);
+        if (e != cudaSuccess) return cuda_fail(e, "stream matvec launch");
+    }
+    return LQ_OK;
+}
+
+// Widest batch width the streaming kernel takes for these columns (4, 2, 1).
+int batch_width(int64_t cols, int batch) {
+    const int64_t ng = cols / 64;
+    int B = batch >= 3 ? 4 : batch;
+    while (B > 1 && (cols % 64 != 0 || ng * B > 512)) B /= 2;
+    return B;
+}
+
+Seg plain_seg(int fmt, const void* W, int64_t rows, const float* x, float* y, int64_t ld_y, int b0,
+              int nb) {
+    Seg s;
+    memset(&s, 0, sizeof s);
+    s.w = static_cast<const uint8_t*>(W);
+    s.x = x;
+    s.y = y;
+    s.ld_y = ld_y;
+    s.nout = (int32_t)rows;
+    s.fmt = fmt;
+    s.mode = MODE_PLAIN;
+    s.b0 = b0;
+    s.nbatch = nb;
+    return s;
+}
+
+int check_mat(int fmt, const void* W, int64_t rows, int64_t cols, const char* name) {
+    if (!fmt_ok(fmt)) return fail(LQ_EINVAL, "%s: unknown format %d", name, fmt);
+    if (rows < 0 || cols <= 0) return fail(LQ_ESHAPE, "%s: rows %lld cols %lld", name, (long long)rows, (long long)cols);
+    if (cols % block_elems_of(fmt) != 0)
+        return fail(LQ_ESHAPE, "%s: cols %lld not a multiple of %d", name, (long long)cols, block_elems_of(fmt));
+    if (rows > (int64_t)1 << 30 || cols > (int64_t)1 << 20)
+        return fail(LQ_ESHAPE, "%s: size out of range", name);
+    if (rows > 0 && !W) return fail(LQ_EINVAL, "%s: null weights", name);
+    if (W && !al(W, 2)) return fail(LQ_EALIGN, "%s: weights not 2-byte aligned", name);
+    return LQ_OK;
+}
+
+int check_f32(const void* p, const char* name) {
+    if (!p) return fail(LQ_EINVAL, "%s is null", name);
+    if (!al(p, 4)) return fail(LQ_EALIGN, "%s not 4-byte aligned", name);
+    return LQ_OK;
+}
+
+}  // namespace
+}  // namespace lq
+
+using namespace lq;
+
+extern "C" {
+
+size_t lq_block_bytes(int fmt) { return fmt_ok(fmt) ? (size_t)block_bytes_of(fmt) : 0; }
+int lq_block_elems(int fmt) { return fmt_ok(fmt) ? block_elems_of(fmt) : 0; }
+int64_t lq_row_bytes(int fmt, int64_t cols) {
+    if (!fmt_ok(fmt) || cols < 0 || cols % block_elems_of(fmt)) return 0;
+    return rowbytes(fmt, cols);
+}
+
+const char* lq_status_str(int s) {
+    switch (s) {
+        case LQ_OK: return "LQ_OK";
+        case LQ_EINVAL: return "LQ_EINVAL: invalid argument";
+        case LQ_EALIGN: return "LQ_EALIGN: misaligned pointer";
+        case LQ_ESHAPE: return "LQ_ESHAPE: unsupported shape";
+        case LQ_EWORKSPACE: return "LQ_EWORKSPACE: workspace too small";
+        case LQ_ECUDA: return "LQ_ECUDA: CUDA error";
+        case LQ_ETIMEOUT: return "LQ_ETIMEOUT: a bounded device wait ran out";
+        case LQ_EUNSUPPORTED: return "LQ_EUNSUPPORTED: not implemented";
+        default: return "unknown lq status";
+    }
+}
+
+const char* lq_last_error(void) { return g_err; }
+
+void lq_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_mat(fmt, W, rows, cols, "W");
+    if (rc) return rc;
+    if (rows == 0) return LQ_OK;
+    if ((rc = check_f32(out, "out"))) return rc;
+    cudaError_t e = launch_dequant(fmt, static_cast<const uint8_t*>(W), rows, cols, out,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "dequant launch");
+}
+
+int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+              int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_mat(fmt, W, rows, cols, "W");
+    if (rc) return rc;
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (rows == 0) return LQ_OK;
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
+    const int B = batch_width(cols, batch);
+    std::vector<Seg> segs;
+    for (int b0 = 0; b0 < batch; b0 += B)
+        segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(B, batch - b0)));
+    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
+                 const void* Wv, int64_t nv, int64_t cols, const float* x, float* q, float* k,
+                 float* v, int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_mat(fq, Wq, nq, cols, "Wq")) || (rc = check_mat(fk, Wk, nk, cols, "Wk")) ||
+        (rc = check_mat(fv, Wv, nv, cols, "Wv")))
+        return rc;
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (nq + nk + nv == 0) return LQ_OK;
+    if ((rc = check_f32(x, "x"))) return rc;
+    if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
+        (nv && (rc = check_f32(v, "v"))))
+        return rc;
+    const int B = batch_width(cols, batch);
+    std::vector<Seg> segs;
+    for (int b0 = 0; b0 < batch; b0 += B) {
+        const int nb = std::min(B, batch - b0);
+        if (nq) segs.push_back(plain_seg(fq, Wq, nq, x, q, nq, b0, nb));
+        if (nk) segs.push_back(plain_seg(fk, Wk, nk, x, k, nk, b0, nb));
+        if (nv) segs.push_back(plain_seg(fv, Wv, nv, x, v, nv, b0, nb));
+    }
+    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int64_t cols,
+                    void* Wgu_out, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_mat(fmt, Wg, inter, cols, "Wg")) || (rc = check_mat(fmt, Wu, inter, cols, "Wu")))
+        return rc;
+    if (inter == 0) return LQ_OK;
+    if (!Wgu_out) return fail(LQ_EINVAL, "Wgu_out is null");
+    if (!al(Wgu_out, 2)) return fail(LQ_EALIGN, "Wgu_out not 2-byte aligned");
+    cudaError_t e = launch_interleave(static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu),
+                                      inter, rowbytes(fmt, cols), static_cast<uint8_t*>(Wgu_out),
+                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "interleave launch");
+}
+
+int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
+                       float* h, int batch, int act, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_mat(fmt, Wgu, 2 * inter, cols, "Wgu");
+    if (rc) return rc;
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    if (inter == 0) return LQ_OK;
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
+    const int B = batch_width(cols, batch);
+    std::vector<Seg> segs;
+    for (int b0 = 0; b0 < batch; b0 += B) {
+        Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(B, batch - b0));
+        s.mode = MODE_PAIR_INTERLEAVED;
+        s.act = act;
+        segs.push_back(s);
+    }
+    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t lq_moe_workspace_bytes(int E, int topk, int ntok, int64_t hidden, int64_t inter) {
+    if (E < 1 || topk < 1 || ntok < 0 || hidden < 0 || inter < 0) return 0;
+    const size_t ns = (size_t)ntok * topk;
+    return align256(ns * 4) * 4 + align256((size_t)E * 4) * 2 + align256(ns * inter * 4) +
+           align256(ns * hidden * 4);
+}
+
+int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const* W1,
+               const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
+               const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+               void* workspace, size_t ws_bytes, lq_stream_t stream) {
+    g_err[0] = 0;
+    if (E < 1 || E > 256) return fail(LQ_EINVAL, "n_experts %d", E);
+    if (topk < 1 || topk > E) return fail(LQ_EINVAL, "topk %d with %d experts", topk, E);
+    if (ntok < 0) return fail(LQ_EINVAL, "ntok %d", ntok);
+    if (!W1 || !W3 || !W2) return fail(LQ_EINVAL, "expert pointer arrays are null");
+    int rc;
+    for (int e = 0; e < E; ++e) {
+        if ((rc = check_mat(fmt, W1[e], inter, hidden, "W1")) || (rc = check_mat(fmt, W3[e], inter, hidden, "W3")) ||
+            (rc = check_mat(fmt, W2[e], hidden, inter, "W2")))
+            return rc;
+        if (!W1[e] || !W3[e] || !W2[e]) return fail(LQ_EINVAL, "expert %d weights null", e);
+    }
+    if (ntok == 0) return LQ_OK;
+    if ((long long)ntok * E * 4 > 48 * 1024) return fail(LQ_ESHAPE, "ntok * n_experts too large");
+    if ((rc = check_f32(router, "router")) || (rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y")))
+        return rc;
+    if ((topk_idx && !al(topk_idx, 4)) || (topk_w && !al(topk_w, 4)))
+        return fail(LQ_EALIGN, "topk outputs not 4-byte aligned");
+    const size_t need = lq_moe_workspace_bytes(E, topk, ntok, hidden, inter);
+    if (!workspace || ws_bytes < need)
+        return fail(LQ_EWORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    if (!al(workspace, 256)) return fail(LQ_EALIGN, "workspace not 256-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    const size_t ns = (size_t)ntok * topk;
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    MoeWs ws;
+    ws.idx = reinterpret_cast<int32_t*>(p); p += align256(ns * 4);
+    ws.w = reinterpret_cast<float*>(p); p += align256(ns * 4);
+    ws.tok_of = reinterpret_cast<int32_t*>(p); p += align256(ns * 4);
+    ws.slot_row = reinterpret_cast<int32_t*>(p); p += align256(ns * 4);
+    ws.grp_off = reinterpret_cast<int32_t*>(p); p += align256((size_t)E * 4);
+    ws.grp_cnt = reinterpret_cast<int32_t*>(p); p += align256((size_t)E * 4);
+    ws.hbuf = reinterpret_cast<float*>(p); p += align256(ns * inter * 4);
+    ws.ybuf = reinterpret_cast<float*>(p);
+    if (topk_idx) ws.idx = topk_idx;
+    if (topk_w) ws.w = topk_w;
+
+    cudaError_t e = launch_moe_route(router, E, hidden, X, ntok, topk, ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe route launch");
+
+    // grouped expert gate+up (+SwiGLU): segment per (expert, chunk of B rows)
+    {
+        const int B = batch_width(hidden, ntok);
+        std::vector<Seg> segs;
+        for (int c = 0; c * B < ntok; ++c)
+            for (int ex = 0; ex < E; ++ex) {
+                Seg s;
+                memset(&s, 0, sizeof s);
+                s.w = static_cast<const uint8_t*>(W1[ex]);
+                s.w2 = static_cast<const uint8_t*>(W3[ex]);
+                s.x = X;
+                s.xmap = ws.tok_of;
+                s.y = ws.hbuf;
+                s.boff = ws.grp_off + ex;
+                s.bcnt = ws.grp_cnt + ex;
+                s.ld_y = inter;
+                s.nout = (int32_t)inter;
+                s.fmt = fmt;
+                s.mode = MODE_PAIR_TWO;
+                s.act = ACT_SWIGLU;
+                s.b0 = c * B;
+                segs.push_back(s);
+            }
+        if ((rc = run_segments(segs, B, hidden, st))) return rc;
+    }
+    // grouped expert down: x rows are the grouped hidden activations
+    {
+        const int B = batch_width(inter, ntok);
+        std::vector<Seg> segs;
+        for (int c = 0; c * B < ntok; ++c)
+            for (int ex = 0; ex < E; ++ex) {
+                Seg s;
+                memset(&s, 0, sizeof s);
+                s.w = static_cast<const uint8_t*>(W2[ex]);
+                s.x = ws.hbuf;
+                s.y = ws.ybuf;
+                s.boff = ws.grp_off + ex;
+                s.bcnt = ws.grp_cnt + ex;
+                s.ld_y = hidden;
+                s.nout = (int32_t)hidden;
+                s.fmt = fmt;
+                s.mode = MODE_PLAIN;
+                s.b0 = c * B;
+                segs.push_back(s);
+            }
+        if ((rc = run_segments(segs, B, inter, st))) return rc;
+    }
+    e = launch_moe_combine(ws.ybuf, hidden, ntok, topk, ws, Y, st);
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "moe combine launch");
+}
+
+int lq_device_status(lq_stream_t stream, uint32_t* bits) {
+    g_err[0] = 0;
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned v = 0;
+    e = cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read status");
+    const unsigned zero = 0;
+    e = cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    if (bits) *bits = v;
+    return (v & STATUS_TIMEOUT) ? fail(LQ_ETIMEOUT, "device status 0x%x", v) : LQ_OK;
+}
+
+int lq_probe_timeout(uint64_t timeout_ns, lq_stream_t stream) {
+    g_err[0] = 0;
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    cudaError_t e = launch_timeout_probe(timeout_ns, dev->status, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "probe launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// lq_internal.h -- launchers shared between the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "lq_stream.cuh"
+
+namespace lq {
+
+// MoE workspace views (device memory carved from the caller's workspace).
+struct MoeWs {
+    int32_t* idx;        // [ntok*topk] selected experts
+    float* w;            // [ntok*topk] renormalised weights
+    int32_t* tok_of;     // [ntok*topk] token of each grouped row
+    int32_t* slot_row;   // [ntok*topk] grouped row of each (token, slot)
+    int32_t* grp_off;    // [E] first grouped row of each expert
+    int32_t* grp_cnt;    // [E] grouped rows of each expert
+    float* hbuf;         // [ntok*topk][inter] expert hidden activations
+    float* ybuf;         // [ntok*topk][hidden] expert outputs
+};
+
+// streaming matvec kernel (lq_stream.cu), batch width B in {1, 2, 4}
+cudaError_t stream_set_smem_limit(int bytes);
+cudaError_t stream_occupancy(int B, int nt, size_t smem, int* per_sm);
+cudaError_t stream_launch(int B, const StreamParams& P, int grid, int nt, size_t smem,
+                          cudaStream_t st);
+
+cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,
+                           cudaStream_t st);
+cudaError_t launch_interleave(const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t rb,
+                              uint8_t* out, cudaStream_t st);
+cudaError_t launch_direct(const Seg& S, int64_t cols, int maxb, cudaStream_t st);
+cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float* X, int ntok,
+                             int topk, const MoeWs& ws, cudaStream_t st);
+cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int topk,
+                               const MoeWs& ws, float* Y, cudaStream_t st);
+cudaError_t launch_timeout_probe(uint64_t timeout_ns, unsigned* status, cudaStream_t st);
+
+}  // namespace lq

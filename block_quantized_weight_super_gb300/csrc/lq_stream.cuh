@@ -1,0 +1,50 @@
+// lq_stream.cuh -- parameters of the streaming matvec kernel (shared by the
+// kernel translation unit and the host launchers).
+#pragma once
+#include <cstdint>
+
+namespace lq {
+
+constexpr int MAX_SEG = 36;
+
+enum { MODE_PLAIN = 0, MODE_PAIR_INTERLEAVED = 1, MODE_PAIR_TWO = 2 };
+enum { ACT_NONE = 0, ACT_GEGLU_TANH = 1, ACT_SWIGLU = 2 };
+
+// One weight matrix (or gate/up matrix pair) of a launch, with where its x
+// rows come from and where its outputs go.  Batch row b of the segment is
+// rho_b = (*boff or 0) + b0 + b; its x row is x + (xmap ? xmap[rho_b] : rho_b)
+// * cols and its output row is y + rho_b * ld_y.
+struct Seg {
+    const uint8_t* w;      // matrix (plain / interleaved pairs) or gate matrix
+    const uint8_t* w2;     // up matrix (MODE_PAIR_TWO)
+    const float* x;
+    const int32_t* xmap;   // optional device gather list
+    float* y;
+    const int32_t* boff;   // optional device offset of batch row 0
+    const int32_t* bcnt;   // optional device count of rows from boff (valid rows: b0 + b < cnt)
+    int64_t ld_y;
+    int32_t nout;          // output rows (plain) or output pairs (pair modes)
+    int32_t fmt;
+    int32_t mode;
+    int32_t act;
+    int32_t b0;
+    int32_t nbatch;        // valid batch rows when bcnt is null
+    int32_t tile0;         // first global tile index of this segment
+    int32_t ntiles;
+};
+
+struct StreamParams {
+    Seg seg[MAX_SEG];
+    int32_t nseg;
+    int32_t ntiles;        // total tiles over all segments
+    int32_t cols;
+    int32_t ngroups;       // cols / 64
+    int32_t RT;            // matrix rows per tile (even)
+    int32_t k;             // row slots: threads = ngroups * B * k
+    int32_t nstages;
+    int32_t stage_bytes;   // bytes per stage buffer (multiple of 16, + 16 pad)
+    uint64_t timeout_ns;
+    unsigned* status;      // device status word (timeouts are recorded here)
+};
+
+}  // namespace lq

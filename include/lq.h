@@ -1,0 +1,143 @@
+/* lq.h -- C ABI of the block-quantized decode matvec library (liblq.so).
+ *
+ * The library computes the matrix-vector products of LLM decoding against
+ * GGUF-style block-quantized weights on one NVIDIA GB300 (sm_103a).  Every
+ * call is asynchronous on the caller's CUDA stream, validates its arguments
+ * on the host before launching anything, allocates nothing, and returns an
+ * lq_status (LQ_OK = 0).  No C++ exception crosses this boundary.
+ *
+ * Sources of the operations (pages cited by title and section):
+ *  - larql "Architecture -> Metal shader map": the Gemma 3 table names the
+ *    production kernels of one decode layer -- q4k_q6k_qkv_proj (QKV,
+ *    Q4_K Q/K + Q6_K V), q4k_matvec_8sg (O projection), q4k_ffn_gate_up_8sg +
+ *    geglu (FFN gate+up, GELU-tanh), q6k_matvec (FFN down), q4k_matvec
+ *    (lm_head); the Llama table the SiLU variant; the dispatch-predicate table
+ *    the 144-byte Q4_K ("Q4_KF", GGUF-direct) block; the Gemma 4 26B-A4B table
+ *    the MoE gate scoring (f32_gemv), per-expert gate_up + down, and combine.
+ *  - dotLLM PR #320: the Q8_0 GEMV (matmul_q8_0) and its row-stride fix
+ *    (row stride = blocksPerRow * 34 bytes); the LoRA Q8_0 commit (inputs
+ *    must be a multiple of the 32-element group, otherwise rejected); the MoE
+ *    commit (MoeSwiGluMlp: softmax over experts, top-k with the lower index
+ *    winning ties, renormalise by the selected sum, per-expert SwiGLU,
+ *    weighted sum); ForwardBatch (batched rows of activations [sum N_i][K]).
+ *
+ * Layout conventions (all calls):
+ *  - W is row-major block rows: row r starts at W + r * lq_row_bytes(fmt, cols)
+ *    and holds cols / lq_block_elems(fmt) consecutive blocks.  W must be
+ *    2-byte aligned (16-byte alignment is the fast path, not a requirement).
+ *  - x is [batch][cols] fp32 row-major, y is [batch][rows] fp32 row-major
+ *    (4-byte aligned).
+ *  - cols must be a multiple of the format's block (LQ_ESHAPE otherwise);
+ *    rows == 0 (or ntok == 0) returns LQ_OK without launching.
+ *  - Numerics: dequantized weights are exact fp32 (Q4_K: one rounding of
+ *    d*sc*q - dmin*m; Q6_K, Q8_0: exact); dot products accumulate in fp32
+ *    with short fixed-order chains; each output is within
+ *    1e-5 * sum_j |w_ij x_j| + 1e-6 of the exact value.  Results are
+ *    deterministic and do not depend on the batch size.
+ *  - Pointers are device pointers unless stated; the caller owns all memory.
+ *  - stream may be NULL (the legacy default stream).
+ */
+#ifndef LQ_H_
+#define LQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* lq_stream_t; /* a cudaStream_t */
+
+typedef enum { LQ_Q4_K = 1, LQ_Q6_K = 2, LQ_Q8_0 = 3 } lq_fmt;
+typedef enum { LQ_ACT_GEGLU_TANH = 1, LQ_ACT_SWIGLU = 2 } lq_act;
+typedef enum {
+    LQ_OK = 0,
+    LQ_EINVAL = 1,      /* null pointer, batch < 1, bad topk, unknown enum      */
+    LQ_EALIGN = 2,      /* W not 2-byte aligned, or x / y not 4-byte aligned     */
+    LQ_ESHAPE = 3,      /* cols not a multiple of the block, sizes out of range  */
+    LQ_EWORKSPACE = 4,  /* workspace smaller than lq_moe_workspace_bytes         */
+    LQ_ECUDA = 5,       /* a CUDA launch or query failed (see lq_last_error)     */
+    LQ_ETIMEOUT = 6,    /* a kernel's bounded wait ran out (lq_device_status)    */
+    LQ_EUNSUPPORTED = 7 /* a combination this build does not implement           */
+} lq_status;
+
+/* Format facts.  Q4_K: 144 bytes / 256 weights; Q6_K: 210 / 256; Q8_0: 34 / 32.
+ * Unknown formats return 0. */
+size_t lq_block_bytes(int fmt);
+int lq_block_elems(int fmt);
+int64_t lq_row_bytes(int fmt, int64_t cols); /* 0 if cols is not a block multiple */
+
+const char* lq_status_str(int status);
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* lq_last_error(void);
+
+/* lq_dequant -- out[r][c] = w_rc as fp32 for a rows x cols matrix.
+ * Exact: equals the definition bit for bit.  out: [rows][cols] fp32. */
+int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out,
+               lq_stream_t stream);
+
+/* lq_matvec -- y[b][r] = sum_j w_rj x[b][j] for b < batch (batch >= 1).
+ * larql Gemma 3 table (q4k_matvec, q6k_matvec); dotLLM matmul_q8_0 GEMV. */
+int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+              int batch, lq_stream_t stream);
+
+/* lq_qkv_mixed -- q = Wq.x, k = Wk.x, v = Wv.x in ONE launch over a shared
+ * x (larql q4k_q6k_qkv_proj: Q/K Q4_K and V Q6_K, or uniform formats).
+ * Each matrix has its own format and row count; all share cols.
+ * q: [batch][nq], k: [batch][nk], v: [batch][nv]. */
+int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
+                 const void* Wv, int64_t nv, int64_t cols, const float* x, float* q, float* k,
+                 float* v, int batch, lq_stream_t stream);
+
+/* lq_pack_gate_up -- one-time repack of separate gate and up matrices
+ * (inter x cols each, same format) into the interleaved layout the fused
+ * kernel reads: row 2i = gate row i, row 2i+1 = up row i.
+ * Wgu_out: 2 * inter * lq_row_bytes(fmt, cols) bytes. */
+int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int64_t cols,
+                    void* Wgu_out, lq_stream_t stream);
+
+/* lq_ffn_gate_up_act -- h[b][i] = act(g) * u with g = (gate row i).x_b,
+ * u = (up row i).x_b, from the interleaved Wgu (lq_pack_gate_up), the
+ * activation fused before the store.  act: LQ_ACT_GEGLU_TANH
+ * (0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3)))) or LQ_ACT_SWIGLU
+ * (g / (1 + exp(-g))).  larql q4k_ffn_gate_up_8sg + geglu.  h: [batch][inter]. */
+int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
+                       float* h, int batch, int act, lq_stream_t stream);
+
+/* MoE expert FFN (dotLLM MoeSwiGluMlp rule; larql Gemma 4 26B-A4B table).
+ * router: [E][hidden] fp32; logits l_e = router_e . x_t, p = softmax(l),
+ * top-k experts (lower index wins ties), weights p / sum of selected p;
+ * Y_t = sum_k w_tk * W2_e (silu(W1_e x_t) * (W3_e x_t)), e = the k-th pick
+ * (W1 = gate, W3 = up: inter x hidden; W2 = down: hidden x inter; all fmt).
+ * W1, W3, W2 are HOST arrays of E device pointers.  X, Y: [ntok][hidden].
+ * topk_idx / topk_w (optional, may be NULL): [ntok][topk] outputs of the
+ * routing.  workspace: device memory of at least lq_moe_workspace_bytes
+ * bytes, 256-byte aligned; its contents are scratch. */
+size_t lq_moe_workspace_bytes(int n_experts, int topk, int ntok, int64_t hidden, int64_t inter);
+int lq_moe_ffn(const float* router, int n_experts, int topk, int fmt, const void* const* W1,
+               const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
+               const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+               void* workspace, size_t ws_bytes, lq_stream_t stream);
+
+/* lq_device_status -- synchronises `stream`, then reads and clears the
+ * device status word that kernels set when a bounded wait runs out.
+ * *bits = the word (0 = clean).  Returns LQ_ETIMEOUT if the timeout bit was
+ * set, LQ_OK otherwise (LQ_ECUDA on a CUDA error). */
+int lq_device_status(lq_stream_t stream, uint32_t* bits);
+
+/* lq_set_wait_timeout_ns -- wall-time limit of every bounded wait in later
+ * launches (default 1e9 ns).  Process-wide. */
+void lq_set_wait_timeout_ns(uint64_t ns);
+
+/* lq_probe_timeout -- failure-detection check: launches a kernel that waits,
+ * with the bounded wait, on a barrier nothing completes; after timeout_ns it
+ * records the timeout in the device status word and exits.  Follow with
+ * lq_device_status to observe LQ_ETIMEOUT. */
+int lq_probe_timeout(uint64_t timeout_ns, lq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LQ_H_ */

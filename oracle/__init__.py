@@ -66,6 +66,7 @@ def lib():
         L.orc_moe_ffn.argtypes = [i32, vp, vp, vp, i64, i64, vp, i32, i32, vp, vp, vp, vp, vp,
                                   vp, vp, vp, vp, vp, i32]
         L.orc_abs_matvec.argtypes = [i32, vp, i64, i64, vp, vp, i32]
+        L.orc_moe_weights.argtypes = [vp, i32, i32, vp, i32, vp]
         _lib = L
     return _lib
 
@@ -158,6 +159,16 @@ def moe_route(R, X, topk: int):
     return idx, w, logits, labs
 
 
+def moe_weights(logits, idx):
+    """routing weights of a given selection idx [ntok][topk] from fp64 logits [ntok][E]."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    ntok, E = logits.shape
+    w = np.empty(idx.shape, dtype=np.float64)
+    lib().orc_moe_weights(_p(logits), E, ntok, _p(idx), idx.shape[1], _p(w))
+    return w
+
+
 def moe_ffn(fmt: int, W1, W3, W2, hidden: int, inter: int, X, idx, w, nthreads: int = 1):
     """expert FFN + weighted combine for a given routing (idx, w)."""
     W1 = [_u8(a) for a in W1]
@@ -229,3 +240,39 @@ def gate_up_bound(g, u, Sg, Su, act: int):
     a = act_abs(g, act)
     au = np.abs(u) + eu
     return 1.2 * eg * au + a * eu + 8 * U32 * (a + 1.2 * eg) * au
+
+
+def moe_check(fmt: int, W1, W3, W2, hidden: int, inter: int, X, logits, labs, idx_gpu,
+              nthreads: int = 1):
+    """Oracle result and per-element bound for the MoE evaluated on the GPU's
+    expert selection idx_gpu [ntok][topk].
+
+    Returns dict: Y (fp64 reference), bound, w (oracle weights of the selection),
+    admissible (bool per token: the selection is a valid top-k within the
+    logits' error e_l = 1e-5*sum|R x| + 1e-6).
+    Bound per output: sum_k w_k B_y,k + |y_k| (2 w_k e_lmax + 8 u32 w_k), with
+    B_y = 1e-5 Sy + 1e-6 + sum_j |w2_ij| B_h,j and B_h the gate/up bound."""
+    idx_gpu = np.ascontiguousarray(idx_gpu, dtype=np.int32)
+    ntok, topk = idx_gpu.shape
+    E = logits.shape[1]
+    el = 1e-5 * np.asarray(labs) + 1e-6
+    adm = np.zeros(ntok, dtype=bool)
+    for t in range(ntok):
+        sel = set(int(e) for e in idx_gpu[t])
+        if len(sel) != topk or min(sel) < 0 or max(sel) >= E:
+            continue
+        rest = [e for e in range(E) if e not in sel]
+        ok = all(logits[t, a] + el[t, a] >= logits[t, b] - el[t, b] for a in sel for b in rest)
+        adm[t] = ok
+    w = moe_weights(logits, idx_gpu)
+    out = moe_ffn(fmt, W1, W3, W2, hidden, inter, X, idx_gpu, w, nthreads)
+    Bh = gate_up_bound(out["g"], out["u"], out["Sg"], out["Su"], ACT_SWIGLU)
+    bound = np.zeros((ntok, hidden))
+    for t in range(ntok):
+        elmax = el[t].max()
+        for k in range(topk):
+            s = t * topk + k
+            e = int(idx_gpu[t, k])
+            By = 1e-5 * out["Sy"][s] + 1e-6 + abs_matvec(fmt, W2[e], hidden, inter, Bh[s], nthreads)
+            bound[t] += w[t, k] * By + np.abs(out["ye"][s]) * (2 * w[t, k] * elmax + 8 * U32 * w[t, k])
+    return {"Y": out["Y"], "bound": bound, "w": w, "admissible": adm, "el": el, "ye": out["ye"]}

@@ -284,6 +284,23 @@ void orc_moe_route(const float* R, int E, int64_t hidden, const float* X, int nt
     }
 }
 
+// Routing weights of a given selection: p = softmax(l) over all E experts,
+// w_k = p_{idx_k} / sum of the selected p (renormalised by the sum).
+void orc_moe_weights(const double* logits, int E, int ntok, const int32_t* idx, int topk,
+                     double* w) {
+    for (int t = 0; t < ntok; ++t) {
+        const double* l = logits + (int64_t)t * E;
+        double mx = l[0];
+        for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += std::exp(l[e] - mx);
+        double sel = 0.0;
+        for (int k = 0; k < topk; ++k) sel += std::exp(l[idx[t * topk + k]] - mx) / z;
+        for (int k = 0; k < topk; ++k)
+            w[t * topk + k] = (std::exp(l[idx[t * topk + k]] - mx) / z) / sel;
+    }
+}
+
 // MoE expert FFN given a routing (idx, w): for token t,
 //   Y_t = sum_k w_tk * W2_e (silu(W1_e x_t) * (W3_e x_t)),  e = idx[t][k]
 // (w1 = gate, w3 = up, w2 = down, Mixtral naming).  Y: [ntok][hidden].

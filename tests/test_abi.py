@@ -1,0 +1,114 @@
+"""The C-ABI library (liblq.so) loads on the host, exports every entry point
+that include/lq.h declares, and validates arguments before touching the GPU
+(these calls return before any CUDA call, so they run without a GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "lq.h")
+
+
+@pytest.fixture(scope="module")
+def lq():
+    import block_quantized_weight_super_gb300 as pkg
+    from block_quantized_weight_super_gb300 import build
+    build.build()
+    pkg.lib()
+    return pkg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lq_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ["lq_dequant", "lq_matvec", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
+              "lq_moe_workspace_bytes", "lq_moe_ffn"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lq):
+    L = C.CDLL(lq.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert sorted(lq.EXPORTS) == declared_functions()
+
+
+def test_format_facts(lq):
+    assert lq.lq_block_bytes(1) == 144 and lq.lq_block_elems(1) == 256
+    assert lq.lq_block_bytes(2) == 210 and lq.lq_block_elems(2) == 256
+    assert lq.lq_block_bytes(3) == 34 and lq.lq_block_elems(3) == 32
+    assert lq.lq_block_bytes(9) == 0 and lq.lq_block_elems(0) == 0
+    assert lq.lq_row_bytes(1, 2560) == 1440
+    assert lq.lq_row_bytes(2, 2560) == 2100
+    assert lq.lq_row_bytes(3, 96) == 102
+    assert lq.lq_row_bytes(3, 100) == 0
+
+
+def test_status_strings(lq):
+    for s in range(8):
+        assert lq.lq_status_str(s).startswith("LQ_")
+
+
+# Arguments rejected on the host: no CUDA call is made on these paths.
+FAKE = 0x10000      # a 16-byte aligned non-null address never dereferenced here
+
+
+def _rc(f, *a):
+    return getattr(C.CDLL(__import__("block_quantized_weight_super_gb300").LIB_PATH), f)(*a)
+
+
+def test_matvec_validation(lq):
+    L = lq.lib()
+    i64 = C.c_int64
+    assert L.lq_matvec(1, None, 4, 256, FAKE, FAKE, 1, None) == lq.LQ_EINVAL
+    assert L.lq_matvec(1, FAKE, 4, 250, FAKE, FAKE, 1, None) == lq.LQ_ESHAPE
+    assert L.lq_matvec(3, FAKE, 4, 48, FAKE, FAKE, 1, None) == lq.LQ_ESHAPE
+    assert L.lq_matvec(1, FAKE, 4, 256, FAKE, FAKE, 0, None) == lq.LQ_EINVAL
+    assert L.lq_matvec(7, FAKE, 4, 256, FAKE, FAKE, 1, None) == lq.LQ_EINVAL
+    assert L.lq_matvec(1, FAKE + 1, 4, 256, FAKE, FAKE, 1, None) == lq.LQ_EALIGN
+    assert L.lq_matvec(1, FAKE, 4, 256, FAKE + 2, FAKE, 1, None) == lq.LQ_EALIGN
+    assert L.lq_matvec(1, FAKE, 4, 256, FAKE, FAKE + 1, 1, None) == lq.LQ_EALIGN
+    assert L.lq_matvec(1, FAKE, 4, 256, None, FAKE, 1, None) == lq.LQ_EINVAL
+    assert L.lq_matvec(1, FAKE, -1, 256, FAKE, FAKE, 1, None) == lq.LQ_ESHAPE
+    # rows == 0: nothing to do, no launch
+    assert L.lq_matvec(1, FAKE, 0, 256, FAKE, FAKE, 1, None) == lq.LQ_OK
+    assert "batch" in lq.lq_last_error() or lq.lq_last_error() == ""
+
+
+def test_other_entry_validation(lq):
+    L = lq.lib()
+    assert L.lq_dequant(2, FAKE, 3, 100, FAKE, None) == lq.LQ_ESHAPE
+    assert L.lq_dequant(2, FAKE, 0, 256, FAKE, None) == lq.LQ_OK
+    assert L.lq_ffn_gate_up_act(1, FAKE, 4, 256, FAKE, FAKE, 1, 3, None) == lq.LQ_EINVAL
+    assert L.lq_ffn_gate_up_act(1, FAKE, 0, 256, FAKE, FAKE, 1, 1, None) == lq.LQ_OK
+    assert L.lq_pack_gate_up(1, FAKE, FAKE, 4, 256, None, None) == lq.LQ_EINVAL
+    assert L.lq_qkv_mixed(1, FAKE, 4, 1, FAKE, 4, 2, FAKE, 4, 300, FAKE, FAKE, FAKE, FAKE, 1,
+                          None) == lq.LQ_ESHAPE
+    assert L.lq_qkv_mixed(1, FAKE, 0, 1, FAKE, 0, 2, FAKE, 0, 256, FAKE, FAKE, FAKE, FAKE, 1,
+                          None) == lq.LQ_OK
+
+
+def test_moe_validation(lq):
+    L = lq.lib()
+    P = C.c_void_p * 2
+    w = P(FAKE, FAKE)
+    wp = C.cast(w, C.c_void_p)
+    need = lq.lq_moe_workspace_bytes(2, 1, 4, 256, 256)
+    assert need > 0
+    assert lq.lq_moe_workspace_bytes(0, 1, 4, 256, 256) == 0
+    args = lambda E, k, ntok, ws, wsb: L.lq_moe_ffn(FAKE, E, k, 1, wp, wp, wp, 256, 256, FAKE,
+                                                   FAKE, ntok, None, None, ws, wsb, None)
+    assert args(2, 3, 4, FAKE, need) == lq.LQ_EINVAL        # topk > n_experts
+    assert args(2, 0, 4, FAKE, need) == lq.LQ_EINVAL
+    assert args(2, 1, 4, FAKE, need - 1) == lq.LQ_EWORKSPACE
+    assert args(2, 1, 4, None, need) == lq.LQ_EWORKSPACE
+    assert args(2, 1, 4, FAKE + 16, need) == lq.LQ_EALIGN    # workspace 256-aligned
+    assert args(2, 1, 0, FAKE, need) == lq.LQ_OK            # no tokens: no launch

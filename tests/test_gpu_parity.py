@@ -1,0 +1,308 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle on
+seeded inputs, at sizes that span several tiles and a ragged tail, plus the
+edge cases (empty, one row, odd block counts, unaligned bases, batch
+invariance, one-hot inputs, ties in the MoE router)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+Q4_K, Q6_K, Q8_0 = 1, 2, 3
+NTH = oracle.threads_default()
+
+
+@pytest.fixture(scope="module")
+def lq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_weight_super_gb300 as pkg
+    from block_quantized_weight_super_gb300 import build
+    build.build()
+    pkg.lib()
+    yield pkg
+    from gpu_util import status_clean
+    status_clean(pkg)
+
+
+from gpu_util import assert_within, dev, empty, host, status_clean  # noqa: E402
+
+
+def _bits_equal(a, b):
+    a = np.asarray(a, dtype=np.float32).copy()
+    b = np.asarray(b, dtype=np.float32).copy()
+    a[a == 0] = 0.0        # sign of zero ignored
+    b[b == 0] = 0.0
+    return np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# ---------------------------------------------------------------- dequant
+
+@pytest.mark.parametrize("fmt,rows,cols", [
+    (Q4_K, 37, 2560), (Q4_K, 1, 256), (Q6_K, 37, 2560), (Q6_K, 3, 768), (Q6_K, 5, 1280),
+    (Q8_0, 37, 4096), (Q8_0, 8, 32), (Q8_0, 4, 96), (Q8_0, 2, 160),
+])
+def test_dequant_bit_exact(lq, fmt, rows, cols):
+    W = synth.weights(synth.rng(rows * 7 + cols), fmt, rows, cols)
+    out = empty((rows, cols))
+    lq.lq_dequant(fmt, dev(W), rows, cols, out)
+    ref = oracle.dequant(fmt, W, rows, cols, NTH)
+    assert _bits_equal(host(out), ref)
+
+
+def test_dequant_hand_built_extremes(lq):
+    from blockpack import pack_q4k, pack_q6k, pack_q80
+    blocks = [
+        (Q4_K, pack_q4k(65504.0, 65504.0, [63] * 8, [63] * 8, np.full(256, 15))),
+        (Q4_K, pack_q4k(2.0 ** -24, 2.0 ** -24, [1] * 8, [63] * 8, np.arange(256) % 16)),
+        (Q4_K, pack_q4k(-1.5, -0.25, list(range(0, 64, 8)), list(range(7, 64, 8)), np.arange(256) % 16)),
+        (Q6_K, pack_q6k(-2.0, np.array([-128, 127] * 8), np.arange(256) % 64)),
+        (Q8_0, pack_q80(-0.125, np.arange(-128, 128, 8))),
+    ]
+    for fmt, blk in blocks:
+        cols = oracle.block_elems(fmt)
+        out = empty((1, cols))
+        lq.lq_dequant(fmt, dev(blk.reshape(1, -1)), 1, cols, out)
+        assert _bits_equal(host(out), oracle.dequant(fmt, blk.reshape(1, -1), 1, cols))
+
+
+# ---------------------------------------------------------------- matvec
+
+MV_CASES = [
+    (Q4_K, 333, 2560), (Q4_K, 100, 512), (Q4_K, 1, 256), (Q4_K, 70, 2048), (Q4_K, 65, 4096),
+    (Q6_K, 101, 2560), (Q6_K, 3, 768), (Q6_K, 50, 1280), (Q6_K, 45, 10240),
+    (Q8_0, 77, 4096), (Q8_0, 33, 512), (Q8_0, 3, 14336),
+]
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("fmt,rows,cols", MV_CASES)
+def test_matvec_parity(lq, fmt, rows, cols, batch):
+    g = synth.rng(rows + cols + batch)
+    W = synth.weights(g, fmt, rows, cols)
+    x = synth.activations(g, batch, cols)
+    y = empty((batch, rows))
+    lq.lq_matvec(fmt, dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"fmt {fmt} {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+def test_matvec_unaligned_weight_base(lq, fmt):
+    """W starting 2 bytes past a 16-byte boundary: rows are copied by the
+    threads instead of the bulk-copy engine; results identical."""
+    rows, cols = 41, 2048
+    g = synth.rng(5)
+    W = synth.weights(g, fmt, rows, cols)
+    x = synth.activations(g, 2, cols)
+    ya = empty((2, rows))
+    yb = empty((2, rows))
+    lq.lq_matvec(fmt, dev(W), rows, cols, dev(x), ya, 2)
+    keep, p = dev(W, offset_bytes=2)
+    lq.lq_matvec(fmt, p, rows, cols, dev(x), yb, 2)
+    assert np.array_equal(host(ya), host(yb))
+    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    assert_within(host(yb), ref, oracle.matvec_bound(S), "unaligned")
+
+
+@pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336)])
+def test_batch_invariance(lq, fmt, cols):
+    """row b of a batch-M call is bit-identical to a batch-1 call on x_b."""
+    rows = 67
+    g = synth.rng(11)
+    W = synth.weights(g, fmt, rows, cols)
+    X = synth.activations(g, 8, cols)
+    Wd = dev(W)
+    singles = []
+    for b in range(8):
+        y1 = empty((1, rows))
+        lq.lq_matvec(fmt, Wd, rows, cols, dev(X[b:b + 1]), y1, 1)
+        singles.append(host(y1)[0])
+    for M in (2, 3, 4, 8):
+        yM = empty((M, rows))
+        lq.lq_matvec(fmt, Wd, rows, cols, dev(X[:M]), yM, M)
+        got = host(yM)
+        for b in range(M):
+            assert np.array_equal(got[b], singles[b]), (M, b)
+
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+def test_one_hot_x_gives_dequant_column(lq, fmt):
+    rows, cols = 40, 1024
+    W = synth.weights(synth.rng(12), fmt, rows, cols)
+    D = oracle.dequant(fmt, W, rows, cols)
+    Wd = dev(W)
+    for j in (0, 1, 37, 511, 1023):
+        x = np.zeros((1, cols), np.float32)
+        x[0, j] = 1.0
+        y = empty((1, rows))
+        lq.lq_matvec(fmt, Wd, rows, cols, dev(x), y, 1)
+        assert _bits_equal(host(y)[0], D[:, j])
+
+
+def test_q8_0_odd_block_rows(lq):
+    """dotLLM Q8_0 row-stride regression shapes (odd blocks per row)."""
+    from conftest import golden_lines
+    for line in golden_lines("q8_0_stride_shapes.txt"):
+        M, K = map(int, line.split())
+        g = synth.rng(M * 100 + K)
+        W = synth.q8_0(g, M, K)
+        x = synth.activations(g, 1, K)
+        y = empty((1, M))
+        lq.lq_matvec(Q8_0, dev(W), M, K, dev(x), y, 1)
+        ref, S = oracle.matvec(Q8_0, W, M, K, x)
+        assert_within(host(y), ref, oracle.matvec_bound(S), f"Q8_0 {M}x{K}")
+
+
+def test_matvec_zero_rows_and_zero_x(lq):
+    W = synth.q4k(synth.rng(13), 16, 512)
+    y = empty((1, 16))
+    lq.lq_matvec(Q4_K, dev(W), 0, 512, dev(np.zeros((1, 512), np.float32)), y, 1)
+    assert np.isnan(host(y)).all()                      # nothing written
+    lq.lq_matvec(Q4_K, dev(W), 16, 512, dev(np.zeros((1, 512), np.float32)), y, 1)
+    assert (host(y) == 0).all()
+
+
+# ---------------------------------------------------------------- QKV
+
+@pytest.mark.parametrize("fq,fk,fv", [(Q4_K, Q4_K, Q6_K), (Q4_K, Q4_K, Q4_K), (Q8_0, Q8_0, Q8_0)])
+@pytest.mark.parametrize("batch", [1, 2])
+def test_qkv_mixed(lq, fq, fk, fv, batch):
+    cols, nq, nk, nv = 2560, 300, 100, 100
+    g = synth.rng(14)
+    Wq, Wk, Wv = synth.weights(g, fq, nq, cols), synth.weights(g, fk, nk, cols), synth.weights(g, fv, nv, cols)
+    x = synth.activations(g, batch, cols)
+    q, k, v = empty((batch, nq)), empty((batch, nk)), empty((batch, nv))
+    xd = dev(x)
+    lq.lq_qkv_mixed(fq, dev(Wq), nq, fk, dev(Wk), nk, fv, dev(Wv), nv, cols, xd, q, k, v, batch)
+    for f, W, n, out in ((fq, Wq, nq, q), (fk, Wk, nk, k), (fv, Wv, nv, v)):
+        ref, S = oracle.matvec(f, W, n, cols, x, NTH)
+        got = host(out)
+        assert_within(got, ref, oracle.matvec_bound(S), f"qkv fmt {f}")
+        single = empty((batch, n))
+        lq.lq_matvec(f, dev(W), n, cols, xd, single, batch)
+        assert np.array_equal(got, host(single))        # same code path, same bits
+
+
+# ---------------------------------------------------------------- gate + up
+
+@pytest.mark.parametrize("act", [1, 2])
+@pytest.mark.parametrize("fmt,inter,cols,batch", [
+    (Q4_K, 333, 2560, 1), (Q4_K, 160, 4096, 2), (Q4_K, 77, 4096, 4), (Q8_0, 99, 4096, 1),
+    (Q6_K, 50, 2560, 1), (Q4_K, 64, 2560, 8),
+])
+def test_ffn_gate_up_act(lq, fmt, inter, cols, batch, act):
+    g = synth.rng(15 + inter)
+    Wg, Wu = synth.weights(g, fmt, inter, cols), synth.weights(g, fmt, inter, cols)
+    x = synth.activations(g, batch, cols)
+    rb = lq.lq_row_bytes(fmt, cols)
+    Wgu = torch.empty(2 * inter * rb, dtype=torch.uint8, device="cuda")
+    lq.lq_pack_gate_up(fmt, dev(Wg), dev(Wu), inter, cols, Wgu)
+    packed = host(Wgu).reshape(2 * inter, rb)
+    assert np.array_equal(packed[0::2], Wg) and np.array_equal(packed[1::2], Wu)
+    h = empty((batch, inter))
+    xd = dev(x)
+    lq.lq_ffn_gate_up_act(fmt, Wgu, inter, cols, xd, h, batch, act)
+    o = oracle.ffn_gate_up(fmt, Wg, Wu, inter, cols, x, act, NTH)
+    bound = oracle.gate_up_bound(o["g"], o["u"], o["Sg"], o["Su"], act)
+    got = host(h)
+    assert_within(got, o["h"], bound, "gate_up")
+    # the fused epilogue against the unfused GPU g, u (same partial sums):
+    gg, uu = empty((batch, inter)), empty((batch, inter))
+    lq.lq_matvec(fmt, dev(Wg), inter, cols, xd, gg, batch)
+    lq.lq_matvec(fmt, dev(Wu), inter, cols, xd, uu, batch)
+    g64, u64 = host(gg).astype(np.float64), host(uu).astype(np.float64)
+    a = oracle.act_abs(g64, act) * np.sign(g64)
+    # fp32 activation: a few ulps of act(g)*u, plus the rounding of the GELU
+    # argument z (at most ~1.4 u |g| in act)
+    tol = 16 * oracle.U32 * np.abs(a * u64) + 4 * oracle.U32 * np.abs(g64 * u64) + 1e-30
+    assert_within(got, a * u64, tol, "epilogue")
+
+
+# ---------------------------------------------------------------- MoE
+
+def _moe_inputs(E, hidden, inter, ntok, seed, router_scale=1.0):
+    R, W1, W3, W2, X = synth.mixtral_moe(seed, E, hidden, inter, ntok)
+    return (R * np.float32(router_scale)).astype(np.float32), W1, W3, W2, X
+
+
+def _run_moe(lq, R, W1, W3, W2, X, topk, fmt=Q4_K):
+    E, hidden = R.shape
+    inter = W1[0].shape[0]
+    ntok = X.shape[0]
+    Y = empty((ntok, hidden))
+    idx = torch.full((ntok, topk), -1, dtype=torch.int32, device="cuda")
+    w = empty((ntok, topk))
+    nbytes = lq.lq_moe_workspace_bytes(E, topk, ntok, hidden, inter)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d1, d3, d2 = [dev(a) for a in W1], [dev(a) for a in W3], [dev(a) for a in W2]
+    lq.lq_moe_ffn(dev(R), E, topk, fmt, d1, d3, d2, hidden, inter, dev(X), Y, ntok, idx, w, ws, nbytes)
+    return host(Y), host(idx), host(w)
+
+
+@pytest.mark.parametrize("E,topk,ntok,scale", [(4, 2, 5, 1.0), (8, 2, 16, 1.0), (8, 2, 16, 30.0), (6, 3, 9, 5.0), (4, 1, 7, 10.0)])
+def test_moe_parity(lq, E, topk, ntok, scale):
+    hidden, inter = 256, 512
+    R, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=E * 10 + ntok, router_scale=scale)
+    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X, topk)
+    oidx, ow, lg, labs = oracle.moe_route(R, X, topk)
+    chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X, lg, labs, idx, NTH)
+    assert chk["admissible"].all()
+    # a clear margin makes the selection unique: then it must equal the oracle's
+    for t in range(ntok):
+        srt = np.sort(lg[t])[::-1]
+        if srt[topk - 1] - srt[topk] > 4 * chk["el"][t].max():
+            assert sorted(idx[t]) == sorted(oidx[t])
+    elmax = chk["el"].max(axis=1, keepdims=True)
+    assert_within(w, chk["w"], 2 * chk["w"] * elmax + 8 * oracle.U32, "moe weights")
+    assert_within(Y, chk["Y"], chk["bound"], "moe Y")
+
+
+def test_moe_uniform_router_is_expert_average(lq):
+    E, hidden, inter, ntok = 4, 256, 512, 3
+    _, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=1)
+    R = np.zeros((E, hidden), np.float32)
+    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X, 2)
+    assert (idx == [[0, 1]] * ntok).all() and (w == 0.5).all()
+    lg = np.zeros((ntok, E))
+    chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X, lg, np.zeros((ntok, E)), idx, NTH)
+    assert_within(Y, chk["Y"], chk["bound"], "uniform router")
+
+
+def test_moe_one_hot_router_is_single_expert(lq):
+    E, hidden, inter, ntok = 4, 256, 512, 2
+    _, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=2)
+    R = np.zeros((E, hidden), np.float32)
+    R[3] = 100.0 * np.sign(X[0]) / hidden               # token 0 strongly prefers expert 3
+    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X[:1], 1)
+    assert idx[0, 0] == 3 and w[0, 0] == 1.0
+    f = oracle.ffn_gate_up(Q4_K, W1[3], W3[3], inter, hidden, X[:1], oracle.ACT_SWIGLU, NTH)
+    D2 = oracle.dequant(Q4_K, W2[3], hidden, inter).astype(np.float64)
+    ref = f["h"] @ D2.T
+    _, _, lg, labs = oracle.moe_route(R, X[:1], 1)
+    chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X[:1], lg, labs, idx, NTH)
+    assert np.allclose(chk["Y"], ref, rtol=1e-12, atol=1e-12)
+    assert_within(Y, ref, chk["bound"], "one-hot router")
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_reports(lq):
+    """a wait on a barrier nothing completes runs out after its limit; the
+    kernel records it and exits, the context stays usable."""
+    status_clean(lq)
+    lq.lq_probe_timeout(2_000_000)          # 2 ms
+    rc, bits = lq.lq_device_status()
+    assert rc == lq.LQ_ETIMEOUT and bits & 1
+    rc, bits = lq.lq_device_status()        # cleared by the read
+    assert rc == 0 and bits == 0
+    # the context still works
+    W = synth.q4k(synth.rng(3), 8, 256)
+    x = synth.activations(synth.rng(4), 1, 256)
+    y = empty((1, 8))
+    lq.lq_matvec(Q4_K, dev(W), 8, 256, dev(x), y, 1)
+    ref, S = oracle.matvec(Q4_K, W, 8, 256, x)
+    assert_within(host(y), ref, oracle.matvec_bound(S), "after timeout")

@@ -315,3 +315,17 @@ def test_abs_matvec(orc):
     D = np.abs(orc.dequant(Q6_K, W, 5, 512).astype(np.float64))
     v = np.random.default_rng(21).uniform(0, 1, 512)
     assert np.allclose(orc.abs_matvec(Q6_K, W, 5, 512, v), D @ v, rtol=1e-13)
+
+
+def test_moe_weights_of_selection(orc):
+    """weights of a given selection: equal to the router's own when the selection
+    is the router's; renormalised by the selected sum for any other selection."""
+    g_ = synth.rng(22)
+    R = synth.router(g_, 8, 256) * 20
+    X = synth.activations(g_, 6, 256)
+    idx, w, lg, _ = orc.moe_route(R, X, 2)
+    assert np.allclose(orc.moe_weights(lg, idx), w, rtol=1e-15, atol=0)
+    other = np.array([[3, 1]] * 6, dtype=np.int32)
+    wo = orc.moe_weights(lg, other)
+    for t in range(6):
+        assert abs(wo[t, 0] - 1 / (1 + math.exp(lg[t, 1] - lg[t, 3]))) < 1e-14
