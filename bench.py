@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
     ap.add_argument("--layers", type=int, default=NLAYERS)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     return ap.parse_args()
 
 
@@ -348,7 +349,7 @@ def main():
         return
     value = ws * LAYER_BYTES / (ms * 1e-3) / 1e9
     achieved = GATEUP_BYTES / (gate_ms * 1e-3) / 1e9
-    cb = cpu_baseline() if ws == 1 else None
+    cb = cpu_baseline() if (ws == 1 and not args.no_cpu) else None
     line = dict(base, value=value, ms_per_step=ms, us_per_layer=ms * 1e3,
                 frac_of_hbm=value / peak,
                 roofline={"bound": "hbm", "kernel": "ffn gate+up GEGLU (Q4_K 2x10240x2560)",

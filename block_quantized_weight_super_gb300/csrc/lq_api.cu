@@ -1,6 +1,7 @@
 // lq_api.cu -- the C ABI (include/lq.h): argument validation, launch
 // planning and dispatch to the kernels.  Host code only, apart from the
 // device status word.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -64,7 +65,9 @@ int dev_info(DevInfo** out) {
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
         d.status = static_cast<unsigned*>(p);
-        e = stream_set_smem_limit(227 * 1024);
+        e = qmv1_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         d.init = true;
     }
@@ -73,90 +76,85 @@ int dev_info(DevInfo** out) {
 }
 
 // ---------------------------------------------------------------- planning
-struct Plan {
-    int B = 0, k = 0, R = 0, RT = 0, NT = 0, nstages = 0, stage_bytes = 0;
+struct QPlan {
+    int B = 0, R = 0, NC = 0, RT = 0, ipt = 0, nstages = 0, stage_bytes = 0;
     size_t smem = 0;
 };
 
-// Streaming-kernel geometry for batch width B over `cols` with segments of
-// the given formats (their row bytes set the stage size).  False if the
-// kernel cannot take this shape (then the plain-load kernel is used).
-bool plan_stream(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, Plan& p) {
+// Geometry of the quantized matvec kernel for batch width B over `cols`
+// with segments of the given formats.  Consumer threads NC*32 = U*m (U =
+// cols/64 groups per row) so every thread takes the same number of work
+// items (groups of R rows) from every tile of RT = R*m*j rows.  False if the
+// kernel cannot take the shape (then the plain-load kernel is used).
+int fmt_mask(const std::vector<int>& fmts) {
+    int m = 0;
+    for (int f : fmts) m |= f == FMT_Q4_K ? 1 : f == FMT_Q6_K ? 2 : 4;
+    return (m == 5 || m == 6) ? 7 : m;
+}
+
+bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPlan& p) {
     if (cols % 64 != 0 || cols <= 0 || cols > (1 << 20)) return false;
-    const int64_t ngroups = cols / 64;
-    const int64_t U = ngroups * B;
+    const int64_t U = cols / 64;
     if (U > 512) return false;
-    int k = 0;
-    for (int kk = 1; U * kk <= 512; ++kk) {
-        if ((U * kk) % 32) continue;
-        k = kk;
-        if (U * kk >= 256) break;
-    }
-    if (k == 0) return false;
+    const int R = qmv_rows_per_item(B, fmt_mask(fmts));
+    int64_t m = 1;
+    while ((U * m) % 32) m *= 2;
+    while (U * m / 32 < 4 && U * m / 32 * 2 <= 8) m *= 2;
+    const int64_t NC = U * m / 32;
+    if (NC > 8) return false;
     int64_t rbmax = 0;
     for (int f : fmts) rbmax = std::max<int64_t>(rbmax, rowbytes(f, cols));
-    // rows per thread per tile: R*B <= 8, stage <= 48 KB, tile rows even for pairs
-    int R = 0;
-    for (int r = 8 / B; r >= 1; --r) {
-        const int64_t RT = (int64_t)k * r;
+    const int64_t unitrows = R * m;            // rows per tile step
+    int64_t jmax = std::max<int64_t>(1, (32 * 1024) / (unitrows * rbmax));
+    jmax = std::min<int64_t>(jmax, 8);
+    int64_t j = 0;
+    for (int64_t jj = jmax; jj >= 1; --jj) {
+        const int64_t RT = unitrows * jj;
         if (pairs && (RT & 1)) continue;
-        if (RT * rbmax <= 48 * 1024) {
-            // prefer tile sizes whose byte offsets stay 16-aligned for every format
-            bool aligned = true;
-            for (int f : fmts) {
-                const int64_t unit = pairs ? RT / 2 : RT;
-                if ((unit * rowbytes(f, cols)) % 16) aligned = false;
-            }
-            if (aligned || R == 0) R = r;
-            if (aligned) break;
+        bool aligned = true;
+        for (int f : fmts)
+            if (((pairs ? RT / 2 : RT) * rowbytes(f, cols)) % 16) aligned = false;
+        if (j == 0) j = jj;
+        if (aligned) {
+            j = jj;
+            break;
         }
     }
-    if (R == 0) {   // a single tile row set is larger than 48 KB: smallest legal tile
-        R = (pairs && (k & 1)) ? 2 : 1;
-        if ((int64_t)k * R * rbmax > 200 * 1024) return false;
+    if (j == 0) {
+        if (!pairs) return false;
+        j = 2;                                  // odd unitrows: two steps give an even tile
     }
     p.B = B;
-    p.k = k;
     p.R = R;
-    p.RT = k * R;
-    p.NT = (int)(U * k);
+    p.NC = (int)NC;
+    p.ipt = (int)j;
+    p.RT = (int)(unitrows * j);
     p.stage_bytes = (int)(((int64_t)p.RT * rbmax + 15) / 16 * 16 + 16);
-    const size_t red = (size_t)2 * p.RT * B * U * sizeof(float);
-    const size_t budget = 200 * 1024;
-    int S = (int)((budget - red - 64) / p.stage_bytes);
-    if (S > 4) S = 4;
-    if (S < 2) S = 2;
-    p.nstages = S;
-    p.smem = (size_t)S * p.stage_bytes + red + 8 * S;
-    if (p.smem > 227 * 1024) return false;
-    return true;
+    for (int S = 6; S >= 2; --S) {
+        p.nstages = S;
+        p.smem = qmv_smem_bytes(B, (int)U, p.RT, S, p.stage_bytes);
+        if (p.smem <= 110 * 1024) break;
+    }
+    return p.smem <= 227 * 1024;
 }
 
-cudaError_t launch_stream_plan(const StreamParams& P, const Plan& pl, int sms, cudaStream_t st) {
-    int per_sm = 0;
-    cudaError_t e = stream_occupancy(pl.B, pl.NT, pl.smem, &per_sm);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    int grid = sms * per_sm;
-    if (grid > P.ntiles) grid = P.ntiles;
-    if (grid < 1) grid = 1;
-    return stream_launch(pl.B, P, grid, pl.NT, pl.smem, st);
-}
-
-// Run the segments (all sharing cols and the batch width B) with the
-// streaming kernel when it can take the shape, else the plain-load kernel.
+// Run the segments (all sharing cols and the batch width B): the quantized
+// matvec kernel when it can take the shape, else the plain-load kernel.
 int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
+    // formats in order of first appearance (at most two per launch)
     std::vector<int> fmts;
     bool pairs = false;
     for (auto& s : segs) {
-        fmts.push_back(s.fmt);
+        if (std::find(fmts.begin(), fmts.end(), s.fmt) == fmts.end()) fmts.push_back(s.fmt);
         pairs = pairs || s.mode != MODE_PLAIN;
     }
-    Plan pl;
-    if (!plan_stream(B, cols, fmts, pairs, pl)) {
+    bool xal = true;                // the kernel stages x with 16-byte loads
+    for (auto& s : segs) xal = xal && al(s.x, 16);
+    QPlan pl;
+    if (fmts.size() > 2 || !xal || !plan_qmv(B, cols, fmts, pairs, pl)) {
         for (auto& s : segs) {
             if (s.nout <= 0) continue;
             cudaError_t e = launch_direct(s, cols, B, st);
@@ -164,41 +162,72 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         }
         return LQ_OK;
     }
-    for (size_t s0 = 0; s0 < segs.size(); s0 += MAX_SEG) {
-        StreamParams P;
+    // format group 0 segments first, then group 1
+    std::vector<Seg> order;
+    for (int f : fmts)
+        for (auto& s : segs)
+            if (s.fmt == f && s.nout > 0) order.push_back(s);
+    const int nt = (pl.NC + 1) * 32;
+    const int mask = fmt_mask(fmts);
+    int per_sm = 0;
+    cudaError_t e = B == 1 ? qmv1_occupancy(mask, nt, pl.smem, &per_sm)
+                  : B == 2 ? qmv2_occupancy(mask, nt, pl.smem, &per_sm)
+                           : qmv4_occupancy(mask, nt, pl.smem, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy");
+    if (per_sm < 1) per_sm = 1;
+    for (size_t s0 = 0; s0 < order.size(); s0 += MAX_SEG) {
+        QmvParams P;
         memset(&P, 0, sizeof P);
-        int t = 0, n = 0;
-        for (size_t i = s0; i < segs.size() && i < s0 + MAX_SEG; ++i) {
-            Seg s = segs[i];
-            if (s.nout <= 0) continue;
+        int t = 0, n = 0, t0 = -1;
+        P.fmt0 = P.fmt1 = order[s0].fmt;
+        for (size_t i = s0; i < order.size() && i < s0 + MAX_SEG; ++i) {
+            Seg s = order[i];
+            if (s.fmt != P.fmt0 && t0 < 0) {
+                t0 = t;
+                P.fmt1 = s.fmt;
+            }
             const int opt = s.mode == MODE_PLAIN ? pl.RT : pl.RT / 2;
             s.tile0 = t;
             s.ntiles = (s.nout + opt - 1) / opt;
             t += s.ntiles;
             P.seg[n++] = s;
         }
-        if (n == 0) continue;
         P.nseg = n;
         P.ntiles = t;
         P.cols = (int32_t)cols;
-        P.ngroups = (int32_t)(cols / 64);
+        P.U = (int32_t)(cols / 64);
         P.RT = pl.RT;
-        P.k = pl.k;
+        P.R = pl.R;
+        P.ipt = pl.ipt;
         P.nstages = pl.nstages;
         P.stage_bytes = pl.stage_bytes;
         P.timeout_ns = g_timeout_ns.load();
         P.status = dev->status;
-        cudaError_t e = launch_stream_plan(P, pl, dev->sms, st);
-        if (e != cudaSuccess) return cuda_fail(e, "stream matvec launch");
+        int grid = std::min(dev->sms * per_sm, t);
+        if (t0 < 0) {
+            P.tile_split = t;
+            P.cta_split = grid;
+        } else {
+            if (grid < 2) grid = 2;
+            P.tile_split = t0;
+            int g0 = (int)((int64_t)grid * t0 / t);
+            g0 = std::max(1, std::min(grid - 1, g0));
+            P.cta_split = g0;
+        }
+        e = B == 1 ? qmv1_launch(mask, P, grid, nt, pl.smem, st)
+          : B == 2 ? qmv2_launch(mask, P, grid, nt, pl.smem, st)
+                   : qmv4_launch(mask, P, grid, nt, pl.smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "qmv launch");
     }
     return LQ_OK;
 }
 
-// Widest batch width the streaming kernel takes for these columns (4, 2, 1).
-int batch_width(int64_t cols, int batch) {
-    const int64_t ng = cols / 64;
+// Widest batch width (4, 2 or 1) the quantized matvec kernel can plan for
+// these columns and formats (x for B rows must fit in shared memory).
+int batch_width(int64_t cols, int batch, const std::vector<int>& fmts, bool pairs) {
     int B = batch >= 3 ? 4 : batch;
-    while (B > 1 && (cols % 64 != 0 || ng * B > 512)) B /= 2;
+    QPlan pl;
+    while (B > 1 && !plan_qmv(B, cols, fmts, pairs, pl)) B /= 2;
     return B;
 }
 
@@ -287,7 +316,7 @@ int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
     if (rows == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
-    const int B = batch_width(cols, batch);
+    const int B = batch_width(cols, batch, {fmt}, false);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B)
         segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(B, batch - b0)));
@@ -308,7 +337,7 @@ int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int
     if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
         (nv && (rc = check_f32(v, "v"))))
         return rc;
-    const int B = batch_width(cols, batch);
+    const int B = batch_width(cols, batch, {fq, fk, fv}, false);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B) {
         const int nb = std::min(B, batch - b0);
@@ -343,7 +372,7 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
     if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
     if (inter == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
-    const int B = batch_width(cols, batch);
+    const int B = batch_width(cols, batch, {fmt}, true);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B) {
         Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(B, batch - b0));
@@ -410,7 +439,7 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
 
     // grouped expert gate+up (+SwiGLU): segment per (expert, chunk of B rows)
     {
-        const int B = batch_width(hidden, ntok);
+        const int B = batch_width(hidden, ntok, {fmt}, true);
         std::vector<Seg> segs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {
@@ -435,7 +464,7 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
     }
     // grouped expert down: x rows are the grouped hidden activations
     {
-        const int B = batch_width(inter, ntok);
+        const int B = batch_width(inter, ntok, {fmt}, false);
         std::vector<Seg> segs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {

@@ -3,7 +3,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "lq_stream.cuh"
+#include "lq_qmv.cuh"
 
 namespace lq {
 
@@ -19,11 +19,16 @@ struct MoeWs {
     float* ybuf;         // [ntok*topk][hidden] expert outputs
 };
 
-// streaming matvec kernel (lq_stream.cu), batch width B in {1, 2, 4}
-cudaError_t stream_set_smem_limit(int bytes);
-cudaError_t stream_occupancy(int B, int nt, size_t smem, int* per_sm);
-cudaError_t stream_launch(int B, const StreamParams& P, int grid, int nt, size_t smem,
-                          cudaStream_t st);
+// quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
+cudaError_t qmv1_set_smem(int bytes);
+cudaError_t qmv2_set_smem(int bytes);
+cudaError_t qmv4_set_smem(int bytes);
+cudaError_t qmv1_occupancy(int mask, int nt, size_t smem, int* per_sm);
+cudaError_t qmv2_occupancy(int mask, int nt, size_t smem, int* per_sm);
+cudaError_t qmv4_occupancy(int mask, int nt, size_t smem, int* per_sm);
+cudaError_t qmv1_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
+cudaError_t qmv2_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
+cudaError_t qmv4_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 
 cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,
                            cudaStream_t st);

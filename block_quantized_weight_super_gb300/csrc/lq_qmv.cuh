@@ -1,0 +1,46 @@
+// lq_qmv.cuh -- parameters of the quantized matvec kernel (lq_qmv.cu),
+// shared with the host launcher.
+#pragma once
+#include <cstdint>
+
+#include "lq_stream.cuh"
+
+namespace lq {
+
+constexpr int XS_STRIDE = 68;   // floats per 64-value x group slot in shared memory
+
+struct QmvParams {
+    Seg seg[MAX_SEG];
+    int32_t nseg;
+    int32_t ntiles;          // total tiles (format group 0 first)
+    int32_t cols;
+    int32_t U;               // groups of 64 weights per row
+    int32_t RT;              // matrix rows per tile
+    int32_t R;               // rows per work item (interleaved in a thread)
+    int32_t ipt;             // work items per thread per tile
+    int32_t nstages;
+    int32_t stage_bytes;
+    int32_t fmt0, fmt1;      // formats of CTA groups 0 and 1
+    int32_t cta_split;       // CTAs [0, cta_split) run format group 0
+    int32_t tile_split;      // tiles [0, tile_split) belong to format group 0
+    uint64_t timeout_ns;
+    unsigned* status;
+};
+
+// Rows of W per work item for batch width B and block-format mask (bit 0
+// Q4_K, bit 1 Q6_K, bit 2 Q8_0): as many as the registers allow.
+__host__ __device__ constexpr int qmv_rows_per_item(int B, int mask) {
+    return (void)mask, B == 1 ? 2 : 1;
+}
+
+__host__ __device__ inline size_t qmv_smem_bytes(int B, int U, int RT, int nstages, int stage_bytes) {
+    size_t off = (size_t)nstages * stage_bytes;
+    off += (size_t)B * U * XS_STRIDE * sizeof(float);
+    off += (size_t)B * U * 2 * sizeof(float);
+    off += (size_t)(nstages + 1) * RT * B * U * sizeof(float);
+    off = (off + 7) & ~size_t(7);
+    off += (size_t)2 * nstages * sizeof(uint64_t) + (size_t)(nstages + 2) * sizeof(int);
+    return off;
+}
+
+}  // namespace lq

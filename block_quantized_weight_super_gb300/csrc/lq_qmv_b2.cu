@@ -1,0 +1,14 @@
+// lq_qmv_b2.cu -- instantiations of the quantized matvec kernel for 2 x row(s).
+#include "lq_qmv_impl.cuh"
+
+namespace lq {
+
+cudaError_t qmv2_set_smem(int bytes) { return QmvTable<2>::set_smem(bytes); }
+cudaError_t qmv2_occupancy(int mask, int nt, size_t smem, int* per_sm) {
+    return QmvTable<2>::occupancy(mask, nt, smem, per_sm);
+}
+cudaError_t qmv2_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st) {
+    return QmvTable<2>::launch(mask, P, grid, nt, smem, st);
+}
+
+}  // namespace lq

@@ -1,0 +1,14 @@
+// lq_qmv_b4.cu -- instantiations of the quantized matvec kernel for 4 x row(s).
+#include "lq_qmv_impl.cuh"
+
+namespace lq {
+
+cudaError_t qmv4_set_smem(int bytes) { return QmvTable<4>::set_smem(bytes); }
+cudaError_t qmv4_occupancy(int mask, int nt, size_t smem, int* per_sm) {
+    return QmvTable<4>::occupancy(mask, nt, smem, per_sm);
+}
+cudaError_t qmv4_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st) {
+    return QmvTable<4>::launch(mask, P, grid, nt, smem, st);
+}
+
+}  // namespace lq

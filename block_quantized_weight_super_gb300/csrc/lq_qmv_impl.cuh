@@ -1,0 +1,724 @@
+#pragma once
+// lq_qmv_impl.cuh -- the quantized matvec kernel (batch 1, 2 or 4 rows of x).
+//
+// y = W.x for Q4_K / Q6_K / Q8_0 weight rows (larql "Architecture -> Metal
+// shader map", Gemma 3 table: q4k_matvec, q6k_matvec, q4k_q6k_qkv_proj,
+// q4k_ffn_gate_up + geglu; dotLLM PR #320: matmul_q8_0 GEMV), over a list of
+// segments (several matrices sharing x in one launch; gate/up row pairs with
+// the activation fused before the store; MoE experts with gathered rows).
+//
+// GB300 structure:
+//  * warp NC (the producer) streams row tiles of W into a ring of shared-
+//    memory stages with 1-D bulk copies (TMA) on "full" mbarriers and reuses
+//    a stage once its "empty" mbarrier says the consumers are done with it;
+//  * warps 0..NC-1 (consumers) never synchronise with each other per tile:
+//    each processes a fixed share of work items of every tile (an item = one
+//    64-weight group of R consecutive rows, dequantized once and multiplied
+//    with B x rows read from shared memory), writes per-group partials, and
+//    the warp that finishes a tile last (shared counter) releases the stage
+//    and sums that tile's partials in a fixed order into y;
+//  * x for the current matrix is staged in shared memory (64-float group
+//    slots padded to 68 floats so a warp's 16-byte reads hit distinct banks),
+//    with per-sub-block sums of x for the Q4_K re-centred form;
+//  * a CTA runs one block format (template), so the hot loop has no format
+//    branch; mixed-format launches split the grid into two CTA groups;
+//  * every wait is bounded by %globaltimer; on expiry the CTA records
+//    STATUS_TIMEOUT, stops waiting, drains its copies (bounded) and exits.
+// Results do not depend on B (each (row, x row) dot product is computed by
+// the same instruction sequence) and are deterministic.
+#include "lq_group.cuh"
+#include "lq_internal.h"
+#include "lq_qmv.cuh"
+
+namespace lq {
+namespace {
+
+// ---------------------------------------------------------------- tiles
+
+__device__ __forceinline__ int qseg_of(const QmvParams& P, int t, int hint) {
+    int s = hint;
+    while (s + 1 < P.nseg && t >= P.seg[s + 1].tile0) ++s;
+    while (s > 0 && t < P.seg[s].tile0) --s;
+    return s;
+}
+
+__device__ __forceinline__ int qseg_nval(const Seg& S, int B) {
+    int n = S.bcnt ? (*S.bcnt - S.b0) : S.nbatch;
+    return n < 0 ? 0 : (n > B ? B : n);
+}
+
+__device__ __forceinline__ int qseg_boff(const Seg& S) { return (S.boff ? *S.boff : 0) + S.b0; }
+
+__device__ __forceinline__ int64_t qrow_bytes(int fmt, int cols) {
+    return (int64_t)(cols / block_elems_of(fmt)) * block_bytes_of(fmt);
+}
+
+struct QTile {
+    const uint8_t* src1;
+    const uint8_t* src2;
+    uint32_t bytes1, bytes2, dst2;
+    int n_o, o0;
+    bool tma;
+};
+
+__device__ __forceinline__ QTile qtile(const QmvParams& P, const Seg& S, int t) {
+    QTile g;
+    const int64_t rb = qrow_bytes(S.fmt, P.cols);
+    const int lt = t - S.tile0;
+    const int opt = S.mode == MODE_PLAIN ? P.RT : P.RT / 2;
+    g.o0 = lt * opt;
+    g.n_o = min(opt, S.nout - g.o0);
+    g.src2 = nullptr;
+    g.bytes2 = 0;
+    g.dst2 = 0;
+    if (S.mode == MODE_PLAIN) {
+        g.src1 = S.w + (int64_t)g.o0 * rb;
+        g.bytes1 = (uint32_t)(g.n_o * rb);
+    } else if (S.mode == MODE_PAIR_INTERLEAVED) {
+        g.src1 = S.w + (int64_t)g.o0 * 2 * rb;
+        g.bytes1 = (uint32_t)(2 * g.n_o * rb);
+    } else {
+        g.src1 = S.w + (int64_t)g.o0 * rb;
+        g.bytes1 = (uint32_t)(g.n_o * rb);
+        g.src2 = S.w2 + (int64_t)g.o0 * rb;
+        g.bytes2 = g.bytes1;
+        g.dst2 = (uint32_t)((P.RT / 2) * rb);
+    }
+    g.tma = ((reinterpret_cast<uintptr_t>(g.src1) | g.bytes1) & 15u) == 0;
+    if (S.mode == MODE_PAIR_TWO)
+        g.tma = g.tma && ((reinterpret_cast<uintptr_t>(g.src2) | g.bytes2 | g.dst2) & 15u) == 0;
+    return g;
+}
+
+// This CTA's tile walk: t = t0, t0 + step, ... < t_end over tiles of active
+// segments (segments whose device-side row count is zero are skipped).
+struct Walk {
+    int t, step, end, hint;
+};
+
+template <int B>
+__device__ __forceinline__ void walk_fix(const QmvParams& P, Walk& w) {
+    while (w.t < w.end) {
+        w.hint = qseg_of(P, w.t, w.hint);
+        if (qseg_nval(P.seg[w.hint], B) > 0) return;
+        w.t += w.step;
+    }
+}
+
+// 32 lanes copy n bytes global -> shared with plain loads (2-byte aligned)
+__device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, uint32_t n, int lane) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    if ((a & 3u) == 0 && (n & 3u) == 0) {
+        const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
+        uint32_t* d = reinterpret_cast<uint32_t*>(dst);
+        for (uint32_t i = lane; i < n / 4; i += 32) d[i] = __ldg(s + i);
+    } else {
+        const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+        uint16_t* d = reinterpret_cast<uint16_t*>(dst);
+        for (uint32_t i = lane; i < n / 2; i += 32) d[i] = __ldg(s + i);
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync(int nct) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nct) : "memory");
+}
+
+__device__ __forceinline__ float4 lds_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ __forceinline__ float act_q(int act, float g) {
+    if (act == ACT_GEGLU_TANH) {
+        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
+        return g / (1.0f + expf(-2.0f * z));
+    }
+    return g / (1.0f + expf(-g));
+}
+
+// ---------------------------------------------------------------- x staging
+
+// column of x value i (0..63) of group G in the format's group order
+template <int FMT>
+__device__ __forceinline__ int qxcol(int G, int i) {
+    if (FMT == FMT_Q6_K) {
+        const int blk = G >> 2, gm = G & 3, h = gm >> 1, l0 = 16 * (gm & 1);
+        return 256 * blk + 128 * h + 32 * (i >> 4) + l0 + (i & 15);
+    }
+    return 64 * G + i;
+}
+
+// Stage the B x rows of segment S into xs[(b*U + G)*68 + i] (Q4_K: high
+// columns pre-scaled by 1/16) and, for Q4_K, sxs[(b*U + G)*2 + {0,1}] = sums
+// of the low / high 32 columns (fixed sequential order).  A work unit is 16
+// consecutive columns (one 64-byte run of x) loaded as four independent
+// float4 (x rows are 16-byte aligned: the host checks).  Ends with the
+// consumer barrier; the caller brackets it with one before.
+template <int FMT, int B>
+__device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs, int ct, int nct) {
+    const int U = P.U;
+    const int nval = qseg_nval(S, B);
+    const int boff = qseg_boff(S);
+    const int units = B * U * 4;
+    for (int e = ct; e < units; e += nct) {
+        const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
+        float4 v[4];
+        if (b < nval) {
+            const int rho = boff + b;
+            const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * P.cols;
+            const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (FMT == FMT_Q4_K && q >= 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[k].x *= 0.0625f;
+                v[k].y *= 0.0625f;
+                v[k].z *= 0.0625f;
+                v[k].w *= 0.0625f;
+            }
+        }
+        float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = v[k];
+    }
+    consumer_sync(nct);
+    if (FMT == FMT_Q4_K) {
+        for (int e = ct; e < B * U * 2; e += nct) {
+            const int b = e / (U * 2), G = (e % (U * 2)) >> 1, hi = e & 1;
+            const float* xg = xs + (b * U + G) * XS_STRIDE + 32 * hi;
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s += xg[i];
+            sxs[(b * U + G) * 2 + hi] = hi ? s * 16.0f : s;     // exact: power-of-two scale
+        }
+        consumer_sync(nct);
+    }
+}
+
+// ---------------------------------------------------------------- items
+
+struct Q4Row {
+    float c0, c1, dsc0, dsc1, e0, e1;
+};
+
+// Scales of quant group g of a Q4_K super-block (see lq_group.cuh) and the
+// re-centring constants of its two sub-blocks.
+__device__ __forceinline__ Q4Row q4k_row(const uint4 hdr, const Q4Sel& sl, const GroupConsts& K) {
+    const uint32_t s_sc = sl.hi ? hdr.w : hdr.y;
+    const uint32_t s_m = sl.hi ? (hdr.w >> 4) : hdr.z;
+    const uint32_t scw = ((s_sc >> sl.sh) & sl.mlo) | ((hdr.y >> (sl.sh + 2)) & sl.mhi);
+    const uint32_t mw = ((s_m >> sl.sh) & sl.mlo) | ((hdr.z >> (sl.sh + 2)) & sl.mhi);
+    const uint32_t sc_h = hsub2_u32(__byte_perm(scw, K.magic, 0x7150), K.magic);
+    const uint32_t m_h = hsub2_u32(__byte_perm(mw, K.magic, 0x7150), K.magic);
+    Q4Row q;
+    q.dsc0 = hmul_lo_lo(hdr.x, sc_h, 0.0f);
+    q.dsc1 = hmul_lo_hi(hdr.x, sc_h, 0.0f);
+    const float dm0 = hmul_hi_lo(hdr.x, m_h, 0.0f);
+    const float dm1 = hmul_hi_hi(hdr.x, m_h, 0.0f);
+    const float qb0 = rintf(fminf(fmaxf(dm0 * rcp_approx(q.dsc0), -16.0f), 15.0f));
+    const float qb1 = rintf(fminf(fmaxf(dm1 * rcp_approx(q.dsc1), -16.0f), 15.0f));
+    q.e0 = fmaf(q.dsc0, qb0, -dm0);
+    q.e1 = fmaf(q.dsc1, qb1, -dm1);
+    q.c0 = -1024.0f - qb0;
+    q.c1 = fmaf(qb1, -16.0f, -1024.0f);
+    return q;
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One Q4_K item: group G of rows rp[0..R-1], B x rows.  part[r][b].
+template <int B, int R>
+__device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, const float* xs,
+                                         const float* sxs, int U, const Q4Sel& sl,
+                                         const GroupConsts& K, float (&part)[R][B]) {
+    const int boff = 144 * (G >> 2);
+    const int qoff = boff + 16 + 32 * (G & 3);
+    Q4Row rc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) rc[r] = q4k_row(*reinterpret_cast<const uint4*>(rp[r] + boff), sl, K);
+    float a[R][B][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a[r][b][k] = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        uint4 q[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) q[r] = *reinterpret_cast<const uint4*>(rp[r] + qoff + 16 * hf);
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) {
+            const int w = 4 * hf + ww;
+            float4 xl[B], xh[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const float* xg = xs + (b * U + G) * XS_STRIDE;
+                xl[b] = lds_f4(xg + 4 * w);
+                xh[b] = lds_f4(xg + 32 + 4 * w);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t W = comp(q[r], ww), W8 = W >> 8;
+                const uint32_t h0 = lop_and_or(W, K.m4lo, K.magic);
+                const uint32_t h1 = lop_and_or(W, K.m4hi, K.magic);
+                const uint32_t h2 = lop_and_or(W8, K.m4lo, K.magic);
+                const uint32_t h3 = lop_and_or(W8, K.m4hi, K.magic);
+                const float v0 = h2f_lo(h0, rc[r].c0), v2 = h2f_hi(h0, rc[r].c0);
+                const float v1 = h2f_lo(h2, rc[r].c0), v3 = h2f_hi(h2, rc[r].c0);
+                const float u0 = h2f_lo(h1, rc[r].c1), u2 = h2f_hi(h1, rc[r].c1);
+                const float u1 = h2f_lo(h3, rc[r].c1), u3 = h2f_hi(h3, rc[r].c1);
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    a[r][b][0] = fmaf(v0, xl[b].x, a[r][b][0]);
+                    a[r][b][1] = fmaf(v2, xl[b].z, a[r][b][1]);
+                    a[r][b][2] = fmaf(v1, xl[b].y, a[r][b][2]);
+                    a[r][b][3] = fmaf(v3, xl[b].w, a[r][b][3]);
+                    a[r][b][4] = fmaf(u0, xh[b].x, a[r][b][4]);
+                    a[r][b][5] = fmaf(u2, xh[b].z, a[r][b][5]);
+                    a[r][b][6] = fmaf(u1, xh[b].y, a[r][b][6]);
+                    a[r][b][7] = fmaf(u3, xh[b].w, a[r][b][7]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        const float sxl = sxs[(b * U + G) * 2], sxh = sxs[(b * U + G) * 2 + 1];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float A = (a[r][b][0] + a[r][b][1]) + (a[r][b][2] + a[r][b][3]);
+            const float Bs = (a[r][b][4] + a[r][b][5]) + (a[r][b][6] + a[r][b][7]);
+            part[r][b] = fmaf(rc[r].dsc0, A, fmaf(rc[r].e0, sxl, fmaf(rc[r].dsc1, Bs, rc[r].e1 * sxh)));
+        }
+    }
+}
+
+// One Q6_K item (group = half h, column run l0, four quarters).
+template <int B, int R>
+__device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, const float* xs,
+                                         int U, const GroupConsts& K, float (&part)[R][B]) {
+    const int gm = G & 3, h = gm >> 1, l0 = 16 * (gm & 1);
+    const int boff = 210 * (G >> 2);
+    const uint32_t o = (uint32_t)(l0 >> 4);
+    const uint32_t sel = 0x7050u | ((2u + o) << 8) | o;
+    float ds[R][4];
+    uint32_t A[R][4], Bw[R][4], H[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint8_t* bp = rp[r] + boff;
+        lds_words_any2<4>(bp + 64 * h + l0, A[r]);
+        lds_words_any2<4>(bp + 64 * h + 32 + l0, Bw[r]);
+        lds_words_any2<4>(bp + 128 + 32 * h + l0, H[r]);
+        uint32_t scw[2];
+        lds_words_any2<2>(bp + 192 + 8 * h, scw);
+        const uint32_t dw = lds_u32_any2(bp + 208);
+        const uint32_t s01 = hsub2_u32(__byte_perm(scw[0], K.magic, sel) ^ 0x00800080u, 0x64806480u);
+        const uint32_t s23 = hsub2_u32(__byte_perm(scw[1], K.magic, sel) ^ 0x00800080u, 0x64806480u);
+        ds[r][0] = hmul_lo_lo(dw, s01, 0.0f);
+        ds[r][1] = hmul_lo_hi(dw, s01, 0.0f);
+        ds[r][2] = hmul_lo_lo(dw, s23, 0.0f);
+        ds[r][3] = hmul_lo_hi(dw, s23, 0.0f);
+    }
+    float a[R][B][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[r][b][q] = 0.f;
+    const float cq = -1056.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float4 xq[B][4];
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xq[b][q] = lds_f4(xs + (b * U + G) * XS_STRIDE + 16 * q + 4 * w);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t c[4] = {(A[r][w] & 0x0F0F0F0Fu) | ((H[r][w] << 4) & 0x30303030u),
+                                   (Bw[r][w] & 0x0F0F0F0Fu) | ((H[r][w] << 2) & 0x30303030u),
+                                   ((A[r][w] >> 4) & 0x0F0F0F0Fu) | (H[r][w] & 0x30303030u),
+                                   ((Bw[r][w] >> 4) & 0x0F0F0F0Fu) | ((H[r][w] >> 2) & 0x30303030u)};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t hA = lop_and_or(c[q], K.m6, K.magic);
+                const uint32_t hB = lop_and_or(c[q] >> 8, K.m6, K.magic);
+                const float v0 = h2f_lo(hA, cq), v1 = h2f_lo(hB, cq);
+                const float v2 = h2f_hi(hA, cq), v3 = h2f_hi(hB, cq);
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    float t = a[r][b][q];
+                    t = fmaf(v0, xq[b][q].x, t);
+                    t = fmaf(v1, xq[b][q].y, t);
+                    t = fmaf(v2, xq[b][q].z, t);
+                    t = fmaf(v3, xq[b][q].w, t);
+                    a[r][b][q] = t;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+            part[r][b] = fmaf(ds[r][0], a[r][b][0],
+                              fmaf(ds[r][1], a[r][b][1], fmaf(ds[r][2], a[r][b][2], ds[r][3] * a[r][b][3])));
+}
+
+// One Q8_0 item (group = two 34-byte blocks, 4-byte aligned in the stage).
+template <int B, int R>
+__device__ __forceinline__ void q80_item(const uint8_t* const (&rp)[R], int G, const float* xs,
+                                         int U, const GroupConsts& K, float (&part)[R][B]) {
+    const float cq = -1152.0f;
+    float a[R][B][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) a[r][b][k] = 0.f;
+    float d[R][2];
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t wv[R][9];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(rp[r] + 68 * G) + 8 * blk;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) wv[r][i] = q[i];
+            d[r][blk] = blk == 0 ? h2f_lo(wv[r][0], 0.0f) : h2f_hi(wv[r][0], 0.0f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 xv[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) xv[b] = lds_f4(xs + (b * U + G) * XS_STRIDE + 32 * blk + 4 * i);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t Q = blk == 0 ? __funnelshift_r(wv[r][i], wv[r][i + 1], 16) : wv[r][i + 1];
+                const uint32_t hA = lop_and_xor(Q, K.m8, K.x8);
+                const uint32_t hB = lop_and_xor(Q >> 8, K.m8, K.x8);
+                const float v0 = h2f_lo(hA, cq), v1 = h2f_lo(hB, cq);
+                const float v2 = h2f_hi(hA, cq), v3 = h2f_hi(hB, cq);
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    a[r][b][2 * blk] = fmaf(v0, xv[b].x, a[r][b][2 * blk]);
+                    a[r][b][2 * blk + 1] = fmaf(v1, xv[b].y, a[r][b][2 * blk + 1]);
+                    a[r][b][2 * blk] = fmaf(v2, xv[b].z, a[r][b][2 * blk]);
+                    a[r][b][2 * blk + 1] = fmaf(v3, xv[b].w, a[r][b][2 * blk + 1]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+            part[r][b] = fmaf(d[r][0], a[r][b][0] + a[r][b][1], d[r][1] * (a[r][b][2] + a[r][b][3]));
+}
+
+template <int FMT, int B, int R>
+__device__ __forceinline__ void run_item(const uint8_t* const (&rp)[R], int G, const float* xs,
+                                         const float* sxs, int U, const Q4Sel& sl,
+                                         const GroupConsts& K, float (&part)[R][B]) {
+    if (FMT == FMT_Q4_K) q4k_item<B, R>(rp, G, xs, sxs, U, sl, K, part);
+    else if (FMT == FMT_Q6_K) q6k_item<B, R>(rp, G, xs, U, K, part);
+    else q80_item<B, R>(rp, G, xs, U, K, part);
+}
+
+// ---------------------------------------------------------------- the CTA
+
+struct Smem {
+    uint8_t* stages;
+    float* xs;
+    float* sxs;
+    float* red;
+    uint64_t* full;
+    uint64_t* empty;
+    int* cnt;
+    int* abort_flag;
+};
+
+template <int FMT, int B, int R>
+__device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm, Walk walk0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NC = (blockDim.x >> 5) - 1;          // consumer warps
+    const int NCT = NC * 32;
+    const int S_ = P.nstages;
+    const int NRED = S_ + 1;
+    const int U = P.U;
+    const int red_tile = P.RT * B * U;
+
+    if (warp == NC) {
+        // ------------------------------------------------ producer warp
+        uint64_t policy = policy_evict_first();
+        Walk w = walk0;
+        walk_fix<B>(P, w);
+        uint32_t ephase = 0;
+        int last_use[8];                  // last bulk-copied use of each stage (-1: none)
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
+        int n = 0;
+        bool ok = true;
+        for (; w.t < w.end; ++n) {
+            if (*reinterpret_cast<volatile int*>(sm.abort_flag)) break;
+            const int s = n % S_;
+            if (n >= S_) {            // wait until the consumers released stage s
+                if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                ephase ^= 1u << s;
+                if (!ok) break;
+            }
+            const Seg& S = P.seg[w.hint];
+            const QTile g = qtile(P, S, w.t);
+            uint8_t* dst = sm.stages + (size_t)s * P.stage_bytes;
+            if (g.tma) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sm.full[s], g.bytes1 + g.bytes2);
+                    bulk_g2s_stream(dst, g.src1, g.bytes1, &sm.full[s], policy);
+                    if (g.bytes2) bulk_g2s_stream(dst + g.dst2, g.src2, g.bytes2, &sm.full[s], policy);
+                }
+                last_use[s] = n / S_;
+            } else {
+                warp_copy(dst, g.src1, g.bytes1, lane);
+                if (g.bytes2) warp_copy(dst + g.dst2, g.src2, g.bytes2, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.full[s]);
+            }
+            w.t += w.step;
+            walk_fix<B>(P, w);
+        }
+        if (!ok && lane == 0) {
+            record_status(P.status, STATUS_TIMEOUT);
+            atomicExch(sm.abort_flag, 1);
+        }
+        // never leave a bulk copy in flight: wait (bounded) for the last
+        // copy into each stage (already complete unless the CTA aborted)
+        if (lane == 0) {
+            for (int s2 = 0; s2 < S_; ++s2)
+                if (last_use[s2] >= 0)
+                    mbar_wait_bounded(&sm.full[s2], (uint32_t)last_use[s2] & 1u, P.timeout_ns);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    Walk w = walk0;
+    walk_fix<B>(P, w);
+    int cur_seg = -1;
+    uint32_t fphase = 0;
+    bool aborted = false;
+    for (int n = 0; w.t < w.end; ++n) {
+        const int s = n % S_;
+        const Seg& S = P.seg[w.hint];
+        if (w.hint != cur_seg) {
+            consumer_sync(NCT);          // every consumer is done with the previous x
+            stage_x<FMT, B>(P, S, sm.xs, sm.sxs, tid, NCT);
+            cur_seg = w.hint;
+        }
+        const QTile g = qtile(P, S, w.t);
+        if (!aborted) {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_bounded(&sm.full[s], (fphase >> s) & 1u, P.timeout_ns);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok || *reinterpret_cast<volatile int*>(sm.abort_flag)) {
+                aborted = true;
+                if (lane == 0 && !ok) {
+                    record_status(P.status, STATUS_TIMEOUT);
+                    atomicExch(sm.abort_flag, 1);
+                }
+            }
+        }
+        fphase ^= 1u << s;
+        const int64_t rb = qrow_bytes(FMT, P.cols);
+        const uint8_t* st = sm.stages + (size_t)s * P.stage_bytes;
+        float* red = sm.red + (size_t)(n % NRED) * red_tile;
+        const int mode = S.mode;
+        const int half = P.RT / 2;
+        if (!aborted) {
+            for (int q = 0; q < P.ipt; ++q) {
+                const int it = tid + q * NCT;
+                const int G = it % U;
+                const int row0 = (it / U) * R;
+                const uint8_t* rp[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) rp[r] = st + (int64_t)(row0 + r) * rb;
+                float part[R][B];
+                const Q4Sel sel = q4_sel(G & 3);
+                run_item<FMT, B, R>(rp, G, sm.xs, sm.sxs, U, sel, K, part);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int rho = row0 + r;
+                    bool valid;
+                    if (mode == MODE_PLAIN) valid = rho < g.n_o;
+                    else if (mode == MODE_PAIR_INTERLEAVED) valid = rho < 2 * g.n_o;
+                    else valid = (rho % half) < g.n_o;
+#pragma unroll
+                    for (int b = 0; b < B; ++b) red[(rho * B + b) * U + G] = valid ? part[r][b] : 0.f;
+                }
+            }
+        }
+        // last warp to finish this tile releases the stage and reduces
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            // counters only grow: each use of a slot adds NC
+            const int old = atomicAdd(&sm.cnt[n % NRED], 1);
+            last = (old % NC) == NC - 1;
+            if (last) mbar_arrive(&sm.empty[s]);
+        }
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (last && !aborted) {
+            // 4 lanes per output, each summing a fixed quarter of the U group
+            // partials in order, combined as (q0 + q1) + (q2 + q3): the order
+            // depends only on U, so results do not depend on B or the tile.
+            __threadfence_block();
+            const int nval = qseg_nval(S, B);
+            const int boff = qseg_boff(S);
+            float* y = S.y;
+            const int64_t ldy = S.ld_y;
+            const int act = S.act;
+            const int chunk = (U + 3) / 4;
+            const int c = lane & 3;
+            const int g0 = c * chunk, g1 = min(U, g0 + chunk);
+            const int n_out = g.n_o * B;
+            for (int ob = 0; ob < n_out; ob += 8) {
+                const int o = ob + (lane >> 2);
+                const bool live = o < n_out;
+                const int pi = live ? o / B : 0, b = live ? o % B : 0;
+                const int rg = mode == MODE_PAIR_INTERLEAVED ? 2 * pi : pi;
+                float vg = 0.f;
+                const float* rr = red + (rg * B + b) * U;
+                for (int G = g0; G < g1; ++G) vg += rr[G];
+                vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 1);
+                vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 2);
+                float v = vg;
+                if (mode != MODE_PLAIN) {
+                    const int ru = mode == MODE_PAIR_INTERLEAVED ? 2 * pi + 1 : pi + half;
+                    float vu = 0.f;
+                    const float* ru_p = red + (ru * B + b) * U;
+                    for (int G = g0; G < g1; ++G) vu += ru_p[G];
+                    vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 1);
+                    vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 2);
+                    v = act_q(act, vg) * vu;
+                }
+                if (live && c == 0 && b < nval) y[(int64_t)(boff + b) * ldy + g.o0 + pi] = v;
+            }
+        }
+        w.t += w.step;
+        walk_fix<B>(P, w);
+    }
+}
+
+}  // namespace
+
+// Kernel: B x rows, R rows per work item, MASK = block formats compiled in
+// (bit 0 Q4_K, bit 1 Q6_K, bit 2 Q8_0).
+template <int B, int R, int MASK>
+__global__ void __launch_bounds__(288, 2) qmv_kernel(const __grid_constant__ QmvParams P,
+                                                      const GroupConsts K) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S_ = P.nstages;
+    const int U = P.U;
+    Smem sm;
+    size_t off = 0;
+    sm.stages = smem;
+    off += (size_t)S_ * P.stage_bytes;
+    sm.xs = reinterpret_cast<float*>(smem + off);
+    off += (size_t)B * U * XS_STRIDE * sizeof(float);
+    sm.sxs = reinterpret_cast<float*>(smem + off);
+    off += (size_t)B * U * 2 * sizeof(float);
+    sm.red = reinterpret_cast<float*>(smem + off);
+    off += (size_t)(S_ + 1) * P.RT * B * U * sizeof(float);
+    off = (off + 7) & ~size_t(7);
+    sm.full = reinterpret_cast<uint64_t*>(smem + off);
+    sm.empty = sm.full + S_;
+    sm.cnt = reinterpret_cast<int*>(sm.empty + S_);
+    sm.abort_flag = sm.cnt + (S_ + 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S_; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int s = 0; s <= S_; ++s) sm.cnt[s] = 0;
+        *sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool g1 = (int)blockIdx.x >= P.cta_split;
+    Walk w;
+    w.hint = 0;
+    if (!g1) {
+        w.t = blockIdx.x;
+        w.step = P.cta_split;
+        w.end = P.tile_split;
+    } else {
+        w.t = P.tile_split + (blockIdx.x - P.cta_split);
+        w.step = gridDim.x - P.cta_split;
+        w.end = P.ntiles;
+    }
+    const int fmt = g1 ? P.fmt1 : P.fmt0;
+    if ((MASK & 1) && fmt == FMT_Q4_K) qmv_cta<FMT_Q4_K, B, R>(P, K, sm, w);
+    else if ((MASK & 2) && fmt == FMT_Q6_K) qmv_cta<FMT_Q6_K, B, R>(P, K, sm, w);
+    else if ((MASK & 4) && fmt == FMT_Q8_0) qmv_cta<FMT_Q8_0, B, R>(P, K, sm, w);
+}
+
+inline GroupConsts group_consts() {
+    GroupConsts K;
+    K.magic = 0x64006400u;
+    K.m4lo = 0x000F000Fu;
+    K.m4hi = 0x00F000F0u;
+    K.m8 = 0x00FF00FFu;
+    K.x8 = 0x64806480u;
+    K.m6 = 0x003F003Fu;
+    return K;
+}
+
+// Host-side access to the instantiations of one batch width B.
+template <int B>
+struct QmvTable {
+    template <int MASK>
+    static void* fn() {
+        return reinterpret_cast<void*>(qmv_kernel<B, qmv_rows_per_item(B, MASK), MASK>);
+    }
+    static void* get(int mask) {
+        switch (mask) {
+            case 1: return fn<1>();
+            case 2: return fn<2>();
+            case 4: return fn<4>();
+            case 3: return fn<3>();
+            default: return fn<7>();
+        }
+    }
+    static cudaError_t set_smem(int bytes) {
+        const int masks[5] = {1, 2, 4, 3, 7};
+        for (int m : masks) {
+            cudaError_t e = cudaFuncSetAttribute(get(m), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    static cudaError_t occupancy(int mask, int nt, size_t smem, int* per_sm) {
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, get(mask), nt, smem);
+    }
+    static cudaError_t launch(int mask, const QmvParams& P, int grid, int nt, size_t smem,
+                              cudaStream_t st) {
+        const GroupConsts K = group_consts();
+        void* args[2] = {const_cast<QmvParams*>(&P), const_cast<GroupConsts*>(&K)};
+        return cudaLaunchKernel(get(mask), dim3(grid), dim3(nt), args, smem, st);
+    }
+};
+
+}  // namespace lq
