@@ -55,6 +55,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread (up to hint_ns) until
+// the phase completes, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, unsigned parity,
+                                                   unsigned hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier to complete, giving up after
 // timeout_ns of wall time.  Returns false on timeout (the caller records it).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
@@ -62,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }

@@ -40,6 +40,8 @@ __host__ __device__ inline size_t qmv_smem_bytes(int B, int U, int RT, int nstag
     off += (size_t)(nstages + 1) * RT * B * U * sizeof(float);
     off = (off + 7) & ~size_t(7);
     off += (size_t)2 * nstages * sizeof(uint64_t) + (size_t)(nstages + 2) * sizeof(int);
+    off = (off + 15) & ~size_t(15);
+    off += (size_t)MAX_SEG * sizeof(Seg);          // shared copy of the segment table
     return off;
 }
 

@@ -96,11 +96,18 @@ struct Walk {
     int t, step, end, hint;
 };
 
+__device__ __forceinline__ int qseg_of_s(const Seg* segs, int nseg, int t, int hint) {
+    int s = hint;
+    while (s + 1 < nseg && t >= segs[s + 1].tile0) ++s;
+    while (s > 0 && t < segs[s].tile0) --s;
+    return s;
+}
+
 template <int B>
-__device__ __forceinline__ void walk_fix(const QmvParams& P, Walk& w) {
+__device__ __forceinline__ void walk_fix(const Seg* segs, int nseg, Walk& w) {
     while (w.t < w.end) {
-        w.hint = qseg_of(P, w.t, w.hint);
-        if (qseg_nval(P.seg[w.hint], B) > 0) return;
+        w.hint = qseg_of_s(segs, nseg, w.t, w.hint);
+        if (qseg_nval(segs[w.hint], B) > 0) return;
         w.t += w.step;
     }
 }
@@ -440,6 +447,8 @@ __device__ __forceinline__ void run_item(const uint8_t* const (&rp)[R], int G, c
 // ---------------------------------------------------------------- the CTA
 
 struct Smem {
+    const Seg* segs;        // copy of the segment table (parameter reads with a
+                            // dynamic index are slow; shared memory is not)
     uint8_t* stages;
     float* xs;
     float* sxs;
@@ -464,7 +473,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         // ------------------------------------------------ producer warp
         uint64_t policy = policy_evict_first();
         Walk w = walk0;
-        walk_fix<B>(P, w);
+        walk_fix<B>(sm.segs, P.nseg, w);
         uint32_t ephase = 0;
         int last_use[8];                  // last bulk-copied use of each stage (-1: none)
 #pragma unroll
@@ -480,7 +489,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
                 ephase ^= 1u << s;
                 if (!ok) break;
             }
-            const Seg& S = P.seg[w.hint];
+            const Seg& S = sm.segs[w.hint];
             const QTile g = qtile(P, S, w.t);
             uint8_t* dst = sm.stages + (size_t)s * P.stage_bytes;
             if (g.tma) {
@@ -497,7 +506,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
                 if (lane == 0) mbar_arrive(&sm.full[s]);
             }
             w.t += w.step;
-            walk_fix<B>(P, w);
+            walk_fix<B>(sm.segs, P.nseg, w);
         }
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
@@ -515,13 +524,13 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
 
     // ---------------------------------------------------- consumer warps
     Walk w = walk0;
-    walk_fix<B>(P, w);
+    walk_fix<B>(sm.segs, P.nseg, w);
     int cur_seg = -1;
     uint32_t fphase = 0;
     bool aborted = false;
     for (int n = 0; w.t < w.end; ++n) {
         const int s = n % S_;
-        const Seg& S = P.seg[w.hint];
+        const Seg& S = sm.segs[w.hint];
         if (w.hint != cur_seg) {
             consumer_sync(NCT);          // every consumer is done with the previous x
             stage_x<FMT, B>(P, S, sm.xs, sm.sxs, tid, NCT);
@@ -618,7 +627,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             }
         }
         w.t += w.step;
-        walk_fix<B>(P, w);
+        walk_fix<B>(sm.segs, P.nseg, w);
     }
 }
 
@@ -647,6 +656,16 @@ __global__ void __launch_bounds__(288, 2) qmv_kernel(const __grid_constant__ Qmv
     sm.empty = sm.full + S_;
     sm.cnt = reinterpret_cast<int*>(sm.empty + S_);
     sm.abort_flag = sm.cnt + (S_ + 1);
+    size_t seg_off = off + (size_t)2 * S_ * sizeof(uint64_t) + (size_t)(S_ + 2) * sizeof(int);
+    seg_off = (seg_off + 15) & ~size_t(15);                  // as in qmv_smem_bytes
+    Seg* segs = reinterpret_cast<Seg*>(smem + seg_off);
+    {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.seg[0]);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(segs);
+        const int nw = P.nseg * (int)(sizeof(Seg) / 4);
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) dst[i] = src[i];
+    }
+    sm.segs = segs;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_; ++s) {
             mbar_init(&sm.full[s], 1);
