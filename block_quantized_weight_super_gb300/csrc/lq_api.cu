@@ -196,6 +196,9 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         P.ntiles = t;
         P.cols = (int32_t)cols;
         P.U = (int32_t)(cols / 64);
+        P.UP = qmv_red_stride(P.U);
+        for (int i = 0; i < n; ++i)
+            if (P.seg[i].bcnt || P.seg[i].boff) P.dev_counts = 1;
         P.RT = pl.RT;
         P.R = pl.R;
         P.ipt = pl.ipt;

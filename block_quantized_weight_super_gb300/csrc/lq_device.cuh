@@ -109,6 +109,21 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start
+// launching (its blocks are scheduled as resources free up), and wait until
+// the preceding kernel has completed and its writes are visible.  Both are
+// no-ops for a kernel launched without the programmatic-serialization
+// attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Hint: bring `bytes` (multiple of 16) at a 16-byte aligned address into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void record_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }

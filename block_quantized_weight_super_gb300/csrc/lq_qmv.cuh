@@ -15,6 +15,7 @@ struct QmvParams {
     int32_t ntiles;          // total tiles (format group 0 first)
     int32_t cols;
     int32_t U;               // groups of 64 weights per row
+    int32_t UP;              // row stride of the per-group partials (qmv_red_stride)
     int32_t RT;              // matrix rows per tile
     int32_t R;               // rows per work item (interleaved in a thread)
     int32_t ipt;             // work items per thread per tile
@@ -23,6 +24,7 @@ struct QmvParams {
     int32_t fmt0, fmt1;      // formats of CTA groups 0 and 1
     int32_t cta_split;       // CTAs [0, cta_split) run format group 0
     int32_t tile_split;      // tiles [0, tile_split) belong to format group 0
+    int32_t dev_counts;      // some segment reads its row count / offset from device memory
     uint64_t timeout_ns;
     unsigned* status;
 };
@@ -33,11 +35,15 @@ __host__ __device__ constexpr int qmv_rows_per_item(int B, int mask) {
     return (void)mask, B == 1 ? 2 : 1;
 }
 
+// Row stride of the per-group partials: at least U and 8 mod 32, so the
+// reduction's four concurrent rows fall in distinct banks.
+__host__ __device__ constexpr int qmv_red_stride(int U) { return U + (((8 - U) % 32) + 32) % 32; }
+
 __host__ __device__ inline size_t qmv_smem_bytes(int B, int U, int RT, int nstages, int stage_bytes) {
     size_t off = (size_t)nstages * stage_bytes;
     off += (size_t)B * U * XS_STRIDE * sizeof(float);
     off += (size_t)B * U * 2 * sizeof(float);
-    off += (size_t)(nstages + 1) * RT * B * U * sizeof(float);
+    off += (size_t)(nstages + 1) * RT * B * qmv_red_stride(U) * sizeof(float);
     off = (off + 7) & ~size_t(7);
     off += (size_t)2 * nstages * sizeof(uint64_t) + (size_t)(nstages + 2) * sizeof(int);
     off = (off + 15) & ~size_t(15);

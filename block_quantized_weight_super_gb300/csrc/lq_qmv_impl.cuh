@@ -158,10 +158,12 @@ __device__ __forceinline__ int qxcol(int G, int i) {
 
 // Stage the B x rows of segment S into xs[(b*U + G)*68 + i] (Q4_K: high
 // columns pre-scaled by 1/16) and, for Q4_K, sxs[(b*U + G)*2 + {0,1}] = sums
-// of the low / high 32 columns (fixed sequential order).  A work unit is 16
-// consecutive columns (one 64-byte run of x) loaded as four independent
-// float4 (x rows are 16-byte aligned: the host checks).  Ends with the
-// consumer barrier; the caller brackets it with one before.
+// of the low / high 32 columns (fixed sequential order).  Each run of four
+// columns is stored in the order (0, 2, 1, 3) to match the code pairs of the
+// work items.  A work unit is 16 consecutive columns (one 64-byte run of x)
+// loaded as four independent float4 (x rows are 16-byte aligned: the host
+// checks).  Ends with the consumer barrier; the caller brackets it with one
+// before.
 template <int FMT, int B>
 __device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs, int ct, int nct) {
     const int U = P.U;
@@ -181,18 +183,10 @@ __device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs,
 #pragma unroll
             for (int k = 0; k < 4; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (FMT == FMT_Q4_K && q >= 2) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                v[k].x *= 0.0625f;
-                v[k].y *= 0.0625f;
-                v[k].z *= 0.0625f;
-                v[k].w *= 0.0625f;
-            }
-        }
+        const float sc = (FMT == FMT_Q4_K && q >= 2) ? 0.0625f : 1.0f;     // exact
         float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = v[k];
+        for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[k].x * sc, v[k].z * sc, v[k].y * sc, v[k].w * sc);
     }
     consumer_sync(nct);
     if (FMT == FMT_Q4_K) {
@@ -209,6 +203,11 @@ __device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs,
 }
 
 // ---------------------------------------------------------------- items
+//
+// An item is one 64-weight group G of R consecutive rows of the stage (row
+// pointers rp) against B staged x rows; part[r][b] receives the dot
+// product.  Accumulators are fp32 pairs (even / odd code positions of a
+// word), combined in a fixed order at the end.
 
 struct Q4Row {
     float c0, c1, dsc0, dsc1, e0, e1;
@@ -241,7 +240,12 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// One Q4_K item: group G of rows rp[0..R-1], B x rows.  part[r][b].
+__device__ __forceinline__ float pair_sum(uint64_t a, uint64_t b) {
+    return (lo_f(a) + hi_f(a)) + (lo_f(b) + hi_f(b));
+}
+
+// Q4_K: quant bytes 32g'..32g'+31 of the group's super-block hold columns
+// l (low nibble) and 32 + l (high nibble, arrives as 16 q).
 template <int B, int R>
 __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, const float* xs,
                                          const float* sxs, int U, const Q4Sel& sl,
@@ -251,13 +255,13 @@ __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, c
     Q4Row rc[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) rc[r] = q4k_row(*reinterpret_cast<const uint4*>(rp[r] + boff), sl, K);
-    float a[R][B][8];
+    uint64_t a[R][B][4];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int b = 0; b < B; ++b)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) a[r][b][k] = 0.f;
+            for (int k = 0; k < 4; ++k) a[r][b][k] = 0;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         uint4 q[R];
@@ -266,34 +270,26 @@ __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, c
 #pragma unroll
         for (int ww = 0; ww < 4; ++ww) {
             const int w = 4 * hf + ww;
-            float4 xl[B], xh[B];
+            X2 xl[B], xh[B];
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 const float* xg = xs + (b * U + G) * XS_STRIDE;
-                xl[b] = lds_f4(xg + 4 * w);
-                xh[b] = lds_f4(xg + 32 + 4 * w);
+                xl[b] = lds_x2(xg + 4 * w);
+                xh[b] = lds_x2(xg + 32 + 4 * w);
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t W = comp(q[r], ww), W8 = W >> 8;
-                const uint32_t h0 = lop_and_or(W, K.m4lo, K.magic);
-                const uint32_t h1 = lop_and_or(W, K.m4hi, K.magic);
-                const uint32_t h2 = lop_and_or(W8, K.m4lo, K.magic);
-                const uint32_t h3 = lop_and_or(W8, K.m4hi, K.magic);
-                const float v0 = h2f_lo(h0, rc[r].c0), v2 = h2f_hi(h0, rc[r].c0);
-                const float v1 = h2f_lo(h2, rc[r].c0), v3 = h2f_hi(h2, rc[r].c0);
-                const float u0 = h2f_lo(h1, rc[r].c1), u2 = h2f_hi(h1, rc[r].c1);
-                const float u1 = h2f_lo(h3, rc[r].c1), u3 = h2f_hi(h3, rc[r].c1);
+                const uint64_t v02 = h2f_pair(lop_and_or(W, K.m4lo, K.magic), rc[r].c0);
+                const uint64_t v13 = h2f_pair(lop_and_or(W8, K.m4lo, K.magic), rc[r].c0);
+                const uint64_t u02 = h2f_pair(lop_and_or(W, K.m4hi, K.magic), rc[r].c1);
+                const uint64_t u13 = h2f_pair(lop_and_or(W8, K.m4hi, K.magic), rc[r].c1);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    a[r][b][0] = fmaf(v0, xl[b].x, a[r][b][0]);
-                    a[r][b][1] = fmaf(v2, xl[b].z, a[r][b][1]);
-                    a[r][b][2] = fmaf(v1, xl[b].y, a[r][b][2]);
-                    a[r][b][3] = fmaf(v3, xl[b].w, a[r][b][3]);
-                    a[r][b][4] = fmaf(u0, xh[b].x, a[r][b][4]);
-                    a[r][b][5] = fmaf(u2, xh[b].z, a[r][b][5]);
-                    a[r][b][6] = fmaf(u1, xh[b].y, a[r][b][6]);
-                    a[r][b][7] = fmaf(u3, xh[b].w, a[r][b][7]);
+                    a[r][b][0] = ffma2(v02, xl[b].a, a[r][b][0]);
+                    a[r][b][1] = ffma2(v13, xl[b].b, a[r][b][1]);
+                    a[r][b][2] = ffma2(u02, xh[b].a, a[r][b][2]);
+                    a[r][b][3] = ffma2(u13, xh[b].b, a[r][b][3]);
                 }
             }
         }
@@ -303,14 +299,17 @@ __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, c
         const float sxl = sxs[(b * U + G) * 2], sxh = sxs[(b * U + G) * 2 + 1];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float A = (a[r][b][0] + a[r][b][1]) + (a[r][b][2] + a[r][b][3]);
-            const float Bs = (a[r][b][4] + a[r][b][5]) + (a[r][b][6] + a[r][b][7]);
+            const float A = pair_sum(a[r][b][0], a[r][b][1]);
+            const float Bs = pair_sum(a[r][b][2], a[r][b][3]);
             part[r][b] = fmaf(rc[r].dsc0, A, fmaf(rc[r].e0, sxl, fmaf(rc[r].dsc1, Bs, rc[r].e1 * sxh)));
         }
     }
 }
 
-// One Q6_K item (group = half h, column run l0, four quarters).
+// Q6_K: group = half h (128 weights) x column run l0..l0+15 (l0 in {0, 16})
+// of a super-block, over its four quarters q (column 128h + 32q + l).
+// w = d * sc * (code - 32): exact, no cancellation, so the factored form
+// sum_q d*sc_q * sum (code - 32) x is within a few gamma_n * sum |w x|.
 template <int B, int R>
 __device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, const float* xs,
                                          int U, const GroupConsts& K, float (&part)[R][B]) {
@@ -336,21 +335,21 @@ __device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, c
         ds[r][2] = hmul_lo_lo(dw, s23, 0.0f);
         ds[r][3] = hmul_lo_hi(dw, s23, 0.0f);
     }
-    float a[R][B][4];
+    uint64_t a[R][B][4];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int b = 0; b < B; ++b)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) a[r][b][q] = 0.f;
-    const float cq = -1056.0f;
+            for (int q = 0; q < 4; ++q) a[r][b][q] = 0;
+    const float cq = -1056.0f;                          // -(1024 + 32)
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        float4 xq[B][4];
+        X2 xq[B][4];
 #pragma unroll
         for (int b = 0; b < B; ++b)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) xq[b][q] = lds_f4(xs + (b * U + G) * XS_STRIDE + 16 * q + 4 * w);
+            for (int q = 0; q < 4; ++q) xq[b][q] = lds_x2(xs + (b * U + G) * XS_STRIDE + 16 * q + 4 * w);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint32_t c[4] = {(A[r][w] & 0x0F0F0F0Fu) | ((H[r][w] << 4) & 0x30303030u),
@@ -359,18 +358,12 @@ __device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, c
                                    ((Bw[r][w] >> 4) & 0x0F0F0F0Fu) | ((H[r][w] >> 2) & 0x30303030u)};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint32_t hA = lop_and_or(c[q], K.m6, K.magic);
-                const uint32_t hB = lop_and_or(c[q] >> 8, K.m6, K.magic);
-                const float v0 = h2f_lo(hA, cq), v1 = h2f_lo(hB, cq);
-                const float v2 = h2f_hi(hA, cq), v3 = h2f_hi(hB, cq);
+                const uint64_t v02 = h2f_pair(lop_and_or(c[q], K.m6, K.magic), cq);
+                const uint64_t v13 = h2f_pair(lop_and_or(c[q] >> 8, K.m6, K.magic), cq);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    float t = a[r][b][q];
-                    t = fmaf(v0, xq[b][q].x, t);
-                    t = fmaf(v1, xq[b][q].y, t);
-                    t = fmaf(v2, xq[b][q].z, t);
-                    t = fmaf(v3, xq[b][q].w, t);
-                    a[r][b][q] = t;
+                    a[r][b][q] = ffma2(v02, xq[b][q].a, a[r][b][q]);
+                    a[r][b][q] = ffma2(v13, xq[b][q].b, a[r][b][q]);
                 }
             }
         }
@@ -378,23 +371,25 @@ __device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, c
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int b = 0; b < B; ++b)
-            part[r][b] = fmaf(ds[r][0], a[r][b][0],
-                              fmaf(ds[r][1], a[r][b][1], fmaf(ds[r][2], a[r][b][2], ds[r][3] * a[r][b][3])));
+        for (int b = 0; b < B; ++b) {
+            float t[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) t[q] = lo_f(a[r][b][q]) + hi_f(a[r][b][q]);
+            part[r][b] = fmaf(ds[r][0], t[0], fmaf(ds[r][1], t[1], fmaf(ds[r][2], t[2], ds[r][3] * t[3])));
+        }
 }
 
-// One Q8_0 item (group = two 34-byte blocks, 4-byte aligned in the stage).
+// Q8_0: group = two consecutive 34-byte blocks (68 bytes, 4-byte aligned in
+// the stage).  w = d * q exact; factored per block.
 template <int B, int R>
 __device__ __forceinline__ void q80_item(const uint8_t* const (&rp)[R], int G, const float* xs,
                                          int U, const GroupConsts& K, float (&part)[R][B]) {
-    const float cq = -1152.0f;
-    float a[R][B][4];
+    const float cq = -1152.0f;                          // -(1024 + 128)
+    uint64_t a[R][B][2];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int b = 0; b < B; ++b)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) a[r][b][k] = 0.f;
+        for (int b = 0; b < B; ++b) a[r][b][0] = a[r][b][1] = 0;
     float d[R][2];
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
@@ -408,22 +403,18 @@ __device__ __forceinline__ void q80_item(const uint8_t* const (&rp)[R], int G, c
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float4 xv[B];
+            X2 xv[B];
 #pragma unroll
-            for (int b = 0; b < B; ++b) xv[b] = lds_f4(xs + (b * U + G) * XS_STRIDE + 32 * blk + 4 * i);
+            for (int b = 0; b < B; ++b) xv[b] = lds_x2(xs + (b * U + G) * XS_STRIDE + 32 * blk + 4 * i);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t Q = blk == 0 ? __funnelshift_r(wv[r][i], wv[r][i + 1], 16) : wv[r][i + 1];
-                const uint32_t hA = lop_and_xor(Q, K.m8, K.x8);
-                const uint32_t hB = lop_and_xor(Q >> 8, K.m8, K.x8);
-                const float v0 = h2f_lo(hA, cq), v1 = h2f_lo(hB, cq);
-                const float v2 = h2f_hi(hA, cq), v3 = h2f_hi(hB, cq);
+                const uint64_t v02 = h2f_pair(lop_and_xor(Q, K.m8, K.x8), cq);
+                const uint64_t v13 = h2f_pair(lop_and_xor(Q >> 8, K.m8, K.x8), cq);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    a[r][b][2 * blk] = fmaf(v0, xv[b].x, a[r][b][2 * blk]);
-                    a[r][b][2 * blk + 1] = fmaf(v1, xv[b].y, a[r][b][2 * blk + 1]);
-                    a[r][b][2 * blk] = fmaf(v2, xv[b].z, a[r][b][2 * blk]);
-                    a[r][b][2 * blk + 1] = fmaf(v3, xv[b].w, a[r][b][2 * blk + 1]);
+                    a[r][b][blk] = ffma2(v02, xv[b].a, a[r][b][blk]);
+                    a[r][b][blk] = ffma2(v13, xv[b].b, a[r][b][blk]);
                 }
             }
         }
@@ -432,7 +423,8 @@ __device__ __forceinline__ void q80_item(const uint8_t* const (&rp)[R], int G, c
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int b = 0; b < B; ++b)
-            part[r][b] = fmaf(d[r][0], a[r][b][0] + a[r][b][1], d[r][1] * (a[r][b][2] + a[r][b][3]));
+            part[r][b] = fmaf(d[r][0], lo_f(a[r][b][0]) + hi_f(a[r][b][0]),
+                              d[r][1] * (lo_f(a[r][b][1]) + hi_f(a[r][b][1])));
 }
 
 template <int FMT, int B, int R>
@@ -442,6 +434,70 @@ __device__ __forceinline__ void run_item(const uint8_t* const (&rp)[R], int G, c
     if (FMT == FMT_Q4_K) q4k_item<B, R>(rp, G, xs, sxs, U, sl, K, part);
     else if (FMT == FMT_Q6_K) q6k_item<B, R>(rp, G, xs, U, K, part);
     else q80_item<B, R>(rp, G, xs, U, K, part);
+}
+
+// ---------------------------------------------------------------- reduction
+
+// sum of r[j], r[j + 8], r[j + 16], ... (< U) in that order; loads issued
+// eight at a time so their latencies overlap
+__device__ __forceinline__ float lane_sum8(const float* r, int j, int U) {
+    float acc = 0.f;
+    int G = j;
+    for (; G + 56 < U; G += 64) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = r[G + 8 * k];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc += v[k];
+    }
+    for (; G < U; G += 8) acc += r[G];
+    return acc;
+}
+
+// Sum the per-group partials of tile t (segment S) into y, with the gated
+// activation for row pairs: passes pass0, pass0 + pstep, ... of four
+// outputs each, so the consumer warps share a tile.  8 lanes per output, lane j summing
+// groups j, j + 8, ... in order, then a fixed butterfly: the order depends
+// only on U, so results do not depend on B or the tile.  Four outputs per
+// pass read rows UP floats apart (UP = 8 mod 32): no bank conflicts.
+template <int B>
+__device__ __forceinline__ void reduce_tile(const QmvParams& P, const Seg& S, int t, const float* red,
+                                            int lane, int pass0, int pstep) {
+    const int U = P.U, UP = P.UP, mode = S.mode;
+    const int half = P.RT / 2;
+    const int lt = t - S.tile0;
+    const int opt = mode == MODE_PLAIN ? P.RT : half;
+    const int o0 = lt * opt;
+    const int n_o = min(opt, S.nout - o0);
+    const int nval = qseg_nval(S, B);
+    const int boff = qseg_boff(S);
+    float* y = S.y;
+    const int64_t ldy = S.ld_y;
+    const int j = lane & 7;
+    const int n_out = n_o * B;
+    const float* up_plane = red + (size_t)half * B * UP;
+    for (int ob = 4 * pass0; ob < n_out; ob += 4 * pstep) {
+        const int o = ob + (lane >> 3);
+        const bool live = o < n_out;
+        const int oo = live ? o : 0;
+        const float* rr = red + (size_t)oo * UP;
+        const float vg0 = lane_sum8(rr, j, U);
+        float vg = vg0;
+        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 1);
+        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 2);
+        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 4);
+        float v = vg;
+        if (mode != MODE_PLAIN) {
+            const float* ru = up_plane + (size_t)oo * UP;
+            float vu = lane_sum8(ru, j, U);
+            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 1);
+            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 2);
+            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 4);
+            v = act_q(S.act, vg) * vu;
+        }
+        const int pi = oo / B, b = oo % B;
+        if (live && j == 0 && b < nval) y[(int64_t)(boff + b) * ldy + o0 + pi] = v;
+    }
 }
 
 // ---------------------------------------------------------------- the CTA
@@ -465,24 +521,43 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     const int NC = (blockDim.x >> 5) - 1;          // consumer warps
     const int NCT = NC * 32;
     const int S_ = P.nstages;
-    const int NRED = S_ + 1;
     const int U = P.U;
-    const int red_tile = P.RT * B * U;
+    const int red_tile = P.RT * B * P.UP;
+    const int NRED = S_ + 1;             // partial slots
 
     if (warp == NC) {
         // ------------------------------------------------ producer warp
-        uint64_t policy = policy_evict_first();
+        // Streams tile n into stage n % S once the consumers released tile
+        // n - S, then reduces tile n - S (its partials are complete when that
+        // stage's empty barrier completes).  The last S tiles are reduced by
+        // the consumer warps after their loop.
+        const uint64_t policy = policy_evict_first();
         Walk w = walk0;
+        if (!P.dev_counts) {
+            // weights do not depend on the preceding kernel: warm L2 with the
+            // first tiles while it finishes (a hint; L2 stays coherent)
+            walk_fix<B>(sm.segs, P.nseg, w);
+            Walk wp = w;
+            for (int k = 0; k < S_ && wp.t < wp.end; ++k) {
+                const QTile g = qtile(P, sm.segs[wp.hint], wp.t);
+                if (lane == 0 && g.tma) {
+                    prefetch_l2_bulk(g.src1, g.bytes1);
+                    if (g.bytes2) prefetch_l2_bulk(g.src2, g.bytes2);
+                }
+                wp.t += wp.step;
+                walk_fix<B>(sm.segs, P.nseg, wp);
+            }
+        }
+        pdl_wait();
         walk_fix<B>(sm.segs, P.nseg, w);
+        Walk wr = w;                      // reduction walk, S tiles behind
         uint32_t ephase = 0;
         int last_use[8];                  // last bulk-copied use of each stage (-1: none)
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
-        int n = 0;
         bool ok = true;
-        for (; w.t < w.end; ++n) {
+        for (int n = 0, s = 0; w.t < w.end; ++n) {
             if (*reinterpret_cast<volatile int*>(sm.abort_flag)) break;
-            const int s = n % S_;
             if (n >= S_) {            // wait until the consumers released stage s
                 if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -505,8 +580,15 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.full[s]);
             }
+            if (n >= S_) {
+                __syncwarp();
+                reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)((n - S_) % NRED) * red_tile, lane, 0, 1);
+                wr.t += wr.step;
+                walk_fix<B>(sm.segs, P.nseg, wr);
+            }
             w.t += w.step;
             walk_fix<B>(sm.segs, P.nseg, w);
+            if (++s == S_) s = 0;
         }
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
@@ -523,20 +605,31 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     }
 
     // ---------------------------------------------------- consumer warps
+    // Per tile: wait for the stage, run the items, write the partials into
+    // slot n % (S + 1), release the stage (the producer reduces the tile S
+    // tiles later).  After the loop the consumer warps share the reduction
+    // of the last S tiles.
     Walk w = walk0;
-    walk_fix<B>(sm.segs, P.nseg, w);
     int cur_seg = -1;
     uint32_t fphase = 0;
     bool aborted = false;
-    for (int n = 0; w.t < w.end; ++n) {
-        const int s = n % S_;
+    const int UP = P.UP;
+    const int half = P.RT / 2;
+    const int rb = (int)qrow_bytes(FMT, P.cols);
+    // Item it = tid + q*NCT of every tile covers group it % U of rows
+    // (it / U)*R .. +R-1: the same for every tile, so it is stepped, not divided.
+    const int G_first = tid % U, row_first = (tid / U) * R;
+    const int dG = NCT % U, dRow = (NCT / U) * R;
+    pdl_wait();                          // x and device row counts come from the preceding kernel
+    walk_fix<B>(sm.segs, P.nseg, w);
+    int slot_n = 0, ntl = 0;
+    for (int n = 0, s = 0; w.t < w.end; ++n) {
         const Seg& S = sm.segs[w.hint];
         if (w.hint != cur_seg) {
             consumer_sync(NCT);          // every consumer is done with the previous x
             stage_x<FMT, B>(P, S, sm.xs, sm.sxs, tid, NCT);
             cur_seg = w.hint;
         }
-        const QTile g = qtile(P, S, w.t);
         if (!aborted) {
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(&sm.full[s], (fphase >> s) & 1u, P.timeout_ns);
@@ -550,84 +643,67 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             }
         }
         fphase ^= 1u << s;
-        const int64_t rb = qrow_bytes(FMT, P.cols);
-        const uint8_t* st = sm.stages + (size_t)s * P.stage_bytes;
-        float* red = sm.red + (size_t)(n % NRED) * red_tile;
         const int mode = S.mode;
-        const int half = P.RT / 2;
+        const uint8_t* st = sm.stages + (size_t)s * P.stage_bytes;
+        float* red = sm.red + (size_t)slot_n * red_tile;
         if (!aborted) {
+            int G = G_first, row0 = row_first;
             for (int q = 0; q < P.ipt; ++q) {
-                const int it = tid + q * NCT;
-                const int G = it % U;
-                const int row0 = (it / U) * R;
                 const uint8_t* rp[R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) rp[r] = st + (int64_t)(row0 + r) * rb;
+                for (int r = 0; r < R; ++r) rp[r] = st + (row0 + r) * rb;
                 float part[R][B];
                 const Q4Sel sel = q4_sel(G & 3);
                 run_item<FMT, B, R>(rp, G, sm.xs, sm.sxs, U, sel, K, part);
+                // partial row slot: gate rows of interleaved pairs first, then up rows
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int rho = row0 + r;
-                    bool valid;
-                    if (mode == MODE_PLAIN) valid = rho < g.n_o;
-                    else if (mode == MODE_PAIR_INTERLEAVED) valid = rho < 2 * g.n_o;
-                    else valid = (rho % half) < g.n_o;
+                    const int slot = mode == MODE_PAIR_INTERLEAVED ? (rho & 1) * half + (rho >> 1) : rho;
 #pragma unroll
-                    for (int b = 0; b < B; ++b) red[(rho * B + b) * U + G] = valid ? part[r][b] : 0.f;
+                    for (int b = 0; b < B; ++b) red[(slot * B + b) * UP + G] = part[r][b];
+                }
+                G += dG;
+                row0 += dRow;
+                if (G >= U) {
+                    G -= U;
+                    row0 += R;
                 }
             }
         }
-        // last warp to finish this tile releases the stage and reduces
+        // release the stage; the empty barrier (all consumer warps, release
+        // order) also publishes the partials to whoever reduces the tile
         __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            // counters only grow: each use of a slot adds NC
-            const int old = atomicAdd(&sm.cnt[n % NRED], 1);
-            last = (old % NC) == NC - 1;
-            if (last) mbar_arrive(&sm.empty[s]);
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last && !aborted) {
-            // 4 lanes per output, each summing a fixed quarter of the U group
-            // partials in order, combined as (q0 + q1) + (q2 + q3): the order
-            // depends only on U, so results do not depend on B or the tile.
-            __threadfence_block();
-            const int nval = qseg_nval(S, B);
-            const int boff = qseg_boff(S);
-            float* y = S.y;
-            const int64_t ldy = S.ld_y;
-            const int act = S.act;
-            const int chunk = (U + 3) / 4;
-            const int c = lane & 3;
-            const int g0 = c * chunk, g1 = min(U, g0 + chunk);
-            const int n_out = g.n_o * B;
-            for (int ob = 0; ob < n_out; ob += 8) {
-                const int o = ob + (lane >> 2);
-                const bool live = o < n_out;
-                const int pi = live ? o / B : 0, b = live ? o % B : 0;
-                const int rg = mode == MODE_PAIR_INTERLEAVED ? 2 * pi : pi;
-                float vg = 0.f;
-                const float* rr = red + (rg * B + b) * U;
-                for (int G = g0; G < g1; ++G) vg += rr[G];
-                vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 1);
-                vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 2);
-                float v = vg;
-                if (mode != MODE_PLAIN) {
-                    const int ru = mode == MODE_PAIR_INTERLEAVED ? 2 * pi + 1 : pi + half;
-                    float vu = 0.f;
-                    const float* ru_p = red + (ru * B + b) * U;
-                    for (int G = g0; G < g1; ++G) vu += ru_p[G];
-                    vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 1);
-                    vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 2);
-                    v = act_q(act, vg) * vu;
-                }
-                if (live && c == 0 && b < nval) y[(int64_t)(boff + b) * ldy + g.o0 + pi] = v;
-            }
-        }
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
         w.t += w.step;
         walk_fix<B>(sm.segs, P.nseg, w);
+        if (++s == S_) s = 0;
+        if (++slot_n == NRED) slot_n = 0;
+        ntl = n + 1;
+    }
+    // the last S tiles: tile m's partials are complete when the empty
+    // barrier of stage m % S completes its use m / S
+    if (!aborted) {
+        Walk wr = walk0;
+        walk_fix<B>(sm.segs, P.nseg, wr);
+        for (int m = 0; m < ntl; ++m) {
+            if (m >= ntl - S_) {
+                bool ok = true;
+                if (lane == 0)
+                    ok = mbar_wait_bounded(&sm.empty[m % S_], (uint32_t)(m / S_) & 1u, P.timeout_ns);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        record_status(P.status, STATUS_TIMEOUT);
+                        atomicExch(sm.abort_flag, 1);
+                    }
+                    break;
+                }
+                reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)(m % NRED) * red_tile, lane, warp, NC);
+            }
+            wr.t += wr.step;
+            walk_fix<B>(sm.segs, P.nseg, wr);
+        }
     }
 }
 
@@ -639,6 +715,7 @@ template <int B, int R, int MASK>
 __global__ void __launch_bounds__(288, 2) qmv_kernel(const __grid_constant__ QmvParams P,
                                                       const GroupConsts K) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
     const int S_ = P.nstages;
     const int U = P.U;
     Smem sm;
@@ -650,7 +727,7 @@ __global__ void __launch_bounds__(288, 2) qmv_kernel(const __grid_constant__ Qmv
     sm.sxs = reinterpret_cast<float*>(smem + off);
     off += (size_t)B * U * 2 * sizeof(float);
     sm.red = reinterpret_cast<float*>(smem + off);
-    off += (size_t)(S_ + 1) * P.RT * B * U * sizeof(float);
+    off += (size_t)(S_ + 1) * P.RT * B * P.UP * sizeof(float);
     off = (off + 7) & ~size_t(7);
     sm.full = reinterpret_cast<uint64_t*>(smem + off);
     sm.empty = sm.full + S_;
@@ -669,7 +746,7 @@ __global__ void __launch_bounds__(288, 2) qmv_kernel(const __grid_constant__ Qmv
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.empty[s], (blockDim.x >> 5) - 1);   // every consumer warp arrives
         }
         for (int s = 0; s <= S_; ++s) sm.cnt[s] = 0;
         *sm.abort_flag = 0;
@@ -732,11 +809,24 @@ struct QmvTable {
     static cudaError_t occupancy(int mask, int nt, size_t smem, int* per_sm) {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, get(mask), nt, smem);
     }
+    // Launched with programmatic stream serialization: the kernel may start
+    // while the preceding kernel of the stream finishes; it reads x, device
+    // row counts and (after an L2 prefetch hint) W only after griddepcontrol.wait.
     static cudaError_t launch(int mask, const QmvParams& P, int grid, int nt, size_t smem,
                               cudaStream_t st) {
         const GroupConsts K = group_consts();
         void* args[2] = {const_cast<QmvParams*>(&P), const_cast<GroupConsts*>(&K)};
-        return cudaLaunchKernel(get(mask), dim3(grid), dim3(nt), args, smem, st);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(nt);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelExC(&cfg, get(mask), args);
     }
 };
 

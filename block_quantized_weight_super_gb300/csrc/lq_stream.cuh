@@ -1,5 +1,5 @@
-// lq_stream.cuh -- parameters of the streaming matvec kernel (shared by the
-// kernel translation unit and the host launchers).
+// lq_stream.cuh -- segment descriptors of the quantized matvec kernel
+// (shared by the kernel translation units and the host launchers).
 #pragma once
 #include <cstdint>
 
@@ -31,20 +31,6 @@ struct Seg {
     int32_t nbatch;        // valid batch rows when bcnt is null
     int32_t tile0;         // first global tile index of this segment
     int32_t ntiles;
-};
-
-struct StreamParams {
-    Seg seg[MAX_SEG];
-    int32_t nseg;
-    int32_t ntiles;        // total tiles over all segments
-    int32_t cols;
-    int32_t ngroups;       // cols / 64
-    int32_t RT;            // matrix rows per tile (even)
-    int32_t k;             // row slots: threads = ngroups * B * k
-    int32_t nstages;
-    int32_t stage_bytes;   // bytes per stage buffer (multiple of 16, + 16 pad)
-    uint64_t timeout_ns;
-    unsigned* status;      // device status word (timeouts are recorded here)
 };
 
 }  // namespace lq
