@@ -22,8 +22,10 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
            "lq_dequant", "lq_matvec", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
-           "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_device_status", "lq_set_wait_timeout_ns",
-           "lq_probe_timeout"]
+           "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_static", "lq_device_status",
+           "lq_set_wait_timeout_ns", "lq_probe_timeout"]
+
+LQ_MOE_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class LqError(RuntimeError):
@@ -56,6 +58,7 @@ def lib():
             "lq_ffn_gate_up_act": ([i32, vp, i64, i64, vp, vp, i32, i32, vp], i32),
             "lq_moe_workspace_bytes": ([i32, i32, i32, i64, i64], sz),
             "lq_moe_ffn": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, sz, vp], i32),
+            "lq_moe_ffn_static": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp], i32),
             "lq_device_status": ([vp, C.POINTER(C.c_uint32)], i32),
             "lq_set_wait_timeout_ns": ([u64], None),
             "lq_probe_timeout": ([u64, vp], i32),
@@ -150,6 +153,15 @@ def lq_moe_ffn(router, n_experts, topk, fmt, W1, W3, W2, hidden, inter, X, Y, nt
                                    C.cast(a3, C.c_void_p), C.cast(a2, C.c_void_p), hidden, inter,
                                    _ptr(X), _ptr(Y), ntok, _ptr(topk_idx), _ptr(topk_w),
                                    _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def lq_moe_ffn_static(router, n_experts, topk, fmt, W1, W3, W2, hidden, inter, X, Y, ntok,
+                      topk_idx=None, topk_w=None, stream=None):
+    a1, a3, a2 = _ptr_array(W1), _ptr_array(W3), _ptr_array(W2)
+    return _check(lib().lq_moe_ffn_static(_ptr(router), n_experts, topk, fmt, C.cast(a1, C.c_void_p),
+                                          C.cast(a3, C.c_void_p), C.cast(a2, C.c_void_p), hidden, inter,
+                                          _ptr(X), _ptr(Y), ntok, _ptr(topk_idx), _ptr(topk_w),
+                                          _stream(stream)))
 
 
 def lq_device_status(stream=None):

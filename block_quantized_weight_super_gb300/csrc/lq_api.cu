@@ -273,6 +273,13 @@ int check_f32(const void* p, const char* name) {
 
 using namespace lq;
 
+// Scratch of lq_moe_ffn_static: a file-scope device array (no allocation),
+// one instance per device.
+static __device__ __align__(256) uint8_t g_moe_scratch[LQ_MOE_STATIC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+static std::mutex g_moe_scratch_mu;
+static void* g_moe_scratch_ptr[kMaxDevices] = {};
+
 extern "C" {
 
 size_t lq_block_bytes(int fmt) { return fmt_ok(fmt) ? (size_t)block_bytes_of(fmt) : 0; }
@@ -489,6 +496,36 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
     }
     e = launch_moe_combine(ws.ybuf, hidden, ntok, topk, ws, Y, st);
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "moe combine launch");
+}
+
+// No-allocation variant: the scratch is a static device array of this
+// module, its address looked up once per device (with that device current).
+int lq_moe_ffn_static(const float* router, int E, int topk, int fmt, const void* const* W1,
+                      const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
+                      const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+                      lq_stream_t stream) {
+    g_err[0] = 0;
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (d < 0 || d >= kMaxDevices) return fail(LQ_EINVAL, "device %d out of range", d);
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_moe_scratch_mu);
+        if (!g_moe_scratch_ptr[d]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_moe_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static MoE scratch)");
+            g_moe_scratch_ptr[d] = ptr;
+        }
+        scratch = g_moe_scratch_ptr[d];
+    }
+    const size_t need = lq_moe_workspace_bytes(E, topk, ntok, hidden, inter);
+    if (need > (size_t)LQ_MOE_STATIC_SCRATCH_BYTES)
+        return fail(LQ_EWORKSPACE, "MoE needs %zu bytes of scratch; the static scratch holds %zu", need,
+                    (size_t)LQ_MOE_STATIC_SCRATCH_BYTES);
+    return lq_moe_ffn(router, E, topk, fmt, W1, W3, W2, hidden, inter, X, Y, ntok, topk_idx, topk_w,
+                      scratch, (size_t)LQ_MOE_STATIC_SCRATCH_BYTES, stream);
 }
 
 int lq_device_status(lq_stream_t stream, uint32_t* bits) {

@@ -121,6 +121,31 @@ int lq_moe_ffn(const float* router, int n_experts, int topk, int fmt, const void
                const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
                void* workspace, size_t ws_bytes, lq_stream_t stream);
 
+/* lq_moe_ffn_static -- lq_moe_ffn without a caller-supplied workspace: the
+ * scratch is a static device array of LQ_MOE_STATIC_SCRATCH_BYTES (4 MiB)
+ * inside the library, one per device, and the call allocates no device
+ * memory (no cudaMalloc / cudaFree or allocating routine, on any call).
+ * The method's description has no such call; it is for callers that cannot
+ * allocate, e.g. a plain C caller without a device allocator, or a serving
+ * process whose device memory is all reserved by another allocator, where a
+ * cudaMalloc would fail and a cudaFree would synchronise the device.
+ *   Arguments, results and errors are those of lq_moe_ffn (without
+ * workspace, ws_bytes).  Shapes whose lq_moe_workspace_bytes exceeds
+ * LQ_MOE_STATIC_SCRATCH_BYTES are rejected with LQ_EWORKSPACE (e.g.
+ * hidden 4096, inter 14336 fit up to ntok * topk = 56).
+ *   The first call on a device does the set-up (looks up the scratch
+ * address with that device current) and returns LQ_ECUDA if that fails;
+ * make it before any stream capture.  No part of the scratch needs to start
+ * at zero: every word a call reads was written earlier in the same call.
+ * All calls on a device share the one scratch: calls that overlap in time
+ * (on different streams, or from different host threads without ordering)
+ * race on it; calls in order on one stream do not. */
+#define LQ_MOE_STATIC_SCRATCH_BYTES (4u << 20)
+int lq_moe_ffn_static(const float* router, int n_experts, int topk, int fmt, const void* const* W1,
+                      const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
+                      const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+                      lq_stream_t stream);
+
 /* lq_device_status -- synchronises `stream`, then reads and clears the
  * device status word that kernels set when a bounded wait runs out.
  * *bits = the word (0 = clean).  Returns LQ_ETIMEOUT if the timeout bit was
