@@ -9,7 +9,8 @@ step by step, so the weights never sit in the 129 MB L2 between uses.
 
 Headline metric: effective weight GB/s = weight-block bytes of the layer per
 second (60,518,400 B per step), with us/layer = ms_per_step * 1000.  The
-device-timed number replays one CUDA graph per layer with inputs resident;
+device-timed number replays the decode pass (all layer copies in one CUDA
+graph, so consecutive launches overlap) with inputs resident;
 `e2e` times the C ABI calls directly with the step's x copied in from pinned
 host memory and the layer output copied back, every step.
 
@@ -194,19 +195,25 @@ def bench_lq(args, ws, rank, local):
     rc, bits = lq.lq_device_status()
     assert rc == 0
 
-    # one CUDA graph per layer copy
-    graphs = []
+    # The decode pass: all n layer copies in one CUDA graph (a model's depth,
+    # so consecutive layers' launches overlap as in a real decode step).  K
+    # timed steps = K layers: K // n full passes plus one partial pass.
+    def capture(ws_):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for w in ws_:
+                lay.run(w, st)
+        return g
+
     with torch.cuda.stream(st):
         for w in layers:        # warm the kernels once outside capture
             lay.run(w, st)
         st.synchronize()
-        for w in layers:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=st):
-                lay.run(w, st)
-            graphs.append(g)
+        full = capture(layers)
+        rem = args.steps % len(layers)
+        part = capture(layers[:rem]) if rem else None
     torch.cuda.synchronize()
-    n = len(graphs)
+    n = len(layers)
 
     def barrier():
         if ws > 1:
@@ -214,15 +221,18 @@ def bench_lq(args, ws, rank, local):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        graphs[i % n].replay()
+    with torch.cuda.stream(st):
+        for _ in range(max(1, -(-args.warmup // n))):     # >= W warm-up layers
+            full.replay()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(st):
             e0.record(st)
-            for i in range(args.steps):
-                graphs[i % n].replay()
+            for _ in range(args.steps // n):
+                full.replay()
+            if part is not None:
+                part.replay()
             e1.record(st)
         barrier()
     ms = e0.elapsed_time(e1) / args.steps
@@ -313,6 +323,35 @@ def cpu_baseline(sample_layers=1, rows_frac=0.25):
                       f"({nbytes} weight bytes), fp64, {nth} threads"}
 
 
+# DRAM bytes (read + write) of one gate+up launch, from the ncu capture in
+# profiles/qmv_gate_up_q4k_and_down_q6k.md, valid while the kernel sources
+# hash to the value they had when it was taken.
+GATEUP_TRAFFIC = {"csrc_sha256": "948e2282b5d20070aeac72a6265e5b3dc39c6f02b4f2060f9afd9ae6eefdacec", "bytes": 29563136}
+
+
+def csrc_sha256():
+    import hashlib
+    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_quantized_weight_super_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def l2_bytes():
+    """L2 size of GPU 0 (129 MB on GB300 when no device is visible)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(0).L2_cache_size)
+    except Exception:
+        pass
+    return 129_000_000
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args)
@@ -323,7 +362,9 @@ def main():
             "config": {"workload": "Gemma-3-4B-shaped decode layer, batch 1, hidden 2560: QKV "
                                    "(Q/K Q4_K, V Q6_K), O Q4_K, gate+up Q4_K GEGLU-tanh, down Q6_K",
                        "layer_weight_bytes": LAYER_BYTES, "layer_copies": args.layers,
-                       "l2": "inputs larger than L2 (34 rotating layer copies, 2.06 GB)",
+                       "l2": ("inputs larger than L2" if args.layers * LAYER_BYTES > l2_bytes() else
+                              "inputs NOT larger than L2") +
+                             f" ({args.layers} rotating layer copies, {args.layers * LAYER_BYTES / 1e9:.2f} GB)",
                        "parallelism": f"replicas x{ws}"}}
     if args.impl == "reference":
         if rank != 0:
@@ -354,7 +395,10 @@ def main():
                 frac_of_hbm=value / peak,
                 roofline={"bound": "hbm", "kernel": "ffn gate+up GEGLU (Q4_K 2x10240x2560)",
                           "achieved": achieved, "peak": peak, "peak_source": peak_src,
-                          "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                          "unit": "GB/s", "frac": achieved / peak,
+                          "traffic": (GATEUP_TRAFFIC["bytes"] if csrc_sha256() == GATEUP_TRAFFIC["csrc_sha256"]
+                                      else None),
+                          "traffic_source": "profiles/qmv_gate_up_q4k_and_down_q6k.md (ncu dram bytes per launch)",
                           "us_per_launch": gate_ms * 1e3},
                 clocks=clocks, e2e=e2e, gpu_launches=4 * args.steps, cpu_baseline=cb)
     print(json.dumps(line))
