@@ -8,10 +8,10 @@
 //     (exact);
 //   * one mixed-precision add (add.rn.f32.f16): float(1024 + code) + c, with
 //     c = -(1024 + centre), giving code - centre exactly in fp32;
-//   * half of a packed FMA (fma.rn.f32x2) with the fp32 x values.  The two
-//     halves of a LOP3 result hold bytes 0 and 2 (or 1 and 3) of a 32-bit
-//     code word, so x is staged with each run of four columns in the order
-//     (0, 2, 1, 3) and a 16-byte shared load yields the two matching pairs.
+//   * half of a packed FMA (fma.rn.f32x2) with the fp32 x values: the low
+//     halves of the LOP3 results of bytes (0, 2) and (1, 3) of a code word
+//     form the pair of columns (0, 1), the high halves (2, 3), matching the
+//     two pairs of a 16-byte shared load of x in natural order.
 // Block scales are applied once per 16-32 weights (factored form).
 //
 // Q4_K: w_j = d*sc*q_j - dmin*m.  The factored sum d*sc*sum(q x) -
@@ -126,9 +126,13 @@ __device__ __forceinline__ X2 lds_x2(const float* p) {       // p 16-byte aligne
     const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
     return X2{v.x, v.y};
 }
-// code - centre of the two halves of a LOP3 result, as a pair
-__device__ __forceinline__ uint64_t h2f_pair(uint32_t h, float c) {
-    return pk2(h2f_lo(h, c), h2f_hi(h, c));
+// Codes of bytes 0..3 of a word, as (code - centre) pairs in column order:
+// hA holds bytes 0 and 2 (low / high half), hB bytes 1 and 3, so the low
+// halves give columns (0, 1) and the high halves columns (2, 3).
+__device__ __forceinline__ void h2f_pairs(uint32_t hA, uint32_t hB, float c, uint64_t& c01,
+                                          uint64_t& c23) {
+    c01 = pk2(h2f_lo(hA, c), h2f_lo(hB, c));
+    c23 = pk2(h2f_hi(hA, c), h2f_hi(hB, c));
 }
 
 // ---------------------------------------------------------------- Q4_K

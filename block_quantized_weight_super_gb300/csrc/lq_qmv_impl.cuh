@@ -156,50 +156,57 @@ __device__ __forceinline__ int qxcol(int G, int i) {
     return 64 * G + i;
 }
 
-// Stage the B x rows of segment S into xs[(b*U + G)*68 + i] (Q4_K: high
-// columns pre-scaled by 1/16) and, for Q4_K, sxs[(b*U + G)*2 + {0,1}] = sums
-// of the low / high 32 columns (fixed sequential order).  Each run of four
-// columns is stored in the order (0, 2, 1, 3) to match the code pairs of the
-// work items.  A work unit is 16 consecutive columns (one 64-byte run of x)
-// loaded as four independent float4 (x rows are 16-byte aligned: the host
-// checks).  Ends with the consumer barrier; the caller brackets it with one
-// before.
+// Stage the B x rows of segment S into xs[(b*U + G)*68 + i] (64-float group
+// slots padded to 68 floats) and, for Q4_K, sxs[(b*U + G)*2 + {0,1}] = sums
+// of the low / high 32 columns of group G.  A unit is 16 consecutive columns
+// (one 64-byte run of x, four float4; x rows are 16-byte aligned: the host
+// checks); each thread loads two units before storing, and the sub-block
+// sums come from registers: the 16-column sum of a unit (in column order)
+// plus that of its neighbour unit (lane ^ 1).  Ends with the consumer barrier;
+// the caller brackets it with one before.
 template <int FMT, int B>
 __device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs, int ct, int nct) {
     const int U = P.U;
     const int nval = qseg_nval(S, B);
     const int boff = qseg_boff(S);
     const int units = B * U * 4;
-    for (int e = ct; e < units; e += nct) {
-        const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
-        float4 v[4];
-        if (b < nval) {
-            const int rho = boff + b;
-            const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * P.cols;
-            const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
+    const int wbase = ct & ~31;                  // loop bound uniform over the warp
+    for (int e0 = ct, w0 = wbase; w0 < units; e0 += 2 * nct, w0 += 2 * nct) {
+        float4 v[2][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
-        } else {
+        for (int h = 0; h < 2; ++h) {
+            const int e = e0 + h * nct;
+            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
+            if (e < units && b < nval) {
+                const int rho = boff + b;
+                const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * P.cols;
+                const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 4; ++k) v[h][k] = __ldg(src + k);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[h][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        const float sc = (FMT == FMT_Q4_K && q >= 2) ? 0.0625f : 1.0f;     // exact
-        float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[k].x * sc, v[k].z * sc, v[k].y * sc, v[k].w * sc);
+        for (int h = 0; h < 2; ++h) {
+            const int e = e0 + h * nct;
+            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
+            if (e < units) {
+                float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = v[h][k];
+            }
+            if (FMT == FMT_Q4_K) {
+                float s16 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s16 = ((s16 + v[h][k].x) + v[h][k].y) + v[h][k].z + v[h][k].w;
+                const float s32 = s16 + __shfl_xor_sync(0xFFFFFFFFu, s16, 1);
+                if (e < units && (q & 1) == 0) sxs[(b * U + G) * 2 + (q >> 1)] = s32;
+            }
+        }
     }
     consumer_sync(nct);
-    if (FMT == FMT_Q4_K) {
-        for (int e = ct; e < B * U * 2; e += nct) {
-            const int b = e / (U * 2), G = (e % (U * 2)) >> 1, hi = e & 1;
-            const float* xg = xs + (b * U + G) * XS_STRIDE + 32 * hi;
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s += xg[i];
-            sxs[(b * U + G) * 2 + hi] = hi ? s * 16.0f : s;     // exact: power-of-two scale
-        }
-        consumer_sync(nct);
-    }
 }
 
 // ---------------------------------------------------------------- items
@@ -280,16 +287,15 @@ __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, c
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t W = comp(q[r], ww), W8 = W >> 8;
-                const uint64_t v02 = h2f_pair(lop_and_or(W, K.m4lo, K.magic), rc[r].c0);
-                const uint64_t v13 = h2f_pair(lop_and_or(W8, K.m4lo, K.magic), rc[r].c0);
-                const uint64_t u02 = h2f_pair(lop_and_or(W, K.m4hi, K.magic), rc[r].c1);
-                const uint64_t u13 = h2f_pair(lop_and_or(W8, K.m4hi, K.magic), rc[r].c1);
+                uint64_t v01, v23, u01, u23;      // u: high nibbles, 16 (q - qb) exactly
+                h2f_pairs(lop_and_or(W, K.m4lo, K.magic), lop_and_or(W8, K.m4lo, K.magic), rc[r].c0, v01, v23);
+                h2f_pairs(lop_and_or(W, K.m4hi, K.magic), lop_and_or(W8, K.m4hi, K.magic), rc[r].c1, u01, u23);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    a[r][b][0] = ffma2(v02, xl[b].a, a[r][b][0]);
-                    a[r][b][1] = ffma2(v13, xl[b].b, a[r][b][1]);
-                    a[r][b][2] = ffma2(u02, xh[b].a, a[r][b][2]);
-                    a[r][b][3] = ffma2(u13, xh[b].b, a[r][b][3]);
+                    a[r][b][0] = ffma2(v01, xl[b].a, a[r][b][0]);
+                    a[r][b][1] = ffma2(v23, xl[b].b, a[r][b][1]);
+                    a[r][b][2] = ffma2(u01, xh[b].a, a[r][b][2]);
+                    a[r][b][3] = ffma2(u23, xh[b].b, a[r][b][3]);
                 }
             }
         }
@@ -300,7 +306,7 @@ __device__ __forceinline__ void q4k_item(const uint8_t* const (&rp)[R], int G, c
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float A = pair_sum(a[r][b][0], a[r][b][1]);
-            const float Bs = pair_sum(a[r][b][2], a[r][b][3]);
+            const float Bs = pair_sum(a[r][b][2], a[r][b][3]) * 0.0625f;   // exact
             part[r][b] = fmaf(rc[r].dsc0, A, fmaf(rc[r].e0, sxl, fmaf(rc[r].dsc1, Bs, rc[r].e1 * sxh)));
         }
     }
@@ -358,12 +364,12 @@ __device__ __forceinline__ void q6k_item(const uint8_t* const (&rp)[R], int G, c
                                    ((Bw[r][w] >> 4) & 0x0F0F0F0Fu) | ((H[r][w] >> 2) & 0x30303030u)};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint64_t v02 = h2f_pair(lop_and_or(c[q], K.m6, K.magic), cq);
-                const uint64_t v13 = h2f_pair(lop_and_or(c[q] >> 8, K.m6, K.magic), cq);
+                uint64_t v01, v23;
+                h2f_pairs(lop_and_or(c[q], K.m6, K.magic), lop_and_or(c[q] >> 8, K.m6, K.magic), cq, v01, v23);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    a[r][b][q] = ffma2(v02, xq[b][q].a, a[r][b][q]);
-                    a[r][b][q] = ffma2(v13, xq[b][q].b, a[r][b][q]);
+                    a[r][b][q] = ffma2(v01, xq[b][q].a, a[r][b][q]);
+                    a[r][b][q] = ffma2(v23, xq[b][q].b, a[r][b][q]);
                 }
             }
         }
@@ -409,12 +415,12 @@ __device__ __forceinline__ void q80_item(const uint8_t* const (&rp)[R], int G, c
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t Q = blk == 0 ? __funnelshift_r(wv[r][i], wv[r][i + 1], 16) : wv[r][i + 1];
-                const uint64_t v02 = h2f_pair(lop_and_xor(Q, K.m8, K.x8), cq);
-                const uint64_t v13 = h2f_pair(lop_and_xor(Q >> 8, K.m8, K.x8), cq);
+                uint64_t v01, v23;
+                h2f_pairs(lop_and_xor(Q, K.m8, K.x8), lop_and_xor(Q >> 8, K.m8, K.x8), cq, v01, v23);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    a[r][b][blk] = ffma2(v02, xv[b].a, a[r][b][blk]);
-                    a[r][b][blk] = ffma2(v13, xv[b].b, a[r][b][blk]);
+                    a[r][b][blk] = ffma2(v01, xv[b].a, a[r][b][blk]);
+                    a[r][b][blk] = ffma2(v23, xv[b].b, a[r][b][blk]);
                 }
             }
         }
@@ -438,20 +444,27 @@ __device__ __forceinline__ void run_item(const uint8_t* const (&rp)[R], int G, c
 
 // ---------------------------------------------------------------- reduction
 
-// sum of r[j], r[j + 8], r[j + 16], ... (< U) in that order; loads issued
-// eight at a time so their latencies overlap
-__device__ __forceinline__ float lane_sum8(const float* r, int j, int U) {
-    float acc = 0.f;
-    int G = j;
-    for (; G + 56 < U; G += 64) {
-        float v[8];
+// s1 = r[j] + r[j + 8] + r[j + 16] + ... (< U) in that order, and the same
+// for r2 when `two`; the loads of a round of eight (both rows) are issued
+// before any add, so their latencies overlap (absent terms add +0).
+__device__ __forceinline__ void lane_sums(const float* r, const float* r2, bool two, int j, int U,
+                                          float& s1, float& s2) {
+    s1 = 0.f;
+    s2 = 0.f;
+    for (int G0 = j; G0 < U; G0 += 64) {
+        float v[8], u[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = r[G + 8 * k];
+        for (int k = 0; k < 8; ++k) {
+            const bool in = G0 + 8 * k < U;
+            v[k] = in ? r[G0 + 8 * k] : 0.f;
+            u[k] = (in && two) ? r2[G0 + 8 * k] : 0.f;
+        }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc += v[k];
+        for (int k = 0; k < 8; ++k) {
+            s1 += v[k];
+            s2 += u[k];
+        }
     }
-    for (; G < U; G += 8) acc += r[G];
-    return acc;
 }
 
 // Sum the per-group partials of tile t (segment S) into y, with the gated
@@ -480,21 +493,15 @@ __device__ __forceinline__ void reduce_tile(const QmvParams& P, const Seg& S, in
         const int o = ob + (lane >> 3);
         const bool live = o < n_out;
         const int oo = live ? o : 0;
-        const float* rr = red + (size_t)oo * UP;
-        const float vg0 = lane_sum8(rr, j, U);
-        float vg = vg0;
-        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 1);
-        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 2);
-        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 4);
-        float v = vg;
-        if (mode != MODE_PLAIN) {
-            const float* ru = up_plane + (size_t)oo * UP;
-            float vu = lane_sum8(ru, j, U);
-            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 1);
-            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 2);
-            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, 4);
-            v = act_q(S.act, vg) * vu;
+        const bool pair = mode != MODE_PLAIN;
+        float vg, vu;
+        lane_sums(red + (size_t)oo * UP, up_plane + (size_t)oo * UP, pair, j, U, vg, vu);
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+            vg += __shfl_xor_sync(0xFFFFFFFFu, vg, m);
+            vu += __shfl_xor_sync(0xFFFFFFFFu, vu, m);
         }
+        const float v = pair ? act_q(S.act, vg) * vu : vg;
         const int pi = oo / B, b = oo % B;
         if (live && j == 0 && b < nval) y[(int64_t)(boff + b) * ldy + o0 + pi] = v;
     }
@@ -529,8 +536,8 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         // ------------------------------------------------ producer warp
         // Streams tile n into stage n % S once the consumers released tile
         // n - S, then reduces tile n - S (its partials are complete when that
-        // stage's empty barrier completes).  The last S tiles are reduced by
-        // the consumer warps after their loop.
+        // stage's empty barrier completes).  After the last issue it goes on
+        // reducing all but the last two tiles, which the consumer warps share.
         const uint64_t policy = policy_evict_first();
         Walk w = walk0;
         if (!P.dev_counts) {
@@ -556,6 +563,14 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
         bool ok = true;
+        int nr = 0, ntiles = 0;           // tiles reduced / issued
+        auto reduce_next = [&]() {
+            __syncwarp();
+            reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)(nr % NRED) * red_tile, lane, 0, 1);
+            ++nr;
+            wr.t += wr.step;
+            walk_fix<B>(sm.segs, P.nseg, wr);
+        };
         for (int n = 0, s = 0; w.t < w.end; ++n) {
             if (*reinterpret_cast<volatile int*>(sm.abort_flag)) break;
             if (n >= S_) {            // wait until the consumers released stage s
@@ -580,15 +595,20 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.full[s]);
             }
-            if (n >= S_) {
-                __syncwarp();
-                reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)((n - S_) % NRED) * red_tile, lane, 0, 1);
-                wr.t += wr.step;
-                walk_fix<B>(sm.segs, P.nseg, wr);
-            }
+            if (n >= S_) reduce_next();   // tile n - S
             w.t += w.step;
             walk_fix<B>(sm.segs, P.nseg, w);
             if (++s == S_) s = 0;
+            ntiles = n + 1;
+        }
+        // tiles before the last two are reduced here while the consumers
+        // finish; the consumer warps share the last two
+        while (ok && nr < ntiles - 2 && !*reinterpret_cast<volatile int*>(sm.abort_flag)) {
+            const int s2 = nr % S_;
+            if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s2], (ephase >> s2) & 1u, P.timeout_ns);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            ephase ^= 1u << s2;
+            if (ok) reduce_next();
         }
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
@@ -606,9 +626,9 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
 
     // ---------------------------------------------------- consumer warps
     // Per tile: wait for the stage, run the items, write the partials into
-    // slot n % (S + 1), release the stage (the producer reduces the tile S
-    // tiles later).  After the loop the consumer warps share the reduction
-    // of the last S tiles.
+    // slot n % (S + 1), release the stage (the producer reduces the tile
+    // later).  After the loop the consumer warps share the reduction of the
+    // last two tiles.
     Walk w = walk0;
     int cur_seg = -1;
     uint32_t fphase = 0;
@@ -622,7 +642,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     const int dG = NCT % U, dRow = (NCT / U) * R;
     pdl_wait();                          // x and device row counts come from the preceding kernel
     walk_fix<B>(sm.segs, P.nseg, w);
-    int slot_n = 0, ntl = 0;
+    int slot_n = 0, ntl = 0, last_hint = 0, last_t = 0, prev_hint = 0, prev_t = 0;
     for (int n = 0, s = 0; w.t < w.end; ++n) {
         const Seg& S = sm.segs[w.hint];
         if (w.hint != cur_seg) {
@@ -675,35 +695,35 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         // order) also publishes the partials to whoever reduces the tile
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);
+        prev_hint = last_hint;
+        prev_t = last_t;
+        last_hint = w.hint;
+        last_t = w.t;
         w.t += w.step;
         walk_fix<B>(sm.segs, P.nseg, w);
         if (++s == S_) s = 0;
         if (++slot_n == NRED) slot_n = 0;
         ntl = n + 1;
     }
-    // the last S tiles: tile m's partials are complete when the empty
-    // barrier of stage m % S completes its use m / S
-    if (!aborted) {
-        Walk wr = walk0;
-        walk_fix<B>(sm.segs, P.nseg, wr);
-        for (int m = 0; m < ntl; ++m) {
-            if (m >= ntl - S_) {
-                bool ok = true;
-                if (lane == 0)
-                    ok = mbar_wait_bounded(&sm.empty[m % S_], (uint32_t)(m / S_) & 1u, P.timeout_ns);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_status(P.status, STATUS_TIMEOUT);
-                        atomicExch(sm.abort_flag, 1);
-                    }
-                    break;
-                }
-                reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)(m % NRED) * red_tile, lane, warp, NC);
+    // the last two tiles, shared by the consumer warps (passes of the second
+    // assigned from the last warp down); tile m's partials are complete when
+    // the empty barrier of stage m % S completes its use m / S
+    for (int k = 0; k < 2 && !aborted; ++k) {
+        const int m = ntl - 2 + k;
+        if (m < 0) continue;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(&sm.empty[m % S_], (uint32_t)(m / S_) & 1u, P.timeout_ns);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) {
+            aborted = true;
+            if (lane == 0) {
+                record_status(P.status, STATUS_TIMEOUT);
+                atomicExch(sm.abort_flag, 1);
             }
-            wr.t += wr.step;
-            walk_fix<B>(sm.segs, P.nseg, wr);
+            break;
         }
+        reduce_tile<B>(P, sm.segs[k ? last_hint : prev_hint], k ? last_t : prev_t,
+                       sm.red + (size_t)(m % NRED) * red_tile, lane, k ? NC - 1 - warp : warp, NC);
     }
 }
 
