@@ -92,7 +92,8 @@ int fmt_mask(const std::vector<int>& fmts) {
     return (m == 5 || m == 6) ? 7 : m;
 }
 
-bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPlan& p) {
+bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPlan& p,
+              int64_t rows = 0, int ctas = 0) {
     if (cols % 64 != 0 || cols <= 0 || cols > (1 << 20)) return false;
     const int64_t U = cols / 64;
     if (U > 512) return false;
@@ -107,6 +108,8 @@ bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPl
     const int64_t unitrows = R * m;            // rows per tile step
     int64_t jmax = std::max<int64_t>(1, (32 * 1024) / (unitrows * rbmax));
     jmax = std::min<int64_t>(jmax, 8);
+    // small matrices: keep at least `ctas` tiles so every CTA slot has work
+    if (rows > 0 && ctas > 0) jmax = std::min<int64_t>(jmax, std::max<int64_t>(1, rows / (unitrows * ctas)));
     int64_t j = 0;
     for (int64_t jj = jmax; jj >= 1; --jj) {
         const int64_t RT = unitrows * jj;
@@ -153,8 +156,10 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     }
     bool xal = true;                // the kernel stages x with 16-byte loads
     for (auto& s : segs) xal = xal && al(s.x, 16);
+    int64_t rows = 0;               // matrix rows over all segments and batch chunks
+    for (auto& s : segs) rows += (s.mode == MODE_PLAIN ? 1 : 2) * (int64_t)s.nout;
     QPlan pl;
-    if (fmts.size() > 2 || !xal || !plan_qmv(B, cols, fmts, pairs, pl)) {
+    if (fmts.size() > 2 || !xal || !plan_qmv(B, cols, fmts, pairs, pl, rows, 2 * dev->sms)) {
         for (auto& s : segs) {
             if (s.nout <= 0) continue;
             cudaError_t e = launch_direct(s, cols, B, st);
