@@ -100,9 +100,10 @@ bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPl
     const int R = qmv_rows_per_item(B, fmt_mask(fmts));
     int64_t m = 1;
     while ((U * m) % 32) m *= 2;
-    while (U * m / 32 < 4 && U * m / 32 * 2 <= 8) m *= 2;
+    const int ncmax = qmv_max_consumer_warps(R);
+    while (U * m / 32 < 4 && U * m / 32 * 2 <= ncmax) m *= 2;
     const int64_t NC = U * m / 32;
-    if (NC > 8) return false;
+    if (NC > ncmax) return false;
     int64_t rbmax = 0;
     for (int f : fmts) rbmax = std::max<int64_t>(rbmax, rowbytes(f, cols));
     const int64_t unitrows = R * m;            // rows per tile step

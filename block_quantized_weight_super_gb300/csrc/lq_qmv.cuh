@@ -30,10 +30,16 @@ struct QmvParams {
 };
 
 // Rows of W per work item for batch width B and block-format mask (bit 0
-// Q4_K, bit 1 Q6_K, bit 2 Q8_0): as many as the registers allow.
+// Q4_K, bit 1 Q6_K, bit 2 Q8_0): as many as the registers allow.  Batch 1
+// Q4_K / Q8_0 items take four rows (x reads shared by more rows); Q6_K items,
+// which need more registers per row, two.
 __host__ __device__ constexpr int qmv_rows_per_item(int B, int mask) {
-    return (void)mask, B == 1 ? 2 : 1;
+    return B == 1 ? ((mask & 2) ? 2 : 4) : 1;
 }
+
+// Consumer warps at most: four-row items use 128 registers per thread, so
+// their CTAs are limited to 256 threads (two CTAs per SM).
+__host__ __device__ constexpr int qmv_max_consumer_warps(int R) { return R == 4 ? 7 : 8; }
 
 // Row stride of the per-group partials: at least U and 8 mod 32, so the
 // reduction's four concurrent rows fall in distinct banks.
