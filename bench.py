@@ -45,8 +45,8 @@ METRIC = "effective weight GB/s per quantized matvec (decode layer, batch 1)"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=8 * NLAYERS)
+    ap.add_argument("--warmup", type=int, default=NLAYERS)
     ap.add_argument("--impl", default="lq", choices=["lq", "reference"])
     ap.add_argument("--layers", type=int, default=NLAYERS)
     ap.add_argument("--no-e2e", action="store_true")
