@@ -47,6 +47,7 @@ struct DevInfo {
     bool init = false;
     int sms = 0;
     unsigned* status = nullptr;
+    int qmm_res[3] = {0, 0, 0};   // resident tensor-core CTAs / clusters of 2 / of 4
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -68,7 +69,12 @@ int dev_info(DevInfo** out) {
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmm_set_smem((int)qmm_smem_bytes(QMM_STAGES, QMM_MAX_CSIZE));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+        for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE; ++i, cs *= 2) {
+            e = qmm_max_resident(cs, qmm_smem_bytes(QMM_STAGES, cs), d.sms, &d.qmm_res[i]);
+            if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
+        }
         d.init = true;
     }
     *out = &d;
@@ -231,6 +237,75 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     return LQ_OK;
 }
 
+// ---------------------------------------------------------------- tensor-core path
+// Q4_K segments of up to QMM_NT x rows whose columns are a multiple of the
+// tile width, with 16-byte aligned weights and x (1-D bulk copies).
+bool qmm_eligible(const std::vector<Seg>& segs, int64_t cols) {
+    if (cols % QMM_KC != 0 || cols > (1 << 20)) return false;
+    for (auto& s : segs) {
+        if (s.fmt != FMT_Q4_K) return false;
+        if (!al(s.w, 16) || (s.w2 && !al(s.w2, 16)) || !al(s.x, 16)) return false;
+    }
+    return true;
+}
+
+// Run segments on the tensor-core kernel.  Row blocks are QMM_RT weight rows
+// (pairs count twice); a cluster of csize CTAs splits a row block's column
+// chunks when there are too few row blocks to fill the resident CTAs.
+int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    const int nchunk = (int)(cols / QMM_KC);
+    auto blocks_of = [](const Seg& s) {
+        const int64_t r = (s.mode == MODE_PLAIN ? 1 : 2) * (int64_t)s.nout;
+        return (r + QMM_RT - 1) / QMM_RT;
+    };
+    int64_t nb_all = 0;
+    for (auto& s : segs) nb_all += blocks_of(s);
+    if (nb_all == 0) return LQ_OK;
+    // cluster size: fewest (rounds of row blocks) x (chunks per CTA), a small
+    // charge per extra rank for the partial-sum exchange
+    int ci = 0;
+    double best = 0.0;
+    for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE && cs <= nchunk; ++i, cs *= 2) {
+        const int res = dev->qmm_res[i];
+        if (res < 1) continue;
+        const double t = (double)((nb_all + res - 1) / res) * ((nchunk + cs - 1) / cs) * (1.0 + 0.05 * (cs - 1));
+        if (best == 0.0 || t < best) {
+            best = t;
+            ci = i;
+        }
+    }
+    const int cs = 1 << ci, res = std::max(1, dev->qmm_res[ci]);
+    const size_t smem = qmm_smem_bytes(QMM_STAGES, cs);
+    for (size_t s0 = 0; s0 < segs.size(); s0 += MAX_SEG) {
+        QmmParams P;
+        memset(&P, 0, sizeof P);
+        int t = 0, n = 0;
+        for (size_t i = s0; i < segs.size() && i < s0 + MAX_SEG; ++i) {
+            Seg s = segs[i];
+            s.tile0 = t;
+            s.ntiles = (int32_t)blocks_of(s);
+            t += s.ntiles;
+            P.seg[n++] = s;
+        }
+        if (t == 0) continue;
+        P.nseg = n;
+        P.nblocks = t;
+        P.cols = (int32_t)cols;
+        P.nchunk = nchunk;
+        P.nstages = QMM_STAGES;
+        P.csize = cs;
+        P.timeout_ns = g_timeout_ns.load();
+        P.status = dev->status;
+        const int grid = cs * std::min(res, t);
+        cudaError_t e = qmm_launch(P, grid, smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec launch");
+    }
+    return LQ_OK;
+}
+
 // Widest batch width (4, 2 or 1) the quantized matvec kernel can plan for
 // these columns and formats (x for B rows must fit in shared memory).
 int batch_width(int64_t cols, int batch, const std::vector<int>& fmts, bool pairs) {
@@ -332,6 +407,12 @@ int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
     if (rows == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
+    if (batch >= QMM_MIN_BATCH && fmt == FMT_Q4_K) {
+        std::vector<Seg> segs;
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT)
+            segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(QMM_NT, batch - b0)));
+        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
+    }
     const int B = batch_width(cols, batch, {fmt}, false);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B)
@@ -353,6 +434,16 @@ int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int
     if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
         (nv && (rc = check_f32(v, "v"))))
         return rc;
+    if (batch >= QMM_MIN_BATCH) {
+        std::vector<Seg> segs;
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
+            const int nb = std::min(QMM_NT, batch - b0);
+            if (nq) segs.push_back(plain_seg(fq, Wq, nq, x, q, nq, b0, nb));
+            if (nk) segs.push_back(plain_seg(fk, Wk, nk, x, k, nk, b0, nb));
+            if (nv) segs.push_back(plain_seg(fv, Wv, nv, x, v, nv, b0, nb));
+        }
+        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
+    }
     const int B = batch_width(cols, batch, {fq, fk, fv}, false);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B) {
@@ -388,6 +479,16 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
     if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
     if (inter == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
+    if (batch >= QMM_MIN_BATCH && fmt == FMT_Q4_K) {
+        std::vector<Seg> segs;
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
+            Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(QMM_NT, batch - b0));
+            s.mode = MODE_PAIR_INTERLEAVED;
+            s.act = act;
+            segs.push_back(s);
+        }
+        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
+    }
     const int B = batch_width(cols, batch, {fmt}, true);
     std::vector<Seg> segs;
     for (int b0 = 0; b0 < batch; b0 += B) {
@@ -454,8 +555,12 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
     if (e != cudaSuccess) return cuda_fail(e, "moe route launch");
 
     // grouped expert gate+up (+SwiGLU): segment per (expert, chunk of B rows)
+    // tensor-core path: Q4_K, both widths multiples of the tile, aligned rows
+    bool tc = ntok >= QMM_MOE_MIN_TOKENS && fmt == FMT_Q4_K && hidden % QMM_KC == 0 &&
+              inter % QMM_KC == 0 && al(X, 16);
+    for (int ex = 0; tc && ex < E; ++ex) tc = al(W1[ex], 16) && al(W3[ex], 16) && al(W2[ex], 16);
     {
-        const int B = batch_width(hidden, ntok, {fmt}, true);
+        const int B = tc ? QMM_NT : batch_width(hidden, ntok, {fmt}, true);
         std::vector<Seg> segs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {
@@ -476,11 +581,12 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
                 s.b0 = c * B;
                 segs.push_back(s);
             }
-        if ((rc = run_segments(segs, B, hidden, st))) return rc;
+        rc = tc ? run_qmm(segs, hidden, st) : run_segments(segs, B, hidden, st);
+        if (rc) return rc;
     }
     // grouped expert down: x rows are the grouped hidden activations
     {
-        const int B = batch_width(inter, ntok, {fmt}, false);
+        const int B = tc ? QMM_NT : batch_width(inter, ntok, {fmt}, false);
         std::vector<Seg> segs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {
@@ -498,7 +604,8 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
                 s.b0 = c * B;
                 segs.push_back(s);
             }
-        if ((rc = run_segments(segs, B, inter, st))) return rc;
+        rc = tc ? run_qmm(segs, inter, st) : run_segments(segs, B, inter, st);
+        if (rc) return rc;
     }
     e = launch_moe_combine(ws.ybuf, hidden, ntok, topk, ws, Y, st);
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "moe combine launch");

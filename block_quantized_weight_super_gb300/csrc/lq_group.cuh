@@ -158,6 +158,34 @@ __device__ __forceinline__ Q4Sel q4_sel(int g) {
 
 
 
+// Scales and re-centring of the two sub-blocks (2g, 2g+1) of quant group g
+// of a Q4_K super-block (hdr = its first 16 bytes: d, dmin, scales):
+// dsc = d*sc and dm = dmin*m exactly in fp32, the centre
+// qb = round(dm / dsc) clamped to [-16, 15], and e = dsc*qb - dm (one
+// rounding).  magic = 0x64006400 (half2 1024, 1024).
+struct Q4Cent {
+    float dsc0, dsc1, qb0, qb1, e0, e1;
+};
+
+__device__ __forceinline__ Q4Cent q4k_centres(const uint4 hdr, const Q4Sel& sl, uint32_t magic) {
+    const uint32_t s_sc = sl.hi ? hdr.w : hdr.y;
+    const uint32_t s_m = sl.hi ? (hdr.w >> 4) : hdr.z;
+    const uint32_t scw = ((s_sc >> sl.sh) & sl.mlo) | ((hdr.y >> (sl.sh + 2)) & sl.mhi);
+    const uint32_t mw = ((s_m >> sl.sh) & sl.mlo) | ((hdr.z >> (sl.sh + 2)) & sl.mhi);
+    const uint32_t sc_h = hsub2_u32(__byte_perm(scw, magic, 0x7150), magic);
+    const uint32_t m_h = hsub2_u32(__byte_perm(mw, magic, 0x7150), magic);
+    Q4Cent q;
+    q.dsc0 = hmul_lo_lo(hdr.x, sc_h, 0.0f);
+    q.dsc1 = hmul_lo_hi(hdr.x, sc_h, 0.0f);
+    const float dm0 = hmul_hi_lo(hdr.x, m_h, 0.0f);
+    const float dm1 = hmul_hi_hi(hdr.x, m_h, 0.0f);
+    q.qb0 = rintf(fminf(fmaxf(dm0 * rcp_approx(q.dsc0), -16.0f), 15.0f));
+    q.qb1 = rintf(fminf(fmaxf(dm1 * rcp_approx(q.dsc1), -16.0f), 15.0f));
+    q.e0 = fmaf(q.dsc0, q.qb0, -dm0);
+    q.e1 = fmaf(q.dsc1, q.qb1, -dm1);
+    return q;
+}
+
 // 32-bit word at a 2-byte-aligned shared address
 // (the aligned address is formed by pointer arithmetic, not an integer
 // round trip, so the compiler keeps the shared address space: LDS, not LD)

@@ -19,6 +19,31 @@ struct MoeWs {
     float* ybuf;         // [ntok*topk][hidden] expert outputs
 };
 
+// tensor-core matvec for up to QMM_NT x rows of Q4_K (lq_qmm.cu): tiles of
+// QMM_RT weight rows x QMM_KC columns; segments' tile0 = first row block.
+constexpr int QMM_NT = 8;
+constexpr int QMM_RT = 64;
+constexpr int QMM_KC = 512;
+struct QmmParams {
+    Seg seg[MAX_SEG];
+    int32_t nseg;
+    int32_t nblocks;         // row blocks over all segments
+    int32_t cols;
+    int32_t nchunk;          // cols / QMM_KC
+    int32_t nstages;
+    int32_t csize;           // CTAs per cluster splitting a row block's columns (1, 2 or 4)
+    uint64_t timeout_ns;
+    unsigned* status;
+};
+constexpr int QMM_MAX_CSIZE = 4;
+constexpr int QMM_STAGES = 2;
+constexpr int QMM_MIN_BATCH = 3;          // dense calls with at least this many x rows
+constexpr int QMM_MOE_MIN_TOKENS = 2;     // MoE calls with at least this many tokens
+cudaError_t qmm_set_smem(int bytes);
+size_t qmm_smem_bytes(int nstages, int csize);
+cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out);
+cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t st);
+
 // quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
 cudaError_t qmv1_set_smem(int bytes);
 cudaError_t qmv2_set_smem(int bytes);

@@ -126,10 +126,6 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, uint
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ void consumer_sync(int nct) {
     asm volatile("bar.sync 1, %0;" ::"r"(nct) : "memory");
 }
@@ -223,23 +219,14 @@ struct Q4Row {
 // Scales of quant group g of a Q4_K super-block (see lq_group.cuh) and the
 // re-centring constants of its two sub-blocks.
 __device__ __forceinline__ Q4Row q4k_row(const uint4 hdr, const Q4Sel& sl, const GroupConsts& K) {
-    const uint32_t s_sc = sl.hi ? hdr.w : hdr.y;
-    const uint32_t s_m = sl.hi ? (hdr.w >> 4) : hdr.z;
-    const uint32_t scw = ((s_sc >> sl.sh) & sl.mlo) | ((hdr.y >> (sl.sh + 2)) & sl.mhi);
-    const uint32_t mw = ((s_m >> sl.sh) & sl.mlo) | ((hdr.z >> (sl.sh + 2)) & sl.mhi);
-    const uint32_t sc_h = hsub2_u32(__byte_perm(scw, K.magic, 0x7150), K.magic);
-    const uint32_t m_h = hsub2_u32(__byte_perm(mw, K.magic, 0x7150), K.magic);
+    const Q4Cent c = q4k_centres(hdr, sl, K.magic);
     Q4Row q;
-    q.dsc0 = hmul_lo_lo(hdr.x, sc_h, 0.0f);
-    q.dsc1 = hmul_lo_hi(hdr.x, sc_h, 0.0f);
-    const float dm0 = hmul_hi_lo(hdr.x, m_h, 0.0f);
-    const float dm1 = hmul_hi_hi(hdr.x, m_h, 0.0f);
-    const float qb0 = rintf(fminf(fmaxf(dm0 * rcp_approx(q.dsc0), -16.0f), 15.0f));
-    const float qb1 = rintf(fminf(fmaxf(dm1 * rcp_approx(q.dsc1), -16.0f), 15.0f));
-    q.e0 = fmaf(q.dsc0, qb0, -dm0);
-    q.e1 = fmaf(q.dsc1, qb1, -dm1);
-    q.c0 = -1024.0f - qb0;
-    q.c1 = fmaf(qb1, -16.0f, -1024.0f);
+    q.dsc0 = c.dsc0;
+    q.dsc1 = c.dsc1;
+    q.e0 = c.e0;
+    q.e1 = c.e1;
+    q.c0 = -1024.0f - c.qb0;
+    q.c1 = fmaf(c.qb1, -16.0f, -1024.0f);
     return q;
 }
 

@@ -108,9 +108,21 @@ def test_matvec_unaligned_weight_base(lq, fmt):
     assert_within(host(yb), ref, oracle.matvec_bound(S), "unaligned")
 
 
-@pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336)])
+# Q4_K calls with at least this many x rows and columns a multiple of 512
+# run on the tensor cores (a different summation order from the batch-1
+# kernel, so only the oracle's bound relates the two).
+TC_MIN_BATCH = 3
+
+
+def _tensor_path(fmt, cols, M):
+    return fmt == Q4_K and cols % 512 == 0 and M >= TC_MIN_BATCH
+
+
+@pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336), (Q4_K, 2304)])
 def test_batch_invariance(lq, fmt, cols):
-    """row b of a batch-M call is bit-identical to a batch-1 call on x_b."""
+    """row b of a batch-M call is bit-identical to the same x row in any other
+    call that takes the same kernel: a batch-1 call for the CUDA-core kernel,
+    the batch-8 call for the tensor-core one (each x row is its own MMA column)."""
     rows = 67
     g = synth.rng(11)
     W = synth.weights(g, fmt, rows, cols)
@@ -121,12 +133,18 @@ def test_batch_invariance(lq, fmt, cols):
         y1 = empty((1, rows))
         lq.lq_matvec(fmt, Wd, rows, cols, dev(X[b:b + 1]), y1, 1)
         singles.append(host(y1)[0])
-    for M in (2, 3, 4, 8):
+    y8 = empty((8, rows))
+    lq.lq_matvec(fmt, Wd, rows, cols, dev(X), y8, 8)
+    full = host(y8)
+    ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
+    for M in (2, 3, 4, 5, 8):
         yM = empty((M, rows))
         lq.lq_matvec(fmt, Wd, rows, cols, dev(X[:M]), yM, M)
         got = host(yM)
         for b in range(M):
-            assert np.array_equal(got[b], singles[b]), (M, b)
+            same = full[b] if _tensor_path(fmt, cols, M) else singles[b]
+            assert np.array_equal(got[b], same), (M, b)
+        assert_within(got, ref[:M], oracle.matvec_bound(S[:M]), f"batch {M}")
 
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
@@ -169,7 +187,7 @@ def test_matvec_zero_rows_and_zero_x(lq):
 # ---------------------------------------------------------------- QKV
 
 @pytest.mark.parametrize("fq,fk,fv", [(Q4_K, Q4_K, Q6_K), (Q4_K, Q4_K, Q4_K), (Q8_0, Q8_0, Q8_0)])
-@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
 def test_qkv_mixed(lq, fq, fk, fv, batch):
     cols, nq, nk, nv = 2560, 300, 100, 100
     g = synth.rng(14)
@@ -182,9 +200,10 @@ def test_qkv_mixed(lq, fq, fk, fv, batch):
         ref, S = oracle.matvec(f, W, n, cols, x, NTH)
         got = host(out)
         assert_within(got, ref, oracle.matvec_bound(S), f"qkv fmt {f}")
-        single = empty((batch, n))
-        lq.lq_matvec(f, dev(W), n, cols, xd, single, batch)
-        assert np.array_equal(got, host(single))        # same code path, same bits
+        if batch < TC_MIN_BATCH:
+            single = empty((batch, n))
+            lq.lq_matvec(f, dev(W), n, cols, xd, single, batch)
+            assert np.array_equal(got, host(single))    # same code path, same bits
 
 
 # ---------------------------------------------------------------- gate + up
@@ -220,6 +239,70 @@ def test_ffn_gate_up_act(lq, fmt, inter, cols, batch, act):
     # argument z (at most ~1.4 u |g| in act)
     tol = 16 * oracle.U32 * np.abs(a * u64) + 4 * oracle.U32 * np.abs(g64 * u64) + 1e-30
     assert_within(got, a * u64, tol, "epilogue")
+
+
+# ---------------------------------------------------------------- tensor-core path
+
+@pytest.mark.parametrize("rows,cols,batch", [
+    (67, 512, 3),        # one chunk, a ragged second row block
+    (130, 1024, 9),      # a full pass of 8 x rows and a pass of 1
+    (64, 2560, 16),      # two full passes, one row block
+    (333, 14336, 5),     # 28 column chunks split over a cluster
+    (1, 512, 8),         # a single weight row
+    (1000, 4096, 8),     # many row blocks
+])
+def test_tensor_core_matvec(lq, rows, cols, batch):
+    g = synth.rng(rows * 3 + cols + batch)
+    W = synth.weights(g, Q4_K, rows, cols)
+    x = synth.activations(g, batch, cols)
+    y = empty((batch, rows))
+    lq.lq_matvec(Q4_K, dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(Q4_K, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"tc {rows}x{cols} b{batch}")
+
+
+def test_tensor_core_extreme_scales(lq):
+    """fp16 scale extremes (subnormal d, 65504 dmin, zero scales) through the
+    tensor-core path: the bf16 codes q - qb are exact whatever the scales."""
+    rows, cols, batch = 70, 1024, 6
+    g = synth.rng(77)
+    W = synth.q4k(g, rows, cols).copy()
+    blk = W.reshape(rows, cols // 256, 144)
+    blk[0::7, :, 0:2] = np.frombuffer(np.float16(2.0 ** -24).tobytes(), np.uint8)
+    blk[1::7, :, 2:4] = np.frombuffer(np.float16(65504.0).tobytes(), np.uint8)
+    blk[2::7, :, 4:16] = 0
+    x = synth.activations(g, batch, cols)
+    y = empty((batch, rows))
+    lq.lq_matvec(Q4_K, dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(Q4_K, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), "tc extremes")
+
+
+def test_tensor_core_misaligned_weights_fall_back(lq):
+    """a 2-byte offset weight base cannot be bulk-copied by rows: the call
+    takes the CUDA-core kernel, with the same bound."""
+    rows, cols, batch = 45, 1024, 4
+    g = synth.rng(78)
+    W = synth.q4k(g, rows, cols)
+    x = synth.activations(g, batch, cols)
+    keep, p = dev(W, offset_bytes=2)
+    y = empty((batch, rows))
+    lq.lq_matvec(Q4_K, p, rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(Q4_K, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), "fallback")
+
+
+@pytest.mark.parametrize("E,topk,ntok", [(4, 2, 6), (8, 2, 16), (3, 1, 20)])
+def test_tensor_core_moe(lq, E, topk, ntok):
+    """grouped experts with widths that take the tensor-core path (an expert
+    may see more than 8 tokens: two passes)."""
+    hidden, inter = 512, 1024
+    R, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=E * 7 + ntok)
+    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X, topk)
+    _, _, lg, labs = oracle.moe_route(R, X, topk)
+    chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X, lg, labs, idx, NTH)
+    assert chk["admissible"].all()
+    assert_within(Y, chk["Y"], chk["bound"], "tc moe Y")
 
 
 # ---------------------------------------------------------------- MoE
