@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/lq.h"
@@ -69,10 +70,10 @@ int dev_info(DevInfo** out) {
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
-        if (e == cudaSuccess) e = qmm_set_smem((int)qmm_smem_bytes(QMM_STAGES, QMM_MAX_CSIZE));
+        if (e == cudaSuccess) e = qmm_set_smem((int)qmm_smem_bytes(3, QMM_MAX_CSIZE));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE; ++i, cs *= 2) {
-            e = qmm_max_resident(cs, qmm_smem_bytes(QMM_STAGES, cs), d.sms, &d.qmm_res[i]);
+            e = qmm_max_resident(cs, qmm_smem_bytes(qmm_stages_for(cs), cs), d.sms, &d.qmm_res[i]);
             if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
         }
         d.init = true;
@@ -237,9 +238,69 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     return LQ_OK;
 }
 
+// ---------------------------------------------------------------- tensor maps
+// 2-D tensor maps over quantized matrices (uint32 elements, a matrix row per
+// tensor row), encoded once per (base, rows, row bytes, stride, box rows)
+// through the driver entry point and cached.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapKey {
+    const void* base;
+    int64_t rows, rowbytes, stride;
+    int box_rows;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && rowbytes == o.rowbytes && stride == o.stride &&
+               box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.base);
+        for (int64_t v : {k.rows, k.rowbytes, k.stride, (int64_t)k.box_rows})
+            h = h * 1000003u ^ std::hash<int64_t>()(v);
+        return h;
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+EncodeTiledFn g_encode = nullptr;
+
+int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbytes, int64_t stride, int box_rows) {
+    const MapKey key{base, rows, rowbytes, stride, box_rows};
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+        *out = it->second;
+        return LQ_OK;
+    }
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(LQ_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)(rowbytes / 4), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride};
+    const cuuint32_t box[2] = {(cuuint32_t)(QMM_KC / 256 * 144 / 4), (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LQ_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    if (g_maps.size() >= 4096) g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return LQ_OK;
+}
+
 // ---------------------------------------------------------------- tensor-core path
 // Q4_K segments of up to QMM_NT x rows whose columns are a multiple of the
-// tile width, with 16-byte aligned weights and x (1-D bulk copies).
+// tile width, with 16-byte aligned weights and x (tensor maps, bulk copies).
 bool qmm_eligible(const std::vector<Seg>& segs, int64_t cols) {
     if (cols % QMM_KC != 0 || cols > (1 << 20)) return false;
     for (auto& s : segs) {
@@ -278,16 +339,28 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
         }
     }
     const int cs = 1 << ci, res = std::max(1, dev->qmm_res[ci]);
-    const size_t smem = qmm_smem_bytes(QMM_STAGES, cs);
-    for (size_t s0 = 0; s0 < segs.size(); s0 += MAX_SEG) {
+    const int nstages = qmm_stages_for(cs);
+    const size_t smem = qmm_smem_bytes(nstages, cs);
+    const int64_t rb = cols / 256 * 144;
+    for (size_t s0 = 0; s0 < segs.size(); s0 += QMM_MAX_SEG) {
         QmmParams P;
         memset(&P, 0, sizeof P);
         int t = 0, n = 0;
-        for (size_t i = s0; i < segs.size() && i < s0 + MAX_SEG; ++i) {
+        for (size_t i = s0; i < segs.size() && i < s0 + QMM_MAX_SEG; ++i) {
             Seg s = segs[i];
             s.tile0 = t;
             s.ntiles = (int32_t)blocks_of(s);
             t += s.ntiles;
+            if (s.mode == MODE_PLAIN) {
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, QMM_RT);
+            } else if (s.mode == MODE_PAIR_TWO) {
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, QMM_PAIR_BOX);
+                if (!rc) rc = tensor_map(&P.tm[n][1], s.w2, s.nout, rb, rb, QMM_PAIR_BOX);
+            } else {                        // packed gate / up: rows 2i and 2i + 1
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, 2 * rb, QMM_PAIR_BOX);
+                if (!rc) rc = tensor_map(&P.tm[n][1], s.w + rb, s.nout, rb, 2 * rb, QMM_PAIR_BOX);
+            }
+            if (rc) return rc;
             P.seg[n++] = s;
         }
         if (t == 0) continue;
@@ -295,7 +368,7 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
         P.nblocks = t;
         P.cols = (int32_t)cols;
         P.nchunk = nchunk;
-        P.nstages = QMM_STAGES;
+        P.nstages = nstages;
         P.csize = cs;
         P.timeout_ns = g_timeout_ns.load();
         P.status = dev->status;

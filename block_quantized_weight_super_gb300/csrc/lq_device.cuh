@@ -163,6 +163,19 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, unsi
         : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared (a box of the tensor map at
+// coordinates (x, y), x in elements of the innermost dimension), completion
+// signalled on `bar` as tx bytes (the whole box, out-of-range rows zero
+// filled).  dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

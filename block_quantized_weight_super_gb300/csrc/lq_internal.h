@@ -1,6 +1,7 @@
 // lq_internal.h -- launchers shared between the library's translation units.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "lq_qmv.cuh"
@@ -21,11 +22,18 @@ struct MoeWs {
 
 // tensor-core matvec for up to QMM_NT x rows of Q4_K (lq_qmm.cu): tiles of
 // QMM_RT weight rows x QMM_KC columns; segments' tile0 = first row block.
+// Weights are fetched through 2-D tensor maps (uint32 elements, one row of
+// the matrix per tensor row): per segment map 0 is the plain matrix (boxes of
+// QMM_RT rows) or the gate rows of a pair segment, map 1 the up rows (boxes
+// of 8 rows; packed gate/up matrices use a row stride of two rows).
 constexpr int QMM_NT = 8;
 constexpr int QMM_RT = 64;
 constexpr int QMM_KC = 512;
+constexpr int QMM_MAX_SEG = 16;
+constexpr int QMM_PAIR_BOX = 8;
 struct QmmParams {
-    Seg seg[MAX_SEG];
+    CUtensorMap tm[QMM_MAX_SEG][2];
+    Seg seg[QMM_MAX_SEG];
     int32_t nseg;
     int32_t nblocks;         // row blocks over all segments
     int32_t cols;
@@ -36,11 +44,12 @@ struct QmmParams {
     unsigned* status;
 };
 constexpr int QMM_MAX_CSIZE = 4;
-constexpr int QMM_STAGES = 2;
+constexpr int QMM_GROUP = 4;              // row blocks sharing one staging of x
 constexpr int QMM_MIN_BATCH = 3;          // dense calls with at least this many x rows
 constexpr int QMM_MOE_MIN_TOKENS = 2;     // MoE calls with at least this many tokens
 cudaError_t qmm_set_smem(int bytes);
 size_t qmm_smem_bytes(int nstages, int csize);
+int qmm_stages_for(int csize);
 cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out);
 cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t st);
 

@@ -13,30 +13,39 @@
 //    shifted down first) and a bf16x2 subtraction of 128 + qb leaves q - qb.
 //  * B operand: x = hi + lo with hi = bf16(x), lo = bf16(x - hi); the
 //    residual is at most 2^-18 |x|, so the pieces carry x to well inside the
-//    1e-5 relative tolerance.  Columns 0..7 of one MMA are the hi pieces of
-//    the eight x rows, of a second MMA the lo pieces.
+//    1e-5 relative tolerance.  The hi and lo MMAs of a sub-block chain into
+//    one fp32 accumulator (exact products, fp32 sums).
 //  * mma.sync m16n8k16 (bf16 in, fp32 accumulate) over the two 16-column
-//    slices of a sub-block gives sum (q - qb) x_piece for 16 rows x 8 x rows;
-//    the epilogue multiplies by dsc and adds e * sum x into fp32
-//    accumulators held in registers.
-// The k index inside a 16-column slice is permuted identically for A and B:
-// lane (g, c) takes the bytes 4c..4c+3 of a row's 16-byte quant run, bytes
-// (0, 2) fill its k pair (2c, 2c+1), bytes (1, 3) the pair (2c+8, 2c+9).
+//    slices of a sub-block gives sum (q - qb) x for 16 rows x 8 x rows; the
+//    epilogue multiplies by dsc and adds e * sum x (packed fp32 FMAs).
+// The k index of a slice is permuted identically for A and B so that a lane
+// loads its codes for both slices and both nibbles of a 32-byte quant run
+// with one 8-byte shared load: lane (g, c) takes bytes 8c..8c+7 of the run;
+// slice h uses bytes 8c+4h..8c+4h+3, whose bytes (0, 2) fill its k pair
+// (2c, 2c+1) and bytes (1, 3) the pair (2c+8, 2c+9).
 //
-// GB300 structure: a CTA has four consumer warps (16 weight rows each) and a
-// producer warp.  A tile is 64 weight rows x 512 columns plus the eight x
-// rows' 512 columns, streamed into a ring of shared-memory stages by 1-D
-// bulk copies (TMA), one per row, on full / empty mbarriers (bounded waits).
-// A CTA walks its row blocks one after another, all column chunks of a row
-// block in order, so every output's sum runs in a fixed order: the result is
+// GB300 structure: a CTA has eight consumer warps and a producer warp.
+// Tiles are 64 weight rows x 512 columns, streamed into a ring of
+// shared-memory stages by 2-D tensor copies (TMA, one box per tile, or eight
+// 8-row boxes for gate / up pairs) on full / empty mbarriers (bounded waits).
+// Warps w and w + 4 take the same 16 rows, the first and the second
+// super-block of every tile, and add their partial sums at the end.  A cluster of CTAs owns a
+// contiguous range of row blocks and takes them in groups of up to four
+// that read the same x rows; for each column chunk the x rows are staged
+// once (their own bulk copies and barriers), converted once into B
+// fragments and per-sub-block sums, and used by every row block of the
+// group, whose partial sums stay in registers.  Each warp decodes the scales
+// of its own 16 rows into a private table, so a tile needs no CTA-wide
+// barrier.  Every output's sum runs in a fixed order: the result is
 // deterministic.  Matrices with few row blocks (a down projection: 4096 rows
-// but 14336 columns) split the columns over the CTAs of a thread-block
-// cluster: rank r takes an even share of the column chunks, ranks 1.. store
-// their partial sums into rank 0's shared memory (distributed shared memory,
-// an mbarrier per direction, bounded waits) and rank 0 adds them in rank
-// order and writes the outputs.  Gate / up pairs: the producer lays gate row i and up row i
-// of a pair segment out as tile rows 2i and 2i+1 (also for two separate
-// matrices), and the activation is applied across that lane pair.
+// but 14336 columns) split the column chunks over the CTAs of the cluster:
+// ranks 1.. store their partial sums into rank 0's shared memory
+// (distributed shared memory, an mbarrier per direction, bounded waits) and
+// rank 0 adds them in rank order and writes the outputs.  Gate / up pairs:
+// the producer lays the gate rows of pairs 8q .. 8q+7 of a tile out as tile
+// rows 16q .. 16q+7 and their up rows as 16q+8 .. 16q+15 (an MMA lane holds
+// rows g and g + 8), and the activation is
+// applied within the lane that holds both.
 #include "lq_group.cuh"
 #include "lq_internal.h"
 
@@ -46,44 +55,90 @@ namespace {
 constexpr int NT = QMM_NT;                 // x rows per pass
 constexpr int RT = QMM_RT;                 // weight rows per tile
 constexpr int KC = QMM_KC;                 // columns per tile
-constexpr int NW = RT / 16;                // consumer warps
+constexpr int GR = QMM_GROUP;              // row blocks sharing one staging of x
+constexpr int RW = RT / 16;                // warps per column half (16 rows each)
+constexpr int NW = 2 * RW;                 // consumer warps: (row quarter, super-block of the tile)
 constexpr int SB = KC / 32;                // sub-blocks per tile
+constexpr int SBW = SB / 2;                // sub-blocks per warp
 constexpr int WROW = KC / 256 * 144;       // weight bytes of a row per tile
-constexpr int WBYTES = RT * WROW;          // weight bytes per stage
-constexpr int XBYTES = NT * KC * 4;        // x bytes per stage
-constexpr int STAGE = WBYTES + XBYTES;
+constexpr int WSTAGE = RT * WROW;          // weight bytes per stage
+constexpr int XSTR = KC * 4 + 16;          // shared stride of an x row (bank spread)
+static_assert(KC == 512, "a warp takes one super-block of the tile");
+
+// Scales of one (row, sub-block), paired for the packed FMAs of the
+// epilogue: (dsc, dsc, e, e).  The bf16x2 subtrahends 128 + qb of rows g and
+// g + 8 sit side by side in a separate table (one 8-byte load).
+struct SbScale {
+    float dsc, dsc2, e, e2;
+};
+
+struct Layout {
+    size_t wst, xraw, bfr, sx, scl, sub, half, red, bars, total;
+};
+
+__host__ __device__ inline Layout qmm_layout(int nstages, int csize) {
+    Layout L;
+    size_t o = 0;
+    L.wst = o;  o += (size_t)nstages * WSTAGE;
+    L.xraw = o; o += (size_t)NT * XSTR;
+    L.bfr = o;  o += sizeof(uint4) * 2 * SB * 32;
+    L.sx = o;   o += sizeof(float) * SB * NT;
+    L.scl = o;  o += sizeof(SbScale) * NW * SBW * 16;
+    L.sub = o;  o += sizeof(uint32_t) * NW * SBW * 16;
+    L.half = o; o += sizeof(float4) * RW * 32;
+    L.red = o;  o += sizeof(float4) * (csize - 1) * RW * 32;
+    L.bars = o; o += sizeof(uint64_t) * (2 * nstages + 4) + 16;
+    L.total = o;
+    return L;
+}
 
 __device__ __forceinline__ int seg_nval(const Seg& S) {
     int n = S.bcnt ? (*S.bcnt - S.b0) : S.nbatch;
     return n < 0 ? 0 : (n > NT ? NT : n);
 }
 __device__ __forceinline__ int seg_boff(const Seg& S) { return (S.boff ? *S.boff : 0) + S.b0; }
-// weight rows of a segment (pairs count twice)
-__device__ __forceinline__ int seg_rows(const Seg& S) { return S.mode == MODE_PLAIN ? S.nout : 2 * S.nout; }
-
-struct QWalk {
-    int rb, step, end, hint;               // row-block index (global over segments)
-};
-
-__device__ __forceinline__ void qwalk_fix(const Seg* segs, int nseg, QWalk& w) {
-    while (w.rb < w.end) {
-        int s = w.hint;
-        while (s + 1 < nseg && w.rb >= segs[s + 1].tile0) ++s;
-        while (s > 0 && w.rb < segs[s].tile0) --s;
-        w.hint = s;
-        if (seg_nval(segs[s]) > 0) return;
-        w.rb += w.step;
-    }
+__device__ __forceinline__ bool same_x(const Seg& a, const Seg& b) {
+    return a.x == b.x && a.xmap == b.xmap && a.boff == b.boff && a.bcnt == b.bcnt && a.b0 == b.b0 &&
+           a.nbatch == b.nbatch;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                         const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
+// Up to GR row blocks with x rows to process, from [pos, end), all reading
+// the x rows of the first; segments' tile0 = first row block.
+struct Group {
+    int n;
+    int rb[GR];
+    int sg[GR];
+};
+
+__device__ __forceinline__ bool next_group(const Seg* segs, int nseg, int& pos, int end, int& hint, Group& G) {
+    G.n = 0;
+    while (pos < end && G.n < GR) {
+        int s = hint;
+        while (s + 1 < nseg && pos >= segs[s + 1].tile0) ++s;
+        while (s > 0 && pos < segs[s].tile0) --s;
+        hint = s;
+        if (seg_nval(segs[s]) <= 0) {              // nothing to do for this segment
+            pos = min(end, segs[s].tile0 + segs[s].ntiles);
+            continue;
+        }
+        if (G.n > 0 && !same_x(segs[G.sg[0]], segs[s])) break;
+#pragma unroll
+        for (int k = 0; k < GR; ++k)
+            if (k == G.n) {
+                G.rb[k] = pos;
+                G.sg[k] = s;
+            }
+        ++G.n;
+        ++pos;
+    }
+    return G.n > 0;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -99,6 +154,14 @@ __device__ __forceinline__ uint32_t bf16x2_pack(float hi, float lo) {
 }
 __device__ __forceinline__ float bf16_lo_f(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// bf16x2 (v, v) of a float with at most 8 significant bits (exact: the
+// upper half of its fp32 encoding)
+__device__ __forceinline__ uint32_t bf16_dup(float v) { return __byte_perm(__float_as_uint(v), 0u, 0x3232); }
+__device__ __forceinline__ uint64_t u64_of(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
 
 __device__ __forceinline__ float act_f(int act, float g) {
     if (act == ACT_GEGLU_TANH) {
@@ -108,71 +171,50 @@ __device__ __forceinline__ float act_f(int act, float g) {
     return g / (1.0f + expf(-g));
 }
 
-// Scales of one (row, sub-block): the bf16x2 subtrahend (base + qb term),
-// the multiplier of the MMA sum and e.
-struct SbScale {
-    uint32_t sub;
-    float dsc, e, pad;
-};
-
-struct Smem {
-    uint8_t* stages;
-    SbScale* scl;            // [RT][SB]
-    uint4* bfr;              // [2*SB k-slices][32 lanes]: b0 hi, b1 hi, b0 lo, b1 lo
-    float4* red;             // [csize-1][NW*32] partial sums of ranks 1.. (rank 0 only)
-    float* sx;               // [NT][SB] sums of x per sub-block
-    Seg* segs;
-    uint64_t* full;
-    uint64_t* empty;
-    uint64_t* red_full;      // rank 0: partials of a row block have arrived
-    uint64_t* red_free;      // ranks 1..: rank 0 has read the previous partials
-    int* abort_flag;
-};
-
 __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
+}
+
+// bounded wait by lane 0, result broadcast to the warp
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(bar, parity, timeout_ns);
+    return __shfl_sync(0xFFFFFFFFu, ok, 0);
 }
 
 __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
-    const int S_ = P.nstages;
-    Smem sm;
-    size_t off = 0;
-    sm.stages = smem;
-    off += (size_t)S_ * STAGE;
-    sm.scl = reinterpret_cast<SbScale*>(smem + off);
-    off += sizeof(SbScale) * RT * SB;
-    sm.bfr = reinterpret_cast<uint4*>(smem + off);
-    off += sizeof(uint4) * 2 * SB * 32;
-    const int cs = P.csize;
-    sm.red = reinterpret_cast<float4*>(smem + off);
-    off += sizeof(float4) * (cs - 1) * NW * 32;
-    sm.sx = reinterpret_cast<float*>(smem + off);
-    off += sizeof(float) * NT * SB;
-    sm.segs = reinterpret_cast<Seg*>(smem + off);
-    off += sizeof(Seg) * MAX_SEG;
-    sm.full = reinterpret_cast<uint64_t*>(smem + off);
-    sm.empty = sm.full + S_;
-    sm.red_full = sm.empty + S_;
-    sm.red_free = sm.red_full + 1;
-    sm.abort_flag = reinterpret_cast<int*>(sm.red_free + 1);
-    {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.seg[0]);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(sm.segs);
-        const int nw = P.nseg * (int)(sizeof(Seg) / 4);
-        for (int i = threadIdx.x; i < nw; i += blockDim.x) dst[i] = src[i];
-    }
+    const int S_ = P.nstages, cs = P.csize;
+    const Layout L = qmm_layout(S_, cs);
+    uint8_t* wst = smem + L.wst;
+    uint8_t* xraw = smem + L.xraw;
+    uint4* bfr = reinterpret_cast<uint4*>(smem + L.bfr);       // [2*SB k-slices][32 lanes]
+    float* sxs = reinterpret_cast<float*>(smem + L.sx);        // [SB][NT] sums of x per sub-block
+    SbScale* scl = reinterpret_cast<SbScale*>(smem + L.scl);   // [NW][SBW][16 rows]
+    uint32_t* subt = reinterpret_cast<uint32_t*>(smem + L.sub); // [NW][SBW][8][rows g, g+8]
+    float4* halfb = reinterpret_cast<float4*>(smem + L.half);  // [RW*32] second-half partial sums
+    float4* red = reinterpret_cast<float4*>(smem + L.red);     // [csize-1][RW*32]
+    const Seg* segs = P.seg;                                    // kernel parameter space
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + S_;
+    uint64_t* xfull = empty + S_;
+    uint64_t* xempty = xfull + 1;
+    uint64_t* red_full = xempty + 1;          // rank 0: partials of a row block have arrived
+    uint64_t* red_free = red_full + 1;        // ranks 1..: rank 0 has read the previous partials
+    int* abort_flag = reinterpret_cast<int*>(red_free + 1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], NW);
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
         }
+        mbar_init(xfull, 1);
+        mbar_init(xempty, NW);
         if (cs > 1) {
-            mbar_init(sm.red_full, (cs - 1) * NW * 32);
-            mbar_init(sm.red_free, NW * 32);
+            mbar_init(red_full, (cs - 1) * RW * 32);
+            mbar_init(red_free, RW * 32);
         }
-        *sm.abort_flag = 0;
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -181,80 +223,86 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
     const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nchunk = P.nchunk;
     // this rank's column chunks of every row block
-    const int c0 = (int)((int64_t)rank * nchunk / cs), c1 = (int)((int64_t)(rank + 1) * nchunk / cs);
-    const int64_t rowb = (int64_t)(P.cols / 256) * 144;
-    QWalk w0;
-    w0.rb = blockIdx.x / cs;                    // cluster index
-    w0.step = gridDim.x / cs;
-    w0.end = P.nblocks;
-    w0.hint = 0;
+    const int c0 = (int)((int64_t)rank * P.nchunk / cs), c1 = (int)((int64_t)(rank + 1) * P.nchunk / cs);
+    // this cluster's row blocks: a contiguous range
+    const int ncl = gridDim.x / cs, cid = blockIdx.x / cs;
+    const int rb_begin = (int)((int64_t)cid * P.nblocks / ncl);
+    const int rb_end = (int)((int64_t)(cid + 1) * P.nblocks / ncl);
 
     if (warp == NW) {
         // ------------------------------------------------ producer warp
         pdl_wait();                                  // x, row counts: preceding kernel
         const uint64_t policy = policy_evict_first();
-        QWalk w = w0;
-        qwalk_fix(sm.segs, P.nseg, w);
+        int pos = rb_begin, hint = 0;
+        Group G;
         uint32_t ephase = 0;
         int last_use[8];
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
         bool ok = true;
-        int n = 0, s = 0;
-        for (; w.rb < w.end && ok; w.rb += w.step, qwalk_fix(sm.segs, P.nseg, w)) {
-            const Seg& S = sm.segs[w.hint];
-            const int nval = seg_nval(S), boff = seg_boff(S);
-            const int lrb = w.rb - S.tile0;          // row block within the segment
-            const int nrow = seg_rows(S);
-            for (int c = c0; c < c1; ++c, ++n) {
-                if (*reinterpret_cast<volatile int*>(sm.abort_flag)) {
+        int n = 0, s = 0, xn = 0;
+        while (ok && next_group(segs, P.nseg, pos, rb_end, hint, G)) {
+            const Seg& S0 = segs[G.sg[0]];
+            const int nval = seg_nval(S0), boff = seg_boff(S0);
+            for (int c = c0; c < c1 && ok; ++c) {
+                if (*reinterpret_cast<volatile int*>(abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (n >= S_) {
-                    if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                    ephase ^= 1u << s;
-                    if (!ok) break;
-                }
-                uint8_t* dst = sm.stages + (size_t)s * STAGE;
-                // bytes of this tile: rows that exist, x rows that are valid
-                int nr = 0;
-                for (int tr = 0; tr < RT; ++tr) nr += (lrb * RT + tr < nrow) ? 1 : 0;
-                if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(nr * WROW + nval * KC * 4));
+                // x rows of this chunk (the buffer is free once converted)
+                if (xn > 0 && !(ok = warp_wait(xempty, (uint32_t)(xn - 1) & 1u, P.timeout_ns, lane))) break;
+                if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(nval * KC * 4));
                 __syncwarp();
-#pragma unroll
-                for (int h = 0; h < RT / 32; ++h) {
-                    const int tr = lane + 32 * h;        // tile row
-                    const int r = lrb * RT + tr;          // weight row of the segment (pairs interleaved)
-                    if (r < nrow) {
-                        const uint8_t* src;
-                        if (S.mode == MODE_PAIR_TWO)
-                            src = ((r & 1) ? S.w2 : S.w) + (int64_t)(r >> 1) * rowb;
-                        else
-                            src = S.w + (int64_t)r * rowb;
-                        bulk_g2s_stream(dst + tr * WROW, src + (int64_t)c * WROW, WROW, &sm.full[s], policy);
-                    }
-                }
                 if (lane < nval) {
                     const int rho = boff + lane;
-                    const float* xr = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * P.cols + (int64_t)c * KC;
-                    bulk_g2s(dst + WBYTES + lane * KC * 4, xr, KC * 4, &sm.full[s]);
+                    const float* xr = S0.x + (int64_t)(S0.xmap ? S0.xmap[rho] : rho) * P.cols + (int64_t)c * KC;
+                    bulk_g2s(xraw + lane * XSTR, xr, KC * 4, xfull);
                 }
-                last_use[s] = n / S_;
-                if (++s == S_) s = 0;
+                ++xn;
+                for (int k = 0; k < G.n && ok; ++k) {
+                    int rbk = G.rb[0], sgk = G.sg[0];
+#pragma unroll
+                    for (int kk = 1; kk < GR; ++kk)
+                        if (kk == k) {
+                            rbk = G.rb[kk];
+                            sgk = G.sg[kk];
+                        }
+                    const Seg& S = segs[sgk];
+                    const int lrb = rbk - S.tile0;                // row block within the segment
+                    if (n >= S_) {
+                        ok = warp_wait(&empty[s], (ephase >> s) & 1u, P.timeout_ns, lane);
+                        ephase ^= 1u << s;
+                        if (!ok) break;
+                    }
+                    uint8_t* dst = wst + (size_t)s * WSTAGE;
+                    // the whole tile (rows past the matrix are zero filled)
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)WSTAGE);
+                    __syncwarp();
+                    const int xw = c * (WROW / 4);                   // chunk start, uint32 elements
+                    if (S.mode == MODE_PLAIN) {
+                        if (lane == 0) tma_load_2d(dst, &P.tm[sgk][0], xw, lrb * RT, &full[s], policy);
+                    } else if (lane < 2 * RW) {
+                        // rows 16q .. 16q+7: gate rows of pairs p0 + 8q ..; 16q+8 ..: their up rows
+                        const int q = lane >> 1, u = lane & 1;
+                        tma_load_2d(dst + (16 * q + 8 * u) * WROW, &P.tm[sgk][u], xw,
+                                    lrb * (RT / 2) + QMM_PAIR_BOX * q, &full[s], policy);
+                    }
+                    last_use[s] = n / S_;
+                    ++n;
+                    if (++s == S_) s = 0;
+                }
             }
         }
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
-            atomicExch(sm.abort_flag, 1);
+            atomicExch(abort_flag, 1);
         }
+        // no copy may still be in flight when the CTA exits
         if (lane == 0) {
             for (int s2 = 0; s2 < S_; ++s2)
-                if (last_use[s2] >= 0)
-                    mbar_wait_bounded(&sm.full[s2], (uint32_t)last_use[s2] & 1u, P.timeout_ns);
+                if (last_use[s2] >= 0) mbar_wait_bounded(&full[s2], (uint32_t)last_use[s2] & 1u, P.timeout_ns);
+            if (xn > 0) mbar_wait_bounded(xfull, (uint32_t)(xn - 1) & 1u, P.timeout_ns);
         }
         __syncwarp();
         if (cs > 1) cluster_sync_all();         // no CTA leaves while a peer may address it
@@ -264,178 +312,202 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
     // ---------------------------------------------------- consumer warps
     pdl_wait();
     const int g = lane >> 2, cq = lane & 3;
-    const int ct = tid;                          // 0 .. NW*32-1
-    QWalk w = w0;
-    qwalk_fix(sm.segs, P.nseg, w);
-    uint32_t fphase = 0;
+    const int rq = warp % RW, hb = warp / RW;    // rows 16*rq .. +15, super-block hb of each tile
+    const int r0w = 16 * rq;
+    int pos = rb_begin, hint = 0;
+    Group G;
+    uint32_t fphase = 0, xph = 0;
     bool aborted = false;
-    int s = 0, kb = 0;                           // kb: row blocks done by this CTA
+    int s = 0, kb = 0;                           // kb: row blocks reduced by this CTA
     const uint32_t magic16 = 0x64006400u;        // half2 (1024, 1024), for the scale decode
-    for (; w.rb < w.end; w.rb += w.step, qwalk_fix(sm.segs, P.nseg, w)) {
-        const Seg& S = sm.segs[w.hint];
-        const int nval = seg_nval(S), boff = seg_boff(S);
-        float acc_hi[4] = {0.f, 0.f, 0.f, 0.f}, acc_lo[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int c = c0; c < c1; ++c) {
-            if (!aborted) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(&sm.full[s], (fphase >> s) & 1u, P.timeout_ns);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok || *reinterpret_cast<volatile int*>(sm.abort_flag)) {
-                    aborted = true;
-                    if (lane == 0 && !ok) {
-                        record_status(P.status, STATUS_TIMEOUT);
-                        atomicExch(sm.abort_flag, 1);
-                    }
-                }
-            }
-            fphase ^= 1u << s;
-            const uint8_t* st = sm.stages + (size_t)s * STAGE;
-            const float* xs = reinterpret_cast<const float*>(st + WBYTES);
-            if (!aborted) {
-                // ---- phase A (all consumers): scales, x pieces, x sums
-                // scales: (tile row, super-block) pairs, all 8 sub-blocks each
-                for (int e = ct; e < RT * (SB / 8); e += NW * 32) {
-                    const int tr = e / (SB / 8), sbk = e % (SB / 8);
-                    const uint4 hdr = *reinterpret_cast<const uint4*>(st + tr * WROW + sbk * 144);
+    SbScale* sw = scl + warp * (SBW * 16);       // this warp's rows: [SBW][16]
+    uint32_t* subw = subt + warp * (SBW * 16);   // [SBW][8][2]
+    auto fail = [&](void) {
+        aborted = true;
+        if (lane == 0) {
+            record_status(P.status, STATUS_TIMEOUT);
+            atomicExch(abort_flag, 1);
+        }
+    };
+    while (next_group(segs, P.nseg, pos, rb_end, hint, G)) {
+        const int nval = seg_nval(segs[G.sg[0]]);
+        float acc[GR][4];
 #pragma unroll
-                    for (int gq = 0; gq < 4; ++gq) {
-                        const Q4Sel sl = q4_sel(gq);
-                        const Q4Cent qc = q4k_centres(hdr, sl, magic16);
-                        SbScale* o = sm.scl + tr * SB + sbk * 8 + 2 * gq;
-                        // codes arrive as 128 + q; subtract 128 + qb (exact in bf16)
-                        const uint32_t s0 = bf16x2_pack(128.0f + qc.qb0, 128.0f + qc.qb0);
-                        const uint32_t s1 = bf16x2_pack(128.0f + qc.qb1, 128.0f + qc.qb1);
-                        o[0] = SbScale{s0, qc.dsc0, qc.e0, 0.f};
-                        o[1] = SbScale{s1, qc.dsc1, qc.e1, 0.f};
-                    }
-                }
-                // x pieces in B-fragment order: unit = (k-slice, lane)
-                for (int e = ct; e < 2 * SB * 32; e += NW * 32) {
-                    const int ks = e >> 5, ln = e & 31, tok = ln >> 2, c4 = ln & 3;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (tok < nval) {
-                        const float4 x = *reinterpret_cast<const float4*>(xs + tok * KC + 16 * ks + 4 * c4);
-                        const uint32_t h0 = bf16x2_pack(x.z, x.x);      // (k 2c, 2c+1) = cols (4c, 4c+2)
-                        const uint32_t h1 = bf16x2_pack(x.w, x.y);      // (k 2c+8, 2c+9) = cols (4c+1, 4c+3)
-                        const uint32_t l0 = bf16x2_pack(x.z - bf16_hi_f(h0), x.x - bf16_lo_f(h0));
-                        const uint32_t l1 = bf16x2_pack(x.w - bf16_hi_f(h1), x.y - bf16_lo_f(h1));
-                        v = make_uint4(h0, h1, l0, l1);
-                    }
-                    sm.bfr[e] = v;
-                }
-                // sums of x per (x row, sub-block), in column order
-                for (int e = ct; e < NT * SB; e += NW * 32) {
-                    const int tok = e / SB, j = e % SB;
+        for (int k = 0; k < GR; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
+        for (int c = c0; c < c1; ++c) {
+            consumer_bar();                      // B fragments of the previous chunk no longer read
+            if (!aborted && !warp_wait(xfull, xph, P.timeout_ns, lane)) fail();
+            xph ^= 1u;
+            if (!aborted) {
+                // x chunk -> B fragments (hi, lo per k slice) and sums per sub-block:
+                // unit (sub-block j, lane (tok, c4)) covers columns 32j + 8c4 .. +7
+                const int tok = lane >> 2, c4 = lane & 3;
+#pragma unroll
+                for (int it = 0; it < SB / NW; ++it) {
+                    const int j = warp + NW * it;
+                    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
                     float sum = 0.f;
                     if (tok < nval) {
-                        const float* xr = xs + tok * KC + 32 * j;
-                        for (int i = 0; i < 32; ++i) sum += xr[i];
+                        const float* xr = reinterpret_cast<const float*>(xraw + tok * XSTR) + 32 * j + 8 * c4;
+                        const float4 a = *reinterpret_cast<const float4*>(xr);
+                        const float4 b = *reinterpret_cast<const float4*>(xr + 4);
+                        uint32_t h0 = bf16x2_pack(a.z, a.x), h1 = bf16x2_pack(a.w, a.y);
+                        v0 = make_uint4(h0, h1, bf16x2_pack(a.z - bf16_hi_f(h0), a.x - bf16_lo_f(h0)),
+                                        bf16x2_pack(a.w - bf16_hi_f(h1), a.y - bf16_lo_f(h1)));
+                        h0 = bf16x2_pack(b.z, b.x);
+                        h1 = bf16x2_pack(b.w, b.y);
+                        v1 = make_uint4(h0, h1, bf16x2_pack(b.z - bf16_hi_f(h0), b.x - bf16_lo_f(h0)),
+                                        bf16x2_pack(b.w - bf16_hi_f(h1), b.y - bf16_lo_f(h1)));
+                        sum = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
                     }
-                    sm.sx[e] = sum;
+                    bfr[(2 * j) * 32 + lane] = v0;
+                    bfr[(2 * j + 1) * 32 + lane] = v1;
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                    if (c4 == 0) sxs[j * NT + tok] = sum;
                 }
             }
-            consumer_bar();
-            if (!aborted) {
-                // ---- phase B: warp rows r0 .. r0+15
-                const int r0 = 16 * warp;
-                const uint8_t* wg = st + (r0 + g) * WROW;
-                const uint8_t* wg8 = st + (r0 + g + 8) * WROW;
-#pragma unroll 2
-                for (int j = 0; j < SB; ++j) {
-                    const int sbk = j >> 3, jj = j & 7;
-                    const int qoff = sbk * 144 + 16 + 32 * (jj >> 1) + 4 * cq;
-                    const uint32_t nsh = (jj & 1) ? 4u : 0u;  // high nibbles: shift down
-                    const SbScale sa = sm.scl[(r0 + g) * SB + j];
-                    const SbScale sb = sm.scl[(r0 + g + 8) * SB + j];
-                    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int hs = 0; hs < 2; ++hs) {
-                        const uint32_t Wa = *reinterpret_cast<const uint32_t*>(wg + qoff + 16 * hs) >> nsh;
-                        const uint32_t Wb = *reinterpret_cast<const uint32_t*>(wg8 + qoff + 16 * hs) >> nsh;
-                        const uint32_t msk = 0x000F000Fu, mag = 0x43004300u;
-                        uint32_t a[4];
-                        a[0] = bf16x2_sub(lop_and_or(Wa, msk, mag), sa.sub);
-                        a[1] = bf16x2_sub(lop_and_or(Wb, msk, mag), sb.sub);
-                        a[2] = bf16x2_sub(lop_and_or(Wa >> 8, msk, mag), sa.sub);
-                        a[3] = bf16x2_sub(lop_and_or(Wb >> 8, msk, mag), sb.sub);
-                        const uint4 bf = sm.bfr[(2 * j + hs) * 32 + lane];
-                        mma_bf16(dh, a, bf.x, bf.y, dh);
-                        mma_bf16(dl, a, bf.z, bf.w, dl);
-                    }
-                    // epilogue: rows g, g+8; x rows 2cq, 2cq+1
-                    const float sx0 = sm.sx[(2 * cq) * SB + j], sx1 = sm.sx[(2 * cq + 1) * SB + j];
-                    acc_hi[0] = fmaf(sa.e, sx0, fmaf(sa.dsc, dh[0], acc_hi[0]));
-                    acc_hi[1] = fmaf(sa.e, sx1, fmaf(sa.dsc, dh[1], acc_hi[1]));
-                    acc_hi[2] = fmaf(sb.e, sx0, fmaf(sb.dsc, dh[2], acc_hi[2]));
-                    acc_hi[3] = fmaf(sb.e, sx1, fmaf(sb.dsc, dh[3], acc_hi[3]));
-                    acc_lo[0] = fmaf(sa.dsc, dl[0], acc_lo[0]);
-                    acc_lo[1] = fmaf(sa.dsc, dl[1], acc_lo[1]);
-                    acc_lo[2] = fmaf(sb.dsc, dl[2], acc_lo[2]);
-                    acc_lo[3] = fmaf(sb.dsc, dl[3], acc_lo[3]);
-                }
-            }
-            // release the stage and the per-tile tables
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-            consumer_bar();
-            if (++s == S_) s = 0;
-        }
-        if (aborted) continue;
-        float v[4];
+            if (lane == 0) mbar_arrive(xempty);      // raw x may be overwritten
+            consumer_bar();                          // B fragments ready
+            for (int k = 0; k < G.n; ++k) {
+                if (!aborted && !warp_wait(&full[s], (fphase >> s) & 1u, P.timeout_ns, lane)) fail();
+                fphase ^= 1u << s;
+                const uint8_t* st = wst + (size_t)s * WSTAGE;
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                if (!aborted) {
+                    // scales of this warp's 16 rows in super-block hb:
+                    // lane -> (row lane & 15, sub-block pairs 2 (lane >> 4) + {0, 1})
+                    {
+                        const int rr = lane & 15, gh = lane >> 4;
+                        const uint4 hdr = *reinterpret_cast<const uint4*>(st + (r0w + rr) * WROW + hb * 144);
+                        const int si = ((rr & 7) << 1) | (rr >> 3);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = acc_hi[i] + acc_lo[i];
-        if (cs > 1) {
-            // ---- split columns: partial sums meet in rank 0, added in rank order
-            const int k = kb++;
-            if (rank != 0) {
-                if (k > 0 && !mbar_wait_bounded_cluster(sm.red_free, (uint32_t)(k - 1) & 1u, P.timeout_ns)) {
-                    aborted = true;
-                    record_status(P.status, STATUS_TIMEOUT);
-                    atomicExch(sm.abort_flag, 1);
+                        for (int gi = 0; gi < 2; ++gi) {
+                            const int gq = 2 * gh + gi;
+                            const Q4Cent qc = q4k_centres(hdr, q4_sel(gq), magic16);
+                            const int j0 = 2 * gq;
+                            sw[j0 * 16 + rr] = SbScale{qc.dsc0, qc.dsc0, qc.e0, qc.e0};
+                            sw[(j0 + 1) * 16 + rr] = SbScale{qc.dsc1, qc.dsc1, qc.e1, qc.e1};
+                            subw[j0 * 16 + si] = bf16_dup(128.0f + qc.qb0);
+                            subw[(j0 + 1) * 16 + si] = bf16_dup(128.0f + qc.qb1);
+                        }
+                    }
+                    __syncwarp();
+                    const uint8_t* wg = st + (r0w + g) * WROW + hb * 144 + 16 + 8 * cq;  // this lane's 8 bytes of a run
+                    const uint8_t* wg8 = wg + 8 * WROW;
+                    uint64_t t01 = pk2(0.f, 0.f), t23 = pk2(0.f, 0.f);   // rows g, g+8 x tokens 2cq, 2cq+1
+                    const SbScale* swa = sw + g;
+                    const uint2* subg = reinterpret_cast<const uint2*>(subw) + g;
+                    const uint4* bfl = bfr + (2 * SBW * hb) * 32 + lane;
+                    const float* sxq = sxs + SBW * hb * NT + 2 * cq;
+#pragma unroll
+                    for (int m = 0; m < SBW / 2; ++m) {                  // sub-block pairs (2m, 2m+1)
+                        const uint2 wa = *reinterpret_cast<const uint2*>(wg + 32 * m);
+                        const uint2 wb = *reinterpret_cast<const uint2*>(wg8 + 32 * m);
+#pragma unroll
+                        for (int nib = 0; nib < 2; ++nib) {
+                            const int j = 2 * m + nib;                    // sub-block within the warp's half
+                            const uint4 sa = *reinterpret_cast<const uint4*>(swa + j * 16);
+                            const uint4 sb = *reinterpret_cast<const uint4*>(swa + j * 16 + 8);
+                            const uint2 sub = subg[j * 8];                   // rows g, g + 8
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int hs = 0; hs < 2; ++hs) {
+                                const uint32_t Wa = (hs ? wa.y : wa.x) >> (4 * nib);
+                                const uint32_t Wb = (hs ? wb.y : wb.x) >> (4 * nib);
+                                const uint32_t msk = 0x000F000Fu, mag = 0x43004300u;
+                                uint32_t a[4];
+                                a[0] = bf16x2_sub(lop_and_or(Wa, msk, mag), sub.x);
+                                a[1] = bf16x2_sub(lop_and_or(Wb, msk, mag), sub.y);
+                                a[2] = bf16x2_sub(lop_and_or(Wa >> 8, msk, mag), sub.x);
+                                a[3] = bf16x2_sub(lop_and_or(Wb >> 8, msk, mag), sub.y);
+                                const uint4 bf = bfl[(2 * j + hs) * 32];
+                                mma_bf16(d, a, bf.x, bf.y);
+                                mma_bf16(d, a, bf.z, bf.w);
+                            }
+                            const uint64_t sxv = *reinterpret_cast<const uint64_t*>(sxq + j * NT);
+                            t01 = ffma2(u64_of(sa.x, sa.y), pk2(d[0], d[1]), t01);
+                            t01 = ffma2(u64_of(sa.z, sa.w), sxv, t01);
+                            t23 = ffma2(u64_of(sb.x, sb.y), pk2(d[2], d[3]), t23);
+                            t23 = ffma2(u64_of(sb.z, sb.w), sxv, t23);
+                        }
+                    }
+                    t[0] = lo_f(t01);
+                    t[1] = hi_f(t01);
+                    t[2] = lo_f(t23);
+                    t[3] = hi_f(t23);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (++s == S_) s = 0;
+#pragma unroll
+                for (int kk = 0; kk < GR; ++kk)
+                    if (kk == k) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[kk][i] += t[i];
+                    }
+            }
+        }
+        // ---- outputs of the group's row blocks (the barriers run for every
+        // warp whatever its state, so that none is left waiting)
+#pragma unroll
+        for (int k = 0; k < GR; ++k) {
+            if (k >= G.n) break;
+            consumer_bar();                          // the half buffer is free
+            if (hb == 1) halfb[rq * 32 + lane] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+            consumer_bar();
+            if (hb == 1 || aborted) continue;
+            // super-block 0 + super-block 1 of every chunk of this rank
+            const float4 o = halfb[rq * 32 + lane];
+            float v[4] = {acc[k][0] + o.x, acc[k][1] + o.y, acc[k][2] + o.z, acc[k][3] + o.w};
+            const int rt = rq * 32 + lane;           // 0 .. RW*32-1
+            if (cs > 1) {
+                // split columns: partial sums meet in rank 0, added in rank order
+                const int kk = kb++;
+                if (rank != 0) {
+                    if (kk > 0 && !mbar_wait_bounded_cluster(red_free, (uint32_t)(kk - 1) & 1u, P.timeout_ns)) {
+                        fail();
+                        continue;
+                    }
+                    const uint32_t slot = smem_u32(red + (size_t)(rank - 1) * RW * 32 + rt);
+                    st_cluster_f4(mapa_shared(slot, 0), v[0], v[1], v[2], v[3]);
+                    mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
+                    continue;                        // rank 0 writes the outputs
+                }
+                if (!mbar_wait_bounded_cluster(red_full, (uint32_t)kk & 1u, P.timeout_ns)) {
+                    fail();
                     continue;
                 }
-                const uint32_t slot = smem_u32(sm.red + (size_t)(rank - 1) * NW * 32 + ct);
-                st_cluster_f4(mapa_shared(slot, 0), v[0], v[1], v[2], v[3]);
-                mbar_arrive_remote(mapa_shared(smem_u32(sm.red_full), 0));
-                continue;                        // rank 0 writes the outputs
+                for (int r = 1; r < cs; ++r) {
+                    const float4 p = red[(size_t)(r - 1) * RW * 32 + rt];
+                    v[0] += p.x;
+                    v[1] += p.y;
+                    v[2] += p.z;
+                    v[3] += p.w;
+                }
+                for (int r = 1; r < cs; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_free), (uint32_t)r));
             }
-            if (!mbar_wait_bounded_cluster(sm.red_full, (uint32_t)k & 1u, P.timeout_ns)) {
-                aborted = true;
-                record_status(P.status, STATUS_TIMEOUT);
-                atomicExch(sm.abort_flag, 1);
-                continue;
-            }
-            for (int r = 1; r < cs; ++r) {
-                const float4 p = sm.red[(size_t)(r - 1) * NW * 32 + ct];
-                v[0] += p.x;
-                v[1] += p.y;
-                v[2] += p.z;
-                v[3] += p.w;
-            }
-            for (int r = 1; r < cs; ++r) mbar_arrive_remote(mapa_shared(smem_u32(sm.red_free), (uint32_t)r));
-        }
-        // ---- outputs of this row block: rows r0+g, r0+g+8 x rows 2cq, 2cq+1
-        const int lrb = w.rb - S.tile0;
-        const int trg = 16 * warp + g;                  // tile row of v[0], v[1]; +8 for v[2], v[3]
-        if (S.mode == MODE_PLAIN) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = lrb * RT + trg + (i >> 1) * 8;
-                const int tok = 2 * cq + (i & 1);
-                if (row < S.nout && tok < nval) S.y[(int64_t)(boff + tok) * S.ld_y + row] = v[i];
-            }
-        } else {
-            // gate rows are even tile rows, up rows odd: partner lane g ^ 1
-            float u[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], 4);
-            if ((g & 1) == 0) {
+            // rows r0w+g, r0w+g+8 of the tile x tokens 2cq, 2cq+1
+            const Seg& S = segs[G.sg[k]];
+            const int boff = seg_boff(S);
+            const int lrb = G.rb[k] - S.tile0;
+            const int trg = r0w + g;
+            if (S.mode == MODE_PLAIN) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int out = (lrb * RT + trg + (i >> 1) * 8) >> 1;
+                    const int row = lrb * RT + trg + (i >> 1) * 8;
                     const int tok = 2 * cq + (i & 1);
+                    if (row < S.nout && tok < nval) S.y[(int64_t)(boff + tok) * S.ld_y + row] = v[i];
+                }
+            } else {
+                // row g is the gate row of pair p0 + 8 rq + g, row g + 8 its up row
+                const int out = lrb * (RT / 2) + QMM_PAIR_BOX * rq + g;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = 2 * cq + i;
                     if (out < S.nout && tok < nval)
-                        S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_f(S.act, v[i]) * u[i];
+                        S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_f(S.act, v[i]) * v[2 + i];
                 }
             }
         }
@@ -449,10 +521,14 @@ cudaError_t qmm_set_smem(int bytes) {
     return cudaFuncSetAttribute(qmm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-size_t qmm_smem_bytes(int nstages, int csize) {
-    return (size_t)nstages * STAGE + sizeof(SbScale) * RT * SB + sizeof(uint4) * 2 * SB * 32 +
-           sizeof(float4) * (csize - 1) * NW * 32 + sizeof(float) * NT * SB + sizeof(Seg) * MAX_SEG +
-           (2 * nstages + 2) * sizeof(uint64_t) + 16;
+size_t qmm_smem_bytes(int nstages, int csize) { return qmm_layout(nstages, csize).total; }
+
+// Most stages (up to 3) that keep two CTAs resident on an SM (228 KB of
+// shared memory, 1 KB of it reserved per CTA).
+int qmm_stages_for(int csize) {
+    for (int S = 3; S > 2; --S)
+        if (2 * (qmm_layout(S, csize).total + 1024) <= 228 * 1024) return S;
+    return 2;
 }
 
 // Clusters of `csize` CTAs that can be resident at once (CTAs for csize 1).
