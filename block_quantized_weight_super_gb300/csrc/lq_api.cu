@@ -44,6 +44,13 @@ int64_t rowbytes(int fmt, int64_t cols) { return cols / block_elems_of(fmt) * bl
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Per-device facts and one-time set-up.
+// Stages and partial-sum slots of the tensor-core kernel per cluster size
+// (two CTAs per SM: at most 113 KB of shared memory each).
+struct QmmCfg {
+    int nstages, gmax;
+};
+QmmCfg qmm_cfg(int csize) { return csize >= 4 ? QmmCfg{2, 2} : QmmCfg{2, QMM_GROUP}; }
+
 struct DevInfo {
     bool init = false;
     int sms = 0;
@@ -70,10 +77,11 @@ int dev_info(DevInfo** out) {
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
-        if (e == cudaSuccess) e = qmm_set_smem((int)qmm_smem_bytes(3, QMM_MAX_CSIZE));
+        if (e == cudaSuccess) e = qmm_set_smem(227 * 1024);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE; ++i, cs *= 2) {
-            e = qmm_max_resident(cs, qmm_smem_bytes(qmm_stages_for(cs), cs), d.sms, &d.qmm_res[i]);
+            const QmmCfg q = qmm_cfg(cs);
+            e = qmm_max_resident(cs, qmm_smem_bytes(q.nstages, cs, q.gmax), d.sms, &d.qmm_res[i]);
             if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
         }
         d.init = true;
@@ -339,8 +347,8 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
         }
     }
     const int cs = 1 << ci, res = std::max(1, dev->qmm_res[ci]);
-    const int nstages = qmm_stages_for(cs);
-    const size_t smem = qmm_smem_bytes(nstages, cs);
+    const QmmCfg qc = qmm_cfg(cs);
+    const size_t smem = qmm_smem_bytes(qc.nstages, cs, qc.gmax);
     const int64_t rb = cols / 256 * 144;
     for (size_t s0 = 0; s0 < segs.size(); s0 += QMM_MAX_SEG) {
         QmmParams P;
@@ -368,11 +376,19 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
         P.nblocks = t;
         P.cols = (int32_t)cols;
         P.nchunk = nchunk;
-        P.nstages = nstages;
+        // units of gmax row blocks, dealt round robin to the clusters: as
+        // large as the slots allow while every cluster still gets one
+        const int ncl0 = std::min(res, t);
+        const int gmax = std::max(1, std::min(qc.gmax, (t + ncl0 - 1) / ncl0));
+        const int ncl = std::min(res, (t + gmax - 1) / gmax);
+        P.nstages = qc.nstages;
         P.csize = cs;
+        P.gmax = gmax;
+        for (int i = 0; i < n; ++i)
+            if (P.seg[i].bcnt || P.seg[i].boff) P.dev_counts = 1;
         P.timeout_ns = g_timeout_ns.load();
         P.status = dev->status;
-        const int grid = cs * std::min(res, t);
+        const int grid = cs * ncl;
         cudaError_t e = qmm_launch(P, grid, smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec launch");
     }

@@ -99,6 +99,25 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// Split form of the cluster barrier: arrive (release) early, wait (acquire)
+// just before the first access to another CTA's shared memory.  A thread
+// waits once between two arrives.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// Store 16 bytes into another CTA's shared memory, completion counted as tx
+// bytes on an mbarrier of that CTA (both addresses shared::cluster).
+__device__ __forceinline__ void st_async_f4(uint32_t a, float4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// Bring a tensor map (kernel parameter or global) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // Shared::cluster address of the variable at shared address `a` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
     uint32_t r;

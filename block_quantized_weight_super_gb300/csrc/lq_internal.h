@@ -40,6 +40,8 @@ struct QmmParams {
     int32_t nchunk;          // cols / QMM_KC
     int32_t nstages;
     int32_t csize;           // CTAs per cluster splitting a row block's columns (1, 2 or 4)
+    int32_t gmax;            // row blocks per group (<= QMM_GROUP): partial-sum slots
+    int32_t dev_counts;      // segments read row counts / offsets written by the preceding kernel
     uint64_t timeout_ns;
     unsigned* status;
 };
@@ -48,8 +50,7 @@ constexpr int QMM_GROUP = 4;              // row blocks sharing one staging of x
 constexpr int QMM_MIN_BATCH = 3;          // dense calls with at least this many x rows
 constexpr int QMM_MOE_MIN_TOKENS = 2;     // MoE calls with at least this many tokens
 cudaError_t qmm_set_smem(int bytes);
-size_t qmm_smem_bytes(int nstages, int csize);
-int qmm_stages_for(int csize);
+size_t qmm_smem_bytes(int nstages, int csize, int gmax);
 cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out);
 cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t st);
 

@@ -29,9 +29,10 @@
 // shared-memory stages by 2-D tensor copies (TMA, one box per tile, or eight
 // 8-row boxes for gate / up pairs) on full / empty mbarriers (bounded waits).
 // Warps w and w + 4 take the same 16 rows, the first and the second
-// super-block of every tile, and add their partial sums at the end.  A cluster of CTAs owns a
-// contiguous range of row blocks and takes them in groups of up to four
-// that read the same x rows; for each column chunk the x rows are staged
+// super-block of every tile, and add their partial sums at the end.  Row
+// blocks are dealt to the clusters in units of up to four, round robin; a
+// cluster takes the blocks of a unit that read the same x rows as one
+// group, and for each column chunk the x rows are staged
 // once (their own bulk copies and barriers), converted once into B
 // fragments and per-sub-block sums, and used by every row block of the
 // group, whose partial sums stay in registers.  Each warp decodes the scales
@@ -76,7 +77,9 @@ struct Layout {
     size_t wst, xraw, bfr, sx, scl, sub, half, red, bars, total;
 };
 
-__host__ __device__ inline Layout qmm_layout(int nstages, int csize) {
+// red: [csize-1][gmax][RW*32] partial sums of the other ranks (rank 0 only);
+// half: [gmax][RW*32] partial sums of the second super-block warps.
+__host__ __device__ inline Layout qmm_layout(int nstages, int csize, int gmax) {
     Layout L;
     size_t o = 0;
     L.wst = o;  o += (size_t)nstages * WSTAGE;
@@ -85,8 +88,8 @@ __host__ __device__ inline Layout qmm_layout(int nstages, int csize) {
     L.sx = o;   o += sizeof(float) * SB * NT;
     L.scl = o;  o += sizeof(SbScale) * NW * SBW * 16;
     L.sub = o;  o += sizeof(uint32_t) * NW * SBW * 16;
-    L.half = o; o += sizeof(float4) * RW * 32;
-    L.red = o;  o += sizeof(float4) * (csize - 1) * RW * 32;
+    L.half = o; o += sizeof(float4) * gmax * RW * 32;
+    L.red = o;  o += sizeof(float4) * (csize - 1) * gmax * RW * 32;
     L.bars = o; o += sizeof(uint64_t) * (2 * nstages + 4) + 16;
     L.total = o;
     return L;
@@ -102,36 +105,60 @@ __device__ __forceinline__ bool same_x(const Seg& a, const Seg& b) {
            a.nbatch == b.nbatch;
 }
 
-// Up to GR row blocks with x rows to process, from [pos, end), all reading
-// the x rows of the first; segments' tile0 = first row block.
+// Row blocks are dealt to the clusters in units of gmax consecutive blocks,
+// round robin (unit u goes to cluster u mod ncl), so that blocks with nothing
+// to do (a grouped-MoE segment past its expert's token count) spread over
+// the clusters.  A group is up to gmax blocks of one unit that have x rows
+// to process and read the x rows of the first; segments' tile0 = first row
+// block.
 struct Group {
     int n;
     int rb[GR];
     int sg[GR];
 };
 
-__device__ __forceinline__ bool next_group(const Seg* segs, int nseg, int& pos, int end, int& hint, Group& G) {
-    G.n = 0;
-    while (pos < end && G.n < GR) {
-        int s = hint;
-        while (s + 1 < nseg && pos >= segs[s + 1].tile0) ++s;
-        while (s > 0 && pos < segs[s].tile0) --s;
-        hint = s;
-        if (seg_nval(segs[s]) <= 0) {              // nothing to do for this segment
-            pos = min(end, segs[s].tile0 + segs[s].ntiles);
-            continue;
+struct Walk {
+    int u, pos, end, hint;
+};
+
+__device__ __forceinline__ void walk_start(Walk& w, int cid, int gmax, int nblocks) {
+    w.u = cid;
+    w.pos = cid * gmax;
+    w.end = min(nblocks, w.pos + gmax);
+    w.hint = 0;
+}
+
+__device__ __forceinline__ bool next_group(const Seg* segs, int nseg, int gmax, int nblocks, int ncl, Walk& w,
+                                           Group& G) {
+    for (;;) {
+        if (w.pos >= w.end) {                      // next unit of this cluster
+            w.u += ncl;
+            w.pos = w.u * gmax;
+            if (w.pos >= nblocks) return false;
+            w.end = min(nblocks, w.pos + gmax);
         }
-        if (G.n > 0 && !same_x(segs[G.sg[0]], segs[s])) break;
-#pragma unroll
-        for (int k = 0; k < GR; ++k)
-            if (k == G.n) {
-                G.rb[k] = pos;
-                G.sg[k] = s;
+        G.n = 0;
+        while (w.pos < w.end) {
+            int s = w.hint;
+            while (s + 1 < nseg && w.pos >= segs[s + 1].tile0) ++s;
+            while (s > 0 && w.pos < segs[s].tile0) --s;
+            w.hint = s;
+            if (seg_nval(segs[s]) <= 0) {          // nothing to do for this segment
+                w.pos = min(w.end, segs[s].tile0 + segs[s].ntiles);
+                continue;
             }
-        ++G.n;
-        ++pos;
+            if (G.n > 0 && !same_x(segs[G.sg[0]], segs[s])) break;
+#pragma unroll
+            for (int k = 0; k < GR; ++k)
+                if (k == G.n) {
+                    G.rb[k] = w.pos;
+                    G.sg[k] = s;
+                }
+            ++G.n;
+            ++w.pos;
+        }
+        if (G.n > 0) return true;
     }
-    return G.n > 0;
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -139,6 +166,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d = a . b (no accumulator input)
+__device__ __forceinline__ void mma_bf16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -174,6 +209,10 @@ __device__ __forceinline__ float act_f(int act, float g) {
 __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
 }
+// the first super-block warps only
+__device__ __forceinline__ void half_bar() {
+    asm volatile("bar.sync 2, %0;" ::"r"(RW * 32) : "memory");
+}
 
 // bounded wait by lane 0, result broadcast to the warp
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int lane) {
@@ -185,25 +224,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
-    const int S_ = P.nstages, cs = P.csize;
-    const Layout L = qmm_layout(S_, cs);
+    const int S_ = P.nstages, cs = P.csize, gmax = P.gmax;
+    const Layout L = qmm_layout(S_, cs, gmax);
     uint8_t* wst = smem + L.wst;
     uint8_t* xraw = smem + L.xraw;
     uint4* bfr = reinterpret_cast<uint4*>(smem + L.bfr);       // [2*SB k-slices][32 lanes]
     float* sxs = reinterpret_cast<float*>(smem + L.sx);        // [SB][NT] sums of x per sub-block
     SbScale* scl = reinterpret_cast<SbScale*>(smem + L.scl);   // [NW][SBW][16 rows]
     uint32_t* subt = reinterpret_cast<uint32_t*>(smem + L.sub); // [NW][SBW][8][rows g, g+8]
-    float4* halfb = reinterpret_cast<float4*>(smem + L.half);  // [RW*32] second-half partial sums
-    float4* red = reinterpret_cast<float4*>(smem + L.red);     // [csize-1][RW*32]
+    float4* halfb = reinterpret_cast<float4*>(smem + L.half);  // [gmax][RW*32]
+    float4* red = reinterpret_cast<float4*>(smem + L.red);     // [csize-1][gmax][RW*32]
     const Seg* segs = P.seg;                                    // kernel parameter space
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + S_;
     uint64_t* xfull = empty + S_;
     uint64_t* xempty = xfull + 1;
-    uint64_t* red_full = xempty + 1;          // rank 0: partials of a row block have arrived
-    uint64_t* red_free = red_full + 1;        // ranks 1..: rank 0 has read the previous partials
+    uint64_t* red_full = xempty + 1;          // rank 0: the other ranks' partial sums of a group have landed
+    uint64_t* red_free = red_full + 1;        // ranks 1..: rank 0 has read them
     int* abort_flag = reinterpret_cast<int*>(red_free + 1);
-    if (threadIdx.x == 0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (warp == NW && lane < P.nseg) {
+        prefetch_tensormap(&P.tm[lane][0]);
+        if (segs[lane].mode != MODE_PLAIN) prefetch_tensormap(&P.tm[lane][1]);
+    }
+    if (tid == 0) {
         for (int s = 0; s < S_; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NW);
@@ -211,47 +255,87 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
         mbar_init(xfull, 1);
         mbar_init(xempty, NW);
         if (cs > 1) {
-            mbar_init(red_full, (cs - 1) * RW * 32);
-            mbar_init(red_free, RW * 32);
+            mbar_init(red_full, 1);
+            mbar_init(red_free, 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    // peers' barriers are initialised before any remote arrive
-    if (cs > 1) cluster_sync_all();
+    // peers' barriers are initialised before any remote access: each thread
+    // waits on this arrive before its first one
+    bool cw = cs <= 1;
+    if (cs > 1) cluster_arrive();
     const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // this rank's column chunks of every row block
     const int c0 = (int)((int64_t)rank * P.nchunk / cs), c1 = (int)((int64_t)(rank + 1) * P.nchunk / cs);
-    // this cluster's row blocks: a contiguous range
+    // this cluster's units of row blocks
     const int ncl = gridDim.x / cs, cid = blockIdx.x / cs;
-    const int rb_begin = (int)((int64_t)cid * P.nblocks / ncl);
-    const int rb_end = (int)((int64_t)(cid + 1) * P.nblocks / ncl);
 
     if (warp == NW) {
         // ------------------------------------------------ producer warp
-        pdl_wait();                                  // x, row counts: preceding kernel
         const uint64_t policy = policy_evict_first();
-        int pos = rb_begin, hint = 0;
-        Group G;
+        // weights do not depend on the preceding kernel: unless the row
+        // counts do, the first tiles are requested before waiting for it
+        bool waited = P.dev_counts == 0 ? false : (pdl_wait(), true);
+        Walk wk;
+        walk_start(wk, cid, gmax, P.nblocks);
+        Group G{};
         uint32_t ephase = 0;
         int last_use[8];
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
         bool ok = true;
         int n = 0, s = 0, xn = 0;
-        while (ok && next_group(segs, P.nseg, pos, rb_end, hint, G)) {
+        auto issue_tile = [&](int k, int c) {
+            int rbk = G.rb[0], sgk = G.sg[0];
+#pragma unroll
+            for (int kk = 1; kk < GR; ++kk)
+                if (kk == k) {
+                    rbk = G.rb[kk];
+                    sgk = G.sg[kk];
+                }
+            const Seg& S = segs[sgk];
+            const int lrb = rbk - S.tile0;                // row block within the segment
+            if (n >= S_) {
+                ok = warp_wait(&empty[s], (ephase >> s) & 1u, P.timeout_ns, lane);
+                ephase ^= 1u << s;
+                if (!ok) return;
+            }
+            uint8_t* dst = wst + (size_t)s * WSTAGE;
+            // the whole tile (rows past the matrix are zero filled)
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)WSTAGE);
+            __syncwarp();
+            const int xw = c * (WROW / 4);                   // chunk start, uint32 elements
+            if (S.mode == MODE_PLAIN) {
+                if (lane == 0) tma_load_2d(dst, &P.tm[sgk][0], xw, lrb * RT, &full[s], policy);
+            } else if (lane < 2 * RW) {
+                // rows 16q .. 16q+7: gate rows of pairs p0 + 8q ..; 16q+8 ..: their up rows
+                const int q = lane >> 1, u = lane & 1;
+                tma_load_2d(dst + (16 * q + 8 * u) * WROW, &P.tm[sgk][u], xw, lrb * (RT / 2) + QMM_PAIR_BOX * q,
+                            &full[s], policy);
+            }
+            last_use[s] = n / S_;
+            ++n;
+            if (++s == S_) s = 0;
+        };
+        while (ok && next_group(segs, P.nseg, gmax, P.nblocks, ncl, wk, G)) {
             const Seg& S0 = segs[G.sg[0]];
-            const int nval = seg_nval(S0), boff = seg_boff(S0);
             for (int c = c0; c < c1 && ok; ++c) {
                 if (*reinterpret_cast<volatile int*>(abort_flag)) {
                     ok = false;
                     break;
                 }
+                int k = 0;
+                if (!waited) {                   // first chunk: tiles into the free stages first
+                    for (; k < G.n && k < S_; ++k) issue_tile(k, c);
+                    pdl_wait();
+                    waited = true;
+                }
                 // x rows of this chunk (the buffer is free once converted)
                 if (xn > 0 && !(ok = warp_wait(xempty, (uint32_t)(xn - 1) & 1u, P.timeout_ns, lane))) break;
+                const int nval = seg_nval(S0), boff = seg_boff(S0);
                 if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(nval * KC * 4));
                 __syncwarp();
                 if (lane < nval) {
@@ -260,40 +344,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
                     bulk_g2s(xraw + lane * XSTR, xr, KC * 4, xfull);
                 }
                 ++xn;
-                for (int k = 0; k < G.n && ok; ++k) {
-                    int rbk = G.rb[0], sgk = G.sg[0];
-#pragma unroll
-                    for (int kk = 1; kk < GR; ++kk)
-                        if (kk == k) {
-                            rbk = G.rb[kk];
-                            sgk = G.sg[kk];
-                        }
-                    const Seg& S = segs[sgk];
-                    const int lrb = rbk - S.tile0;                // row block within the segment
-                    if (n >= S_) {
-                        ok = warp_wait(&empty[s], (ephase >> s) & 1u, P.timeout_ns, lane);
-                        ephase ^= 1u << s;
-                        if (!ok) break;
-                    }
-                    uint8_t* dst = wst + (size_t)s * WSTAGE;
-                    // the whole tile (rows past the matrix are zero filled)
-                    if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)WSTAGE);
-                    __syncwarp();
-                    const int xw = c * (WROW / 4);                   // chunk start, uint32 elements
-                    if (S.mode == MODE_PLAIN) {
-                        if (lane == 0) tma_load_2d(dst, &P.tm[sgk][0], xw, lrb * RT, &full[s], policy);
-                    } else if (lane < 2 * RW) {
-                        // rows 16q .. 16q+7: gate rows of pairs p0 + 8q ..; 16q+8 ..: their up rows
-                        const int q = lane >> 1, u = lane & 1;
-                        tma_load_2d(dst + (16 * q + 8 * u) * WROW, &P.tm[sgk][u], xw,
-                                    lrb * (RT / 2) + QMM_PAIR_BOX * q, &full[s], policy);
-                    }
-                    last_use[s] = n / S_;
-                    ++n;
-                    if (++s == S_) s = 0;
-                }
+                for (; k < G.n && ok; ++k) issue_tile(k, c);
             }
         }
+        if (!waited) pdl_wait();
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
             atomicExch(abort_flag, 1);
@@ -305,7 +359,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
             if (xn > 0) mbar_wait_bounded(xfull, (uint32_t)(xn - 1) & 1u, P.timeout_ns);
         }
         __syncwarp();
-        if (cs > 1) cluster_sync_all();         // no CTA leaves while a peer may address it
+        if (cs > 1) {                            // no CTA leaves while a peer may address it
+            cluster_wait();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -314,11 +371,13 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
     const int g = lane >> 2, cq = lane & 3;
     const int rq = warp % RW, hb = warp / RW;    // rows 16*rq .. +15, super-block hb of each tile
     const int r0w = 16 * rq;
-    int pos = rb_begin, hint = 0;
-    Group G;
+    const int rt = rq * 32 + lane;               // slot of this lane's partial sums
+    Walk wk;
+    walk_start(wk, cid, gmax, P.nblocks);
+    Group G{};
     uint32_t fphase = 0, xph = 0;
     bool aborted = false;
-    int s = 0, kb = 0;                           // kb: row blocks reduced by this CTA
+    int s = 0, grp = 0;
     const uint32_t magic16 = 0x64006400u;        // half2 (1024, 1024), for the scale decode
     SbScale* sw = scl + warp * (SBW * 16);       // this warp's rows: [SBW][16]
     uint32_t* subw = subt + warp * (SBW * 16);   // [SBW][8][2]
@@ -329,13 +388,13 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
             atomicExch(abort_flag, 1);
         }
     };
-    while (next_group(segs, P.nseg, pos, rb_end, hint, G)) {
+    while (next_group(segs, P.nseg, gmax, P.nblocks, ncl, wk, G)) {
         const int nval = seg_nval(segs[G.sg[0]]);
         float acc[GR][4];
 #pragma unroll
         for (int k = 0; k < GR; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
         for (int c = c0; c < c1; ++c) {
-            consumer_bar();                      // B fragments of the previous chunk no longer read
+            consumer_bar();                      // B fragments and half slots no longer read
             if (!aborted && !warp_wait(xfull, xph, P.timeout_ns, lane)) fail();
             xph ^= 1u;
             if (!aborted) {
@@ -411,7 +470,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
                             const uint4 sa = *reinterpret_cast<const uint4*>(swa + j * 16);
                             const uint4 sb = *reinterpret_cast<const uint4*>(swa + j * 16 + 8);
                             const uint2 sub = subg[j * 8];                   // rows g, g + 8
-                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+                            float d[4];
 #pragma unroll
                             for (int hs = 0; hs < 2; ++hs) {
                                 const uint32_t Wa = (hs ? wa.y : wa.x) >> (4 * nib);
@@ -423,7 +482,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
                                 a[2] = bf16x2_sub(lop_and_or(Wa >> 8, msk, mag), sub.x);
                                 a[3] = bf16x2_sub(lop_and_or(Wb >> 8, msk, mag), sub.y);
                                 const uint4 bf = bfl[(2 * j + hs) * 32];
-                                mma_bf16(d, a, bf.x, bf.y);
+                                if (hs == 0)
+                                    mma_bf16_z(d, a, bf.x, bf.y);
+                                else
+                                    mma_bf16(d, a, bf.x, bf.y);
                                 mma_bf16(d, a, bf.z, bf.w);
                             }
                             const uint64_t sxv = *reinterpret_cast<const uint64_t*>(sxq + j * NT);
@@ -449,70 +511,106 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
                     }
             }
         }
-        // ---- outputs of the group's row blocks (the barriers run for every
+        // ---- outputs of the group (barrier counts are the same for every
         // warp whatever its state, so that none is left waiting)
+        if (hb == 1) {
 #pragma unroll
-        for (int k = 0; k < GR; ++k) {
-            if (k >= G.n) break;
-            consumer_bar();                          // the half buffer is free
-            if (hb == 1) halfb[rq * 32 + lane] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
-            consumer_bar();
-            if (hb == 1 || aborted) continue;
+            for (int k = 0; k < GR; ++k)
+                if (k < G.n) halfb[k * (RW * 32) + rt] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+        }
+        consumer_bar();
+        if (hb == 0) {
             // super-block 0 + super-block 1 of every chunk of this rank
-            const float4 o = halfb[rq * 32 + lane];
-            float v[4] = {acc[k][0] + o.x, acc[k][1] + o.y, acc[k][2] + o.z, acc[k][3] + o.w};
-            const int rt = rq * 32 + lane;           // 0 .. RW*32-1
+#pragma unroll
+            for (int k = 0; k < GR; ++k)
+                if (k < G.n) {
+                    const float4 o = halfb[k * (RW * 32) + rt];
+                    acc[k][0] += o.x;
+                    acc[k][1] += o.y;
+                    acc[k][2] += o.z;
+                    acc[k][3] += o.w;
+                }
+            bool write = !aborted;
             if (cs > 1) {
-                // split columns: partial sums meet in rank 0, added in rank order
-                const int kk = kb++;
+                // split columns: partial sums meet in rank 0 (tx-counted remote
+                // stores), added in rank order
+                if (!cw) {
+                    cluster_wait();
+                    cw = true;
+                }
                 if (rank != 0) {
-                    if (kk > 0 && !mbar_wait_bounded_cluster(red_free, (uint32_t)(kk - 1) & 1u, P.timeout_ns)) {
+                    write = false;
+                    if (!aborted && grp > 0 &&
+                        !mbar_wait_bounded_cluster(red_free, (uint32_t)(grp - 1) & 1u, P.timeout_ns))
                         fail();
-                        continue;
+                    if (!aborted) {
+                        const uint32_t rbar = mapa_shared(smem_u32(red_full), 0);
+#pragma unroll
+                        for (int k = 0; k < GR; ++k)
+                            if (k < G.n) {
+                                const float4* slot = red + ((size_t)(rank - 1) * gmax + k) * (RW * 32) + rt;
+                                st_async_f4(mapa_shared(smem_u32(slot), 0),
+                                            make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]), rbar);
+                            }
                     }
-                    const uint32_t slot = smem_u32(red + (size_t)(rank - 1) * RW * 32 + rt);
-                    st_cluster_f4(mapa_shared(slot, 0), v[0], v[1], v[2], v[3]);
-                    mbar_arrive_remote(mapa_shared(smem_u32(red_full), 0));
-                    continue;                        // rank 0 writes the outputs
+                } else {
+                    if (tid == 0)
+                        mbar_arrive_expect_tx(red_full, (uint32_t)((cs - 1) * G.n * RW * 32 * sizeof(float4)));
+                    if (!aborted && !mbar_wait_bounded_cluster(red_full, (uint32_t)grp & 1u, P.timeout_ns)) fail();
+                    if (!aborted) {
+                        for (int r = 1; r < cs; ++r) {
+#pragma unroll
+                            for (int k = 0; k < GR; ++k)
+                                if (k < G.n) {
+                                    const float4 p = red[((size_t)(r - 1) * gmax + k) * (RW * 32) + rt];
+                                    acc[k][0] += p.x;
+                                    acc[k][1] += p.y;
+                                    acc[k][2] += p.z;
+                                    acc[k][3] += p.w;
+                                }
+                        }
+                    }
+                    half_bar();                  // every reader is done with the slots
+                    if (tid == 0)
+                        for (int r = 1; r < cs; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_free), (uint32_t)r));
+                    write = !aborted;
                 }
-                if (!mbar_wait_bounded_cluster(red_full, (uint32_t)kk & 1u, P.timeout_ns)) {
-                    fail();
-                    continue;
-                }
-                for (int r = 1; r < cs; ++r) {
-                    const float4 p = red[(size_t)(r - 1) * RW * 32 + rt];
-                    v[0] += p.x;
-                    v[1] += p.y;
-                    v[2] += p.z;
-                    v[3] += p.w;
-                }
-                for (int r = 1; r < cs; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_free), (uint32_t)r));
             }
-            // rows r0w+g, r0w+g+8 of the tile x tokens 2cq, 2cq+1
-            const Seg& S = segs[G.sg[k]];
-            const int boff = seg_boff(S);
-            const int lrb = G.rb[k] - S.tile0;
-            const int trg = r0w + g;
-            if (S.mode == MODE_PLAIN) {
+            if (write) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = lrb * RT + trg + (i >> 1) * 8;
-                    const int tok = 2 * cq + (i & 1);
-                    if (row < S.nout && tok < nval) S.y[(int64_t)(boff + tok) * S.ld_y + row] = v[i];
-                }
-            } else {
-                // row g is the gate row of pair p0 + 8 rq + g, row g + 8 its up row
-                const int out = lrb * (RT / 2) + QMM_PAIR_BOX * rq + g;
+                for (int k = 0; k < GR; ++k) {
+                    if (k >= G.n) break;
+                    // rows r0w+g, r0w+g+8 of the tile x tokens 2cq, 2cq+1
+                    const float* v = acc[k];
+                    const Seg& S = segs[G.sg[k]];
+                    const int boff = seg_boff(S);
+                    const int lrb = G.rb[k] - S.tile0;
+                    if (S.mode == MODE_PLAIN) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int tok = 2 * cq + i;
-                    if (out < S.nout && tok < nval)
-                        S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_f(S.act, v[i]) * v[2 + i];
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = lrb * RT + r0w + g + (i >> 1) * 8;
+                            const int tok = 2 * cq + (i & 1);
+                            if (row < S.nout && tok < nval) S.y[(int64_t)(boff + tok) * S.ld_y + row] = v[i];
+                        }
+                    } else {
+                        // row g is the gate row of pair p0 + 8 rq + g, row g + 8 its up row
+                        const int out = lrb * (RT / 2) + QMM_PAIR_BOX * rq + g;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int tok = 2 * cq + i;
+                            if (out < S.nout && tok < nval)
+                                S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_f(S.act, v[i]) * v[2 + i];
+                        }
+                    }
                 }
             }
         }
+        ++grp;
     }
-    if (cs > 1) cluster_sync_all();
+    if (cs > 1) {
+        if (!cw) cluster_wait();
+        cluster_sync_all();
+    }
 }
 
 }  // namespace
@@ -521,15 +619,7 @@ cudaError_t qmm_set_smem(int bytes) {
     return cudaFuncSetAttribute(qmm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-size_t qmm_smem_bytes(int nstages, int csize) { return qmm_layout(nstages, csize).total; }
-
-// Most stages (up to 3) that keep two CTAs resident on an SM (228 KB of
-// shared memory, 1 KB of it reserved per CTA).
-int qmm_stages_for(int csize) {
-    for (int S = 3; S > 2; --S)
-        if (2 * (qmm_layout(S, csize).total + 1024) <= 228 * 1024) return S;
-    return 2;
-}
+size_t qmm_smem_bytes(int nstages, int csize, int gmax) { return qmm_layout(nstages, csize, gmax).total; }
 
 // Clusters of `csize` CTAs that can be resident at once (CTAs for csize 1).
 cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out) {
