@@ -47,7 +47,7 @@ struct QmmParams {
 };
 constexpr int QMM_MAX_CSIZE = 4;
 constexpr int QMM_GROUP = 4;              // row blocks sharing one staging of x
-constexpr int QMM_MIN_BATCH = 3;          // dense calls with at least this many x rows
+constexpr int QMM_MIN_BATCH = 2;          // dense calls with at least this many x rows
 constexpr int QMM_MOE_MIN_TOKENS = 2;     // MoE calls with at least this many tokens
 cudaError_t qmm_set_smem(int bytes);
 size_t qmm_smem_bytes(int nstages, int csize, int gmax);
