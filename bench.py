@@ -17,6 +17,14 @@ host memory and the layer output copied back, every step.
 --impl reference runs the CPU oracle (fp64, all host cores) on a bounded
 sample of the same layers as the reference arm.
 
+--workload selects one of the other named shapes instead of the layer, with
+the same JSON line: llama_ffn (SwiGLU FFN 2 x 14336 x 4096 + 4096 x 14336 at
+--batch M, --fmt q4k|q80), lm_head (262144 x 2560 Q4_K, batch 1),
+mixtral_moe (8 experts, top-2, 16 tokens, Q4_K) and matvec_small (Q4_K 256 x
+2560, batch 1).  A step is one call of the workload; weight copies rotate
+so that each step reads weights that are not in L2 (at least three times
+the L2 size in total, one copy when a single one is larger).
+
 Multi-GPU (torchrun): every rank runs an independent replica (the layer has
 no data-path exchange); timing is max over ranks, value is the sum.
 """
@@ -40,6 +48,7 @@ LAYER_BYTES = 6_574_080 + 2_949_120 + 29_491_200 + 21_504_000   # 60,518,400
 GATEUP_BYTES = 29_491_200
 NLAYERS = 34
 METRIC = "effective weight GB/s per quantized matvec (decode layer, batch 1)"
+WORKLOADS = ("gemma_layer", "llama_ffn", "lm_head", "mixtral_moe", "matvec_small")
 
 
 def parse():
@@ -51,7 +60,16 @@ def parse():
     ap.add_argument("--layers", type=int, default=NLAYERS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    return ap.parse_args()
+    ap.add_argument("--workload", default="gemma_layer", choices=list(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=8, help="x rows (llama_ffn)")
+    ap.add_argument("--fmt", default="q4k", choices=["q4k", "q80"], help="weight format (llama_ffn)")
+    a = ap.parse_args()
+    if a.workload != "gemma_layer":
+        if "--steps" not in sys.argv:
+            a.steps = 2200 if a.workload == "matvec_small" else 200   # at least two passes over the copies
+        if "--warmup" not in sys.argv:
+            a.warmup = 20
+    return a
 
 
 def dist_setup(args):
@@ -352,6 +370,225 @@ def l2_bytes():
     return 129_000_000
 
 
+# ---------------------------------------------------------------- other workloads
+
+class Workload:
+    """one named shape: weight copies, the step (one call of the workload),
+    its dominant kernel, and the host-side oracle sample."""
+
+    def __init__(self, args, dev):
+        import torch
+        import block_quantized_weight_super_gb300 as lq
+        import synth
+        self.lq, self.dev = lq, dev
+        f32 = dict(dtype=torch.float32, device=dev)
+        name = args.workload
+        self.name = name
+        up = lambda a: torch.from_numpy(a).to(dev)
+        if name == "llama_ffn":
+            fmt = lq.LQ_Q4_K if args.fmt == "q4k" else lq.LQ_Q8_0
+            M = args.batch
+            W, X = synth.llama_ffn(fmt, M, seed=0)
+            H, I = synth.LLAMA_HIDDEN, synth.LLAMA_INTER
+            rb = lq.lq_row_bytes(fmt, H)
+            wgu = torch.empty(2 * I * rb, dtype=torch.uint8, device=dev)
+            lq.lq_pack_gate_up(fmt, up(W["wg"]), up(W["wu"]), I, H, wgu)
+            base = {"wgu": wgu, "wd": up(W["wd"])}
+            self.bytes = wgu.numel() + base["wd"].numel()
+            self.dom_bytes = wgu.numel()
+            self.x_host = X
+            self.x = up(X)
+            self.h = torch.empty((M, I), **f32)
+            self.y = torch.empty((M, H), **f32)
+            self.desc = (f"Llama-3-8B-shaped SwiGLU FFN, batch {M}, {args.fmt.upper()}: gate+up 2x14336x4096 "
+                         f"fused with SwiGLU, down 4096x14336")
+            self.dom_name = f"ffn gate+up SwiGLU ({args.fmt.upper()} 2x14336x4096, batch {M})"
+            self.launches = 2
+            self._gu = lambda w, st: lq.lq_ffn_gate_up_act(fmt, w["wgu"], I, H, self.x, self.h, M, lq.LQ_ACT_SWIGLU, st)
+            self._down = lambda w, st: lq.lq_matvec(fmt, w["wd"], H, I, self.h, self.y, M, st)
+            self.step = lambda w, st: (self._gu(w, st), self._down(w, st))
+            self.dom = self._gu
+            self.cpu_jobs = [(fmt, W["wg"], H, X), (fmt, W["wu"], H, X), (fmt, W["wd"], I, np.zeros((M, I), np.float32))]
+        elif name in ("lm_head", "matvec_small"):
+            if name == "lm_head":
+                Wn, x = synth.lm_head(0)
+                cols = synth.GEMMA3_HIDDEN
+                self.desc = "large-vocab lm_head: Q4_K 262144x2560 of an RMS-normed x, batch 1, fp32 logits"
+            else:
+                Wn, x = synth.matvec_small(0)
+                cols = 2560
+                self.desc = "single Q4_K matvec 256x2560, batch 1"
+            rows = Wn.shape[0]
+            base = {"w": up(Wn)}
+            self.bytes = self.dom_bytes = Wn.nbytes
+            self.x_host = x
+            self.x = up(x)
+            self.y = torch.empty((1, rows), **f32)
+            self.dom_name = f"Q4_K matvec {rows}x{cols}, batch 1"
+            self.launches = 1
+            self.step = lambda w, st: lq.lq_matvec(lq.LQ_Q4_K, w["w"], rows, cols, self.x, self.y, 1, st)
+            self.dom = self.step
+            self.cpu_jobs = [(lq.LQ_Q4_K, Wn, cols, x)]
+        elif name == "mixtral_moe":
+            R, W1, W3, W2, X = synth.mixtral_moe(0)
+            E, H = R.shape
+            I = W1[0].shape[0]
+            T, K = X.shape[0], synth.MIXTRAL_TOPK
+            base = {"d1": [up(a) for a in W1], "d3": [up(a) for a in W3], "d2": [up(a) for a in W2]}
+            self.R = up(R)
+            self.x_host = X
+            self.x = up(X)
+            self.y = torch.empty((T, H), **f32)
+            self.idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+            self.wts = torch.empty((T, K), **f32)
+            nb = lq.lq_moe_workspace_bytes(E, K, T, H, I)
+            self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            self._moe = lambda w, st: lq.lq_moe_ffn(self.R, E, K, lq.LQ_Q4_K, w["d1"], w["d3"], w["d2"], H, I,
+                                                     self.x, self.y, T, self.idx, self.wts, self.ws, nb, st)
+            self._moe(base, None)
+            torch.cuda.synchronize()
+            touched = len(set(self.idx.cpu().numpy().ravel().tolist()))
+            self.bytes = self.dom_bytes = touched * (W1[0].nbytes + W3[0].nbytes + W2[0].nbytes)
+            self.desc = (f"Mixtral-shaped MoE FFN: 8 experts, top-2, hidden 4096, inter 14336, Q4_K, 16 tokens "
+                         f"({touched} experts touched; weight bytes count those)")
+            self.dom_name = "grouped expert FFN (route + grouped gate+up + grouped down + combine)"
+            self.launches = 4
+            self.step = self._moe
+            self.dom = self._moe
+            e0 = int(self.idx[0, 0].item())
+            self.cpu_jobs = [(lq.LQ_Q4_K, W1[e0], H, X[:1]), (lq.LQ_Q4_K, W3[e0], H, X[:1]),
+                             (lq.LQ_Q4_K, W2[e0], I, np.zeros((1, I), np.float32))]
+        else:
+            raise ValueError(name)
+        # cold L2: copies totalling at least 3x the L2 size
+        ncopy = max(1, min(2048, -(-3 * l2_bytes() // max(1, self.bytes))))
+        if self.bytes > l2_bytes():
+            ncopy = 1
+        self.copies = [base] + [self._clone(base) for _ in range(ncopy - 1)]
+        torch.cuda.synchronize()
+
+    @staticmethod
+    def _clone(d):
+        return {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone()) for k, v in d.items()}
+
+    def cpu(self, rows_frac=0.02):
+        import oracle
+        nth = os.cpu_count() or 1
+        nbytes = 0
+        t0 = time.perf_counter()
+        for fmt, W, cols, xin in self.cpu_jobs:
+            r = max(1, int(W.shape[0] * rows_frac))
+            oracle.matvec(fmt, W[:r], r, cols, xin, nth)
+            nbytes += W[:r].nbytes
+        dt = time.perf_counter() - t0
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
+                "sample": f"first {rows_frac * 100:g}% of the rows of the workload's matrices "
+                          f"({nbytes} weight bytes), fp64, {nth} threads"}
+
+
+def time_graph(fn, copies, steps, warmup, st):
+    """ms per step of fn over the rotating copies, exactly `steps` steps,
+    from CUDA graphs (a full pass over the copies and one partial pass)."""
+    import torch
+
+    def capture(cs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for w in cs:
+                fn(w, st)
+        return g
+
+    n = len(copies)
+    with torch.cuda.stream(st):
+        for w in copies:
+            fn(w, st)
+        st.synchronize()
+        full = capture(copies)
+        rem = steps % n
+        part = capture(copies[:rem]) if rem else None
+        for _ in range(max(1, -(-warmup // n))):
+            full.replay()
+        st.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps // n):
+            full.replay()
+        if part is not None:
+            part.replay()
+        e1.record(st)
+        st.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_workload(args, ws, rank, local, peak, peak_src):
+    import torch
+    import block_quantized_weight_super_gb300 as lq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lq.lib()
+    wl = Workload(args, dev)
+    st = torch.cuda.Stream(device=dev)
+    rc, _ = lq.lq_device_status()
+    assert rc == 0
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = time_graph(wl.step, wl.copies, args.steps, args.warmup, st)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+    ms_all = ms
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_all = float(t.item())
+    dom_ms = ms if wl.dom is wl.step else time_graph(wl.dom, wl.copies, args.steps, args.warmup, st)
+    rc, _ = lq.lq_device_status()
+    assert rc == 0, "device status after timed region"
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(np.ascontiguousarray(wl.x_host)).pin_memory()
+        yh = torch.empty(tuple(wl.y.shape), dtype=torch.float32).pin_memory()
+        n = len(wl.copies)
+        with torch.cuda.stream(st):
+            for i in range(min(args.warmup, 5)):
+                wl.x.copy_(xh, non_blocking=True)
+                wl.step(wl.copies[i % n], st)
+                yh.copy_(wl.y, non_blocking=True)
+            st.synchronize()
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                wl.x.copy_(xh, non_blocking=True)
+                wl.step(wl.copies[i % n], st)
+                yh.copy_(wl.y, non_blocking=True)
+            st.synchronize()
+            t_e2e = (time.perf_counter() - t0) / args.steps
+        e2e = {"value": ws * wl.bytes / t_e2e / 1e9, "unit": "GB/s", "us_per_call": t_e2e * 1e6,
+               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4)}
+    if rank != 0:
+        return
+    achieved = wl.dom_bytes / (dom_ms * 1e-3) / 1e9
+    line = {"metric": "effective weight GB/s per quantized matvec", "value": ws * wl.bytes / (ms_all * 1e-3) / 1e9,
+            "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
+            "us_per_call": ms_all * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded random blocks)",
+            "config": {"workload": wl.desc, "weight_bytes_per_step": wl.bytes, "weight_copies": len(wl.copies),
+                       "l2": ("inputs larger than L2" if len(wl.copies) * wl.bytes > l2_bytes() else
+                              "inputs NOT larger than L2") +
+                             f" ({len(wl.copies)} rotating copies, {len(wl.copies) * wl.bytes / 1e9:.2f} GB)",
+                       "parallelism": f"replicas x{ws}"},
+            "frac_of_hbm": ws * wl.bytes / (ms_all * 1e-3) / 1e9 / peak,
+            "roofline": {"bound": "hbm", "kernel": wl.dom_name, "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "us_per_launch": dom_ms * 1e3},
+            "clocks": clk.summary(), "e2e": e2e, "gpu_launches": wl.launches * args.steps,
+            "cpu_baseline": wl.cpu() if (ws == 1 and not args.no_cpu) else None}
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args)
@@ -366,6 +603,13 @@ def main():
                               "inputs NOT larger than L2") +
                              f" ({args.layers} rotating layer copies, {args.layers * LAYER_BYTES / 1e9:.2f} GB)",
                        "parallelism": f"replicas x{ws}"}}
+    if args.workload != "gemma_layer":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the default workload"}))
+            return
+        bench_workload(args, ws, rank, local, peak, peak_src)
+        return
     if args.impl == "reference":
         if rank != 0:
             return
