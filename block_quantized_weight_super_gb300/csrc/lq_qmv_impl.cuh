@@ -527,22 +527,11 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         // reducing all but the last two tiles, which the consumer warps share.
         const uint64_t policy = policy_evict_first();
         Walk w = walk0;
-        if (!P.dev_counts) {
-            // weights do not depend on the preceding kernel: warm L2 with the
-            // first tiles while it finishes (a hint; L2 stays coherent)
-            walk_fix<B>(sm.segs, P.nseg, w);
-            Walk wp = w;
-            for (int k = 0; k < S_ && wp.t < wp.end; ++k) {
-                const QTile g = qtile(P, sm.segs[wp.hint], wp.t);
-                if (lane == 0 && g.tma) {
-                    prefetch_l2_bulk(g.src1, g.bytes1);
-                    if (g.bytes2) prefetch_l2_bulk(g.src2, g.bytes2);
-                }
-                wp.t += wp.step;
-                walk_fix<B>(sm.segs, P.nseg, wp);
-            }
-        }
-        pdl_wait();
+        // weights do not depend on the preceding kernel: unless the row
+        // counts do, the first tiles go into their stages before waiting
+        // for it (the CTA starts while that kernel finishes)
+        const bool early = !P.dev_counts;
+        if (!early) pdl_wait();
         walk_fix<B>(sm.segs, P.nseg, w);
         Walk wr = w;                      // reduction walk, S tiles behind
         uint32_t ephase = 0;
@@ -559,6 +548,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             walk_fix<B>(sm.segs, P.nseg, wr);
         };
         for (int n = 0, s = 0; w.t < w.end; ++n) {
+            if (early && n == S_) pdl_wait();   // stages full: the rest waits
             if (*reinterpret_cast<volatile int*>(sm.abort_flag)) break;
             if (n >= S_) {            // wait until the consumers released stage s
                 if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
@@ -588,6 +578,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             if (++s == S_) s = 0;
             ntiles = n + 1;
         }
+        if (early && ntiles < S_) pdl_wait();
         // tiles before the last two are reduced here while the consumers
         // finish; the consumer warps share the last two
         while (ok && nr < ntiles - 2 && !*reinterpret_cast<volatile int*>(sm.abort_flag)) {
