@@ -55,7 +55,7 @@ struct DevInfo {
     bool init = false;
     int sms = 0;
     unsigned* status = nullptr;
-    int qmm_res[3] = {0, 0, 0};   // resident tensor-core CTAs / clusters of 2 / of 4
+    int qmm_res[2][3] = {};       // resident tensor-core CTAs / clusters of 2 / of 4 (Q4_K, Q8_0)
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -77,12 +77,16 @@ int dev_info(DevInfo** out) {
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
-        if (e == cudaSuccess) e = qmm_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
+        if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE; ++i, cs *= 2) {
-            const QmmCfg q = qmm_cfg(cs);
-            e = qmm_max_resident(cs, qmm_smem_bytes(q.nstages, cs, q.gmax), d.sms, &d.qmm_res[i]);
-            if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
+        for (int f = 0; f < 2; ++f) {
+            const int fmt = f ? FMT_Q8_0 : FMT_Q4_K;
+            for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE; ++i, cs *= 2) {
+                const QmmCfg q = qmm_cfg(cs);
+                e = qmm_max_resident(fmt, cs, qmm_smem_bytes(fmt, q.nstages, cs, q.gmax), d.sms, &d.qmm_res[f][i]);
+                if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
+            }
         }
         d.init = true;
     }
@@ -257,16 +261,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct MapKey {
     const void* base;
     int64_t rows, rowbytes, stride;
-    int box_rows;
+    int box_inner, box_rows;
     bool operator==(const MapKey& o) const {
         return base == o.base && rows == o.rows && rowbytes == o.rowbytes && stride == o.stride &&
-               box_rows == o.box_rows;
+               box_inner == o.box_inner && box_rows == o.box_rows;
     }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
         size_t h = std::hash<const void*>()(k.base);
-        for (int64_t v : {k.rows, k.rowbytes, k.stride, (int64_t)k.box_rows})
+        for (int64_t v : {k.rows, k.rowbytes, k.stride, (int64_t)k.box_inner, (int64_t)k.box_rows})
             h = h * 1000003u ^ std::hash<int64_t>()(v);
         return h;
     }
@@ -275,8 +279,10 @@ std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 EncodeTiledFn g_encode = nullptr;
 
-int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbytes, int64_t stride, int box_rows) {
-    const MapKey key{base, rows, rowbytes, stride, box_rows};
+// box: box_inner uint32 elements (a row's bytes of one tile) x box_rows rows
+int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbytes, int64_t stride, int box_inner,
+               int box_rows) {
+    const MapKey key{base, rows, rowbytes, stride, box_inner, box_rows};
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
     if (it != g_maps.end()) {
@@ -293,7 +299,7 @@ int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbyte
     }
     const cuuint64_t dims[2] = {(cuuint64_t)(rowbytes / 4), (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)stride};
-    const cuuint32_t box[2] = {(cuuint32_t)(QMM_KC / 256 * 144 / 4), (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUtensorMap m;
     const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
@@ -307,12 +313,14 @@ int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbyte
 }
 
 // ---------------------------------------------------------------- tensor-core path
-// Q4_K segments of up to QMM_NT x rows whose columns are a multiple of the
-// tile width, with 16-byte aligned weights and x (tensor maps, bulk copies).
+// Q4_K or Q8_0 segments (one format) of up to QMM_NT x rows whose columns
+// are a multiple of the tile width, with 16-byte aligned weights and x
+// (tensor maps, bulk copies).
 bool qmm_eligible(const std::vector<Seg>& segs, int64_t cols) {
-    if (cols % QMM_KC != 0 || cols > (1 << 20)) return false;
+    if (segs.empty() || !qmm_format_ok(segs[0].fmt)) return false;
+    if (cols % qmm_kc(segs[0].fmt) != 0 || cols > (1 << 20)) return false;
     for (auto& s : segs) {
-        if (s.fmt != FMT_Q4_K) return false;
+        if (s.fmt != segs[0].fmt) return false;
         if (!al(s.w, 16) || (s.w2 && !al(s.w2, 16)) || !al(s.x, 16)) return false;
     }
     return true;
@@ -325,7 +333,10 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
-    const int nchunk = (int)(cols / QMM_KC);
+    const int fmt = segs[0].fmt;
+    const int f = fmt == FMT_Q8_0 ? 1 : 0;
+    const int nchunk = (int)(cols / qmm_kc(fmt));
+    const int box_inner = qmm_wrow(fmt) / 4;
     auto blocks_of = [](const Seg& s) {
         const int64_t r = (s.mode == MODE_PLAIN ? 1 : 2) * (int64_t)s.nout;
         return (r + QMM_RT - 1) / QMM_RT;
@@ -338,7 +349,7 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
     int ci = 0;
     double best = 0.0;
     for (int i = 0, cs = 1; cs <= QMM_MAX_CSIZE && cs <= nchunk; ++i, cs *= 2) {
-        const int res = dev->qmm_res[i];
+        const int res = dev->qmm_res[f][i];
         if (res < 1) continue;
         const double t = (double)((nb_all + res - 1) / res) * ((nchunk + cs - 1) / cs) * (1.0 + 0.05 * (cs - 1));
         if (best == 0.0 || t < best) {
@@ -346,10 +357,10 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
             ci = i;
         }
     }
-    const int cs = 1 << ci, res = std::max(1, dev->qmm_res[ci]);
+    const int cs = 1 << ci, res = std::max(1, dev->qmm_res[f][ci]);
     const QmmCfg qc = qmm_cfg(cs);
-    const size_t smem = qmm_smem_bytes(qc.nstages, cs, qc.gmax);
-    const int64_t rb = cols / 256 * 144;
+    const size_t smem = qmm_smem_bytes(fmt, qc.nstages, cs, qc.gmax);
+    const int64_t rb = rowbytes(fmt, cols);
     for (size_t s0 = 0; s0 < segs.size(); s0 += QMM_MAX_SEG) {
         QmmParams P;
         memset(&P, 0, sizeof P);
@@ -360,13 +371,13 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
             s.ntiles = (int32_t)blocks_of(s);
             t += s.ntiles;
             if (s.mode == MODE_PLAIN) {
-                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, QMM_RT);
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, box_inner, QMM_RT);
             } else if (s.mode == MODE_PAIR_TWO) {
-                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, QMM_PAIR_BOX);
-                if (!rc) rc = tensor_map(&P.tm[n][1], s.w2, s.nout, rb, rb, QMM_PAIR_BOX);
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, rb, box_inner, QMM_PAIR_BOX);
+                if (!rc) rc = tensor_map(&P.tm[n][1], s.w2, s.nout, rb, rb, box_inner, QMM_PAIR_BOX);
             } else {                        // packed gate / up: rows 2i and 2i + 1
-                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, 2 * rb, QMM_PAIR_BOX);
-                if (!rc) rc = tensor_map(&P.tm[n][1], s.w + rb, s.nout, rb, 2 * rb, QMM_PAIR_BOX);
+                rc = tensor_map(&P.tm[n][0], s.w, s.nout, rb, 2 * rb, box_inner, QMM_PAIR_BOX);
+                if (!rc) rc = tensor_map(&P.tm[n][1], s.w + rb, s.nout, rb, 2 * rb, box_inner, QMM_PAIR_BOX);
             }
             if (rc) return rc;
             P.seg[n++] = s;
@@ -389,10 +400,16 @@ int run_qmm(std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
         P.timeout_ns = g_timeout_ns.load();
         P.status = dev->status;
         const int grid = cs * ncl;
-        cudaError_t e = qmm_launch(P, grid, smem, st);
+        cudaError_t e = qmm_launch(fmt, P, grid, smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec launch");
     }
     return LQ_OK;
+}
+
+// Batch from which a dense call takes the tensor-core kernel (never for
+// formats it does not handle).
+int qmm_min_batch(int fmt) {
+    return fmt == FMT_Q4_K ? QMM_MIN_BATCH : fmt == FMT_Q8_0 ? QMM_MIN_BATCH_Q8 : 1 << 30;
 }
 
 // Widest batch width (4, 2 or 1) the quantized matvec kernel can plan for
@@ -496,7 +513,7 @@ int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
     if (rows == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
-    if (batch >= QMM_MIN_BATCH && fmt == FMT_Q4_K) {
+    if (batch >= qmm_min_batch(fmt)) {
         std::vector<Seg> segs;
         for (int b0 = 0; b0 < batch; b0 += QMM_NT)
             segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(QMM_NT, batch - b0)));
@@ -523,7 +540,7 @@ int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int
     if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
         (nv && (rc = check_f32(v, "v"))))
         return rc;
-    if (batch >= QMM_MIN_BATCH) {
+    if (batch >= qmm_min_batch(fq)) {
         std::vector<Seg> segs;
         for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
             const int nb = std::min(QMM_NT, batch - b0);
@@ -568,7 +585,7 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
     if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
     if (inter == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
-    if (batch >= QMM_MIN_BATCH && fmt == FMT_Q4_K) {
+    if (batch >= qmm_min_batch(fmt)) {
         std::vector<Seg> segs;
         for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
             Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(QMM_NT, batch - b0));
@@ -645,8 +662,8 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
 
     // grouped expert gate+up (+SwiGLU): segment per (expert, chunk of B rows)
     // tensor-core path: Q4_K, both widths multiples of the tile, aligned rows
-    bool tc = ntok >= QMM_MOE_MIN_TOKENS && fmt == FMT_Q4_K && hidden % QMM_KC == 0 &&
-              inter % QMM_KC == 0 && al(X, 16);
+    bool tc = ntok >= QMM_MOE_MIN_TOKENS && qmm_format_ok(fmt) && hidden % qmm_kc(fmt) == 0 &&
+              inter % qmm_kc(fmt) == 0 && al(X, 16);
     for (int ex = 0; tc && ex < E; ++ex) tc = al(W1[ex], 16) && al(W3[ex], 16) && al(W2[ex], 16);
     {
         const int B = tc ? QMM_NT : batch_width(hidden, ntok, {fmt}, true);

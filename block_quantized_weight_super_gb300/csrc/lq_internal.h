@@ -20,15 +20,17 @@ struct MoeWs {
     float* ybuf;         // [ntok*topk][hidden] expert outputs
 };
 
-// tensor-core matvec for up to QMM_NT x rows of Q4_K (lq_qmm.cu): tiles of
-// QMM_RT weight rows x QMM_KC columns; segments' tile0 = first row block.
+// tensor-core matvec for up to QMM_NT x rows of Q4_K or Q8_0 (lq_qmm.cu):
+// tiles of QMM_RT weight rows x QMM_KC (Q4_K) or QMM_KC8 (Q8_0) columns;
+// segments' tile0 = first row block.
 // Weights are fetched through 2-D tensor maps (uint32 elements, one row of
 // the matrix per tensor row): per segment map 0 is the plain matrix (boxes of
 // QMM_RT rows) or the gate rows of a pair segment, map 1 the up rows (boxes
 // of 8 rows; packed gate/up matrices use a row stride of two rows).
 constexpr int QMM_NT = 8;
 constexpr int QMM_RT = 64;
-constexpr int QMM_KC = 512;
+constexpr int QMM_KC = 512;             // Q4_K tile columns (two super-blocks)
+constexpr int QMM_KC8 = 256;            // Q8_0 tile columns (eight blocks)
 constexpr int QMM_MAX_SEG = 16;
 constexpr int QMM_PAIR_BOX = 8;
 struct QmmParams {
@@ -47,12 +49,16 @@ struct QmmParams {
 };
 constexpr int QMM_MAX_CSIZE = 4;
 constexpr int QMM_GROUP = 4;              // row blocks sharing one staging of x
-constexpr int QMM_MIN_BATCH = 2;          // dense calls with at least this many x rows
+constexpr int QMM_MIN_BATCH = 2;          // dense Q4_K calls with at least this many x rows
+constexpr int QMM_MIN_BATCH_Q8 = 3;       // dense Q8_0 calls
 constexpr int QMM_MOE_MIN_TOKENS = 2;     // MoE calls with at least this many tokens
-cudaError_t qmm_set_smem(int bytes);
-size_t qmm_smem_bytes(int nstages, int csize, int gmax);
-cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out);
-cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t st);
+bool qmm_format_ok(int fmt);             // Q4_K, Q8_0
+int qmm_kc(int fmt);                     // columns per tile
+int qmm_wrow(int fmt);                   // weight bytes of a row per tile
+cudaError_t qmm_set_smem(int fmt, int bytes);
+size_t qmm_smem_bytes(int fmt, int nstages, int csize, int gmax);
+cudaError_t qmm_max_resident(int fmt, int csize, size_t smem, int sms, int* out);
+cudaError_t qmm_launch(int fmt, const QmmParams& P, int grid, size_t smem, cudaStream_t st);
 
 // quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
 cudaError_t qmv1_set_smem(int bytes);

@@ -55,16 +55,25 @@ namespace {
 
 constexpr int NT = QMM_NT;                 // x rows per pass
 constexpr int RT = QMM_RT;                 // weight rows per tile
-constexpr int KC = QMM_KC;                 // columns per tile
 constexpr int GR = QMM_GROUP;              // row blocks sharing one staging of x
 constexpr int RW = RT / 16;                // warps per column half (16 rows each)
-constexpr int NW = 2 * RW;                 // consumer warps: (row quarter, super-block of the tile)
-constexpr int SB = KC / 32;                // sub-blocks per tile
-constexpr int SBW = SB / 2;                // sub-blocks per warp
-constexpr int WROW = KC / 256 * 144;       // weight bytes of a row per tile
-constexpr int WSTAGE = RT * WROW;          // weight bytes per stage
-constexpr int XSTR = KC * 4 + 16;          // shared stride of an x row (bank spread)
-static_assert(KC == 512, "a warp takes one super-block of the tile");
+constexpr int NW = 2 * RW;                 // consumer warps: (row quarter, half of the tile's columns)
+
+// Tile geometry per weight format: Q4_K tiles are two super-blocks (512
+// columns, 288 bytes of a row), Q8_0 tiles eight blocks (256 columns, 272
+// bytes).  A (sub-)block is 32 columns either way.
+template <int FMT>
+struct QF {
+    static constexpr int KC = FMT == FMT_Q4_K ? 512 : 256;    // columns per tile
+    static constexpr int WROW = FMT == FMT_Q4_K ? 288 : 272;  // weight bytes of a row per tile
+    static constexpr int SB = KC / 32;                        // 32-column blocks per tile
+    static constexpr int SBW = SB / 2;                        // blocks per warp
+    static constexpr int WSTAGE = RT * WROW;                  // weight bytes per stage
+    static constexpr int XSTR = KC * 4 + 16;                  // shared stride of an x row (bank spread)
+    static constexpr int SCLB = FMT == FMT_Q4_K ? 16 : 8;     // bytes of a (row, block) scale entry
+    static constexpr int SUBB = FMT == FMT_Q4_K ? 4 : 0;      // bytes of a subtrahend entry
+};
+static_assert(QF<FMT_Q4_K>::KC == QMM_KC && QF<FMT_Q8_0>::KC == QMM_KC8, "tile widths");
 
 // Scales of one (row, sub-block), paired for the packed FMAs of the
 // epilogue: (dsc, dsc, e, e).  The bf16x2 subtrahends 128 + qb of rows g and
@@ -78,16 +87,18 @@ struct Layout {
 };
 
 // red: [csize-1][gmax][RW*32] partial sums of the other ranks (rank 0 only);
-// half: [gmax][RW*32] partial sums of the second super-block warps.
+// half: [gmax][RW*32] partial sums of the second-half warps.
+template <int FMT>
 __host__ __device__ inline Layout qmm_layout(int nstages, int csize, int gmax) {
+    using F = QF<FMT>;
     Layout L;
     size_t o = 0;
-    L.wst = o;  o += (size_t)nstages * WSTAGE;
-    L.xraw = o; o += (size_t)NT * XSTR;
-    L.bfr = o;  o += sizeof(uint4) * 2 * SB * 32;
-    L.sx = o;   o += sizeof(float) * SB * NT;
-    L.scl = o;  o += sizeof(SbScale) * NW * SBW * 16;
-    L.sub = o;  o += sizeof(uint32_t) * NW * SBW * 16;
+    L.wst = o;  o += (size_t)nstages * F::WSTAGE;
+    L.xraw = o; o += (size_t)NT * F::XSTR;
+    L.bfr = o;  o += sizeof(uint4) * 2 * F::SB * 32;
+    L.sx = o;   o += sizeof(float) * F::SB * NT;
+    L.scl = o;  o += (size_t)F::SCLB * NW * F::SBW * 16;
+    L.sub = o;  o += (size_t)F::SUBB * NW * F::SBW * 16;
     L.half = o; o += sizeof(float4) * gmax * RW * 32;
     L.red = o;  o += sizeof(float4) * (csize - 1) * gmax * RW * 32;
     L.bars = o; o += sizeof(uint64_t) * (2 * nstages + 4) + 16;
@@ -176,6 +187,35 @@ __device__ __forceinline__ void mma_bf16_z(float (&d)[4], const uint32_t (&a)[4]
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// half2 (lo = b, hi = a), round to nearest
+__device__ __forceinline__ uint32_t f16x2_pack(float hi, float lo) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float f16_lo_f(uint32_t v) { return half_bits_to_float(v); }
+__device__ __forceinline__ float f16_hi_f(uint32_t v) { return half_bits_to_float(v >> 16); }
+// fp16 B fragments of (already scaled) x columns (c0, c1, c2, c3) of one k
+// slice, hi then lo pieces, in the k order of bf16 ones below
+__device__ __forceinline__ uint4 x_frag_h(float4 a) {
+    const uint32_t h0 = f16x2_pack(a.z, a.x), h1 = f16x2_pack(a.w, a.y);
+    return make_uint4(h0, h1, f16x2_pack(a.z - f16_hi_f(h0), a.x - f16_lo_f(h0)),
+                      f16x2_pack(a.w - f16_hi_f(h1), a.y - f16_lo_f(h1)));
+}
+
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -221,16 +261,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
     return __shfl_sync(0xFFFFFFFFu, ok, 0);
 }
 
-__global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_constant__ QmmParams P) {
+template <int FMT>
+__global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_kernel(const __grid_constant__ QmmParams P) {
+    using F = QF<FMT>;
+    constexpr int KC = F::KC, WROW = F::WROW, SB = F::SB, SBW = F::SBW, WSTAGE = F::WSTAGE, XSTR = F::XSTR;
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
     const int S_ = P.nstages, cs = P.csize, gmax = P.gmax;
-    const Layout L = qmm_layout(S_, cs, gmax);
+    const Layout L = qmm_layout<FMT>(S_, cs, gmax);
     uint8_t* wst = smem + L.wst;
     uint8_t* xraw = smem + L.xraw;
     uint4* bfr = reinterpret_cast<uint4*>(smem + L.bfr);       // [2*SB k-slices][32 lanes]
-    float* sxs = reinterpret_cast<float*>(smem + L.sx);        // [SB][NT] sums of x per sub-block
-    SbScale* scl = reinterpret_cast<SbScale*>(smem + L.scl);   // [NW][SBW][16 rows]
+    float* sxs = reinterpret_cast<float*>(smem + L.sx);        // [SB][NT] Q4_K: sums of x per sub-block; Q8_0: x scales
+    uint8_t* sclb = smem + L.scl;                              // [NW][SBW][16 rows] scale entries
     uint32_t* subt = reinterpret_cast<uint32_t*>(smem + L.sub); // [NW][SBW][8][rows g, g+8]
     float4* halfb = reinterpret_cast<float4*>(smem + L.half);  // [gmax][RW*32]
     float4* red = reinterpret_cast<float4*>(smem + L.red);     // [csize-1][gmax][RW*32]
@@ -379,7 +422,8 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
     bool aborted = false;
     int s = 0, grp = 0;
     const uint32_t magic16 = 0x64006400u;        // half2 (1024, 1024), for the scale decode
-    SbScale* sw = scl + warp * (SBW * 16);       // this warp's rows: [SBW][16]
+    SbScale* sw = reinterpret_cast<SbScale*>(sclb + warp * (SBW * 16 * F::SCLB));   // Q4_K: [SBW][16]
+    float2* sw8 = reinterpret_cast<float2*>(sclb + warp * (SBW * 16 * F::SCLB));     // Q8_0: [SBW][16] (d, d)
     uint32_t* subw = subt + warp * (SBW * 16);   // [SBW][8][2]
     auto fail = [&](void) {
         aborted = true;
@@ -397,7 +441,36 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
             consumer_bar();                      // B fragments and half slots no longer read
             if (!aborted && !warp_wait(xfull, xph, P.timeout_ns, lane)) fail();
             xph ^= 1u;
-            if (!aborted) {
+            if (!aborted && FMT == FMT_Q8_0) {
+                // x chunk -> fp16 B fragments of x / s (hi, lo per k slice), s a
+                // power of two per (x row, block) with |x / s| < 2^15: unit
+                // (block j, lane (tok, c4)) covers columns 32j + 8c4 .. +7
+                const int tok = lane >> 2, c4 = lane & 3;
+#pragma unroll
+                for (int it = 0; it < (SB + NW - 1) / NW; ++it) {
+                    const int j = warp + NW * it;
+                    if (j < SB) {
+                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                        if (tok < nval) {
+                            const float* xr = reinterpret_cast<const float*>(xraw + tok * XSTR) + 32 * j + 8 * c4;
+                            a = *reinterpret_cast<const float4*>(xr);
+                            b = *reinterpret_cast<const float4*>(xr + 4);
+                        }
+                        float m = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                        fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+                        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                        const int es = max(1, (int)((__float_as_uint(m) >> 23) & 0xFFu) - 14);  // biased exponent of s
+                        const float inv = __uint_as_float((uint32_t)(254 - es) << 23);        // 1 / s, exact
+                        a = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+                        b = make_float4(b.x * inv, b.y * inv, b.z * inv, b.w * inv);
+                        bfr[(2 * j) * 32 + lane] = x_frag_h(a);
+                        bfr[(2 * j + 1) * 32 + lane] = x_frag_h(b);
+                        if (c4 == 0) sxs[j * NT + tok] = __uint_as_float((uint32_t)es << 23);
+                    }
+                }
+            }
+            if (!aborted && FMT == FMT_Q4_K) {
                 // x chunk -> B fragments (hi, lo per k slice) and sums per sub-block:
                 // unit (sub-block j, lane (tok, c4)) covers columns 32j + 8c4 .. +7
                 const int tok = lane >> 2, c4 = lane & 3;
@@ -434,7 +507,61 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
                 fphase ^= 1u << s;
                 const uint8_t* st = wst + (size_t)s * WSTAGE;
                 float t[4] = {0.f, 0.f, 0.f, 0.f};
-                if (!aborted) {
+                if (!aborted && FMT == FMT_Q8_0) {
+                    // block scales of this warp's 16 rows, blocks 4hb .. 4hb+3:
+                    // lane -> (row lane & 15, blocks 2 (lane >> 4) + {0, 1})
+                    {
+                        const int rr = lane & 15, jq = lane >> 4;
+#pragma unroll
+                        for (int gi = 0; gi < 2; ++gi) {
+                            const int jj = 2 * jq + gi;
+                            const uint16_t dh =
+                                *reinterpret_cast<const uint16_t*>(st + (r0w + rr) * WROW + 34 * (SBW * hb + jj));
+                            const float d = half_bits_to_float(dh);
+                            sw8[jj * 16 + rr] = make_float2(d, d);
+                        }
+                    }
+                    __syncwarp();
+                    // codes: int8 q as fp16 1152 + q (LOP3 with the byte's sign
+                    // bit flipped) minus 1152, exact; one MMA operand per byte
+                    const uint8_t* wg = st + (r0w + g) * WROW + 2 + 8 * cq;   // + 34 j: this lane's 8 codes of block j
+                    const uint8_t* wg8 = wg + 8 * WROW;
+                    uint64_t t01 = pk2(0.f, 0.f), t23 = pk2(0.f, 0.f);
+                    const uint4* bfl = bfr + (2 * SBW * hb) * 32 + lane;
+                    const float* sxq = sxs + SBW * hb * NT + 2 * cq;
+#pragma unroll
+                    for (int jj = 0; jj < SBW; ++jj) {
+                        uint32_t wa[2], wb[2];
+                        lds_words_any2<2>(wg + 34 * (SBW * hb + jj), wa);
+                        lds_words_any2<2>(wg8 + 34 * (SBW * hb + jj), wb);
+                        const float2 da = sw8[jj * 16 + g], db = sw8[jj * 16 + g + 8];
+                        float d[4];
+#pragma unroll
+                        for (int hs = 0; hs < 2; ++hs) {
+                            const uint32_t msk = 0x00FF00FFu, mag = 0x64806480u;   // half2 (1152, 1152)
+                            uint32_t a[4];
+                            a[0] = hsub2_u32(lop_and_xor(wa[hs], msk, mag), mag);
+                            a[1] = hsub2_u32(lop_and_xor(wb[hs], msk, mag), mag);
+                            a[2] = hsub2_u32(lop_and_xor(wa[hs] >> 8, msk, mag), mag);
+                            a[3] = hsub2_u32(lop_and_xor(wb[hs] >> 8, msk, mag), mag);
+                            const uint4 bf = bfl[(2 * jj + hs) * 32];
+                            if (hs == 0)
+                                mma_f16_z(d, a, bf.x, bf.y);
+                            else
+                                mma_f16(d, a, bf.x, bf.y);
+                            mma_f16(d, a, bf.z, bf.w);
+                        }
+                        const uint64_t sv = *reinterpret_cast<const uint64_t*>(sxq + jj * NT);   // s of x rows 2cq, 2cq+1
+                        const uint64_t z = pk2(0.f, 0.f);
+                        t01 = ffma2(ffma2(u64_of(__float_as_uint(da.x), __float_as_uint(da.y)), sv, z), pk2(d[0], d[1]), t01);
+                        t23 = ffma2(ffma2(u64_of(__float_as_uint(db.x), __float_as_uint(db.y)), sv, z), pk2(d[2], d[3]), t23);
+                    }
+                    t[0] = lo_f(t01);
+                    t[1] = hi_f(t01);
+                    t[2] = lo_f(t23);
+                    t[3] = hi_f(t23);
+                }
+                if (!aborted && FMT == FMT_Q4_K) {
                     // scales of this warp's 16 rows in super-block hb:
                     // lane -> (row lane & 15, sub-block pairs 2 (lane >> 4) + {0, 1})
                     {
@@ -615,18 +742,32 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_q4k_kernel(const __grid_
 
 }  // namespace
 
-cudaError_t qmm_set_smem(int bytes) {
-    return cudaFuncSetAttribute(qmm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+namespace {
+const void* qmm_fn(int fmt) {
+    return fmt == FMT_Q8_0 ? reinterpret_cast<const void*>(qmm_kernel<FMT_Q8_0>)
+                           : reinterpret_cast<const void*>(qmm_kernel<FMT_Q4_K>);
+}
+}  // namespace
+
+bool qmm_format_ok(int fmt) { return fmt == FMT_Q4_K || fmt == FMT_Q8_0; }
+int qmm_kc(int fmt) { return fmt == FMT_Q8_0 ? QF<FMT_Q8_0>::KC : QF<FMT_Q4_K>::KC; }
+int qmm_wrow(int fmt) { return fmt == FMT_Q8_0 ? QF<FMT_Q8_0>::WROW : QF<FMT_Q4_K>::WROW; }
+
+cudaError_t qmm_set_smem(int fmt, int bytes) {
+    return cudaFuncSetAttribute(qmm_fn(fmt), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-size_t qmm_smem_bytes(int nstages, int csize, int gmax) { return qmm_layout(nstages, csize, gmax).total; }
+size_t qmm_smem_bytes(int fmt, int nstages, int csize, int gmax) {
+    return fmt == FMT_Q8_0 ? qmm_layout<FMT_Q8_0>(nstages, csize, gmax).total
+                           : qmm_layout<FMT_Q4_K>(nstages, csize, gmax).total;
+}
 
 // Clusters of `csize` CTAs that can be resident at once (CTAs for csize 1).
-cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out) {
+cudaError_t qmm_max_resident(int fmt, int csize, size_t smem, int sms, int* out) {
     *out = 0;
     if (csize <= 1) {
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmm_q4k_kernel, 32 * (NW + 1), smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmm_fn(fmt), 32 * (NW + 1), smem);
         *out = per_sm * sms;
         return e;
     }
@@ -641,10 +782,10 @@ cudaError_t qmm_max_resident(int csize, size_t smem, int sms, int* out) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<void*>(qmm_q4k_kernel), &cfg);
+    return cudaOccupancyMaxActiveClusters(out, qmm_fn(fmt), &cfg);
 }
 
-cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t st) {
+cudaError_t qmm_launch(int fmt, const QmmParams& P, int grid, size_t smem, cudaStream_t st) {
     void* args[1] = {const_cast<QmmParams*>(&P)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -663,7 +804,7 @@ cudaError_t qmm_launch(const QmmParams& P, int grid, size_t smem, cudaStream_t s
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<void*>(qmm_q4k_kernel), args);
+    return cudaLaunchKernelExC(&cfg, qmm_fn(fmt), args);
 }
 
 }  // namespace lq

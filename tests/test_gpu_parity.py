@@ -108,14 +108,16 @@ def test_matvec_unaligned_weight_base(lq, fmt):
     assert_within(host(yb), ref, oracle.matvec_bound(S), "unaligned")
 
 
-# Q4_K calls with at least this many x rows and columns a multiple of 512
-# run on the tensor cores (a different summation order from the batch-1
-# kernel, so only the oracle's bound relates the two).
+# Q4_K calls with at least 2 x rows and columns a multiple of 512, and Q8_0
+# calls with at least 3 x rows and columns a multiple of 256, run on the
+# tensor cores (a different summation order from the batch-1 kernel, so only
+# the oracle's bound relates the two).
 TC_MIN_BATCH = 2
 
 
 def _tensor_path(fmt, cols, M):
-    return fmt == Q4_K and cols % 512 == 0 and M >= TC_MIN_BATCH
+    return ((fmt == Q4_K and cols % 512 == 0 and M >= 2) or
+            (fmt == Q8_0 and cols % 256 == 0 and M >= 3))
 
 
 @pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336), (Q4_K, 2304)])
@@ -200,7 +202,7 @@ def test_qkv_mixed(lq, fq, fk, fv, batch):
         ref, S = oracle.matvec(f, W, n, cols, x, NTH)
         got = host(out)
         assert_within(got, ref, oracle.matvec_bound(S), f"qkv fmt {f}")
-        if batch < TC_MIN_BATCH:
+        if not _tensor_path(f, cols, batch):
             single = empty((batch, n))
             lq.lq_matvec(f, dev(W), n, cols, xd, single, batch)
             assert np.array_equal(got, host(single))    # same code path, same bits
@@ -243,22 +245,41 @@ def test_ffn_gate_up_act(lq, fmt, inter, cols, batch, act):
 
 # ---------------------------------------------------------------- tensor-core path
 
+@pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
 @pytest.mark.parametrize("rows,cols,batch", [
     (67, 512, 3),        # one chunk, a ragged second row block
     (130, 1024, 9),      # a full pass of 8 x rows and a pass of 1
     (64, 2560, 16),      # two full passes, one row block
-    (333, 14336, 5),     # 28 column chunks split over a cluster
+    (333, 14336, 5),     # many column chunks split over a cluster
     (1, 512, 8),         # a single weight row
     (1000, 4096, 8),     # many row blocks
 ])
-def test_tensor_core_matvec(lq, rows, cols, batch):
-    g = synth.rng(rows * 3 + cols + batch)
-    W = synth.weights(g, Q4_K, rows, cols)
+def test_tensor_core_matvec(lq, fmt, rows, cols, batch):
+    g = synth.rng(rows * 3 + cols + batch + fmt)
+    W = synth.weights(g, fmt, rows, cols)
     x = synth.activations(g, batch, cols)
     y = empty((batch, rows))
-    lq.lq_matvec(Q4_K, dev(W), rows, cols, dev(x), y, batch)
-    ref, S = oracle.matvec(Q4_K, W, rows, cols, x, NTH)
-    assert_within(host(y), ref, oracle.matvec_bound(S), f"tc {rows}x{cols} b{batch}")
+    lq.lq_matvec(fmt, dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"tc fmt {fmt} {rows}x{cols} b{batch}")
+
+
+def test_tensor_core_q8_0_x_ranges(lq):
+    """x rows of very different magnitudes (1e-30 .. 1e30, zeros, one huge
+    element per block) through the fp16 x pieces, scaled per (x row, block)."""
+    rows, cols, batch = 70, 1024, 6
+    g = synth.rng(79)
+    W = synth.q8_0(g, rows, cols)
+    x = synth.activations(g, batch, cols)
+    x[0] *= np.float32(1e-30)
+    x[1] *= np.float32(1e30)
+    x[2] = 0.0
+    x[3, ::32] = np.float32(3e4)
+    x[4, 5::32] = np.float32(-1e-20)
+    y = empty((batch, rows))
+    lq.lq_matvec(Q8_0, dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.matvec(Q8_0, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), "tc q8_0 x ranges")
 
 
 def test_tensor_core_extreme_scales(lq):
@@ -292,15 +313,20 @@ def test_tensor_core_misaligned_weights_fall_back(lq):
     assert_within(host(y), ref, oracle.matvec_bound(S), "fallback")
 
 
-@pytest.mark.parametrize("E,topk,ntok", [(4, 2, 6), (8, 2, 16), (3, 1, 20)])
-def test_tensor_core_moe(lq, E, topk, ntok):
+@pytest.mark.parametrize("E,topk,ntok,fmt", [(4, 2, 6, Q4_K), (8, 2, 16, Q4_K), (3, 1, 20, Q4_K), (4, 2, 10, Q8_0)])
+def test_tensor_core_moe(lq, E, topk, ntok, fmt):
     """grouped experts with widths that take the tensor-core path (an expert
     may see more than 8 tokens: two passes)."""
     hidden, inter = 512, 1024
     R, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=E * 7 + ntok)
-    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X, topk)
+    if fmt != Q4_K:
+        g = synth.rng(E * 13 + ntok)
+        W1 = [synth.weights(g, fmt, inter, hidden) for _ in range(E)]
+        W3 = [synth.weights(g, fmt, inter, hidden) for _ in range(E)]
+        W2 = [synth.weights(g, fmt, hidden, inter) for _ in range(E)]
+    Y, idx, w = _run_moe(lq, R, W1, W3, W2, X, topk, fmt)
     _, _, lg, labs = oracle.moe_route(R, X, topk)
-    chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X, lg, labs, idx, NTH)
+    chk = oracle.moe_check(fmt, W1, W3, W2, hidden, inter, X, lg, labs, idx, NTH)
     assert chk["admissible"].all()
     assert_within(Y, chk["Y"], chk["bound"], "tc moe Y")
 
