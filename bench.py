@@ -11,8 +11,10 @@ Headline metric: effective weight GB/s = weight-block bytes of the layer per
 second (60,518,400 B per step), with us/layer = ms_per_step * 1000.  The
 device-timed number replays the decode pass (all layer copies in one CUDA
 graph, so consecutive launches overlap) with inputs resident;
-`e2e` times the C ABI calls directly with the step's x copied in from pinned
-host memory and the layer output copied back, every step.
+`e2e` times the same C ABI calls with every step's x copied in from pinned
+host memory and its layer output copied back to pinned host memory, the
+copies on their own streams overlapping the kernels (double-buffered, one
+CUDA graph per step).
 
 --impl reference runs the CPU oracle (fp64, all host cores) on a bounded
 sample of the same layers as the reference arm.
@@ -185,18 +187,22 @@ class Layer:
         self.y = torch.empty((1, H), **f)
         self.dims = (H, I, NQ, NKV)
 
-    def run(self, w, stream, mark=None):
+    def run(self, w, stream, mark=None, x=None, y=None, x_read=None):
+        """the layer's four calls; x / y override the input and output
+        buffers, and x_read (an event) is recorded once x has been read."""
         import block_quantized_weight_super_gb300 as lq
         H, I, NQ, NKV = self.dims
         lq.lq_qkv_mixed(lq.LQ_Q4_K, w["wq"], NQ, lq.LQ_Q4_K, w["wk"], NKV, lq.LQ_Q6_K, w["wv"], NKV,
-                        H, self.x, self.q, self.k, self.v, 1, stream)
+                        H, self.x if x is None else x, self.q, self.k, self.v, 1, stream)
+        if x_read is not None:
+            x_read.record(stream)
         lq.lq_matvec(lq.LQ_Q4_K, w["wo"], H, NQ, self.q, self.o, 1, stream)
         if mark:
             mark[0].record(stream)
         lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, self.o, self.h, 1, lq.LQ_ACT_GEGLU_TANH, stream)
         if mark:
             mark[1].record(stream)
-        lq.lq_matvec(lq.LQ_Q6_K, w["wd"], H, I, self.h, self.y, 1, stream)
+        lq.lq_matvec(lq.LQ_Q6_K, w["wd"], H, I, self.h, self.y if y is None else y, 1, stream)
 
 
 def bench_lq(args, ws, rank, local):
@@ -287,24 +293,55 @@ def bench_lq(args, ws, rank, local):
         st.synchronize()
     gate_ms = k0.elapsed_time(k1) / (reps * n)
 
-    # e2e through the C ABI: pinned host x in, layer output out, every step
+    # e2e through the C ABI: every step copies its x in from pinned host
+    # memory and its layer output back to pinned host memory.  Step i's
+    # input and output live in device slots i & 1; the copies run on their
+    # own streams so that they overlap the kernels: one CUDA graph per layer
+    # copy c holds [copy-in of step c+1's x] || [layer c] || [copy-out of
+    # step c-1's output], joined at its end.  A copy-in before the first step
+    # and a copy-out after the last complete the K steps.
     e2e = None
     if not args.no_e2e:
         xh = torch.from_numpy(x0).pin_memory()
         yh = torch.empty((1, lay.dims[0]), dtype=torch.float32).pin_memory()
+        cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        xb = [torch.empty_like(lay.x) for _ in range(2)]
+        yb = [torch.empty_like(lay.y) for _ in range(2)]
+
+        def step_graph(i):                       # step i: layer copy i % n, slot i & 1
+            c, k = i % n, i & 1
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                fork = torch.cuda.Event()
+                fork.record(st)
+                cin.wait_event(fork)
+                cout.wait_event(fork)
+                with torch.cuda.stream(cin):
+                    xb[k ^ 1].copy_(xh, non_blocking=True)           # the next step's slot
+                with torch.cuda.stream(cout):
+                    yh.copy_(yb[k ^ 1], non_blocking=True)           # the previous step's slot
+                lay.run(layers[c], st, x=xb[k], y=yb[k])
+                st.wait_stream(cin)
+                st.wait_stream(cout)
+            return g
+
         with torch.cuda.stream(st):
-            for i in range(min(args.warmup, 5)):
-                lay.x.copy_(xh, non_blocking=True)
-                lay.run(layers[i % n], st)
-                yh.copy_(lay.y, non_blocking=True)
-            st.synchronize()
+            ng = n if n % 2 == 0 else 2 * n
+            sg = [step_graph(i) for i in range(ng)]
+            torch.cuda.synchronize()
+
+            def run_steps(k):
+                xb[0].copy_(xh, non_blocking=True)
+                for i in range(k):
+                    sg[i % ng].replay()
+                yh.copy_(yb[(k - 1) & 1], non_blocking=True)
+
+            run_steps(min(args.warmup, 5) or 1)
+            torch.cuda.synchronize()
             barrier()
             t0 = time.perf_counter()
-            for i in range(args.steps):
-                lay.x.copy_(xh, non_blocking=True)
-                lay.run(layers[i % n], st)
-                yh.copy_(lay.y, non_blocking=True)
-            st.synchronize()
+            run_steps(args.steps)
+            torch.cuda.synchronize()
             t_e2e = (time.perf_counter() - t0) / args.steps
         if ws > 1:
             import torch.distributed as dist
@@ -313,7 +350,8 @@ def bench_lq(args, ws, rank, local):
             t_e2e = float(t.item())
         e2e = {"value": ws * LAYER_BYTES / t_e2e / 1e9, "unit": "GB/s",
                "us_per_layer": t_e2e * 1e6,
-               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4)}
+               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4),
+               "copies": "own streams in a graph per step, overlapping the kernels (x and output double-buffered)"}
     return ms_all, gate_ms, clk.summary(), e2e
 
 
