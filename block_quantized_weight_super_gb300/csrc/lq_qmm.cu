@@ -1,11 +1,12 @@
 // lq_qmm.cu -- tensor-core matvec for a batch of up to eight x rows against
-// Q4_K weights (the batched decode / grouped MoE case): Y = X . W^T.
+// Q4_K or Q8_0 weights (the batched decode / grouped MoE case): Y = X . W^T.
 //
 // What it computes is the matvec of lq_matvec (larql "Architecture -> Metal
-// shader map", Gemma 3 / Llama tables; dotLLM PR #320 MoeSwiGluMlp for the
-// grouped experts); the tensor cores only replace the per-x-row multiply-adds.
+// shader map", Gemma 3 / Llama tables; dotLLM matmul_q8_0 GEMV and PR #320
+// MoeSwiGluMlp for the grouped experts); the tensor cores only replace the
+// per-x-row multiply-adds.
 //
-// Each 32-weight Q4_K sub-block is factored as in the CUDA-core kernel
+// Q4_K.  Each 32-weight sub-block is factored as in the CUDA-core kernel
 // (lq_group.cuh): sum_k w_k x_k = dsc * sum_k (q_k - qb) x_k + e * sum_k x_k,
 // qb = round(dmin*m / dsc) clamped to [-16, 15], e = dsc*qb - dmin*m.
 //  * A operand: the codes q - qb, exact in bf16 (|q - qb| <= 31): a LOP3
@@ -18,35 +19,40 @@
 //  * mma.sync m16n8k16 (bf16 in, fp32 accumulate) over the two 16-column
 //    slices of a sub-block gives sum (q - qb) x for 16 rows x 8 x rows; the
 //    epilogue multiplies by dsc and adds e * sum x (packed fp32 FMAs).
+// Q8_0 (w = d q, no offset).  A is q itself in fp16: a LOP3 ORs the byte,
+// sign bit flipped, into a half equal to 1152 + q and a half2 subtraction
+// of 1152 leaves q, exact.  B is x / s in fp16 hi + lo pieces, s a power of
+// two per (x row, 32-column block) with |x / s| < 2^15, so the pieces stay
+// in fp16 range; the epilogue multiplies a block's MMA sum by d * s.
 // The k index of a slice is permuted identically for A and B so that a lane
-// loads its codes for both slices and both nibbles of a 32-byte quant run
-// with one 8-byte shared load: lane (g, c) takes bytes 8c..8c+7 of the run;
-// slice h uses bytes 8c+4h..8c+4h+3, whose bytes (0, 2) fill its k pair
-// (2c, 2c+1) and bytes (1, 3) the pair (2c+8, 2c+9).
+// loads its codes for both slices (and, Q4_K, both nibbles) of a 32-byte
+// quant run with one 8-byte shared load: lane (g, c) takes bytes 8c..8c+7
+// of the run; slice h uses bytes 8c+4h..8c+4h+3, whose bytes (0, 2) fill
+// its k pair (2c, 2c+1) and bytes (1, 3) the pair (2c+8, 2c+9).
 //
 // GB300 structure: a CTA has eight consumer warps and a producer warp.
-// Tiles are 64 weight rows x 512 columns, streamed into a ring of
-// shared-memory stages by 2-D tensor copies (TMA, one box per tile, or eight
-// 8-row boxes for gate / up pairs) on full / empty mbarriers (bounded waits).
-// Warps w and w + 4 take the same 16 rows, the first and the second
-// super-block of every tile, and add their partial sums at the end.  Row
+// Tiles are 64 weight rows x 512 (Q4_K) or 256 (Q8_0) columns, streamed
+// into a ring of shared-memory stages by 2-D tensor copies (TMA, one box
+// per tile, or eight 8-row boxes for gate / up pairs) on full / empty
+// mbarriers (bounded waits).  Warps w and w + 4 take the same 16 rows and
+// the two halves of every tile, and add their partial sums at the end.  Row
 // blocks are dealt to the clusters in units of up to four, round robin; a
 // cluster takes the blocks of a unit that read the same x rows as one
 // group, and for each column chunk the x rows are staged
 // once (their own bulk copies and barriers), converted once into B
-// fragments and per-sub-block sums, and used by every row block of the
-// group, whose partial sums stay in registers.  Each warp decodes the scales
-// of its own 16 rows into a private table, so a tile needs no CTA-wide
-// barrier.  Every output's sum runs in a fixed order: the result is
-// deterministic.  Matrices with few row blocks (a down projection: 4096 rows
-// but 14336 columns) split the column chunks over the CTAs of the cluster:
-// ranks 1.. store their partial sums into rank 0's shared memory
-// (distributed shared memory, an mbarrier per direction, bounded waits) and
-// rank 0 adds them in rank order and writes the outputs.  Gate / up pairs:
-// the producer lays the gate rows of pairs 8q .. 8q+7 of a tile out as tile
+// fragments and per-block sums or scales, and used by every row block of
+// the group, whose partial sums stay in registers.  Each warp decodes the
+// scales of its own 16 rows into a private table, so a tile needs no
+// CTA-wide barrier.  Every output's sum runs in a fixed order: the result
+// is deterministic.  Matrices with few row blocks (a down projection: 4096
+// rows but 14336 columns) split the column chunks over the CTAs of the
+// cluster: ranks 1.. store their partial sums into rank 0's shared memory
+// (distributed shared memory, tx-counted stores, bounded waits) and rank 0
+// adds them in rank order and writes the outputs.  Gate / up pairs: the
+// producer lays the gate rows of pairs 8q .. 8q+7 of a tile out as tile
 // rows 16q .. 16q+7 and their up rows as 16q+8 .. 16q+15 (an MMA lane holds
-// rows g and g + 8), and the activation is
-// applied within the lane that holds both.
+// rows g and g + 8), and the activation is applied within the lane that
+// holds both.
 #include "lq_group.cuh"
 #include "lq_internal.h"
 
