@@ -20,6 +20,9 @@ namespace lq {
 // address is passed to kernels (no relocatable device code needed).
 static __device__ unsigned g_status_word = 0;
 
+// Grid-barrier word of one-launch FFN calls that pass no word of their own.
+static __device__ unsigned g_ffn_bar_word = 0;
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -55,6 +58,7 @@ struct DevInfo {
     bool init = false;
     int sms = 0;
     unsigned* status = nullptr;
+    unsigned* ffn_bar = nullptr;
     int qmm_res[2][3] = {};       // resident tensor-core CTAs / clusters of 2 / of 4 (Q4_K, Q8_0)
 };
 std::mutex g_mu;
@@ -74,9 +78,13 @@ int dev_info(DevInfo** out) {
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
         d.status = static_cast<unsigned*>(p);
+        e = cudaGetSymbolAddress(&p, g_ffn_bar_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(ffn barrier)");
+        d.ffn_bar = static_cast<unsigned*>(p);
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmv_ffn_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -219,14 +227,16 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         }
         P.nseg = n;
         P.ntiles = t;
-        P.cols = (int32_t)cols;
-        P.U = (int32_t)(cols / 64);
-        P.UP = qmv_red_stride(P.U);
+        QGeo& G = P.geo[0];
+        G.cols = (int32_t)cols;
+        G.U = (int32_t)(cols / 64);
+        G.UP = qmv_red_stride(G.U);
+        G.RT = pl.RT;
+        G.ipt = pl.ipt;
+        P.geo[1] = G;
         for (int i = 0; i < n; ++i)
             if (P.seg[i].bcnt || P.seg[i].boff) P.dev_counts = 1;
-        P.RT = pl.RT;
         P.R = pl.R;
-        P.ipt = pl.ipt;
         P.nstages = pl.nstages;
         P.stage_bytes = pl.stage_bytes;
         P.timeout_ns = g_timeout_ns.load();
@@ -248,6 +258,107 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         if (e != cudaSuccess) return cuda_fail(e, "qmv launch");
     }
     return LQ_OK;
+}
+
+// ---------------------------------------------------------------- one-launch FFN
+// Geometry of the batch-1 FFN as one launch: gate/up pairs of format f0 over
+// `hidden` columns (phase 0), down of format f1 over `inter` columns (phase
+// 1).  Both phases run on the same consumer warps, so NC*32 threads must
+// share the items of a tile of either phase evenly: a tile of RT = R*NCT /
+// gcd(NCT, U) rows has exactly NCT*U/gcd(NCT, U) items.  False if no warp
+// count gives both phases tiles of at most 32 KB (then two launches run).
+struct FfnPlan {
+    QGeo geo[2];
+    int NC = 0, nstages = 0, stage_bytes = 0, red_tile = 0, T0 = 0, T1 = 0;
+    size_t smem = 0;
+};
+
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+bool plan_ffn(int f0, int f1, int64_t inter, int64_t hidden, FfnPlan& p) {
+    if (!qmv_ffn_available(f0, f1)) return false;
+    if (hidden <= 0 || inter <= 0 || hidden % 64 || inter % 64) return false;
+    const int64_t U0 = hidden / 64, U1 = inter / 64;
+    if (U0 > 512 || U1 > 512 || inter > (1 << 30)) return false;
+    const int R0 = qmv_rows_per_item(1, fmt_mask({f0})), R1 = qmv_rows_per_item(1, fmt_mask({f1}));
+    const int ncmax = std::min(qmv_max_consumer_warps(R0), qmv_max_consumer_warps(R1));
+    const int64_t rb0 = rowbytes(f0, hidden), rb1 = rowbytes(f1, inter);
+    for (int NC = ncmax; NC >= 4; --NC) {
+        const int64_t NCT = 32 * NC;
+        int64_t RT0 = R0 * NCT / gcd64(NCT, U0);
+        if (RT0 & 1) RT0 *= 2;                    // whole gate/up pairs
+        const int64_t RT1 = R1 * NCT / gcd64(NCT, U1);
+        if (RT0 * rb0 > 32 * 1024 || RT1 * rb1 > 32 * 1024) continue;
+        if ((RT0 * rb0) % 16 || (RT1 * rb1) % 16) continue;   // tiles by bulk copy
+        p.NC = NC;
+        p.geo[0] = QGeo{(int32_t)hidden, (int32_t)U0, qmv_red_stride((int)U0), (int32_t)RT0,
+                        (int32_t)(RT0 * U0 / (R0 * NCT))};
+        p.geo[1] = QGeo{(int32_t)inter, (int32_t)U1, qmv_red_stride((int)U1), (int32_t)RT1,
+                        (int32_t)(RT1 * U1 / (R1 * NCT))};
+        p.stage_bytes = (int)((std::max(RT0 * rb0, RT1 * rb1) + 15) / 16 * 16 + 16);
+        p.red_tile = std::max(p.geo[0].RT * p.geo[0].UP, p.geo[1].RT * p.geo[1].UP);
+        p.T0 = (int)((inter + RT0 / 2 - 1) / (RT0 / 2));
+        p.T1 = (int)((hidden + RT1 - 1) / RT1);
+        for (int S = 4; S >= 2; --S) {
+            p.nstages = S;
+            p.smem = qmv_ffn_smem((int)std::max(U0, U1), p.red_tile, S, p.stage_bytes).total;
+            if (p.smem <= 110 * 1024) return true;
+        }
+        return false;
+    }
+    return false;
+}
+
+Seg plain_seg(int fmt, const void* W, int64_t rows, const float* x, float* y, int64_t ld_y, int b0, int nb);
+
+int run_ffn(const FfnPlan& pl, int f0, const void* Wgu, int f1, const void* Wd, int64_t inter,
+            int64_t hidden, const float* x, float* h, float* y, int act, unsigned* bar, cudaStream_t st) {
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    const int nt = (pl.NC + 1) * 32;
+    int per_sm = 0;
+    cudaError_t e = qmv_ffn_occupancy(f0, f1, nt, pl.smem, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy");
+    if (per_sm < 1) return fail(LQ_ECUDA, "one-launch FFN kernel does not fit on an SM");
+    QmvParams P;
+    memset(&P, 0, sizeof P);
+    Seg s0 = plain_seg(f0, Wgu, inter, x, h, inter, 0, 1);
+    s0.mode = MODE_PAIR_INTERLEAVED;
+    s0.act = act;
+    s0.tile0 = 0;
+    s0.ntiles = pl.T0;
+    Seg s1 = plain_seg(f1, Wd, hidden, h, y, hidden, 0, 1);
+    s1.tile0 = pl.T0;
+    s1.ntiles = pl.T1;
+    P.seg[0] = s0;
+    P.seg[1] = s1;
+    P.nseg = 2;
+    P.ntiles = pl.T0 + pl.T1;
+    P.geo[0] = pl.geo[0];
+    P.geo[1] = pl.geo[1];
+    P.R = qmv_rows_per_item(1, fmt_mask({f0}));
+    P.nstages = pl.nstages;
+    P.stage_bytes = pl.stage_bytes;
+    P.red_tile = pl.red_tile;
+    P.fmt0 = f0;
+    P.fmt1 = f1;
+    P.tile_split = pl.T0;
+    P.timeout_ns = g_timeout_ns.load();
+    P.status = dev->status;
+    P.gbar = bar ? bar : dev->ffn_bar;
+    // every CTA must be resident at once (grid barrier): at most the occupancy
+    const int grid = std::min(dev->sms * per_sm, std::max(pl.T0, pl.T1));
+    P.cta_split = grid;
+    e = qmv_ffn_launch(P, grid, nt, pl.smem, st);
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "one-launch FFN launch");
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -604,6 +715,32 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
         segs.push_back(s);
     }
     return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lq_ffn_launches(int fmt_gu, int fmt_down, int64_t inter, int64_t hidden, int batch) {
+    if (!fmt_ok(fmt_gu) || !fmt_ok(fmt_down) || inter <= 0 || hidden <= 0 || batch < 1) return 0;
+    FfnPlan pl;
+    return batch == 1 && plan_ffn(fmt_gu, fmt_down, inter, hidden, pl) ? 1 : 2;
+}
+
+int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
+           const float* x, float* h, float* y, int batch, int act, uint32_t* sync, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_mat(fmt_gu, Wgu, 2 * inter, hidden, "Wgu")) ||
+        (rc = check_mat(fmt_down, Wd, hidden, inter, "Wd")))
+        return rc;
+    if (inter == 0 || hidden == 0) return fail(LQ_ESHAPE, "inter %lld hidden %lld", (long long)inter, (long long)hidden);
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h")) || (rc = check_f32(y, "y"))) return rc;
+    if (sync && !al(sync, 4)) return fail(LQ_EALIGN, "sync not 4-byte aligned");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    FfnPlan pl;
+    if (batch == 1 && al(x, 16) && al(h, 16) && plan_ffn(fmt_gu, fmt_down, inter, hidden, pl))
+        return run_ffn(pl, fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, act, sync, st);
+    if ((rc = lq_ffn_gate_up_act(fmt_gu, Wgu, inter, hidden, x, h, batch, act, stream))) return rc;
+    return lq_matvec(fmt_down, Wd, hidden, inter, h, y, batch, stream);
 }
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }

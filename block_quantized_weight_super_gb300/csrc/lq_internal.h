@@ -71,6 +71,12 @@ cudaError_t qmv1_launch(int mask, const QmvParams& P, int grid, int nt, size_t s
 cudaError_t qmv2_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 cudaError_t qmv4_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 
+// the batch-1 FFN in one launch (lq_qmv_ffn.cu): gate/up format f0, down f1
+bool qmv_ffn_available(int f0, int f1);
+cudaError_t qmv_ffn_set_smem(int bytes);
+cudaError_t qmv_ffn_occupancy(int f0, int f1, int nt, size_t smem, int* per_sm);
+cudaError_t qmv_ffn_launch(const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
+
 cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,
                            cudaStream_t st);
 cudaError_t launch_interleave(const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t rb,

@@ -61,11 +61,11 @@ struct QTile {
     bool tma;
 };
 
-__device__ __forceinline__ QTile qtile(const QmvParams& P, const Seg& S, int t) {
+__device__ __forceinline__ QTile qtile(const QGeo& Gm, const Seg& S, int t) {
     QTile g;
-    const int64_t rb = qrow_bytes(S.fmt, P.cols);
+    const int64_t rb = qrow_bytes(S.fmt, Gm.cols);
     const int lt = t - S.tile0;
-    const int opt = S.mode == MODE_PLAIN ? P.RT : P.RT / 2;
+    const int opt = S.mode == MODE_PLAIN ? Gm.RT : Gm.RT / 2;
     g.o0 = lt * opt;
     g.n_o = min(opt, S.nout - g.o0);
     g.src2 = nullptr;
@@ -82,7 +82,7 @@ __device__ __forceinline__ QTile qtile(const QmvParams& P, const Seg& S, int t) 
         g.bytes1 = (uint32_t)(g.n_o * rb);
         g.src2 = S.w2 + (int64_t)g.o0 * rb;
         g.bytes2 = g.bytes1;
-        g.dst2 = (uint32_t)((P.RT / 2) * rb);
+        g.dst2 = (uint32_t)((Gm.RT / 2) * rb);
     }
     g.tma = ((reinterpret_cast<uintptr_t>(g.src1) | g.bytes1) & 15u) == 0;
     if (S.mode == MODE_PAIR_TWO)
@@ -126,6 +126,14 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, uint
     }
 }
 
+// The CTA's abort flag as lane 0 reads it, for the whole warp: the warp's
+// control flow (and the full-mask shuffles after it) stays uniform.
+__device__ __forceinline__ bool warp_aborted(const int* flag, int lane) {
+    int v = 0;
+    if (lane == 0) v = *reinterpret_cast<const volatile int*>(flag);
+    return __shfl_sync(0xFFFFFFFFu, v, 0) != 0;
+}
+
 __device__ __forceinline__ void consumer_sync(int nct) {
     asm volatile("bar.sync 1, %0;" ::"r"(nct) : "memory");
 }
@@ -159,10 +167,11 @@ __device__ __forceinline__ int qxcol(int G, int i) {
 // checks); each thread loads two units before storing, and the sub-block
 // sums come from registers: the 16-column sum of a unit (in column order)
 // plus that of its neighbour unit (lane ^ 1).  Ends with the consumer barrier;
-// the caller brackets it with one before.
-template <int FMT, int B>
-__device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs, int ct, int nct) {
-    const int U = P.U;
+// the caller brackets it with one before.  COHERENT: x was written by other
+// CTAs of this kernel, so it is read through L2 (no read-only path).
+template <int FMT, int B, bool COHERENT = false>
+__device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int ct, int nct) {
+    const int U = Gm.U;
     const int nval = qseg_nval(S, B);
     const int boff = qseg_boff(S);
     const int units = B * U * 4;
@@ -175,10 +184,10 @@ __device__ void stage_x(const QmvParams& P, const Seg& S, float* xs, float* sxs,
             const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
             if (e < units && b < nval) {
                 const int rho = boff + b;
-                const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * P.cols;
+                const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * Gm.cols;
                 const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[h][k] = __ldg(src + k);
+                for (int k = 0; k < 4; ++k) v[h][k] = COHERENT ? __ldcg(src + k) : __ldg(src + k);
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[h][k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -461,12 +470,12 @@ __device__ __forceinline__ void lane_sums(const float* r, const float* r2, bool 
 // only on U, so results do not depend on B or the tile.  Four outputs per
 // pass read rows UP floats apart (UP = 8 mod 32): no bank conflicts.
 template <int B>
-__device__ __forceinline__ void reduce_tile(const QmvParams& P, const Seg& S, int t, const float* red,
+__device__ __forceinline__ void reduce_tile(const QGeo& Gm, const Seg& S, int t, const float* red,
                                             int lane, int pass0, int pstep) {
-    const int U = P.U, UP = P.UP, mode = S.mode;
-    const int half = P.RT / 2;
+    const int U = Gm.U, UP = Gm.UP, mode = S.mode;
+    const int half = Gm.RT / 2;
     const int lt = t - S.tile0;
-    const int opt = mode == MODE_PLAIN ? P.RT : half;
+    const int opt = mode == MODE_PLAIN ? Gm.RT : half;
     const int o0 = lt * opt;
     const int n_o = min(opt, S.nout - o0);
     const int nval = qseg_nval(S, B);
@@ -515,8 +524,9 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     const int NC = (blockDim.x >> 5) - 1;          // consumer warps
     const int NCT = NC * 32;
     const int S_ = P.nstages;
-    const int U = P.U;
-    const int red_tile = P.RT * B * P.UP;
+    const QGeo& Gm = P.geo[0];
+    const int U = Gm.U;
+    const int red_tile = Gm.RT * B * Gm.UP;
     const int NRED = S_ + 1;             // partial slots
 
     if (warp == NC) {
@@ -542,14 +552,14 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         int nr = 0, ntiles = 0;           // tiles reduced / issued
         auto reduce_next = [&]() {
             __syncwarp();
-            reduce_tile<B>(P, sm.segs[wr.hint], wr.t, sm.red + (size_t)(nr % NRED) * red_tile, lane, 0, 1);
+            reduce_tile<B>(Gm, sm.segs[wr.hint], wr.t, sm.red + (size_t)(nr % NRED) * red_tile, lane, 0, 1);
             ++nr;
             wr.t += wr.step;
             walk_fix<B>(sm.segs, P.nseg, wr);
         };
         for (int n = 0, s = 0; w.t < w.end; ++n) {
             if (early && n == S_) pdl_wait();   // stages full: the rest waits
-            if (*reinterpret_cast<volatile int*>(sm.abort_flag)) break;
+            if (warp_aborted(sm.abort_flag, lane)) break;
             if (n >= S_) {            // wait until the consumers released stage s
                 if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -557,7 +567,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
                 if (!ok) break;
             }
             const Seg& S = sm.segs[w.hint];
-            const QTile g = qtile(P, S, w.t);
+            const QTile g = qtile(Gm, S, w.t);
             uint8_t* dst = sm.stages + (size_t)s * P.stage_bytes;
             if (g.tma) {
                 if (lane == 0) {
@@ -581,7 +591,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         if (early && ntiles < S_) pdl_wait();
         // tiles before the last two are reduced here while the consumers
         // finish; the consumer warps share the last two
-        while (ok && nr < ntiles - 2 && !*reinterpret_cast<volatile int*>(sm.abort_flag)) {
+        while (ok && nr < ntiles - 2 && !warp_aborted(sm.abort_flag, lane)) {
             const int s2 = nr % S_;
             if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s2], (ephase >> s2) & 1u, P.timeout_ns);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -611,9 +621,9 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     int cur_seg = -1;
     uint32_t fphase = 0;
     bool aborted = false;
-    const int UP = P.UP;
-    const int half = P.RT / 2;
-    const int rb = (int)qrow_bytes(FMT, P.cols);
+    const int UP = Gm.UP;
+    const int half = Gm.RT / 2;
+    const int rb = (int)qrow_bytes(FMT, Gm.cols);
     // Item it = tid + q*NCT of every tile covers group it % U of rows
     // (it / U)*R .. +R-1: the same for every tile, so it is stepped, not divided.
     const int G_first = tid % U, row_first = (tid / U) * R;
@@ -625,14 +635,14 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         const Seg& S = sm.segs[w.hint];
         if (w.hint != cur_seg) {
             consumer_sync(NCT);          // every consumer is done with the previous x
-            stage_x<FMT, B>(P, S, sm.xs, sm.sxs, tid, NCT);
+            stage_x<FMT, B>(Gm, S, sm.xs, sm.sxs, tid, NCT);
             cur_seg = w.hint;
         }
         if (!aborted) {
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(&sm.full[s], (fphase >> s) & 1u, P.timeout_ns);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok || *reinterpret_cast<volatile int*>(sm.abort_flag)) {
+            if (!ok || warp_aborted(sm.abort_flag, lane)) {
                 aborted = true;
                 if (lane == 0 && !ok) {
                     record_status(P.status, STATUS_TIMEOUT);
@@ -646,7 +656,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         float* red = sm.red + (size_t)slot_n * red_tile;
         if (!aborted) {
             int G = G_first, row0 = row_first;
-            for (int q = 0; q < P.ipt; ++q) {
+            for (int q = 0; q < Gm.ipt; ++q) {
                 const uint8_t* rp[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) rp[r] = st + (row0 + r) * rb;
@@ -700,7 +710,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             }
             break;
         }
-        reduce_tile<B>(P, sm.segs[k ? last_hint : prev_hint], k ? last_t : prev_t,
+        reduce_tile<B>(Gm, sm.segs[k ? last_hint : prev_hint], k ? last_t : prev_t,
                        sm.red + (size_t)(m % NRED) * red_tile, lane, k ? NC - 1 - warp : warp, NC);
     }
 }
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_k
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
     const int S_ = P.nstages;
-    const int U = P.U;
+    const int U = P.geo[0].U;
     Smem sm;
     size_t off = 0;
     sm.stages = smem;
@@ -725,7 +735,7 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_k
     sm.sxs = reinterpret_cast<float*>(smem + off);
     off += (size_t)B * U * 2 * sizeof(float);
     sm.red = reinterpret_cast<float*>(smem + off);
-    off += (size_t)(S_ + 1) * P.RT * B * P.UP * sizeof(float);
+    off += (size_t)(S_ + 1) * P.geo[0].RT * B * P.geo[0].UP * sizeof(float);
     off = (off + 7) & ~size_t(7);
     sm.full = reinterpret_cast<uint64_t*>(smem + off);
     sm.empty = sm.full + S_;

@@ -96,6 +96,38 @@ def test_other_entry_validation(lq):
                           None) == lq.LQ_OK
 
 
+def test_ffn_validation(lq):
+    L = lq.lib()
+    ffn = lambda f0, w, f1, wd, inter, hidden, x, h, y, b, act, sync: L.lq_ffn(
+        f0, w, f1, wd, inter, hidden, x, h, y, b, act, sync, None)
+    assert ffn(1, None, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, None, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 250, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE   # hidden % 256
+    assert ffn(1, FAKE, 2, FAKE, 100, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE   # inter % 256 (down cols)
+    assert ffn(1, FAKE, 2, FAKE, 0, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 0, 1, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 3, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 9, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, None, FAKE, 1, 1, None) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE + 2, FAKE, 1, 1, None) == lq.LQ_EALIGN
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, FAKE + 2) == lq.LQ_EALIGN
+
+
+def test_ffn_launch_plan(lq):
+    """Which FFN shapes run as one launch (no device work: host planning only).
+    A shape fuses when some consumer-warp count tiles both matrices evenly
+    with tiles of at most 32 KB."""
+    Q4, Q6, Q8 = 1, 2, 3
+    assert lq.lq_ffn_launches(Q4, Q6, 10240, 2560, 1) == 1      # Gemma-3-4B FFN
+    assert lq.lq_ffn_launches(Q4, Q6, 10240, 2560, 2) == 2      # batch 2: two launches
+    assert lq.lq_ffn_launches(Q4, Q4, 14336, 4096, 1) == 2      # Llama shape: no common tiling
+    assert lq.lq_ffn_launches(Q8, Q8, 512, 512, 1) == 2         # Q8_0 rows: tiles above 32 KB
+    assert lq.lq_ffn_launches(Q8, Q4, 512, 512, 1) == 2         # no kernel for this pair
+    assert lq.lq_ffn_launches(Q4, Q6, 0, 2560, 1) == 0
+    assert lq.lq_ffn_launches(Q4, 7, 256, 256, 1) == 0
+    assert lq.lq_ffn_launches(Q4, Q6, 256, 256, 0) == 0
+
+
 def test_moe_validation(lq):
     L = lq.lib()
     P = C.c_void_p * 2

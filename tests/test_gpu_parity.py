@@ -243,6 +243,95 @@ def test_ffn_gate_up_act(lq, fmt, inter, cols, batch, act):
     assert_within(got, a * u64, tol, "epilogue")
 
 
+# ---------------------------------------------------------------- whole FFN (lq_ffn)
+
+def _ffn_inputs(lq, f0, f1, inter, hidden, batch, seed):
+    g = synth.rng(seed)
+    Wg, Wu = synth.weights(g, f0, inter, hidden), synth.weights(g, f0, inter, hidden)
+    Wd = synth.weights(g, f1, hidden, inter)
+    x = synth.activations(g, batch, hidden)
+    Wgu = torch.empty(2 * inter * lq.lq_row_bytes(f0, hidden), dtype=torch.uint8, device="cuda")
+    return Wg, Wu, Wd, x, Wgu
+
+
+def _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y):
+    """h and y of lq_ffn: bit for bit those of the two separate calls, and
+    within the oracle's bounds (gate/up against the oracle; down against the
+    oracle's matvec of the GPU's own h)."""
+    xd, Wdd = dev(x), dev(Wd)
+    h2, y2 = empty((batch, inter)), empty((batch, hidden))
+    lq.lq_ffn_gate_up_act(f0, Wgu, inter, hidden, xd, h2, batch, act)
+    lq.lq_matvec(f1, Wdd, hidden, inter, h2, y2, batch)
+    got_h, got_y = host(h), host(y)
+    assert _bits_equal(got_h, host(h2)), "h differs from lq_ffn_gate_up_act"
+    assert _bits_equal(got_y, host(y2)), "y differs from lq_matvec on h"
+    o = oracle.ffn_gate_up(f0, Wg, Wu, inter, hidden, x, act, NTH)
+    assert_within(got_h, o["h"], oracle.gate_up_bound(o["g"], o["u"], o["Sg"], o["Su"], act), "h")
+    ref, S = oracle.matvec(f1, Wd, hidden, inter, got_h.astype(np.float64), NTH)
+    assert_within(got_y, ref, oracle.matvec_bound(S), "y")
+
+
+@pytest.mark.parametrize("f0,f1,inter,hidden,act", [
+    (Q4_K, Q6_K, 256, 512, 1),      # five tiles per phase, ragged last tiles of both
+    (Q4_K, Q6_K, 1280, 2560, 2),    # many tiles per CTA
+    (Q4_K, Q4_K, 1024, 256, 1),     # 10 gate/up tiles, 5 down tiles: CTAs with no down tile
+    (Q6_K, Q6_K, 512, 512, 2),
+    (Q4_K, Q4_K, 768, 4096, 2),     # six consumer warps; 128 gate/up tiles, 64 down tiles
+    (Q4_K, Q6_K, 10240, 2560, 1),   # the Gemma-3-4B FFN: 1280 tiles per phase over a full grid
+])
+def test_ffn_one_launch(lq, f0, f1, inter, hidden, act):
+    assert lq.lq_ffn_launches(f0, f1, inter, hidden, 1) == 1
+    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, 1, 41 + inter + hidden)
+    lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
+    h, y = empty((1, inter)), empty((1, hidden))
+    lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, 1, act)
+    status_clean(lq)
+    _ffn_check(lq, f0, f1, inter, hidden, 1, act, Wg, Wu, Wd, x, Wgu, h, y)
+
+
+def test_ffn_one_launch_barrier_reuse(lq):
+    """The grid-barrier word needs no reset: back-to-back calls with different
+    grids on the library's word, and on a caller word starting at zero or at
+    2^31 (the two values a completed call leaves), all give the same results."""
+    shapes = [(Q4_K, Q6_K, 256, 512), (Q4_K, Q4_K, 1024, 256), (Q4_K, Q6_K, 1280, 2560)]
+    runs = []
+    for i, (f0, f1, inter, hidden) in enumerate(shapes):
+        Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, 1, 300 + i)
+        lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
+        runs.append((f0, f1, inter, hidden, Wgu, dev(Wd), dev(x)))
+    ref = []
+    for f0, f1, inter, hidden, Wgu, Wd, x in runs:
+        h, y = empty((1, inter)), empty((1, hidden))
+        lq.lq_ffn_gate_up_act(f0, Wgu, inter, hidden, x, h, 1, 2)
+        lq.lq_matvec(f1, Wd, hidden, inter, h, y, 1)
+        ref.append((host(h), host(y)))
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for start in (None, 0, -2 ** 31):
+        if start is not None:
+            word.fill_(start)
+        for rep in range(3):
+            for (f0, f1, inter, hidden, Wgu, Wd, x), (rh, ry) in zip(runs, ref):
+                h, y = empty((1, inter)), empty((1, hidden))
+                lq.lq_ffn(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 1, 2,
+                          sync=None if start is None else word)
+                assert _bits_equal(host(h), rh) and _bits_equal(host(y), ry), (start, rep, inter, hidden)
+    status_clean(lq)
+
+
+@pytest.mark.parametrize("f0,f1,inter,hidden,batch", [
+    (Q4_K, Q6_K, 1280, 2560, 2),    # batch 2: tensor-core gate/up, then the Q6_K down
+    (Q8_0, Q8_0, 512, 512, 1),      # no one-launch tiling for Q8_0 rows
+    (Q4_K, Q6_K, 768, 2560, 1),     # no warp count tiles both matrices evenly
+])
+def test_ffn_two_launches(lq, f0, f1, inter, hidden, batch):
+    assert lq.lq_ffn_launches(f0, f1, inter, hidden, batch) == 2
+    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, batch, 77 + inter)
+    lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
+    h, y = empty((batch, inter)), empty((batch, hidden))
+    lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, batch, 2)
+    _ffn_check(lq, f0, f1, inter, hidden, batch, 2, Wg, Wu, Wd, x, Wgu, h, y)
+
+
 # ---------------------------------------------------------------- tensor-core path
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
