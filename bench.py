@@ -380,9 +380,9 @@ def cpu_baseline(sample_layers=1, rows_frac=0.25):
 
 
 # DRAM bytes (read + write) of one gate+up launch, from the ncu capture in
-# profiles/qmv_gate_up_q4k_and_down_q6k.md, valid while the sources of that
-# kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "99ab55619d8d45085d587d162531d02d2d4e76cecb62c4b62dce910991700a44", "bytes": 29561344}
+# profiles/qmv_gate_up_and_down_dram_traffic.md, valid while the sources of
+# that kernel hash to the value they had when it was taken.
+GATEUP_TRAFFIC = {"csrc_sha256": "713df550e4e874a1e607a1f7281882f48a8857a0f90eef2e4644c9fa4cc85533", "bytes": 29570816}
 
 
 # the sources the batch-1 gate+up launch is compiled from
@@ -684,7 +684,7 @@ def main():
                           "unit": "GB/s", "frac": achieved / peak,
                           "traffic": (GATEUP_TRAFFIC["bytes"] if csrc_sha256() == GATEUP_TRAFFIC["csrc_sha256"]
                                       else None),
-                          "traffic_source": "profiles/qmv_gate_up_q4k_and_down_q6k.md (ncu dram bytes per launch)",
+                          "traffic_source": "profiles/qmv_gate_up_and_down_dram_traffic.md (ncu dram bytes per launch)",
                           "us_per_launch": gate_ms * 1e3},
                 clocks=clocks, e2e=e2e, gpu_launches=4 * args.steps, cpu_baseline=cb)
     print(json.dumps(line))

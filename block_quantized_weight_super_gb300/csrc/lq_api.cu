@@ -717,14 +717,8 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
     return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int lq_ffn_launches(int fmt_gu, int fmt_down, int64_t inter, int64_t hidden, int batch) {
-    if (!fmt_ok(fmt_gu) || !fmt_ok(fmt_down) || inter <= 0 || hidden <= 0 || batch < 1) return 0;
-    FfnPlan pl;
-    return batch == 1 && plan_ffn(fmt_gu, fmt_down, inter, hidden, pl) ? 1 : 2;
-}
-
 int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
-           const float* x, float* h, float* y, int batch, int act, uint32_t* sync, lq_stream_t stream) {
+           const float* x, float* h, float* y, int batch, int act, lq_stream_t stream) {
     g_err[0] = 0;
     int rc;
     if ((rc = check_mat(fmt_gu, Wgu, 2 * inter, hidden, "Wgu")) ||
@@ -734,13 +728,28 @@ int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t in
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
     if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
     if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h")) || (rc = check_f32(y, "y"))) return rc;
-    if (sync && !al(sync, 4)) return fail(LQ_EALIGN, "sync not 4-byte aligned");
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    FfnPlan pl;
-    if (batch == 1 && al(x, 16) && al(h, 16) && plan_ffn(fmt_gu, fmt_down, inter, hidden, pl))
-        return run_ffn(pl, fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, act, sync, st);
     if ((rc = lq_ffn_gate_up_act(fmt_gu, Wgu, inter, hidden, x, h, batch, act, stream))) return rc;
     return lq_matvec(fmt_down, Wd, hidden, inter, h, y, batch, stream);
+}
+
+int lq_ffn_one_launch(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
+                      const float* x, float* h, float* y, int act, uint32_t* sync, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_mat(fmt_gu, Wgu, 2 * inter, hidden, "Wgu")) ||
+        (rc = check_mat(fmt_down, Wd, hidden, inter, "Wd")))
+        return rc;
+    if (inter == 0 || hidden == 0) return fail(LQ_ESHAPE, "inter %lld hidden %lld", (long long)inter, (long long)hidden);
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h")) || (rc = check_f32(y, "y"))) return rc;
+    if (sync && !al(sync, 4)) return fail(LQ_EALIGN, "sync not 4-byte aligned");
+    if (!al(x, 16) || !al(h, 16)) return fail(LQ_EALIGN, "one-launch FFN: x and h must be 16-byte aligned");
+    FfnPlan pl;
+    if (!plan_ffn(fmt_gu, fmt_down, inter, hidden, pl))
+        return fail(LQ_EUNSUPPORTED, "one-launch FFN: no tiling for formats %d/%d, inter %lld, hidden %lld", fmt_gu,
+                    fmt_down, (long long)inter, (long long)hidden);
+    return run_ffn(pl, fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, act, sync,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }

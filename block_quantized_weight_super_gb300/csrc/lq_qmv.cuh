@@ -66,8 +66,8 @@ __host__ __device__ inline size_t qmv_smem_bytes(int B, int U, int RT, int nstag
 
 // Shared memory of the two-phase (fused FFN, batch 1) kernel: stages sized
 // for the larger tile, x for the wider phase, partial slots of red_tile
-// floats, and besides the stage barriers the grid-barrier handshake between
-// the producer and the consumers (an mbarrier and the word's old value).
+// floats, and besides the stage barriers the bulk-staging barrier and the
+// producer's "h written" signal to the consumers.
 struct FfnSmem {
     size_t stages, xs, sxs, red, bars, segs, total;
 };
@@ -83,8 +83,8 @@ __host__ __device__ inline FfnSmem qmv_ffn_smem(int Umax, int red_tile, int nsta
     L.red = off;
     off += (size_t)(nstages + 1) * red_tile * sizeof(float);
     off = (off + 7) & ~size_t(7);
-    L.bars = off;                                  // full[S], empty[S], gready; cnt[S+1], abort, gold
-    off += (size_t)(2 * nstages + 1) * sizeof(uint64_t) + (size_t)(nstages + 3) * sizeof(int);
+    L.bars = off;                                  // full[S], empty[S], xfull, gready; cnt[S+1], abort
+    off += (size_t)(2 * nstages + 2) * sizeof(uint64_t) + (size_t)(nstages + 2) * sizeof(int);
     off = (off + 15) & ~size_t(15);
     L.segs = off;
     off += 2 * sizeof(Seg);

@@ -51,6 +51,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned* bar, uint32_t old, uin
 struct FfnState {
     int s, slot_n;
     uint32_t fphase;
+    uint32_t xn;            // bulk stagings of x so far (parity of the next)
     bool aborted;
 };
 
@@ -64,9 +65,26 @@ __device__ __forceinline__ void ffn_consume(const QmvParams& P, const GroupConst
     const int S_ = P.nstages, NRED = S_ + 1;
     const int U = Gm.U, UP = Gm.UP, half = Gm.RT / 2;
     const int rb = (int)qrow_bytes(FMT, Gm.cols);
-    consumer_sync(NCT);                  // every consumer is done with the previous x
-    stage_x<FMT, 1, COHERENT>(Gm, S, sm.xs, sm.sxs, tid, NCT);
     const int G_first = tid % U, row_first = (tid / U) * R;
+    consumer_sync(NCT);                  // every consumer is done with the previous x (and,
+                                         // in phase 1, warp 0 has seen the grid barrier)
+    // x of phase 0 (from the preceding kernel) by loads, which start before the
+    // weight tiles already queued on the bulk-copy engine; h (phase 1) by bulk
+    // copies, issued once the grid barrier has passed
+    bool ok = true;
+    if (COHERENT) {
+        ok = stage_x_bulk<FMT, 1>(Gm, S, sm.xs, sm.sxs, sm.xfull, st.xn & 1u, P.timeout_ns, tid, NCT, true);
+        ++st.xn;
+    } else {
+        stage_x<FMT, 1>(Gm, S, sm.xs, sm.sxs, tid, NCT);
+    }
+    if (!ok && !st.aborted) {
+        st.aborted = true;
+        if (lane == 0) {
+            record_status(P.status, STATUS_TIMEOUT);
+            atomicExch(sm.abort_flag, 1);
+        }
+    }
     const int dG = NCT % U, dRow = (NCT / U) * R;
     for (int k = 0; k < ntl; ++k) {
         const int s = st.s;
@@ -116,8 +134,7 @@ __device__ __forceinline__ void ffn_consume(const QmvParams& P, const GroupConst
 }
 
 template <int F0, int R0, int F1, int R1>
-__device__ void qmv_ffn_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm, uint64_t* gready,
-                            uint32_t* gold) {
+__device__ void qmv_ffn_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm, uint64_t* gready) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NC = (blockDim.x >> 5) - 1;
     const int NCT = NC * 32;
@@ -127,53 +144,48 @@ __device__ void qmv_ffn_cta(const QmvParams& P, const GroupConsts& K, const Smem
     const int T0 = P.tile_split;
     const int N0 = phase_tiles(bid, grid, T0), N1 = phase_tiles(bid, grid, P.ntiles - T0);
     const int NT = N0 + N1;
+    // Who sums which tile's partials: the consumer warps share the last two
+    // tiles of each phase ([P0, N0) and [P1, NT)), the producer the others.
+    const int P0 = max(0, N0 - 2), P1 = max(N0, NT - 2);
+    auto by_producer = [&](int m) { return m < P0 || (m >= N0 && m < P1); };
     // tile of this CTA's n-th position: phase 0 first
     auto tile_of = [&](int n) { return n < N0 ? bid + n * grid : T0 + bid + (n - N0) * grid; };
+    // the consumers released tile m (its partials are complete): the m / S-th
+    // completion of its stage's empty barrier, waited for before tile m + S
+    // is issued, so the barrier is never a full two phases ahead
+    auto wait_empty = [&](int m) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(&sm.empty[m % S_], (uint32_t)(m / S_) & 1u, P.timeout_ns);
+        return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    };
 
     if (warp == NC) {
         // ------------------------------------------------ producer warp
         const uint64_t policy = policy_evict_first();
-        uint32_t ephase = 0;
         int last_use[8];
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2) last_use[s2] = -1;
-        bool ok = true, waited = false, arrived = false;
-        int nr = 0, ntiles = 0;
-        auto reduce_next = [&]() {
-            const bool ph = nr >= N0;
+        bool ok = true, ready = false;
+        int ntiles = 0;
+        auto reduce = [&](int m) {
+            const bool ph = m >= N0;
             __syncwarp();
-            reduce_tile<1>(P.geo[ph ? 1 : 0], sm.segs[ph ? 1 : 0], tile_of(nr),
-                           sm.red + (size_t)(nr % NRED) * red_tile, lane, 0, 1);
-            ++nr;
+            reduce_tile<1>(P.geo[ph ? 1 : 0], sm.segs[ph ? 1 : 0], tile_of(m),
+                           sm.red + (size_t)(m % NRED) * red_tile, lane, 0, 1);
         };
-        // arrive once every phase-0 tile of this CTA is reduced (h written),
-        // and never before the preceding kernel has finished: it may have
-        // used the same barrier word
-        auto maybe_arrive = [&](bool force) {
-            if (arrived || !waited || (!force && nr < N0)) return;
+        // tell the consumers once every phase-0 tile of the producer's share is
+        // summed (its h written and fenced); they arrive on the grid barrier
+        auto signal_ready = [&](int done) {
+            if (ready || done < P0) return;
             __threadfence();
             __syncwarp();
-            if (lane == 0) {
-                const uint32_t inc = bid == 0 ? 0x80000000u - (uint32_t)(grid - 1) : 1u;
-                *reinterpret_cast<volatile uint32_t*>(gold) = atomicAdd(P.gbar, inc);
-                mbar_arrive(gready);
-            }
-            __syncwarp();
-            arrived = true;
+            if (lane == 0) mbar_arrive(gready);
+            ready = true;
         };
         for (int n = 0, s = 0; n < NT; ++n) {
-            if (n == S_) {                // stages full: the rest waits for the preceding kernel
-                pdl_wait();
-                waited = true;
-                maybe_arrive(false);
-            }
+            if (n == S_) pdl_wait();      // stages full: the rest waits for the preceding kernel
             if (warp_aborted(sm.abort_flag, lane)) break;
-            if (n >= S_) {
-                if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s], (ephase >> s) & 1u, P.timeout_ns);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                ephase ^= 1u << s;
-                if (!ok) break;
-            }
+            if (n >= S_ && !(ok = wait_empty(n - S_))) break;
             const int ph = n >= N0 ? 1 : 0;
             const QTile g = qtile(P.geo[ph], sm.segs[ph], tile_of(n));
             uint8_t* dst = sm.stages + (size_t)s * P.stage_bytes;
@@ -188,36 +200,25 @@ __device__ void qmv_ffn_cta(const QmvParams& P, const GroupConsts& K, const Smem
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.full[s]);
             }
-            if (n >= S_) {
-                reduce_next();            // tile n - S
-                maybe_arrive(false);
-            }
+            if (n >= S_ && by_producer(n - S_)) reduce(n - S_);
+            if (n >= S_) signal_ready(n - S_ + 1);
             if (++s == S_) s = 0;
             ntiles = n + 1;
         }
-        if (!waited) {
-            pdl_wait();
-            waited = true;
-        }
-        maybe_arrive(false);
-        // the rest of phase 0, then phase 1 but its last two tiles (the
-        // consumer warps share those)
-        const int nprod = min(max(N0, NT - 2), ntiles);
-        while (ok && nr < nprod && !warp_aborted(sm.abort_flag, lane)) {
-            const int s2 = nr % S_;
-            if (lane == 0) ok = mbar_wait_bounded(&sm.empty[s2], (ephase >> s2) & 1u, P.timeout_ns);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            ephase ^= 1u << s2;
-            if (ok) {
-                reduce_next();
-                maybe_arrive(false);
-            }
+        if (ntiles <= S_) pdl_wait();     // (the loop waited iff it reached tile S)
+        // the producer's tiles among the last S issued
+        for (int m = max(0, ntiles - S_); ok && m < ntiles; ++m) {
+            signal_ready(m);
+            if (!by_producer(m)) continue;
+            if (warp_aborted(sm.abort_flag, lane)) break;
+            if (!(ok = wait_empty(m))) break;
+            reduce(m);
         }
         if (!ok && lane == 0) {
             record_status(P.status, STATUS_TIMEOUT);
             atomicExch(sm.abort_flag, 1);
         }
-        maybe_arrive(true);               // a CTA that gave up still counts
+        signal_ready(1 << 30);            // also when it gave up: the consumers never wait in vain
         if (lane == 0) {
             for (int s2 = 0; s2 < S_; ++s2)
                 if (last_use[s2] >= 0)
@@ -228,43 +229,51 @@ __device__ void qmv_ffn_cta(const QmvParams& P, const GroupConsts& K, const Smem
 
     // ---------------------------------------------------- consumer warps
     pdl_wait();                           // x comes from the preceding kernel
-    FfnState st{0, 0, 0u, false};
-    if (N0 > 0) ffn_consume<F0, R0, false>(P, K, sm, P.geo[0], sm.segs[0], N0, NCT, red_tile, st);
-    if (N1 > 0) {
-        // h complete: this CTA's producer has arrived (gold holds the word's
-        // value before its add), then every other CTA.  Warp 0 waits as a
-        // whole; the others wait at the consumer barrier that staging opens with.
-        if (warp == 0) {
-            if (lane == 0) {
-                bool ok = mbar_wait_bounded(gready, 0u, P.timeout_ns);
-                if (ok) ok = grid_wait(P.gbar, *reinterpret_cast<volatile uint32_t*>(gold), P.timeout_ns);
-                __threadfence();
-                if (!ok) {
+    FfnState st{0, 0, 0u, 0u, false};
+    // the consumers' share of the reductions: tiles [m0, m1) of phase ph
+    auto reduce_last = [&](int m0, int m1, int ph) {
+        for (int m = m0; m < m1 && !st.aborted; ++m) {
+            const int k = m - (m1 - 2);
+            if (!wait_empty(m)) {
+                st.aborted = true;
+                if (lane == 0) {
                     record_status(P.status, STATUS_TIMEOUT);
                     atomicExch(sm.abort_flag, 1);
                 }
+                break;
             }
-            __syncwarp();
+            reduce_tile<1>(P.geo[ph], sm.segs[ph], tile_of(m), sm.red + (size_t)(m % NRED) * red_tile, lane,
+                           k ? NC - 1 - warp : warp, NC);
         }
-        ffn_consume<F1, R1, true>(P, K, sm, P.geo[1], sm.segs[1], N1, NCT, red_tile, st);
+    };
+    if (N0 > 0) {
+        ffn_consume<F0, R0, false>(P, K, sm, P.geo[0], sm.segs[0], N0, NCT, red_tile, st);
+        reduce_last(P0, N0, 0);
     }
-    // the last two tiles (phase 1 only), shared by the consumer warps
-    const int mfirst = max(N0, NT - 2);
-    for (int m = mfirst; m < NT && !st.aborted; ++m) {
-        const int k = m - (NT - 2);
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(&sm.empty[m % S_], (uint32_t)(m / S_) & 1u, P.timeout_ns);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) {
-            st.aborted = true;
-            if (lane == 0) {
+    // This CTA's h is written (the consumers' share fenced here, the
+    // producer's before it signals): arrive on the grid barrier, then wait
+    // until every CTA has.  Warp 0 waits as a whole; the others wait at the
+    // consumer barrier that staging opens with.
+    __threadfence();
+    consumer_sync(NCT);
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(gready, 0u, P.timeout_ns);
+            __threadfence();
+            const uint32_t inc = bid == 0 ? 0x80000000u - (uint32_t)(grid - 1) : 1u;
+            const uint32_t old = atomicAdd(P.gbar, inc);
+            if (ok && N1 > 0) ok = grid_wait(P.gbar, old, P.timeout_ns);
+            __threadfence();
+            if (!ok) {
                 record_status(P.status, STATUS_TIMEOUT);
                 atomicExch(sm.abort_flag, 1);
             }
-            break;
         }
-        reduce_tile<1>(P.geo[1], sm.segs[1], tile_of(m), sm.red + (size_t)(m % NRED) * red_tile, lane,
-                       k ? NC - 1 - warp : warp, NC);
+        __syncwarp();
+    }
+    if (N1 > 0) {
+        ffn_consume<F1, R1, true>(P, K, sm, P.geo[1], sm.segs[1], N1, NCT, red_tile, st);
+        reduce_last(P1, NT, 1);
     }
 }
 
@@ -286,10 +295,10 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R0 > R1 ? R0 : R1
     sm.red = reinterpret_cast<float*>(smem + L.red);
     sm.full = reinterpret_cast<uint64_t*>(smem + L.bars);
     sm.empty = sm.full + S_;
-    uint64_t* gready = sm.empty + S_;
+    sm.xfull = sm.empty + S_;
+    uint64_t* gready = sm.xfull + 1;
     sm.cnt = reinterpret_cast<int*>(gready + 1);
     sm.abort_flag = sm.cnt + (S_ + 1);
-    uint32_t* gold = reinterpret_cast<uint32_t*>(sm.abort_flag + 1);
     Seg* segs = reinterpret_cast<Seg*>(smem + L.segs);
     {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.seg[0]);
@@ -303,14 +312,14 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R0 > R1 ? R0 : R1
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], (blockDim.x >> 5) - 1);
         }
+        mbar_init(sm.xfull, 1);
         mbar_init(gready, 1);
         for (int s = 0; s <= S_; ++s) sm.cnt[s] = 0;
         *sm.abort_flag = 0;
-        *gold = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    qmv_ffn_cta<F0, R0, F1, R1>(P, K, sm, gready, gold);
+    qmv_ffn_cta<F0, R0, F1, R1>(P, K, sm, gready);
 }
 
 namespace {

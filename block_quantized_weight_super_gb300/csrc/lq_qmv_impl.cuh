@@ -168,18 +168,19 @@ __device__ __forceinline__ int qxcol(int G, int i) {
 // sums come from registers: the 16-column sum of a unit (in column order)
 // plus that of its neighbour unit (lane ^ 1).  Ends with the consumer barrier;
 // the caller brackets it with one before.  COHERENT: x was written by other
-// CTAs of this kernel, so it is read through L2 (no read-only path).
-template <int FMT, int B, bool COHERENT = false>
+// CTAs of this kernel, so it is read through L2 (no read-only path).  NU:
+// units each thread loads before storing (all in flight at once).
+template <int FMT, int B, bool COHERENT = false, int NU = 2>
 __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int ct, int nct) {
     const int U = Gm.U;
     const int nval = qseg_nval(S, B);
     const int boff = qseg_boff(S);
     const int units = B * U * 4;
     const int wbase = ct & ~31;                  // loop bound uniform over the warp
-    for (int e0 = ct, w0 = wbase; w0 < units; e0 += 2 * nct, w0 += 2 * nct) {
-        float4 v[2][4];
+    for (int e0 = ct, w0 = wbase; w0 < units; e0 += NU * nct, w0 += NU * nct) {
+        float4 v[NU][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NU; ++h) {
             const int e = e0 + h * nct;
             const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
             if (e < units && b < nval) {
@@ -194,7 +195,7 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
             }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NU; ++h) {
             const int e = e0 + h * nct;
             const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
             if (e < units) {
@@ -212,6 +213,142 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
         }
     }
     consumer_sync(nct);
+}
+
+// Bulk staging of x (h in phase 1 of the one-launch FFN, after its grid
+// barrier).  Consumer thread 0 copies the valid x rows in column order with bulk copies
+// (TMA) of at most 8 KB into the top B*U*64 floats of the x area (the padding
+// of the group slots leaves exactly that much room below); the consumer
+// threads then move the units (16 columns of one group, assigned as in
+// stage_x) into the padded slots in rounds: load the round's units, consumer
+// barrier, store them.  A slot ends 4 floats per group above where the raw
+// row runs, so the stores of a round never reach raw values of a later round
+// (Q6_K's permutation stays within a super-block, and a round covers whole
+// super-blocks).  In isolation a few large copies deliver an x that every
+// CTA reads about twice as fast as thread loads (and far faster than one copy
+// per slot); at the start of a launch, though, they queue behind the weight
+// tiles already issued and arrive later than loads, so there x is loaded.
+// Slots and sub-block sums equal stage_x's.  coherent: x was written by
+// other CTAs of this kernel.  Returns false if the wait ran out.
+template <int FMT, int B>
+__device__ bool stage_x_bulk(const QGeo& Gm, const Seg& S, float* xs, float* sxs, uint64_t* xfull,
+                             uint32_t parity, uint64_t timeout_ns, int ct, int nct, bool coherent) {
+    constexpr int NU = 2;                        // units per thread and round
+    const int U = Gm.U, cols = Gm.cols;
+    const int nval = qseg_nval(S, B);
+    const int boff = qseg_boff(S);
+    float* raw = xs + B * U * 4;                 // B rows of cols floats, 16-byte aligned
+    const int lane = ct & 31;
+    if (ct == 0) {
+        if (coherent) asm volatile("fence.proxy.async.global;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the area's generic use
+        mbar_arrive_expect_tx(xfull, (uint32_t)(nval * cols * 4));
+        for (int b = 0; b < nval; ++b) {
+            const int rho = boff + b;
+            const char* src = reinterpret_cast<const char*>(S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * cols);
+            char* dst = reinterpret_cast<char*>(raw + b * cols);
+            for (int off = 0; off < cols * 4; off += 8192)
+                bulk_g2s(dst + off, src + off, (unsigned)min(8192, cols * 4 - off), xfull);
+        }
+    }
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(xfull, parity, timeout_ns);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    const int units = B * U * 4;
+    // the round count depends only on units and nct: every consumer thread
+    // passes every barrier of the loop
+    for (int base = 0; base < units; base += NU * nct) {
+        const int e0 = base + ct;
+        float4 v[NU][4];
+#pragma unroll
+        for (int h = 0; h < NU; ++h) {
+            const int e = e0 + h * nct;
+            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
+            if (ok && e < units && b < nval) {
+                const float4* src = reinterpret_cast<const float4*>(raw + b * cols + qxcol<FMT>(G, 16 * q));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[h][k] = src[k];
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[h][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        consumer_sync(nct);                      // the round's raw values are read before any store
+#pragma unroll
+        for (int h = 0; h < NU; ++h) {
+            const int e = e0 + h * nct;
+            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
+            if (e < units) {
+                float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = v[h][k];
+            }
+            if (FMT == FMT_Q4_K) {
+                float s16 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s16 = ((s16 + v[h][k].x) + v[h][k].y) + v[h][k].z + v[h][k].w;
+                const float s32 = s16 + __shfl_xor_sync(0xFFFFFFFFu, s16, 1);
+                if (e < units && (q & 1) == 0) sxs[(b * U + G) * 2 + (q >> 1)] = s32;
+            }
+        }
+    }
+    consumer_sync(nct);
+    return ok;
+}
+
+// Segments reading the same x rows (QKV: Q and K) need no second staging.
+__device__ __forceinline__ bool same_xsrc(const Seg& a, const Seg& b) {
+    return a.x == b.x && a.xmap == b.xmap && a.boff == b.boff && a.bcnt == b.bcnt && a.b0 == b.b0 &&
+           a.nbatch == b.nbatch;
+}
+
+// Stage group G of the B x rows of segment S for the calling thread alone.
+// For launches with one consumer thread per group (NCT == U: the down
+// projections) every work item of a thread uses the same group, so each
+// thread stages only what it reads itself: no barrier before or after, and
+// a thread starts its items as soon as its own loads land instead of when the
+// whole CTA's x (the L2 bandwidth of all CTAs together) has arrived.  The
+// values and the sub-block sums (same order of additions) equal stage_x's.
+template <int FMT, int B, bool COHERENT = false>
+__device__ __forceinline__ void stage_x_own(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int G) {
+    const int U = Gm.U;
+    const int nval = qseg_nval(S, B);
+    const int boff = qseg_boff(S);
+#pragma unroll 1
+    for (int b = 0; b < B; ++b) {
+        float4 v[4][4];
+        if (b < nval) {
+            const int rho = boff + b;
+            const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * Gm.cols;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[q][k] = COHERENT ? __ldcg(src + k) : __ldg(src + k);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[4 * q + k] = v[q][k];
+        if (FMT == FMT_Q4_K) {
+            float s16[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s16[q] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s16[q] = ((s16[q] + v[q][k].x) + v[q][k].y) + v[q][k].z + v[q][k].w;
+            }
+            sxs[(b * U + G) * 2] = s16[0] + s16[1];
+            sxs[(b * U + G) * 2 + 1] = s16[2] + s16[3];
+        }
+    }
 }
 
 // ---------------------------------------------------------------- items
@@ -514,6 +651,7 @@ struct Smem {
     float* red;
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* xfull;        // bulk staging of x has landed (one-launch FFN)
     int* cnt;
     int* abort_flag;
 };
@@ -634,8 +772,14 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     for (int n = 0, s = 0; w.t < w.end; ++n) {
         const Seg& S = sm.segs[w.hint];
         if (w.hint != cur_seg) {
-            consumer_sync(NCT);          // every consumer is done with the previous x
-            stage_x<FMT, B>(Gm, S, sm.xs, sm.sxs, tid, NCT);
+            if (cur_seg >= 0 && same_xsrc(sm.segs[cur_seg], S)) {
+                // the staged x serves this segment too
+            } else if (NCT == U) {
+                stage_x_own<FMT, B>(Gm, S, sm.xs, sm.sxs, G_first);
+            } else {
+                consumer_sync(NCT);      // every consumer is done with the previous x
+                stage_x<FMT, B>(Gm, S, sm.xs, sm.sxs, tid, NCT);
+            }
             cur_seg = w.hint;
         }
         if (!aborted) {
@@ -739,6 +883,7 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_k
     off = (off + 7) & ~size_t(7);
     sm.full = reinterpret_cast<uint64_t*>(smem + off);
     sm.empty = sm.full + S_;
+    sm.xfull = nullptr;
     sm.cnt = reinterpret_cast<int*>(sm.empty + S_);
     sm.abort_flag = sm.cnt + (S_ + 1);
     size_t seg_off = off + (size_t)2 * S_ * sizeof(uint64_t) + (size_t)(S_ + 2) * sizeof(int);

@@ -114,32 +114,36 @@ int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int6
 int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
                        float* h, int batch, int act, lq_stream_t stream);
 
-/* lq_ffn -- the dense FFN of a decode step: h = act(Wg.x) * (Wu.x) as in
+/* lq_ffn -- the dense FFN of a decode step: h = act(Wg.x) * (Wu.x) by
  * lq_ffn_gate_up_act (interleaved Wgu, format fmt_gu, inter pairs x hidden
- * columns), then y = Wd.h (Wd: hidden rows x inter columns, format fmt_down).
- * larql "Architecture -> Metal shader map", Gemma 3 table: q4k_ffn_gate_up +
- * geglu feeding the Q6_K down projection.
+ * columns), then y = Wd.h by lq_matvec (Wd: hidden rows x inter columns,
+ * format fmt_down).  larql "Architecture -> Metal shader map", Gemma 3 table:
+ * q4k_ffn_gate_up + geglu feeding the Q6_K down projection.
  * x: [batch][hidden], h: [batch][inter] (written: the intermediate), y:
- * [batch][hidden]; h overlaps neither x nor y.  Results are those of
- * lq_ffn_gate_up_act followed by lq_matvec on h, bit for bit.
- * At batch 1, with x and h 16-byte aligned and a shape the one-launch kernel
- * can tile (lq_ffn_launches), both matrices run in ONE launch whose phases
- * meet at a grid-wide barrier; otherwise the two calls run in turn.
- * sync: a device word the one-launch kernel uses as its grid barrier, zero
- * before its first use (every call leaves its low 31 bits zero, ready for the
- * next), or NULL for the library's own word.  Calls that may run at the same time (other streams)
- * need distinct words.  The one-launch kernel needs all its CTAs resident
- * together, so it should not share the GPU with other kernels that hold SMs
- * for long; if its CTAs cannot meet, its bounded waits run out (device
- * status STATUS_TIMEOUT, see lq_device_status) rather than hang.
+ * [batch][hidden]; h overlaps neither x nor y.  Two launches, on stream.
  * inter == 0 or hidden == 0 -> LQ_ESHAPE. */
 int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
-           const float* x, float* h, float* y, int batch, int act, uint32_t* sync, lq_stream_t stream);
+           const float* x, float* h, float* y, int batch, int act, lq_stream_t stream);
 
-/* lq_ffn_launches -- kernel launches lq_ffn makes for these formats and
- * sizes when x and h are 16-byte aligned: 1 (one-launch kernel) or 2; 0 for
- * invalid arguments.  No device work. */
-int lq_ffn_launches(int fmt_gu, int fmt_down, int64_t inter, int64_t hidden, int batch);
+/* lq_ffn_one_launch -- lq_ffn at batch 1 as ONE launch: every CTA runs its
+ * gate/up tiles, the CTAs meet at a grid-wide barrier once h is complete,
+ * then run their down tiles (h staged by bulk copies).  Results equal
+ * lq_ffn's bit for bit.  Measured on GB300 at the Gemma-3-4B FFN it is not
+ * faster than lq_ffn's two launches (the barrier and the distribution of h
+ * to every CTA cost what the second launch did), so lq_ffn does not use it.
+ * x and h 16-byte aligned (LQ_EALIGN otherwise).  Shapes and format pairs
+ * the kernel cannot tile evenly (Q8_0 rows, widths without a common warp
+ * count, formats other than Q4_K->Q6_K, Q4_K->Q4_K, Q6_K->Q6_K) give
+ * LQ_EUNSUPPORTED before any launch.
+ * sync: a device word used as the grid barrier, zero before its first use
+ * (every call leaves its low 31 bits zero), or NULL for the library's own
+ * word; calls that may run at the same time need distinct words.  All CTAs
+ * of the launch must be resident together: if another kernel holds SMs for
+ * long, the bounded waits run out (STATUS_TIMEOUT, lq_device_status) rather
+ * than hang. */
+int lq_ffn_one_launch(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter,
+                      int64_t hidden, const float* x, float* h, float* y, int act, uint32_t* sync,
+                      lq_stream_t stream);
 
 /* MoE expert FFN (dotLLM MoeSwiGluMlp rule; larql Gemma 4 26B-A4B table).
  * router: [E][hidden] fp32; logits l_e = router_e . x_t, p = softmax(l),

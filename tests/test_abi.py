@@ -98,34 +98,37 @@ def test_other_entry_validation(lq):
 
 def test_ffn_validation(lq):
     L = lq.lib()
-    ffn = lambda f0, w, f1, wd, inter, hidden, x, h, y, b, act, sync: L.lq_ffn(
-        f0, w, f1, wd, inter, hidden, x, h, y, b, act, sync, None)
-    assert ffn(1, None, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 2, None, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 2, FAKE, 256, 250, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE   # hidden % 256
-    assert ffn(1, FAKE, 2, FAKE, 100, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE   # inter % 256 (down cols)
-    assert ffn(1, FAKE, 2, FAKE, 0, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_ESHAPE
-    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 0, 1, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 3, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 9, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, None, FAKE, 1, 1, None) == lq.LQ_EINVAL
-    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE + 2, FAKE, 1, 1, None) == lq.LQ_EALIGN
-    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1, FAKE + 2) == lq.LQ_EALIGN
+    ffn = lambda f0, w, f1, wd, inter, hidden, x, h, y, b, act: L.lq_ffn(
+        f0, w, f1, wd, inter, hidden, x, h, y, b, act, None)
+    assert ffn(1, None, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, None, 256, 256, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 250, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_ESHAPE   # hidden % 256
+    assert ffn(1, FAKE, 2, FAKE, 100, 256, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_ESHAPE   # inter % 256 (down cols)
+    assert ffn(1, FAKE, 2, FAKE, 0, 256, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_ESHAPE
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 0, 1) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 3) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 9, FAKE, 256, 256, FAKE, FAKE, FAKE, 1, 1) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, None, FAKE, 1, 1) == lq.LQ_EINVAL
+    assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE + 2, FAKE, 1, 1) == lq.LQ_EALIGN
 
 
-def test_ffn_launch_plan(lq):
-    """Which FFN shapes run as one launch (no device work: host planning only).
-    A shape fuses when some consumer-warp count tiles both matrices evenly
-    with tiles of at most 32 KB."""
+def test_ffn_one_launch_validation(lq):
+    """Shapes and format pairs the one-launch kernel cannot tile evenly, and
+    misaligned x / h / sync, are refused on the host (no device work).  A
+    shape fuses when some consumer-warp count tiles both matrices evenly with
+    tiles of at most 32 KB."""
+    L = lq.lib()
     Q4, Q6, Q8 = 1, 2, 3
-    assert lq.lq_ffn_launches(Q4, Q6, 10240, 2560, 1) == 1      # Gemma-3-4B FFN
-    assert lq.lq_ffn_launches(Q4, Q6, 10240, 2560, 2) == 2      # batch 2: two launches
-    assert lq.lq_ffn_launches(Q4, Q4, 14336, 4096, 1) == 2      # Llama shape: no common tiling
-    assert lq.lq_ffn_launches(Q8, Q8, 512, 512, 1) == 2         # Q8_0 rows: tiles above 32 KB
-    assert lq.lq_ffn_launches(Q8, Q4, 512, 512, 1) == 2         # no kernel for this pair
-    assert lq.lq_ffn_launches(Q4, Q6, 0, 2560, 1) == 0
-    assert lq.lq_ffn_launches(Q4, 7, 256, 256, 1) == 0
-    assert lq.lq_ffn_launches(Q4, Q6, 256, 256, 0) == 0
+    one = lambda f0, f1, inter, hidden, x=FAKE, h=FAKE, sync=None: L.lq_ffn_one_launch(
+        f0, FAKE, f1, FAKE, inter, hidden, x, h, FAKE, 1, sync, None)
+    assert one(Q4, Q4, 14336, 4096) == lq.LQ_EUNSUPPORTED     # Llama widths: no common warp count
+    assert one(Q4, Q6, 768, 2560) == lq.LQ_EUNSUPPORTED
+    assert one(Q8, Q8, 512, 512) == lq.LQ_EUNSUPPORTED        # Q8_0 rows: tiles above 32 KB
+    assert one(Q8, Q4, 512, 512) == lq.LQ_EUNSUPPORTED        # no kernel for this pair
+    assert one(Q4, Q6, 10240, 2560, x=FAKE + 4) == lq.LQ_EALIGN
+    assert one(Q4, Q6, 10240, 2560, h=FAKE + 8) == lq.LQ_EALIGN
+    assert one(Q4, Q6, 10240, 2560, sync=FAKE + 2) == lq.LQ_EALIGN
+    assert one(Q4, Q6, 0, 2560) == lq.LQ_ESHAPE
 
 
 def test_moe_validation(lq):

@@ -255,9 +255,9 @@ def _ffn_inputs(lq, f0, f1, inter, hidden, batch, seed):
 
 
 def _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y):
-    """h and y of lq_ffn: bit for bit those of the two separate calls, and
-    within the oracle's bounds (gate/up against the oracle; down against the
-    oracle's matvec of the GPU's own h)."""
+    """h and y of an FFN call: bit for bit those of the two separate calls,
+    and within the oracle's bounds (gate/up against the oracle; down against
+    the oracle's matvec of the GPU's own h)."""
     xd, Wdd = dev(x), dev(Wd)
     h2, y2 = empty((batch, inter)), empty((batch, hidden))
     lq.lq_ffn_gate_up_act(f0, Wgu, inter, hidden, xd, h2, batch, act)
@@ -271,6 +271,20 @@ def _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y):
     assert_within(got_y, ref, oracle.matvec_bound(S), "y")
 
 
+@pytest.mark.parametrize("f0,f1,inter,hidden,batch,act", [
+    (Q4_K, Q6_K, 1280, 2560, 1, 1),
+    (Q4_K, Q6_K, 1280, 2560, 2, 2),   # batch 2: tensor-core gate/up, then the Q6_K down
+    (Q8_0, Q8_0, 512, 512, 1, 2),
+    (Q4_K, Q4_K, 768, 4096, 3, 1),
+])
+def test_ffn(lq, f0, f1, inter, hidden, batch, act):
+    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, batch, 77 + inter + batch)
+    lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
+    h, y = empty((batch, inter)), empty((batch, hidden))
+    lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, batch, act)
+    _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y)
+
+
 @pytest.mark.parametrize("f0,f1,inter,hidden,act", [
     (Q4_K, Q6_K, 256, 512, 1),      # five tiles per phase, ragged last tiles of both
     (Q4_K, Q6_K, 1280, 2560, 2),    # many tiles per CTA
@@ -280,11 +294,10 @@ def _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y):
     (Q4_K, Q6_K, 10240, 2560, 1),   # the Gemma-3-4B FFN: 1280 tiles per phase over a full grid
 ])
 def test_ffn_one_launch(lq, f0, f1, inter, hidden, act):
-    assert lq.lq_ffn_launches(f0, f1, inter, hidden, 1) == 1
     Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, 1, 41 + inter + hidden)
     lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
     h, y = empty((1, inter)), empty((1, hidden))
-    lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, 1, act)
+    lq.lq_ffn_one_launch(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, act)
     status_clean(lq)
     _ffn_check(lq, f0, f1, inter, hidden, 1, act, Wg, Wu, Wd, x, Wgu, h, y)
 
@@ -302,8 +315,7 @@ def test_ffn_one_launch_barrier_reuse(lq):
     ref = []
     for f0, f1, inter, hidden, Wgu, Wd, x in runs:
         h, y = empty((1, inter)), empty((1, hidden))
-        lq.lq_ffn_gate_up_act(f0, Wgu, inter, hidden, x, h, 1, 2)
-        lq.lq_matvec(f1, Wd, hidden, inter, h, y, 1)
+        lq.lq_ffn(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 1, 2)
         ref.append((host(h), host(y)))
     word = torch.zeros(1, dtype=torch.int32, device="cuda")
     for start in (None, 0, -2 ** 31):
@@ -312,24 +324,18 @@ def test_ffn_one_launch_barrier_reuse(lq):
         for rep in range(3):
             for (f0, f1, inter, hidden, Wgu, Wd, x), (rh, ry) in zip(runs, ref):
                 h, y = empty((1, inter)), empty((1, hidden))
-                lq.lq_ffn(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 1, 2,
-                          sync=None if start is None else word)
+                lq.lq_ffn_one_launch(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 2,
+                                     sync=None if start is None else word)
                 assert _bits_equal(host(h), rh) and _bits_equal(host(y), ry), (start, rep, inter, hidden)
     status_clean(lq)
 
 
-@pytest.mark.parametrize("f0,f1,inter,hidden,batch", [
-    (Q4_K, Q6_K, 1280, 2560, 2),    # batch 2: tensor-core gate/up, then the Q6_K down
-    (Q8_0, Q8_0, 512, 512, 1),      # no one-launch tiling for Q8_0 rows
-    (Q4_K, Q6_K, 768, 2560, 1),     # no warp count tiles both matrices evenly
-])
-def test_ffn_two_launches(lq, f0, f1, inter, hidden, batch):
-    assert lq.lq_ffn_launches(f0, f1, inter, hidden, batch) == 2
-    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, batch, 77 + inter)
-    lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
-    h, y = empty((batch, inter)), empty((batch, hidden))
-    lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, batch, 2)
-    _ffn_check(lq, f0, f1, inter, hidden, batch, 2, Wg, Wu, Wd, x, Wgu, h, y)
+def test_ffn_one_launch_unsupported_raises(lq):
+    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, Q4_K, Q6_K, 768, 2560, 1, 5)
+    h, y = empty((1, 768)), empty((1, 2560))
+    with pytest.raises(lq.LqError):
+        lq.lq_ffn_one_launch(Q4_K, Wgu, Q6_K, dev(Wd), 768, 2560, dev(x), h, y, 1)
+    assert np.isnan(host(y)).all()          # nothing launched
 
 
 # ---------------------------------------------------------------- tensor-core path
