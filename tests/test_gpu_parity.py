@@ -74,6 +74,7 @@ def test_dequant_hand_built_extremes(lq):
 MV_CASES = [
     (Q4_K, 333, 2560), (Q4_K, 100, 512), (Q4_K, 1, 256), (Q4_K, 70, 2048), (Q4_K, 65, 4096),
     (Q6_K, 101, 2560), (Q6_K, 3, 768), (Q6_K, 50, 1280), (Q6_K, 45, 10240),
+    (Q6_K, 1000, 10240), (Q4_K, 301, 8192),      # x of 32-40 KB: one thread per 64-column group
     (Q8_0, 77, 4096), (Q8_0, 33, 512), (Q8_0, 3, 14336),
 ]
 
@@ -120,11 +121,14 @@ def _tensor_path(fmt, cols, M):
             (fmt == Q8_0 and cols % 256 == 0 and M >= 3))
 
 
-@pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336), (Q4_K, 2304)])
+@pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336), (Q4_K, 2304),
+                                      (Q6_K, 10240), (Q4_K, 8192)])
 def test_batch_invariance(lq, fmt, cols):
     """row b of a batch-M call is bit-identical to the same x row in any other
     call that takes the same kernel: a batch-1 call for the CUDA-core kernel,
-    the batch-8 call for the tensor-core one (each x row is its own MMA column)."""
+    the batch-8 call for the tensor-core one (each x row is its own MMA column).
+    At 8192-10240 columns each batch-1 thread stages its own x group; the
+    batch-2/4 calls stage x collectively: the same items and sums."""
     rows = 67
     g = synth.rng(11)
     W = synth.weights(g, fmt, rows, cols)
