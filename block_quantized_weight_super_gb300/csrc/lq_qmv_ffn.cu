@@ -9,11 +9,14 @@
 // of both phases through one ring of stages without a break, so the first
 // down tiles are in shared memory while the last gate/up tiles are computed;
 // separate launches pay a ramp and a drain for each matrix instead.  The
-// producer reduces every phase-0 tile itself (h is written by the producer
-// warps only) and then arrives on a grid barrier; the consumer warps wait for
-// that barrier, stage the whole h as x of phase 1 (through L2, not the
-// read-only path) and go on.  The work items, the reductions and so every
-// result are those of the separate gate/up and down launches, bit for bit.
+// producer sums the partials of the phase-0 tiles but the last two, which the
+// consumer warps share; once the producer has signalled that its share of h
+// is written, consumer thread 0 arrives on a grid barrier and waits for every
+// CTA, then bulk-copies h into shared memory as x of phase 1.  The work
+// items, the reductions and so every result are those of the separate
+// gate/up and down launches, bit for bit.  On GB300 at the Gemma-3-4B FFN
+// this is not faster than the two launches: the barrier and the distribution
+// of h to every CTA cost what the second launch did.
 //
 // Grid barrier: one device word whose low 31 bits are zero between calls
 // (zero before its first use).  CTA 0 adds 2^31 - (grid - 1) and every other
