@@ -21,7 +21,8 @@ sample of the same layers as the reference arm.
 
 --workload selects one of the other named shapes instead of the layer, with
 the same JSON line: llama_ffn (SwiGLU FFN 2 x 14336 x 4096 + 4096 x 14336 at
---batch M, --fmt q4k|q80), lm_head (262144 x 2560 Q4_K, batch 1),
+--batch M, --fmt q4k|q80), lm_head (262144 x 2560 Q4_K, batch 1; --softcap C
+fuses the final-logit soft-cap C * tanh(y / C) into the store),
 mixtral_moe (8 experts, top-2, 16 tokens, Q4_K) and matvec_small (Q4_K 256 x
 2560, batch 1).  A step is one call of the workload; weight copies rotate
 so that each step reads weights that are not in L2 (at least three times
@@ -65,6 +66,8 @@ def parse():
     ap.add_argument("--workload", default="gemma_layer", choices=list(WORKLOADS))
     ap.add_argument("--batch", type=int, default=8, help="x rows (llama_ffn)")
     ap.add_argument("--fmt", default="q4k", choices=["q4k", "q80"], help="weight format (llama_ffn)")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="final-logit soft-cap fused into the store (lm_head; 0 = none)")
     a = ap.parse_args()
     if a.workload != "gemma_layer":
         if "--steps" not in sys.argv:
@@ -382,7 +385,7 @@ def cpu_baseline(sample_layers=1, rows_frac=0.25):
 # DRAM bytes (read + write) of one gate+up launch, from the ncu capture in
 # profiles/qmv_gate_up_and_down_dram_traffic.md, valid while the sources of
 # that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "713df550e4e874a1e607a1f7281882f48a8857a0f90eef2e4644c9fa4cc85533", "bytes": 29570816}
+GATEUP_TRAFFIC = {"csrc_sha256": "9afbb318874b71a27d858d3c6aa7c1990a68de4051ad825eb82a1a4659cc7f17", "bytes": 29572608}
 
 
 # the sources the batch-1 gate+up launch is compiled from
@@ -468,7 +471,14 @@ class Workload:
             self.y = torch.empty((1, rows), **f32)
             self.dom_name = f"Q4_K matvec {rows}x{cols}, batch 1"
             self.launches = 1
-            self.step = lambda w, st: lq.lq_matvec(lq.LQ_Q4_K, w["w"], rows, cols, self.x, self.y, 1, st)
+            cap = args.softcap if name == "lm_head" else 0.0
+            if cap > 0:
+                self.desc += f", final-logit soft-cap {cap:g} fused into the store"
+                self.dom_name += f", soft-cap {cap:g}"
+                self.step = lambda w, st: lq.lq_matvec_softcap(lq.LQ_Q4_K, w["w"], rows, cols, self.x, self.y, 1,
+                                                               cap, st)
+            else:
+                self.step = lambda w, st: lq.lq_matvec(lq.LQ_Q4_K, w["w"], rows, cols, self.x, self.y, 1, st)
             self.dom = self.step
             self.cpu_jobs = [(lq.LQ_Q4_K, Wn, cols, x)]
         elif name == "mixtral_moe":

@@ -21,7 +21,7 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
  LQ_EUNSUPPORTED) = range(8)
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
-           "lq_dequant", "lq_matvec", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
+           "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
            "lq_ffn", "lq_ffn_one_launch", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_static",
            "lq_device_status",
            "lq_set_wait_timeout_ns", "lq_probe_timeout"]
@@ -54,6 +54,7 @@ def lib():
             "lq_last_error": ([], C.c_char_p),
             "lq_dequant": ([i32, vp, i64, i64, vp, vp], i32),
             "lq_matvec": ([i32, vp, i64, i64, vp, vp, i32, vp], i32),
+            "lq_matvec_softcap": ([i32, vp, i64, i64, vp, vp, i32, C.c_float, vp], i32),
             "lq_qkv_mixed": ([i32, vp, i64, i32, vp, i64, i32, vp, i64, i64, vp, vp, vp, vp, i32, vp], i32),
             "lq_pack_gate_up": ([i32, vp, vp, i64, i64, vp, vp], i32),
             "lq_ffn_gate_up_act": ([i32, vp, i64, i64, vp, vp, i32, i32, vp], i32),
@@ -123,6 +124,11 @@ def lq_dequant(fmt, W, rows, cols, out, stream=None):
 
 def lq_matvec(fmt, W, rows, cols, x, y, batch, stream=None):
     return _check(lib().lq_matvec(fmt, _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, _stream(stream)))
+
+
+def lq_matvec_softcap(fmt, W, rows, cols, x, y, batch, cap, stream=None):
+    return _check(lib().lq_matvec_softcap(fmt, _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, float(cap),
+                                          _stream(stream)))
 
 
 def lq_qkv_mixed(fq, Wq, nq, fk, Wk, nk, fv, Wv, nv, cols, x, q, k, v, batch, stream=None):

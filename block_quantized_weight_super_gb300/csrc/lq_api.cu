@@ -2,6 +2,7 @@
 // planning and dispatch to the kernels.  Host code only, apart from the
 // device status word.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -616,9 +617,9 @@ int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, l
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "dequant launch");
 }
 
-int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
-              int batch, lq_stream_t stream) {
-    g_err[0] = 0;
+// y = W.x, each output stored through seg_out (cap 0: as computed)
+static int matvec_impl(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                       float cap, lq_stream_t stream) {
     int rc = check_mat(fmt, W, rows, cols, "W");
     if (rc) return rc;
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
@@ -626,15 +627,32 @@ int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x
     if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
     if (batch >= qmm_min_batch(fmt)) {
         std::vector<Seg> segs;
-        for (int b0 = 0; b0 < batch; b0 += QMM_NT)
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
             segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(QMM_NT, batch - b0)));
+            segs.back().cap = cap;
+        }
         if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
     }
     const int B = batch_width(cols, batch, {fmt}, false);
     std::vector<Seg> segs;
-    for (int b0 = 0; b0 < batch; b0 += B)
+    for (int b0 = 0; b0 < batch; b0 += B) {
         segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(B, batch - b0)));
+        segs.back().cap = cap;
+    }
     return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+              int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    return matvec_impl(fmt, W, rows, cols, x, y, batch, 0.f, stream);
+}
+
+int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                      float cap, lq_stream_t stream) {
+    g_err[0] = 0;
+    if (!(cap > 0.f) || !std::isfinite(cap)) return fail(LQ_EINVAL, "soft-cap %g: not a finite positive value", (double)cap);
+    return matvec_impl(fmt, W, rows, cols, x, y, batch, cap, stream);
 }
 
 int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,

@@ -180,7 +180,7 @@ __global__ void direct_mv_kernel(Seg S, int64_t cols, int maxb) {
         const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * cols;
         float v;
         if (S.mode == MODE_PLAIN) {
-            v = direct_row(S.fmt, S.w + (int64_t)warp * rb, cols, xrow, lane);
+            v = seg_out(S.cap, direct_row(S.fmt, S.w + (int64_t)warp * rb, cols, xrow, lane));
         } else {
             const uint8_t* rg = S.mode == MODE_PAIR_INTERLEAVED ? S.w + (int64_t)(2 * warp) * rb
                                                                : S.w + (int64_t)warp * rb;

@@ -723,7 +723,8 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_kernel(const __grid_cons
                         for (int i = 0; i < 4; ++i) {
                             const int row = lrb * RT + r0w + g + (i >> 1) * 8;
                             const int tok = 2 * cq + (i & 1);
-                            if (row < S.nout && tok < nval) S.y[(int64_t)(boff + tok) * S.ld_y + row] = v[i];
+                            if (row < S.nout && tok < nval)
+                                S.y[(int64_t)(boff + tok) * S.ld_y + row] = seg_out(S.cap, v[i]);
                         }
                     } else {
                         // row g is the gate row of pair p0 + 8 rq + g, row g + 8 its up row

@@ -634,7 +634,7 @@ __device__ __forceinline__ void reduce_tile(const QGeo& Gm, const Seg& S, int t,
             vg += __shfl_xor_sync(0xFFFFFFFFu, vg, m);
             vu += __shfl_xor_sync(0xFFFFFFFFu, vu, m);
         }
-        const float v = pair ? act_q(S.act, vg) * vu : vg;
+        const float v = pair ? act_q(S.act, vg) * vu : seg_out(S.cap, vg);
         const int pi = oo / B, b = oo % B;
         if (live && j == 0 && b < nval) y[(int64_t)(boff + b) * ldy + o0 + pi] = v;
     }

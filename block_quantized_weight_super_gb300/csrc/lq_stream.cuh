@@ -1,6 +1,7 @@
 // lq_stream.cuh -- segment descriptors of the quantized matvec kernel
 // (shared by the kernel translation units and the host launchers).
 #pragma once
+#include <cmath>
 #include <cstdint>
 
 namespace lq {
@@ -31,6 +32,12 @@ struct Seg {
     int32_t nbatch;        // valid batch rows when bcnt is null
     int32_t tile0;         // first global tile index of this segment
     int32_t ntiles;
+    float cap;             // > 0: plain outputs are cap * tanh(y / cap) (final-logit soft-cap)
 };
+
+// The stored value of a plain segment's output y (dotLLM PR #255 soft-cap
+// s -> softCap * tanh(s / softCap), applied to the logits after the lm_head
+// GEMM by PR #274's FinalLogitSoftcap).
+__host__ __device__ inline float seg_out(float cap, float y) { return cap > 0.f ? cap * tanhf(y / cap) : y; }
 
 }  // namespace lq

@@ -91,6 +91,16 @@ int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out,
 int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
               int batch, lq_stream_t stream);
 
+/* lq_matvec_softcap -- lq_matvec with the final-logit soft-cap fused into the
+ * store: y[b][r] = cap * tanh((sum_j w_rj x[b][j]) / cap).  dotLLM PR #255
+ * (soft-cap s -> softCap * tanh(s / softCap)) and PR #274 (FinalLogitSoftcap,
+ * applied to the logits after the lm_head GEMM; Gemma 4 configs carry
+ * final_logit_softcapping = 30).  cap must be finite and > 0 (LQ_EINVAL
+ * otherwise).  Every output lies in [-cap, cap]; its error is the matvec
+ * bound (the map has slope at most 1) plus a few ulps of the fp32 tanh. */
+int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
+                      int batch, float cap, lq_stream_t stream);
+
 /* lq_qkv_mixed -- q = Wq.x, k = Wk.x, v = Wv.x in ONE launch over a shared
  * x (larql q4k_q6k_qkv_proj: Q/K Q4_K and V Q6_K, or uniform formats).
  * Each matrix has its own format and row count; all share cols.

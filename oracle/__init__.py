@@ -58,6 +58,8 @@ def lib():
         L.orc_gelu_tanh.restype = d
         L.orc_silu.argtypes = [d]
         L.orc_silu.restype = d
+        L.orc_softcap.argtypes = [vp, i64, d, vp]
+        L.orc_softcap.restype = None
         L.orc_dequant.argtypes = [i32, vp, i64, i64, vp, i32]
         L.orc_matvec.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, i32]
         L.orc_matvec_rows.argtypes = [i32, vp, i64, vp, i64, vp, i32, vp, vp, i32]
@@ -103,6 +105,14 @@ def gelu_tanh(g: float) -> float:
 
 def silu(g: float) -> float:
     return lib().orc_silu(g)
+
+
+def softcap(y, cap: float) -> np.ndarray:
+    """final-logit soft-cap cap * tanh(y / cap), elementwise, fp64."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    out = np.empty_like(y)
+    lib().orc_softcap(_p(y), y.size, float(cap), _p(out))
+    return out
 
 
 def dequant(fmt: int, W, rows: int, cols: int, nthreads: int = 1) -> np.ndarray:
@@ -218,6 +228,15 @@ U32 = 2.0 ** -24
 def matvec_bound(S):
     """|y_gpu - y| <= 1e-5 * sum_j |w_ij x_j| + 1e-6 per element."""
     return 1e-5 * np.asarray(S) + 1e-6
+
+
+def softcap_bound(S, y, cap: float):
+    """bound on a soft-capped output whose pre-cap value carries the matvec
+    bound: the map has slope at most 1, so that bound carries over; fp32
+    evaluation adds the rounding of y / cap (slope <= 1: u32 |y|), tanhf
+    (2 ulps of the result) and the final product (1 ulp): 8 u32 (|y| + cap)
+    covers them with room."""
+    return matvec_bound(S) + 8 * U32 * (np.abs(np.asarray(y, dtype=np.float64)) + cap)
 
 
 def act_abs(g, act: int):

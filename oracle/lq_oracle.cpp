@@ -17,6 +17,9 @@
 //    the routing rule: softmax over all experts, top-k with the lower index
 //    winning ties, renormalise by the sum of the selected probabilities, then
 //    the weighted sum of per-expert SwiGLU FFNs.
+//  * dotLLM PR #255 (attention soft-cap: a score s becomes softCap *
+//    tanh(s / softCap)) and PR #274 (FinalLogitSoftcap: the same map applied
+//    to the logits after the lm_head GEMM): the final-logit soft-cap.
 //  * The byte layout inside a Q4_K / Q6_K super-block is not printed on the
 //    pages; this file takes the GGUF convention (the "GGUF-direct extract" of
 //    the larql dispatch table).  Parity with real GGUF bytes is therefore
@@ -195,6 +198,11 @@ int orc_block_elems(int fmt) { return block_elems(fmt); }
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }
 double orc_gelu_tanh(double g) { return gelu_tanh(g); }
 double orc_silu(double g) { return silu(g); }
+
+// Final-logit soft-cap of n values: out[i] = cap * tanh(y[i] / cap).
+void orc_softcap(const double* y, int64_t n, double cap, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = cap * std::tanh(y[i] / cap);
+}
 
 // Dequantize rows x cols weights (row-major block rows) to fp32.
 void orc_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,

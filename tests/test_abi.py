@@ -83,6 +83,17 @@ def test_matvec_validation(lq):
     assert "batch" in lq.lq_last_error() or lq.lq_last_error() == ""
 
 
+def test_softcap_validation(lq):
+    L = lq.lib()
+    f = lambda cap, x=FAKE: L.lq_matvec_softcap(1, FAKE, 4, 256, x, FAKE, 1, C.c_float(cap), None)
+    assert f(0.0) == lq.LQ_EINVAL
+    assert f(-30.0) == lq.LQ_EINVAL
+    assert f(float("nan")) == lq.LQ_EINVAL
+    assert f(float("inf")) == lq.LQ_EINVAL
+    assert f(30.0, x=None) == lq.LQ_EINVAL
+    assert L.lq_matvec_softcap(1, FAKE, 0, 256, FAKE, FAKE, 1, C.c_float(30.0), None) == lq.LQ_OK   # no rows
+
+
 def test_other_entry_validation(lq):
     L = lq.lib()
     assert L.lq_dequant(2, FAKE, 3, 100, FAKE, None) == lq.LQ_ESHAPE

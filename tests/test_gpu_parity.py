@@ -190,6 +190,36 @@ def test_matvec_zero_rows_and_zero_x(lq):
     assert (host(y) == 0).all()
 
 
+# ---------------------------------------------------------------- final-logit soft-cap
+
+@pytest.mark.parametrize("fmt,rows,cols,batch,xscale,xoff", [
+    (Q4_K, 333, 2560, 1, 1.0, 0),      # batch-1 kernel
+    (Q4_K, 130, 1024, 4, 1.0, 0),      # tensor cores
+    (Q8_0, 70, 1024, 4, 1.0, 0),       # tensor cores, Q8_0
+    (Q6_K, 101, 2560, 3, 1.0, 0),      # CUDA cores, batch 3
+    (Q4_K, 67, 2560, 1, 1.0, 4),       # x not 16-byte aligned: the plain-load kernel
+    (Q4_K, 200, 2560, 1, 3000.0, 0),   # |y| >> cap: saturation
+])
+def test_matvec_softcap(lq, fmt, rows, cols, batch, xscale, xoff):
+    cap = 30.0
+    g = synth.rng(rows + cols + batch + 7)
+    W = synth.weights(g, fmt, rows, cols)
+    x = (synth.activations(g, batch, cols) * np.float32(xscale)).astype(np.float32)
+    y = empty((batch, rows))
+    if xoff:
+        keep, xp = dev(x, offset_bytes=xoff)
+    else:
+        keep = xp = dev(x)
+    lq.lq_matvec_softcap(fmt, dev(W), rows, cols, xp, y, batch, cap)
+    yr, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    ref = oracle.softcap(yr, cap)
+    got = host(y)
+    assert_within(got, ref, oracle.softcap_bound(S, yr, cap), f"softcap fmt {fmt} b{batch}")
+    assert np.all(np.abs(got) <= cap)
+    if xscale > 1:
+        assert np.mean(np.abs(got) > 0.99 * cap) > 0.5       # most outputs saturate
+
+
 # ---------------------------------------------------------------- QKV
 
 @pytest.mark.parametrize("fq,fk,fv", [(Q4_K, Q4_K, Q6_K), (Q4_K, Q4_K, Q4_K), (Q8_0, Q8_0, Q8_0)])

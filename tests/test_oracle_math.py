@@ -155,6 +155,31 @@ def test_activation_slope_below_bound(orc, act):
     assert np.abs(np.diff(v) / np.diff(g)).max() < 1.2
 
 
+# ---------------------------------------------------------------- final-logit soft-cap
+
+@pytest.mark.parametrize("cap", [30.0, 50.0, 0.5])
+def test_softcap_pins(orc, cap):
+    """cap * tanh(y / cap) against facts outside the formula: zero, odd
+    symmetry, its third-order series, the inverse through the library's
+    atanh, saturation, monotonicity, and the (-cap, cap) band that the dotLLM
+    FinalLogitSoftcap test asserts."""
+    assert orc.softcap(np.array([0.0]), cap)[0] == 0.0
+    y = np.linspace(-20 * cap, 20 * cap, 8001)
+    out = orc.softcap(y, cap)
+    assert np.array_equal(orc.softcap(-y, cap), -out)                    # odd
+    assert np.all(np.abs(out) <= cap) and np.all(np.diff(out) >= 0)       # band, non-decreasing
+    inner = np.abs(y[:-1]) <= 5 * cap                                   # tanh is not yet 1.0 in fp64
+    assert np.all(np.diff(out)[inner] > 0)                              # strictly increasing there
+    assert abs(out[-1] - cap) < 1e-12 * cap                              # saturation at 20 cap
+    small = cap * np.array([1e-4, -3e-4, 1e-3])
+    series = small - small ** 3 / (3 * cap ** 2)                        # tanh t = t - t^3/3 + O(t^5)
+    assert np.all(np.abs(orc.softcap(small, cap) - series) <= 1e-12 * np.abs(small))
+    t = np.array([0.1, 0.5, 0.9, -0.75])
+    assert np.allclose(orc.softcap(cap * np.arctanh(t), cap), cap * t, rtol=1e-14, atol=0)   # inverse
+    grad = np.diff(out) / np.diff(y)
+    assert grad.max() <= 1.0 + 1e-9                                      # slope <= 1 (the bound uses it)
+
+
 # ---------------------------------------------------------------- gated FFN
 
 @pytest.mark.parametrize("act", [1, 2])
