@@ -33,14 +33,15 @@
  *    d*sc*q - dmin*m; Q6_K, Q8_0: exact); dot products accumulate in fp32
  *    with short fixed-order chains; each output is within
  *    1e-5 * sum_j |w_ij x_j| + 1e-6 of the exact value.  Results are
- *    deterministic.  Two kernels compute them: Q4_K calls with batch >= 2
- *    and Q8_0 calls with batch >= 3 whose cols are a multiple of 512 (Q4_K)
- *    or 256 (Q8_0), with W and x 16-byte aligned, run on the tensor cores
- *    (exact bf16 / fp16 codes times x split into two pieces, fp32 sums);
- *    every other call runs the CUDA-core kernel.  Within one kernel row b
+ *    deterministic.  Q4_K calls with batch >= 2 and Q8_0 calls with
+ *    batch >= 3 whose cols are a multiple of 512 (Q4_K) or 256 (Q8_0), with
+ *    W and x 16-byte aligned, run on the tensor cores (exact bf16 / fp16
+ *    codes times x split into two pieces, fp32 sums); every other call runs
+ *    the CUDA-core matvec kernel, or, when x is not 16-byte aligned or the
+ *    width cannot be tiled, a plain-load kernel.  Within one kernel row b
  *    of a batch call equals, bit for bit, the same x row in any other
- *    batch width; across the two kernels results differ only by rounding
- *    (both within the bound).  The grouped MoE expert FFN uses the tensor
+ *    batch width; across kernels results differ only by rounding (all
+ *    within the bound).  The grouped MoE expert FFN uses the tensor
  *    cores for Q4_K / Q8_0 when ntok >= 2.
  *  - Pointers are device pointers unless stated; the caller owns all memory.
  *  - stream may be NULL (the legacy default stream).
