@@ -69,7 +69,7 @@ typedef enum {
     LQ_EWORKSPACE = 4,  /* workspace smaller than lq_moe_workspace_bytes         */
     LQ_ECUDA = 5,       /* a CUDA launch or query failed (see lq_last_error)     */
     LQ_ETIMEOUT = 6,    /* a kernel's bounded wait ran out (lq_device_status)    */
-    LQ_EUNSUPPORTED = 7 /* a combination this build does not implement           */
+    LQ_EUNSUPPORTED = 7 /* a combination the library does not implement          */
 } lq_status;
 
 /* Format facts.  Q4_K: 144 bytes / 256 weights; Q6_K: 210 / 256; Q8_0: 34 / 32.
