@@ -41,6 +41,43 @@ def test_library_exports_every_declared_symbol(lq):
     assert sorted(lq.EXPORTS) == declared_functions()
 
 
+def _declared_params():
+    """(name, [C parameter types]) of every function lq.h declares."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, args in re.findall(r"\b(lq_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src):
+        args = args.strip()
+        out[name] = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
+    return out
+
+
+def _ctype_class(c_param):
+    """the ctypes type a C parameter must be passed as"""
+    t = re.sub(r"\b[a-z_0-9]+$", "", c_param).strip()       # drop the parameter name
+    if "*" in t or t == "lq_stream_t":
+        return "pointer"
+    return {"int": C.c_int, "int64_t": C.c_int64, "uint64_t": C.c_uint64, "size_t": C.c_size_t,
+            "float": C.c_float}[t.replace("const ", "")]
+
+
+def test_binding_signatures_match_header(lq):
+    """every ctypes signature of the binding passes each argument as the type
+    lq.h declares (a count or width mismatch would pass garbage silently)"""
+    L = lq.lib()
+    decl = _declared_params()
+    assert sorted(decl) == declared_functions()
+    for name, params in decl.items():
+        argtypes = getattr(L, name).argtypes or []
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+        for i, (c_param, ct) in enumerate(zip(params, argtypes)):
+            want = _ctype_class(c_param)
+            if want == "pointer":
+                assert ct is C.c_void_p or ct is C.c_char_p or hasattr(ct, "contents") or \
+                    getattr(ct, "_type_", None) is not None and issubclass(ct, C._Pointer), (name, i, c_param, ct)
+            else:
+                assert ct is want, (name, i, c_param, ct)
+
+
 def test_format_facts(lq):
     assert lq.lq_block_bytes(1) == 144 and lq.lq_block_elems(1) == 256
     assert lq.lq_block_bytes(2) == 210 and lq.lq_block_elems(2) == 256
