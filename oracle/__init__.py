@@ -60,6 +60,10 @@ def lib():
         L.orc_silu.restype = d
         L.orc_softcap.argtypes = [vp, i64, d, vp]
         L.orc_softcap.restype = None
+        L.orc_moe_weights_raw.argtypes = [vp, i32, i32, vp, i32, vp]
+        L.orc_moe_weights_raw.restype = None
+        L.orc_moe_shared.argtypes = [i32, vp, vp, vp, i32, i64, i64, vp, i32, vp, vp, vp, i32]
+        L.orc_moe_shared.restype = None
         L.orc_dequant.argtypes = [i32, vp, i64, i64, vp, i32]
         L.orc_matvec.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, i32]
         L.orc_matvec_rows.argtypes = [i32, vp, i64, vp, i64, vp, i32, vp, vp, i32]
@@ -169,14 +173,35 @@ def moe_route(R, X, topk: int):
     return idx, w, logits, labs
 
 
-def moe_weights(logits, idx):
-    """routing weights of a given selection idx [ntok][topk] from fp64 logits [ntok][E]."""
+def moe_weights(logits, idx, norm: bool = True):
+    """routing weights of a given selection idx [ntok][topk] from fp64 logits
+    [ntok][E]: the selected softmax probabilities, renormalised by their sum
+    (norm) or as they are (norm_topk_prob = false)."""
     logits = np.ascontiguousarray(logits, dtype=np.float64)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     ntok, E = logits.shape
     w = np.empty(idx.shape, dtype=np.float64)
-    lib().orc_moe_weights(_p(logits), E, ntok, _p(idx), idx.shape[1], _p(w))
+    f = lib().orc_moe_weights if norm else lib().orc_moe_weights_raw
+    f(_p(logits), E, ntok, _p(idx), idx.shape[1], _p(w))
     return w
+
+
+def moe_shared(fmt: int, Wg, Wu, Wd, hidden: int, inter_s: int, X, gate=None, nthreads: int = 1):
+    """shared-expert branch: gate_t * sum_s Wd_s (silu(Wg_s x_t) * (Wu_s x_t)),
+    gate_t = sigmoid(g . x_t) (or 1 without g).  Returns (S [ntok][hidden],
+    gate_t [ntok]), fp64."""
+    Wg, Wu, Wd = [_u8(a) for a in Wg], [_u8(a) for a in Wu], [_u8(a) for a in Wd]
+    n = len(Wg)
+    P = C.c_void_p * n
+    pg, pu, pd = P(*[_p(a) for a in Wg]), P(*[_p(a) for a in Wu]), P(*[_p(a) for a in Wd])
+    X = _f32(X)
+    ntok = X.shape[0]
+    g = None if gate is None else _f32(gate)
+    S = np.empty((ntok, hidden))
+    gs = np.empty(ntok)
+    lib().orc_moe_shared(fmt, C.cast(pg, C.c_void_p), C.cast(pu, C.c_void_p), C.cast(pd, C.c_void_p), n,
+                         hidden, inter_s, _p(X), ntok, None if g is None else _p(g), _p(S), _p(gs), nthreads)
+    return S, gs
 
 
 def moe_ffn(fmt: int, W1, W3, W2, hidden: int, inter: int, X, idx, w, nthreads: int = 1):

@@ -17,6 +17,12 @@
 //    the routing rule: softmax over all experts, top-k with the lower index
 //    winning ties, renormalise by the sum of the selected probabilities, then
 //    the weighted sum of per-expert SwiGLU FFNs.
+//  * dotLLM PR #320, Qwen-MoE commit: norm_topk_prob = false keeps the
+//    selected experts' softmax probabilities as weights (no renormalisation),
+//    and an optional shared-expert SwiGLU branch is added to the routed sum,
+//    scaled by sigmoid(x . shared_expert_gate) when that gate exists; the
+//    follow-up commit allows N shared experts, summed.  Read here: the gate
+//    scales the sum of the shared experts (one expert: the same either way).
 //  * dotLLM PR #255 (attention soft-cap: a score s becomes softCap *
 //    tanh(s / softCap)) and PR #274 (FinalLogitSoftcap: the same map applied
 //    to the logits after the lm_head GEMM): the final-logit soft-cap.
@@ -306,6 +312,57 @@ void orc_moe_weights(const double* logits, int E, int ntok, const int32_t* idx, 
         for (int k = 0; k < topk; ++k) sel += std::exp(l[idx[t * topk + k]] - mx) / z;
         for (int k = 0; k < topk; ++k)
             w[t * topk + k] = (std::exp(l[idx[t * topk + k]] - mx) / z) / sel;
+    }
+}
+
+// Routing weights without renormalisation (norm_topk_prob = false):
+// w_k = p_{idx_k}, p = softmax(l) over all E experts.
+void orc_moe_weights_raw(const double* logits, int E, int ntok, const int32_t* idx, int topk,
+                         double* w) {
+    for (int t = 0; t < ntok; ++t) {
+        const double* l = logits + (int64_t)t * E;
+        double mx = l[0];
+        for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += std::exp(l[e] - mx);
+        for (int k = 0; k < topk; ++k) w[t * topk + k] = std::exp(l[idx[t * topk + k]] - mx) / z;
+    }
+}
+
+// Shared-expert branch of an MoE layer: for token t,
+//   S_t = gate_t * sum_s Wd_s (silu(Wg_s x_t) * (Wu_s x_t)),
+//   gate_t = sigmoid(sum_j g_j x_tj) if g is given, else 1.
+// nshared experts, each inter_s x hidden (Wg, Wu) and hidden x inter_s (Wd),
+// all fmt.  S: [ntok][hidden], gscale: [ntok] (gate_t), fp64.
+void orc_moe_shared(int fmt, const uint8_t* const* Wg, const uint8_t* const* Wu,
+                    const uint8_t* const* Wd, int nshared, int64_t hidden, int64_t inter_s,
+                    const float* X, int ntok, const float* g, double* S, double* gscale,
+                    int nthreads) {
+    std::vector<double> h(inter_s), gg(inter_s), uu(inter_s);
+    std::vector<float> wrow(inter_s);
+    const int64_t rb = inter_s / block_elems(fmt) * block_bytes(fmt);
+    for (int t = 0; t < ntok; ++t) {
+        const float* x = X + (int64_t)t * hidden;
+        double gate = 1.0;
+        if (g) {
+            double z = 0.0;
+            for (int64_t j = 0; j < hidden; ++j) z += (double)g[j] * (double)x[j];
+            gate = 1.0 / (1.0 + std::exp(-z));
+        }
+        gscale[t] = gate;
+        double* St = S + (int64_t)t * hidden;
+        for (int64_t o = 0; o < hidden; ++o) St[o] = 0.0;
+        for (int sh = 0; sh < nshared; ++sh) {
+            orc_ffn_gate_up(fmt, Wg[sh], Wu[sh], inter_s, hidden, x, 1, 2, h.data(), gg.data(), uu.data(),
+                            nullptr, nullptr, nthreads);
+            for (int64_t o = 0; o < hidden; ++o) {
+                dequant_row(fmt, Wd[sh] + o * rb, inter_s, wrow.data());
+                double acc = 0.0;
+                for (int64_t j = 0; j < inter_s; ++j) acc += (double)wrow[j] * h[j];
+                St[o] += acc;
+            }
+        }
+        for (int64_t o = 0; o < hidden; ++o) St[o] *= gate;
     }
 }
 

@@ -335,6 +335,83 @@ def test_moe_scalar_reference(orc):
             assert np.allclose(out["ye"][t * 2 + k], ye, rtol=1e-13, atol=1e-13)
 
 
+# ---------------------------------------------------------------- MoE variants
+# dotLLM PR #320 Qwen-MoE commit (norm_topk_prob = false, shared expert with
+# an optional sigmoid gate) and its N-shared-experts follow-up.
+
+def test_moe_weights_raw(orc):
+    """norm_topk_prob = false: the selected softmax probabilities themselves."""
+    rng = np.random.default_rng(40)
+    lg = rng.normal(0, 2, (6, 8))
+    idx = np.argsort(-lg, axis=1, kind="stable")[:, :2].astype(np.int32)
+    raw = orc.moe_weights(lg, idx, norm=False)
+    p = torch.softmax(torch.tensor(lg), dim=-1).numpy()
+    assert np.allclose(raw, np.take_along_axis(p, idx, 1), rtol=1e-14, atol=0)
+    # renormalising the raw weights gives the (pinned) renormalised rule
+    assert np.allclose(orc.moe_weights(lg, idx), raw / raw.sum(1, keepdims=True), rtol=1e-14, atol=0)
+    # uniform logits: 1/E each; two experts, top-1: the logistic of the logit gap
+    assert np.allclose(orc.moe_weights(np.zeros((1, 8)), np.array([[3, 5]], np.int32), norm=False), 1 / 8,
+                       rtol=1e-15, atol=0)
+    from scipy.special import expit
+    two = np.array([[1.7, -0.4]])
+    assert abs(orc.moe_weights(two, np.array([[0]], np.int32), norm=False)[0, 0] - expit(2.1)) < 1e-15
+
+
+def _shared_mats(seed, hidden=256, inter=512):
+    g_ = synth.rng(seed)
+    return synth.q4k(g_, inter, hidden), synth.q4k(g_, inter, hidden), synth.q4k(g_, hidden, inter)
+
+
+def test_moe_shared_single_expert_is_dense_swiglu(orc):
+    hidden, inter = 256, 512
+    Wg, Wu, Wd = _shared_mats(41)
+    X = synth.activations(synth.rng(42), 3, hidden)
+    S, gs = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X)
+    assert (gs == 1.0).all()
+    assert np.allclose(S, _dense_swiglu(orc, Wg, Wu, Wd, hidden, inter, X), rtol=1e-13, atol=1e-13)
+
+
+def test_moe_shared_experts_sum(orc):
+    """N shared experts are summed: two distinct ones give the sum of each,
+    two identical ones twice one (the follow-up commit's unit tests)."""
+    hidden, inter = 256, 512
+    a, b = _shared_mats(43), _shared_mats(44)
+    X = synth.activations(synth.rng(45), 2, hidden)
+    one = lambda m: orc.moe_shared(Q4_K, [m[0]], [m[1]], [m[2]], hidden, inter, X)[0]
+    both, _ = orc.moe_shared(Q4_K, [a[0], b[0]], [a[1], b[1]], [a[2], b[2]], hidden, inter, X)
+    assert np.allclose(both, one(a) + one(b), rtol=1e-13, atol=1e-13)
+    twice, _ = orc.moe_shared(Q4_K, [a[0], a[0]], [a[1], a[1]], [a[2], a[2]], hidden, inter, X)
+    assert np.array_equal(twice, 2 * one(a))
+
+
+def test_moe_shared_gate(orc):
+    """sigmoid(g . x) scales the branch: g = 0 halves it exactly, large
+    |g . x| saturates to 0 or 1, and random g agrees with the library logistic."""
+    from scipy.special import expit
+    hidden, inter = 256, 512
+    Wg, Wu, Wd = _shared_mats(46)
+    X = synth.activations(synth.rng(47), 2, hidden)
+    ungated, _ = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X)
+    half, gs = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X, gate=np.zeros(hidden, np.float32))
+    assert (gs == 0.5).all() and np.array_equal(half, 0.5 * ungated)
+    big = (50.0 * np.sign(X[0])).astype(np.float32)
+    hi, gs = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X[:1], gate=big)
+    lo, gs2 = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X[:1], gate=-big)
+    assert gs[0] == 1.0 and np.array_equal(hi, ungated[:1]) and gs2[0] < 1e-300 and np.abs(lo).max() < 1e-290
+    g = synth.activations(synth.rng(48), 1, hidden)[0] * np.float32(0.05)
+    _, gs = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd], hidden, inter, X, gate=g)
+    assert np.allclose(gs, expit(X.astype(np.float64) @ g.astype(np.float64)), rtol=1e-14, atol=0)
+
+
+def test_moe_shared_zero_down_adds_nothing(orc):
+    hidden, inter = 256, 512
+    Wg, Wu, _ = _shared_mats(49)
+    Wd0 = np.zeros((hidden, inter // 256 * 144), np.uint8)     # d = dmin = 0: every weight 0
+    X = synth.activations(synth.rng(50), 2, hidden)
+    S, _ = orc.moe_shared(Q4_K, [Wg], [Wu], [Wd0], hidden, inter, X)
+    assert (S == 0).all()
+
+
 def test_abs_matvec(orc):
     W, _ = _mat(Q6_K, 5, 512, seed=20)
     D = np.abs(orc.dequant(Q6_K, W, 5, 512).astype(np.float64))
