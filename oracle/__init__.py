@@ -60,6 +60,8 @@ def lib():
         L.orc_silu.restype = d
         L.orc_softcap.argtypes = [vp, i64, d, vp]
         L.orc_softcap.restype = None
+        L.orc_rmsnorm.argtypes = [vp, i32, i64, vp, d, vp]
+        L.orc_rmsnorm.restype = None
         L.orc_moe_weights_raw.argtypes = [vp, i32, i32, vp, i32, vp]
         L.orc_moe_weights_raw.restype = None
         L.orc_moe_shared.argtypes = [i32, vp, vp, vp, i32, i64, i64, vp, i32, vp, vp, vp, i32]
@@ -109,6 +111,16 @@ def gelu_tanh(g: float) -> float:
 
 def silu(g: float) -> float:
     return lib().orc_silu(g)
+
+
+def rmsnorm(X, w, eps: float) -> np.ndarray:
+    """RMS-norm of each row of X [ntok][n] with weight w [n]: x * w / sqrt(mean(x^2) + eps), fp64."""
+    X = _f32(X)
+    X2 = X.reshape(-1, X.shape[-1])
+    w = _f32(w)
+    out = np.empty(X2.shape, dtype=np.float64)
+    lib().orc_rmsnorm(_p(X2), X2.shape[0], X2.shape[1], _p(w), float(eps), _p(out))
+    return out.reshape(X.shape)
 
 
 def softcap(y, cap: float) -> np.ndarray:

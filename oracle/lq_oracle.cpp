@@ -23,6 +23,10 @@
 //    scaled by sigmoid(x . shared_expert_gate) when that gate exists; the
 //    follow-up commit allows N shared experts, summed.  Read here: the gate
 //    scales the sum of the shared experts (one expert: the same either way).
+//  * larql "Architecture -> Metal shader map", Gemma 3 table, row "Input
+//    RMS-norm": a standard RMS-norm whose weight already carries the offset
+//    (HF convention), the step the opt-in NORMED QKV variant fuses in front
+//    of the projection: x_i * w_i / sqrt(mean_j x_j^2 + eps).
 //  * dotLLM PR #255 (attention soft-cap: a score s becomes softCap *
 //    tanh(s / softCap)) and PR #274 (FinalLogitSoftcap: the same map applied
 //    to the logits after the lm_head GEMM): the final-logit soft-cap.
@@ -204,6 +208,17 @@ int orc_block_elems(int fmt) { return block_elems(fmt); }
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }
 double orc_gelu_tanh(double g) { return gelu_tanh(g); }
 double orc_silu(double g) { return silu(g); }
+
+// RMS-norm of ntok rows of n values: out = x * w / sqrt(mean(x^2) + eps).
+void orc_rmsnorm(const float* X, int ntok, int64_t n, const float* w, double eps, double* out) {
+    for (int t = 0; t < ntok; ++t) {
+        const float* x = X + (int64_t)t * n;
+        double ss = 0.0;
+        for (int64_t j = 0; j < n; ++j) ss += (double)x[j] * (double)x[j];
+        const double r = 1.0 / std::sqrt(ss / (double)n + eps);
+        for (int64_t j = 0; j < n; ++j) out[(int64_t)t * n + j] = (double)x[j] * r * (double)w[j];
+    }
+}
 
 // Final-logit soft-cap of n values: out[i] = cap * tanh(y[i] / cap).
 void orc_softcap(const double* y, int64_t n, double cap, double* out) {

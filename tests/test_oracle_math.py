@@ -335,6 +335,29 @@ def test_moe_scalar_reference(orc):
             assert np.allclose(out["ye"][t * 2 + k], ye, rtol=1e-13, atol=1e-13)
 
 
+# ---------------------------------------------------------------- input RMS-norm
+
+def test_rmsnorm_pins(orc):
+    """x * w / sqrt(mean(x^2) + eps) against torch's rms_norm, a constant
+    row's closed form, scale invariance at eps = 0, unit mean square at unit
+    weight, and linearity in the weight."""
+    n = 2560
+    X = synth.activations(synth.rng(60), 3, n) * np.float32(3.0)
+    w = (1.0 + 0.1 * synth.activations(synth.rng(61), 1, n)[0]).astype(np.float32)
+    for eps in (1e-6, 1e-5):
+        got = orc.rmsnorm(X, w, eps)
+        ref = torch.nn.functional.rms_norm(torch.tensor(X, dtype=torch.float64), (n,),
+                                           torch.tensor(w, dtype=torch.float64), eps).numpy()
+        assert np.allclose(got, ref, rtol=1e-14, atol=1e-15)
+    c = np.full((1, n), -2.5, np.float32)
+    ones = np.ones(n, np.float32)
+    assert np.allclose(orc.rmsnorm(c, ones, 1e-5), -2.5 / math.sqrt(6.25 + 1e-5), rtol=1e-15, atol=0)
+    u = orc.rmsnorm(X, ones, 0.0)
+    assert np.allclose((u ** 2).mean(axis=1), 1.0, rtol=1e-14)
+    assert np.allclose(orc.rmsnorm(X * np.float32(8.0), ones, 0.0), u, rtol=1e-14, atol=0)   # 8x is exact in fp32
+    assert np.allclose(orc.rmsnorm(X, w * np.float32(2.0), 1e-6), 2 * orc.rmsnorm(X, w, 1e-6), rtol=1e-15, atol=0)
+
+
 # ---------------------------------------------------------------- MoE variants
 # dotLLM PR #320 Qwen-MoE commit (norm_topk_prob = false, shared expert with
 # an optional sigmoid gate) and its N-shared-experts follow-up.
