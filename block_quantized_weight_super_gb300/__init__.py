@@ -22,7 +22,7 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
            "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
-           "lq_ffn", "lq_ffn_one_launch", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_static",
+           "lq_ffn", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_static",
            "lq_device_status",
            "lq_set_wait_timeout_ns", "lq_probe_timeout"]
 
@@ -59,7 +59,6 @@ def lib():
             "lq_pack_gate_up": ([i32, vp, vp, i64, i64, vp, vp], i32),
             "lq_ffn_gate_up_act": ([i32, vp, i64, i64, vp, vp, i32, i32, vp], i32),
             "lq_ffn": ([i32, vp, i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
-            "lq_ffn_one_launch": ([i32, vp, i32, vp, i64, i64, vp, vp, vp, i32, vp, vp], i32),
             "lq_moe_workspace_bytes": ([i32, i32, i32, i64, i64], sz),
             "lq_moe_ffn": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, sz, vp], i32),
             "lq_moe_ffn_static": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp], i32),
@@ -149,11 +148,6 @@ def lq_ffn_gate_up_act(fmt, Wgu, inter, cols, x, h, batch, act, stream=None):
 def lq_ffn(fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, batch, act, stream=None):
     return _check(lib().lq_ffn(fmt_gu, _ptr(Wgu), fmt_down, _ptr(Wd), inter, hidden, _ptr(x), _ptr(h),
                                _ptr(y), batch, act, _stream(stream)))
-
-
-def lq_ffn_one_launch(fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, act, sync=None, stream=None):
-    return _check(lib().lq_ffn_one_launch(fmt_gu, _ptr(Wgu), fmt_down, _ptr(Wd), inter, hidden, _ptr(x),
-                                          _ptr(h), _ptr(y), act, _ptr(sync), _stream(stream)))
 
 
 def lq_moe_workspace_bytes(n_experts, topk, ntok, hidden, inter) -> int:

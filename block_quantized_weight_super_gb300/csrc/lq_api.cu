@@ -13,6 +13,7 @@
 
 #include "../../include/lq.h"
 #include "lq_codec.cuh"
+#include "lq_gv.cuh"
 #include "lq_internal.h"
 
 namespace lq {
@@ -21,8 +22,6 @@ namespace lq {
 // address is passed to kernels (no relocatable device code needed).
 static __device__ unsigned g_status_word = 0;
 
-// Grid-barrier word of one-launch FFN calls that pass no word of their own.
-static __device__ unsigned g_ffn_bar_word = 0;
 
 namespace {
 
@@ -59,7 +58,6 @@ struct DevInfo {
     bool init = false;
     int sms = 0;
     unsigned* status = nullptr;
-    unsigned* ffn_bar = nullptr;
     int qmm_res[2][3] = {};       // resident tensor-core CTAs / clusters of 2 / of 4 (Q4_K, Q8_0)
 };
 std::mutex g_mu;
@@ -79,15 +77,12 @@ int dev_info(DevInfo** out) {
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
         d.status = static_cast<unsigned*>(p);
-        e = cudaGetSymbolAddress(&p, g_ffn_bar_word);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(ffn barrier)");
-        d.ffn_bar = static_cast<unsigned*>(p);
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
-        if (e == cudaSuccess) e = qmv_ffn_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
+        if (e == cudaSuccess) e = gv_set_smem(227 * 1024);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         for (int f = 0; f < 2; ++f) {
             const int fmt = f ? FMT_Q8_0 : FMT_Q4_K;
@@ -170,12 +165,20 @@ bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPl
     return p.smem <= 227 * 1024;
 }
 
-// Run the segments (all sharing cols and the batch width B): the quantized
-// matvec kernel when it can take the shape, else the plain-load kernel.
+constexpr int GV_NOT_ELIGIBLE = -1;
+int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st);
+
+// Run the segments (all sharing cols and the batch width B): at batch 1 the
+// tensor-core kernel when it can take them, else the quantized matvec
+// kernel when it can take the shape, else the plain-load kernel.
 int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
+    if (B == 1) {
+        rc = run_gv(segs, cols, st);
+        if (rc != GV_NOT_ELIGIBLE) return rc;
+    }
     // formats in order of first appearance (at most two per launch)
     std::vector<int> fmts;
     bool pairs = false;
@@ -228,13 +231,12 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         }
         P.nseg = n;
         P.ntiles = t;
-        QGeo& G = P.geo[0];
+        QGeo& G = P.geo;
         G.cols = (int32_t)cols;
         G.U = (int32_t)(cols / 64);
         G.UP = qmv_red_stride(G.U);
         G.RT = pl.RT;
         G.ipt = pl.ipt;
-        P.geo[1] = G;
         for (int i = 0; i < n; ++i)
             if (P.seg[i].bcnt || P.seg[i].boff) P.dev_counts = 1;
         P.R = pl.R;
@@ -259,107 +261,6 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
         if (e != cudaSuccess) return cuda_fail(e, "qmv launch");
     }
     return LQ_OK;
-}
-
-// ---------------------------------------------------------------- one-launch FFN
-// Geometry of the batch-1 FFN as one launch: gate/up pairs of format f0 over
-// `hidden` columns (phase 0), down of format f1 over `inter` columns (phase
-// 1).  Both phases run on the same consumer warps, so NC*32 threads must
-// share the items of a tile of either phase evenly: a tile of RT = R*NCT /
-// gcd(NCT, U) rows has exactly NCT*U/gcd(NCT, U) items.  False if no warp
-// count gives both phases tiles of at most 32 KB (then two launches run).
-struct FfnPlan {
-    QGeo geo[2];
-    int NC = 0, nstages = 0, stage_bytes = 0, red_tile = 0, T0 = 0, T1 = 0;
-    size_t smem = 0;
-};
-
-int64_t gcd64(int64_t a, int64_t b) {
-    while (b) {
-        const int64_t t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
-
-bool plan_ffn(int f0, int f1, int64_t inter, int64_t hidden, FfnPlan& p) {
-    if (!qmv_ffn_available(f0, f1)) return false;
-    if (hidden <= 0 || inter <= 0 || hidden % 64 || inter % 64) return false;
-    const int64_t U0 = hidden / 64, U1 = inter / 64;
-    if (U0 > 512 || U1 > 512 || inter > (1 << 30)) return false;
-    const int R0 = qmv_rows_per_item(1, fmt_mask({f0})), R1 = qmv_rows_per_item(1, fmt_mask({f1}));
-    const int ncmax = std::min(qmv_max_consumer_warps(R0), qmv_max_consumer_warps(R1));
-    const int64_t rb0 = rowbytes(f0, hidden), rb1 = rowbytes(f1, inter);
-    for (int NC = ncmax; NC >= 4; --NC) {
-        const int64_t NCT = 32 * NC;
-        int64_t RT0 = R0 * NCT / gcd64(NCT, U0);
-        if (RT0 & 1) RT0 *= 2;                    // whole gate/up pairs
-        const int64_t RT1 = R1 * NCT / gcd64(NCT, U1);
-        if (RT0 * rb0 > 32 * 1024 || RT1 * rb1 > 32 * 1024) continue;
-        if ((RT0 * rb0) % 16 || (RT1 * rb1) % 16) continue;   // tiles by bulk copy
-        p.NC = NC;
-        p.geo[0] = QGeo{(int32_t)hidden, (int32_t)U0, qmv_red_stride((int)U0), (int32_t)RT0,
-                        (int32_t)(RT0 * U0 / (R0 * NCT))};
-        p.geo[1] = QGeo{(int32_t)inter, (int32_t)U1, qmv_red_stride((int)U1), (int32_t)RT1,
-                        (int32_t)(RT1 * U1 / (R1 * NCT))};
-        p.stage_bytes = (int)((std::max(RT0 * rb0, RT1 * rb1) + 15) / 16 * 16 + 16);
-        p.red_tile = std::max(p.geo[0].RT * p.geo[0].UP, p.geo[1].RT * p.geo[1].UP);
-        p.T0 = (int)((inter + RT0 / 2 - 1) / (RT0 / 2));
-        p.T1 = (int)((hidden + RT1 - 1) / RT1);
-        for (int S = 4; S >= 2; --S) {
-            p.nstages = S;
-            p.smem = qmv_ffn_smem((int)std::max(U0, U1), p.red_tile, S, p.stage_bytes).total;
-            if (p.smem <= 110 * 1024) return true;
-        }
-        return false;
-    }
-    return false;
-}
-
-Seg plain_seg(int fmt, const void* W, int64_t rows, const float* x, float* y, int64_t ld_y, int b0, int nb);
-
-int run_ffn(const FfnPlan& pl, int f0, const void* Wgu, int f1, const void* Wd, int64_t inter,
-            int64_t hidden, const float* x, float* h, float* y, int act, unsigned* bar, cudaStream_t st) {
-    DevInfo* dev = nullptr;
-    int rc = dev_info(&dev);
-    if (rc) return rc;
-    const int nt = (pl.NC + 1) * 32;
-    int per_sm = 0;
-    cudaError_t e = qmv_ffn_occupancy(f0, f1, nt, pl.smem, &per_sm);
-    if (e != cudaSuccess) return cuda_fail(e, "occupancy");
-    if (per_sm < 1) return fail(LQ_ECUDA, "one-launch FFN kernel does not fit on an SM");
-    QmvParams P;
-    memset(&P, 0, sizeof P);
-    Seg s0 = plain_seg(f0, Wgu, inter, x, h, inter, 0, 1);
-    s0.mode = MODE_PAIR_INTERLEAVED;
-    s0.act = act;
-    s0.tile0 = 0;
-    s0.ntiles = pl.T0;
-    Seg s1 = plain_seg(f1, Wd, hidden, h, y, hidden, 0, 1);
-    s1.tile0 = pl.T0;
-    s1.ntiles = pl.T1;
-    P.seg[0] = s0;
-    P.seg[1] = s1;
-    P.nseg = 2;
-    P.ntiles = pl.T0 + pl.T1;
-    P.geo[0] = pl.geo[0];
-    P.geo[1] = pl.geo[1];
-    P.R = qmv_rows_per_item(1, fmt_mask({f0}));
-    P.nstages = pl.nstages;
-    P.stage_bytes = pl.stage_bytes;
-    P.red_tile = pl.red_tile;
-    P.fmt0 = f0;
-    P.fmt1 = f1;
-    P.tile_split = pl.T0;
-    P.timeout_ns = g_timeout_ns.load();
-    P.status = dev->status;
-    P.gbar = bar ? bar : dev->ffn_bar;
-    // every CTA must be resident at once (grid barrier): at most the occupancy
-    const int grid = std::min(dev->sms * per_sm, std::max(pl.T0, pl.T1));
-    P.cta_split = grid;
-    e = qmv_ffn_launch(P, grid, nt, pl.smem, st);
-    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "one-launch FFN launch");
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -422,6 +323,106 @@ int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbyte
     g_maps.emplace(key, m);
     *out = m;
     return LQ_OK;
+}
+
+
+// ---------------------------------------------------------------- batch-1 tensor-core path
+// Segments of one x row (no device counts or gathers), Q4_K alone or Q4_K
+// with Q6_K, whose columns are a multiple of 256, with rows a multiple of 4
+// bytes, weights 4-byte aligned and a 16-row tile of at most
+// GV_MAX_TILE_BYTES.  Returns GV_NOT_ELIGIBLE otherwise: Q6_K alone and Q8_0
+// run faster on the CUDA-core kernel at batch 1 (measured per launch on
+// GB300: the down projection and the Q8_0 FFN).
+//
+// Plan: one CTA per SM; the row blocks are split into contiguous ranges of
+// nearly equal weight bytes, one per CTA; tiles land in a ring of up to
+// GV_MAX_INFLIGHT slots, as many as shared memory holds.
+int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
+    if (segs.empty() || segs.size() > (size_t)GV_MAX_SEG || cols % 256 != 0 || cols > (1 << 20))
+        return GV_NOT_ELIGIBLE;
+    int mask = 0;
+    for (auto& s : segs) {
+        if (s.nbatch != 1 || s.b0 != 0 || s.xmap || s.boff || s.bcnt || s.x != segs[0].x) return GV_NOT_ELIGIBLE;
+        if (s.mode != MODE_PLAIN && s.mode != MODE_PAIR_INTERLEAVED) return GV_NOT_ELIGIBLE;
+        if (s.fmt != FMT_Q4_K && s.fmt != FMT_Q6_K) return GV_NOT_ELIGIBLE;
+        mask |= s.fmt == FMT_Q4_K ? 1 : 2;
+    }
+    if (!(mask & 1)) return GV_NOT_ELIGIBLE;
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    const int nsb = (int)(cols / 256);
+    GvParams P;
+    memset(&P, 0, sizeof P);
+    std::vector<double> rbcost;            // weight bytes of a row block, in Q4_K super-blocks
+    uint32_t slot = 0;
+    int n = 0;
+    for (auto& s : segs) {
+        if (s.nout <= 0) continue;
+        const bool pair = s.mode != MODE_PLAIN;
+        const int64_t rb = rowbytes(s.fmt, cols);
+        if (rb % 4 != 0 || !al(s.w, 4) || GV_ROWS * rb > GV_MAX_TILE_BYTES) return GV_NOT_ELIGIBLE;
+        GvSeg& G = P.seg[n];
+        G.w = s.w;
+        G.y = s.y;
+        G.rowbytes = rb;
+        G.fmt = s.fmt;
+        G.mode = s.mode;
+        G.act = s.act;
+        G.cap = s.cap;
+        G.nout = s.nout;
+        G.nrows = (pair ? 2 : 1) * s.nout;
+        G.nrb = pair ? (s.nout + 7) / 8 : (s.nout + GV_ROWS - 1) / GV_ROWS;
+        G.rb0 = (int32_t)rbcost.size();
+        uint32_t bytes;
+        if (al(s.w, 16) && (G.nrows * rb) % 16 == 0) {
+            G.copy = GV_COPY_TILE;
+            bytes = (uint32_t)(GV_ROWS * rb);
+        } else {
+            G.copy = GV_COPY_CPA;
+            G.pitch = gv_row_pitch(s.fmt, nsb);
+            bytes = (uint32_t)(GV_ROWS * G.pitch);
+        }
+        slot = std::max(slot, (bytes + 127u) & ~127u);
+        const double c = gv_span(s.fmt) / 144.0;
+        for (int i = 0; i < G.nrb; ++i) rbcost.push_back(c);
+        ++n;
+    }
+    if (n == 0) return LQ_OK;
+    const int nrb = (int)rbcost.size();
+    std::vector<double> pre(nrb + 1, 0.0);
+    for (int i = 0; i < nrb; ++i) pre[i + 1] = pre[i] + rbcost[i];
+    const int ncta = std::min(std::min(dev->sms, GV_MAX_CTA), nrb);
+    std::vector<int> b(ncta + 1, 0);
+    b[ncta] = nrb;
+    for (int k = 1; k < ncta; ++k) {
+        const double target = pre[nrb] * k / ncta;
+        int i = (int)(std::lower_bound(pre.begin(), pre.end(), target) - pre.begin());
+        if (i > 0 && target - pre[i - 1] < pre[i] - target) --i;
+        b[k] = std::max(b[k - 1] + 1, std::min(i, nrb - (ncta - k)));
+    }
+    int mxt = 0;
+    for (int k = 0; k < ncta; ++k) mxt = std::max(mxt, b[k + 1] - b[k]);
+    if (mxt > GV_MAX_TILES) return GV_NOT_ELIGIBLE;
+    // a ring of up to GV_MAX_INFLIGHT tiles: enough bytes in flight per SM to
+    // keep HBM busy, few enough that they land one after another and the
+    // warps compute each as it arrives
+    int ns = std::min(GV_MAX_INFLIGHT, std::max(2, mxt));
+    while (ns >= 2 && gv_layout(mask, ns, slot, mxt, nsb).total > GV_SMEM_MAX) --ns;
+    if (ns < 2) return GV_NOT_ELIGIBLE;
+    P.nseg = n;
+    P.x = segs[0].x;
+    P.timeout_ns = g_timeout_ns.load();
+    P.status = dev->status;
+    P.nsb = nsb;
+    P.nslots = ns;
+    P.slot_bytes = slot;
+    P.maxtiles = mxt;
+    P.x16 = al(segs[0].x, 16) ? 1 : 0;
+    for (int k = 0; k <= ncta; ++k) P.cta_rb[k] = b[k];
+    const size_t smem = gv_layout(mask, ns, slot, mxt, nsb).total;
+    cudaError_t e = gv_launch(mask, P, ncta, smem, st);
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "batch-1 tensor-core matvec launch");
 }
 
 // ---------------------------------------------------------------- tensor-core path
@@ -748,26 +749,6 @@ int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t in
     if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h")) || (rc = check_f32(y, "y"))) return rc;
     if ((rc = lq_ffn_gate_up_act(fmt_gu, Wgu, inter, hidden, x, h, batch, act, stream))) return rc;
     return lq_matvec(fmt_down, Wd, hidden, inter, h, y, batch, stream);
-}
-
-int lq_ffn_one_launch(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
-                      const float* x, float* h, float* y, int act, uint32_t* sync, lq_stream_t stream) {
-    g_err[0] = 0;
-    int rc;
-    if ((rc = check_mat(fmt_gu, Wgu, 2 * inter, hidden, "Wgu")) ||
-        (rc = check_mat(fmt_down, Wd, hidden, inter, "Wd")))
-        return rc;
-    if (inter == 0 || hidden == 0) return fail(LQ_ESHAPE, "inter %lld hidden %lld", (long long)inter, (long long)hidden);
-    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
-    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h")) || (rc = check_f32(y, "y"))) return rc;
-    if (sync && !al(sync, 4)) return fail(LQ_EALIGN, "sync not 4-byte aligned");
-    if (!al(x, 16) || !al(h, 16)) return fail(LQ_EALIGN, "one-launch FFN: x and h must be 16-byte aligned");
-    FfnPlan pl;
-    if (!plan_ffn(fmt_gu, fmt_down, inter, hidden, pl))
-        return fail(LQ_EUNSUPPORTED, "one-launch FFN: no tiling for formats %d/%d, inter %lld, hidden %lld", fmt_gu,
-                    fmt_down, (long long)inter, (long long)hidden);
-    return run_ffn(pl, fmt_gu, Wgu, fmt_down, Wd, inter, hidden, x, h, y, act, sync,
-                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }

@@ -1,0 +1,353 @@
+// lq_gv.cu -- the batch-1 tensor-core matvec (one x row): y = W.x for Q4_K
+// matrices and for launches that mix Q4_K and Q6_K matrices sharing x (the
+// Q4_K Q/K + Q6_K V projection), plain matrices or interleaved gate/up pairs
+// with the gated activation fused into the store (larql "Architecture ->
+// Metal shader map", Gemma 3 table: q4k_matvec, q4k_q6k_qkv_proj,
+// q4k_ffn_gate_up + geglu).  The work units and the operand encoding are in
+// lq_gv.cuh.
+//
+// GB300 structure.
+//  * One CTA of 16 warps per SM.  The row blocks (16 matrix rows, or 8
+//    gate/up pairs) of all the launch's matrices are split into contiguous
+//    ranges of nearly equal weight bytes, one per CTA; a tile is one row block
+//    with all of its columns.
+//  * A tile's 16 rows are consecutive, so one bulk copy brings it into a
+//    shared-memory slot (4-byte cp.async copies when the weights are not
+//    16-byte aligned), completion counted on the tile's own single-use
+//    mbarrier.  Every tile that has a slot is requested at kernel entry,
+//    before griddepcontrol.wait (weights never depend on the preceding
+//    kernel); a slot is requested again once every unit of its tile is done.
+//  * A tile's units (16 rows x 256 columns) are dealt in pairs of consecutive
+//    units to the warps, round robin, so all warps work on each tile as it
+//    lands and no tile's last units wait on one warp.
+//  * x (the preceding kernel's output) is read once per CTA after
+//    griddepcontrol.wait and turned into the MMA B images.
+//  * Sums: a lane adds its rows' parts of a pair's units in order, the lane
+//    quad adds in a fixed butterfly, and the warp that completes a tile adds
+//    the tile's pair sums in column order and stores them: every order is
+//    fixed by the shapes, so the result is deterministic and does not depend
+//    on which warp computed what.
+//  * Every mbarrier wait is bounded by %globaltimer; on expiry the warp
+//    records STATUS_TIMEOUT and stops computing, and before exit the CTA waits
+//    (bounded) for every copy it requested.
+#include "lq_internal.h"
+#include "lq_gv.cuh"
+
+namespace lq {
+namespace {
+
+__device__ __forceinline__ void bulk_s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The mbarrier also waits for this thread's earlier cp.async copies (the
+// pending count is raised now and lowered when they complete).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// acquire-release add on a shared counter: the partial sums a warp wrote
+// before its add are visible to the warp that sees the completed count
+__device__ __forceinline__ int atom_add_acqrel_cta(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t h2pack(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+__device__ __forceinline__ float gv_act(int act, float g) {
+    if (act == ACT_GEGLU_TANH) {
+        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
+        return g / (1.0f + expf(-2.0f * z));
+    }
+    return g / (1.0f + expf(-g));
+}
+
+// the segment of row block rb (segs: the shared copy of the table)
+__device__ __forceinline__ const GvSeg& gv_seg(const GvSeg* segs, int nseg, int rb) {
+    int i = 0;
+    while (i + 1 < nseg && rb >= segs[i + 1].rb0) ++i;
+    return segs[i];
+}
+
+// Store the complete sums of row block rb of segment G, MMA rows r and r + 8
+// (for gate/up pairs: gate and up of pair r).
+__device__ __forceinline__ void gv_store(const GvSeg& G, int rb, int r, float v0, float v1) {
+    const int lrb = rb - G.rb0;
+    if (G.mode == MODE_PLAIN) {
+        const int o = GV_ROWS * lrb + r;
+        if (o < G.nout) G.y[o] = seg_out(G.cap, v0);
+        if (o + 8 < G.nout) G.y[o + 8] = seg_out(G.cap, v1);
+    } else {
+        const int o = 8 * lrb + r;
+        if (o < G.nout) G.y[o] = gv_act(G.act, v0) * v1;
+    }
+}
+
+template <int MASK>
+__global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant__ GvParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NS = P.nslots, nsb = P.nsb;
+    const uint32_t SLOT = P.slot_bytes;
+    const GvLayout L = gv_layout(MASK, NS, SLOT, P.maxtiles, nsb);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [tile] its copy has landed
+    int* done = reinterpret_cast<int*>(smem + L.done);          // [tile] units done
+    int* reqd = done + P.maxtiles;                               // [tile] requested
+    // kernel parameters read with a dynamic index are slow (a chain of
+    // constant-cache misses): the segment table and this CTA's row-block
+    // range are copied to shared memory with one round of parallel loads
+    GvSeg* segs = reinterpret_cast<GvSeg*>(smem + L.prm);
+    int* crng = reinterpret_cast<int*>(smem + L.prm + GV_MAX_SEG * sizeof(GvSeg));
+    {
+        const int nw = P.nseg * (int)(sizeof(GvSeg) / 4);
+        if (tid < nw) reinterpret_cast<uint32_t*>(segs)[tid] = reinterpret_cast<const uint32_t*>(P.seg)[tid];
+        if (tid >= 64 && tid < 66) crng[tid - 64] = P.cta_rb[blockIdx.x + tid - 64];
+        for (int i = tid; i < P.maxtiles; i += GV_NW * 32) {
+            done[i] = 0;
+            reqd[i] = 0;
+            mbar_init(&full[i], 1);
+        }
+        fence_mbar_init();
+    }
+    const int nseg = P.nseg;
+    __syncthreads();
+    const int rbA = crng[0], ntile = crng[1] - crng[0];
+    const uint64_t policy = policy_evict_first();
+
+    // Request tile i (local row block) into slot i % NS.  Tile row r holds
+    // matrix row 16 lrb + r (for gate/up pairs the packed rows: gate, up,
+    // gate, ...).
+    auto issue_tile = [&](int i) {
+        const int rb = rbA + i;
+        const GvSeg& G = gv_seg(segs, nseg, rb);
+        const int row0 = GV_ROWS * (rb - G.rb0);
+        const int nval = min(GV_ROWS, G.nrows - row0);
+        const uint32_t dst = sbase + L.slots + (uint32_t)(i % NS) * SLOT;
+        uint64_t* bar = &full[i];
+        if (lane == 0) reqd[i] = 1;
+        if (G.copy == GV_COPY_TILE) {
+            // the rows are contiguous and the matrix ends on a 16-byte boundary
+            if (lane == 0) {
+                const uint32_t bytes = (uint32_t)((nval * G.rowbytes + 15) & ~int64_t(15));
+                mbar_arrive_expect_tx(bar, bytes);
+                bulk_s(dst, G.w + (int64_t)row0 * G.rowbytes, bytes, bar, policy);
+            }
+        } else {
+            // each row (4-byte aligned, a multiple of 4 bytes) at a pitch of G.pitch
+            const int nw = (int)(G.rowbytes >> 2);
+            for (int r = 0; r < nval; ++r) {
+                const uint8_t* p = G.w + (int64_t)(row0 + r) * G.rowbytes;
+                for (int c = lane; c < nw; c += 32) cp_async4(dst + (uint32_t)(r * G.pitch + 4 * c), p + 4 * c);
+            }
+            cp_async_arrive(bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        }
+        __syncwarp();
+    };
+
+    // every tile that has a slot is requested at entry (warp w: tiles w, w + GV_NW, ...)
+    for (int i = warp; i < min(ntile, NS); i += GV_NW) issue_tile(i);
+    pdl_wait();
+
+    // ---- x images: eight threads per 32-column block
+    {
+        const int nblk = 8 * nsb;
+        for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
+            const int bi = bw + (lane >> 3), j = lane & 7;
+            const bool valid = bi < nblk;
+            const int sb = bi >> 3, blk = bi & 7;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid) {
+                const float* xp = P.x + (int64_t)sb * 256 + 32 * blk + 4 * j;
+                if (P.x16) v = __ldcg(reinterpret_cast<const float4*>(xp));
+                else v = make_float4(__ldcg(xp), __ldcg(xp + 1), __ldcg(xp + 2), __ldcg(xp + 3));
+            }
+            float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+            const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+            const int es = max(1, E - 14);                                  // s = 2^(es - 127): |x / s| < 2^15
+            const float inv = __uint_as_float((uint32_t)(254 - es) << 23);  // 1 / s, exact
+            const float sc = __uint_as_float((uint32_t)es << 23);
+            const float a[4] = {v.x * inv, v.y * inv, v.z * inv, v.w * inv};
+            __half hi[4], lo[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                hi[c] = __float2half_rn(a[c]);
+                lo[c] = __float2half_rn(a[c] - __half2float(hi[c]));
+            }
+            const uint2 ph = make_uint2(h2pack(hi[0], hi[2]), h2pack(hi[1], hi[3]));
+            const uint2 pl = make_uint2(h2pack(lo[0], lo[2]), h2pack(lo[1], lo[3]));
+            float sum = (v.x + v.y) + (v.z + v.w);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+            if (valid && (MASK & 1)) {
+                const int tq = blk >> 1, hf = blk & 1, mm = 8 * hf + j;
+                uint8_t* im = smem + L.img4 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+                *reinterpret_cast<uint2*>(im) = ph;
+                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+                if (j == 0) {
+                    float* tb = reinterpret_cast<float*>(smem + L.tab4) + (sb * 4 + tq) * 4;
+                    tb[hf] = sum;
+                    tb[2 + hf] = sc;
+                }
+            }
+            if (valid && (MASK & 2)) {
+                const int h = blk >> 2, q = blk & 3, s6 = j >> 2, i = j & 3;
+                const int tq = 2 * h + s6, mm = 4 * q + i;
+                uint8_t* im = smem + L.img6 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+                *reinterpret_cast<uint2*>(im) = ph;
+                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+                if (j == 0) {
+                    float* tb = reinterpret_cast<float*>(smem + L.tab6) + (sb * 4 + 2 * h) * 4;
+                    const float sq = q >= 2 ? sc * 0.0625f : sc;      // quarters 2, 3 arrive as 16 code
+                    tb[q] = sq;
+                    tb[4 + q] = sq;
+                }
+            }
+        }
+        if (tid < 32) reinterpret_cast<uint32_t*>(smem + L.zero)[tid] = 0u;
+    }
+    __syncthreads();
+
+    // ---- the units: warp w takes the unit pairs v = w, w + GV_NW, ...; pair
+    // v is units 2 (v % hp) and 2 (v % hp) + 1 of tile v / hp (hp pairs per
+    // tile; the last pair of a tile with an odd unit count has one unit)
+    const GvK K = gv_consts();
+    const int g = lane >> 2, t = lane & 3;
+    const bool bact = (g >> 1) == t;                       // lanes holding B values
+    const uint32_t bslot = (uint32_t)(2 * t + (g & 1)) * GV_BSLOT;
+    const uint32_t b4 = bact ? sbase + L.img4 + bslot : sbase + L.zero;
+    const uint32_t b6 = bact ? sbase + L.img6 + bslot : sbase + L.zero;
+    const uint32_t bstr = bact ? GV_BIMG : 0u;
+    const Q4Sel sel4 = q4_sel(t);
+    float* part = reinterpret_cast<float*>(smem + L.part);   // [slot][pair][16]
+    const int hp = (nsb + 1) / 2;
+    int waited = -1;
+    bool aborted = false;
+    for (int v = warp; v < ntile * hp; v += GV_NW) {
+        const int i = v / hp, sb0 = 2 * (v % hp);
+        const int nun = min(2, nsb - sb0);
+        if (i != waited && !aborted) {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_bounded(&full[i], 0u, P.timeout_ns);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+            if (!ok) {
+                aborted = true;
+                if (lane == 0) record_status(P.status, STATUS_TIMEOUT);
+            }
+            waited = i;
+        }
+        const int rb = rbA + i;
+        const GvSeg& G = gv_seg(segs, nseg, rb);
+        float y0 = 0.f, y1 = 0.f;
+        if (!aborted) {
+            const uint32_t tb = sbase + L.slots + (uint32_t)(i % NS) * SLOT;
+            // tile rows of MMA rows g and g + 8 (pairs: gate row 2g, up row 2g + 1)
+            const int ra = G.mode == MODE_PLAIN ? g : 2 * g, rr = G.mode == MODE_PLAIN ? g + 8 : 2 * g + 1;
+            const int pitch = G.copy == GV_COPY_TILE ? (int)G.rowbytes : G.pitch;
+            const uint32_t r0 = tb + (uint32_t)(ra * pitch), r1 = tb + (uint32_t)(rr * pitch);
+            for (int jj = 0; jj < nun; ++jj) {
+                const int sb = sb0 + jj;
+                if ((MASK & 1) && G.fmt == FMT_Q4_K) {
+                    const float4 xs = lds128f(sbase + L.tab4 + (uint32_t)(sb * 4 + t) * 16);
+                    q4k_unit(r0 + 144 * sb, r1 + 144 * sb, t, sel4, b4 + sb * bstr, xs, K, y0, y1);
+                } else if (MASK & 2) {
+                    const float4 xs = lds128f(sbase + L.tab6 + (uint32_t)(sb * 4 + t) * 16);
+                    const uint32_t bb = b6 + sb * bstr;
+                    // rows start on 4-byte boundaries in shared memory, so
+                    // super-block sb is half-word aligned exactly when
+                    // 210 sb = 2 (mod 4)
+                    if ((210 * sb) & 2) q6k_unit<true>(r0 + 210 * sb, r1 + 210 * sb, t, bb, xs, K, y0, y1);
+                    else q6k_unit<false>(r0 + 210 * sb, r1 + 210 * sb, t, bb, xs, K, y0, y1);
+                }
+            }
+        }
+        // the pair's row sums (fixed butterfly over the lane quad)
+        y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 1);
+        y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 2);
+        y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
+        y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 2);
+        float* pu = part + ((i % NS) * hp + sb0 / 2) * 16;
+        if (t == 0) {
+            pu[g] = y0;
+            pu[g + 8] = y1;
+        }
+        // the warp that completes the tile adds its pairs in column order,
+        // stores, and requests tile i + NS into the slot
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atom_add_acqrel_cta(&done[i], nun) + nun == nsb;
+        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+            const float* pt = part + (i % NS) * hp * 16;
+            if (lane < 8) {
+                float v0 = 0.f, v1 = 0.f;
+                for (int k = 0; k < hp; ++k) {
+                    v0 += pt[k * 16 + lane];
+                    v1 += pt[k * 16 + lane + 8];
+                }
+                gv_store(G, rb, lane, v0, v1);
+            }
+            if (i + NS < ntile && !aborted) {
+                __syncwarp();
+                if (lane == 0) fence_proxy_async_smem();   // every warp's reads of the slot come first
+                __syncwarp();
+                issue_tile(i + NS);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // no copy may still be in flight when the CTA exits (every request was
+        // waited for unless a warp gave up): wait, bounded, for each requested tile
+        for (int i = 0; i < ntile; ++i)
+            if (reqd[i]) mbar_wait_bounded(&full[i], 0u, P.timeout_ns);
+    }
+}
+
+void* gv_get(int mask) {
+    return mask == 1 ? reinterpret_cast<void*>(gv_kernel<1>) : reinterpret_cast<void*>(gv_kernel<3>);
+}
+
+}  // namespace
+
+cudaError_t gv_set_smem(int bytes) {
+    for (int m : {1, 3}) {
+        cudaError_t e = cudaFuncSetAttribute(gv_get(m), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st) {
+    void* args[1] = {const_cast<GvParams*>(&P)};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(GV_NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, gv_get(mask), args);
+}
+
+}  // namespace lq

@@ -60,6 +60,48 @@ size_t qmm_smem_bytes(int fmt, int nstages, int csize, int gmax);
 cudaError_t qmm_max_resident(int fmt, int csize, size_t smem, int sms, int* out);
 cudaError_t qmm_launch(int fmt, const QmmParams& P, int grid, size_t smem, cudaStream_t st);
 
+// batch-1 tensor-core matvec (lq_gv.cu): one CTA of GV_NW warps per SM;
+// segments share x and the column count; row blocks of 16 rows (8 gate/up
+// pairs) over all segments are numbered from 0 (seg.rb0 = the first).  CTA k
+// takes row blocks [cta_rb[k], cta_rb[k+1]), each as one tile of whole rows
+// landing in one of nslots shared-memory slots of slot_bytes: GV_COPY_TILE
+// copies the 16 contiguous rows at once (w 16-byte aligned, the matrix a
+// multiple of 16 bytes), GV_COPY_CPA uses 4-byte cp.async copies at a row
+// pitch of `pitch` (w 4-byte aligned); rows are a multiple of 4 bytes.
+// mask: bit 0 Q4_K, bit 1 Q6_K; masks 1 (Q4_K) and 3 (both) are built.
+constexpr int GV_MAX_SEG = 4;
+constexpr int GV_MAX_CTA = 160;
+constexpr int GV_MAX_INFLIGHT = 16;    // tiles in flight per CTA
+constexpr int GV_MAX_TILES = 512;
+constexpr int GV_MAX_TILE_BYTES = 48 * 1024;
+enum { GV_COPY_TILE = 0, GV_COPY_CPA = 1 };
+struct GvSeg {
+    const uint8_t* w;        // plain matrix or interleaved gate/up pairs (row 2i gate, 2i+1 up)
+    float* y;
+    int64_t rowbytes;
+    int32_t fmt, mode, copy, act;
+    int32_t nout;            // outputs: rows (plain) or pairs
+    int32_t nrows;           // matrix rows
+    int32_t rb0, nrb;        // first row block, row blocks
+    int32_t pitch;           // shared row pitch of GV_COPY_CPA tiles
+    float cap;               // > 0: plain outputs are cap * tanh(y / cap)
+};
+struct GvParams {
+    GvSeg seg[GV_MAX_SEG];
+    const float* x;
+    uint64_t timeout_ns;
+    unsigned* status;
+    int32_t nseg;
+    int32_t nsb;             // 256-column units per row
+    int32_t nslots;          // tile slots per CTA
+    uint32_t slot_bytes;
+    int32_t maxtiles;        // most tiles (row blocks) of one CTA
+    int32_t x16;             // x is 16-byte aligned
+    int32_t cta_rb[GV_MAX_CTA + 1];
+};
+cudaError_t gv_set_smem(int bytes);
+cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st);
+
 // quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
 cudaError_t qmv1_set_smem(int bytes);
 cudaError_t qmv2_set_smem(int bytes);
@@ -71,11 +113,6 @@ cudaError_t qmv1_launch(int mask, const QmvParams& P, int grid, int nt, size_t s
 cudaError_t qmv2_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 cudaError_t qmv4_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 
-// the batch-1 FFN in one launch (lq_qmv_ffn.cu): gate/up format f0, down f1
-bool qmv_ffn_available(int f0, int f1);
-cudaError_t qmv_ffn_set_smem(int bytes);
-cudaError_t qmv_ffn_occupancy(int f0, int f1, int nt, size_t smem, int* per_sm);
-cudaError_t qmv_ffn_launch(const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 
 cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,
                            cudaStream_t st);

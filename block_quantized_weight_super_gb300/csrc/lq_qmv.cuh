@@ -9,7 +9,7 @@ namespace lq {
 
 constexpr int XS_STRIDE = 68;   // floats per 64-value x group slot in shared memory
 
-// Shape of the matrices of one launch (or of one phase of a two-phase launch).
+// Shape of the matrices of one launch.
 struct QGeo {
     int32_t cols;
     int32_t U;               // groups of 64 weights per row
@@ -22,18 +22,16 @@ struct QmvParams {
     Seg seg[MAX_SEG];
     int32_t nseg;
     int32_t ntiles;          // total tiles (format group 0 first)
-    QGeo geo[2];             // geo[0]: the launch; geo[1]: phase 1 of a two-phase launch
+    QGeo geo;
     int32_t R;               // rows per work item (interleaved in a thread)
     int32_t nstages;
     int32_t stage_bytes;
-    int32_t red_tile;        // floats per partial-sum slot (two-phase launches)
-    int32_t fmt0, fmt1;      // formats of CTA groups (or phases) 0 and 1
+    int32_t fmt0, fmt1;      // formats of CTA groups 0 and 1
     int32_t cta_split;       // CTAs [0, cta_split) run format group 0
-    int32_t tile_split;      // tiles [0, tile_split) belong to format group (phase) 0
+    int32_t tile_split;      // tiles [0, tile_split) belong to format group 0
     int32_t dev_counts;      // some segment reads its row count / offset from device memory
     uint64_t timeout_ns;
     unsigned* status;
-    unsigned* gbar;          // grid barrier word between the phases of a two-phase launch
 };
 
 // Rows of W per work item for batch width B and block-format mask (bit 0
@@ -62,34 +60,6 @@ __host__ __device__ inline size_t qmv_smem_bytes(int B, int U, int RT, int nstag
     off = (off + 15) & ~size_t(15);
     off += (size_t)MAX_SEG * sizeof(Seg);          // shared copy of the segment table
     return off;
-}
-
-// Shared memory of the two-phase (fused FFN, batch 1) kernel: stages sized
-// for the larger tile, x for the wider phase, partial slots of red_tile
-// floats, and besides the stage barriers the bulk-staging barrier and the
-// producer's "h written" signal to the consumers.
-struct FfnSmem {
-    size_t stages, xs, sxs, red, bars, segs, total;
-};
-__host__ __device__ inline FfnSmem qmv_ffn_smem(int Umax, int red_tile, int nstages, int stage_bytes) {
-    FfnSmem L;
-    size_t off = 0;
-    L.stages = off;
-    off += (size_t)nstages * stage_bytes;
-    L.xs = off;
-    off += (size_t)Umax * XS_STRIDE * sizeof(float);
-    L.sxs = off;
-    off += (size_t)Umax * 2 * sizeof(float);
-    L.red = off;
-    off += (size_t)(nstages + 1) * red_tile * sizeof(float);
-    off = (off + 7) & ~size_t(7);
-    L.bars = off;                                  // full[S], empty[S], xfull, gready; cnt[S+1], abort
-    off += (size_t)(2 * nstages + 2) * sizeof(uint64_t) + (size_t)(nstages + 2) * sizeof(int);
-    off = (off + 15) & ~size_t(15);
-    L.segs = off;
-    off += 2 * sizeof(Seg);
-    L.total = off;
-    return L;
 }
 
 }  // namespace lq

@@ -215,87 +215,6 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
     consumer_sync(nct);
 }
 
-// Bulk staging of x (h in phase 1 of the one-launch FFN, after its grid
-// barrier).  Consumer thread 0 copies the valid x rows in column order with bulk copies
-// (TMA) of at most 8 KB into the top B*U*64 floats of the x area (the padding
-// of the group slots leaves exactly that much room below); the consumer
-// threads then move the units (16 columns of one group, assigned as in
-// stage_x) into the padded slots in rounds: load the round's units, consumer
-// barrier, store them.  A slot ends 4 floats per group above where the raw
-// row runs, so the stores of a round never reach raw values of a later round
-// (Q6_K's permutation stays within a super-block, and a round covers whole
-// super-blocks).  In isolation a few large copies deliver an x that every
-// CTA reads about twice as fast as thread loads (and far faster than one copy
-// per slot); at the start of a launch, though, they queue behind the weight
-// tiles already issued and arrive later than loads, so there x is loaded.
-// Slots and sub-block sums equal stage_x's.  coherent: x was written by
-// other CTAs of this kernel.  Returns false if the wait ran out.
-template <int FMT, int B>
-__device__ bool stage_x_bulk(const QGeo& Gm, const Seg& S, float* xs, float* sxs, uint64_t* xfull,
-                             uint32_t parity, uint64_t timeout_ns, int ct, int nct, bool coherent) {
-    constexpr int NU = 2;                        // units per thread and round
-    const int U = Gm.U, cols = Gm.cols;
-    const int nval = qseg_nval(S, B);
-    const int boff = qseg_boff(S);
-    float* raw = xs + B * U * 4;                 // B rows of cols floats, 16-byte aligned
-    const int lane = ct & 31;
-    if (ct == 0) {
-        if (coherent) asm volatile("fence.proxy.async.global;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the area's generic use
-        mbar_arrive_expect_tx(xfull, (uint32_t)(nval * cols * 4));
-        for (int b = 0; b < nval; ++b) {
-            const int rho = boff + b;
-            const char* src = reinterpret_cast<const char*>(S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * cols);
-            char* dst = reinterpret_cast<char*>(raw + b * cols);
-            for (int off = 0; off < cols * 4; off += 8192)
-                bulk_g2s(dst + off, src + off, (unsigned)min(8192, cols * 4 - off), xfull);
-        }
-    }
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(xfull, parity, timeout_ns);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-    const int units = B * U * 4;
-    // the round count depends only on units and nct: every consumer thread
-    // passes every barrier of the loop
-    for (int base = 0; base < units; base += NU * nct) {
-        const int e0 = base + ct;
-        float4 v[NU][4];
-#pragma unroll
-        for (int h = 0; h < NU; ++h) {
-            const int e = e0 + h * nct;
-            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
-            if (ok && e < units && b < nval) {
-                const float4* src = reinterpret_cast<const float4*>(raw + b * cols + qxcol<FMT>(G, 16 * q));
-#pragma unroll
-                for (int k = 0; k < 4; ++k) v[h][k] = src[k];
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) v[h][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        consumer_sync(nct);                      // the round's raw values are read before any store
-#pragma unroll
-        for (int h = 0; h < NU; ++h) {
-            const int e = e0 + h * nct;
-            const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
-            if (e < units) {
-                float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) dst[k] = v[h][k];
-            }
-            if (FMT == FMT_Q4_K) {
-                float s16 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) s16 = ((s16 + v[h][k].x) + v[h][k].y) + v[h][k].z + v[h][k].w;
-                const float s32 = s16 + __shfl_xor_sync(0xFFFFFFFFu, s16, 1);
-                if (e < units && (q & 1) == 0) sxs[(b * U + G) * 2 + (q >> 1)] = s32;
-            }
-        }
-    }
-    consumer_sync(nct);
-    return ok;
-}
-
 // Segments reading the same x rows (QKV: Q and K) need no second staging.
 __device__ __forceinline__ bool same_xsrc(const Seg& a, const Seg& b) {
     return a.x == b.x && a.xmap == b.xmap && a.boff == b.boff && a.bcnt == b.bcnt && a.b0 == b.b0 &&
@@ -651,7 +570,6 @@ struct Smem {
     float* red;
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* xfull;        // bulk staging of x has landed (one-launch FFN)
     int* cnt;
     int* abort_flag;
 };
@@ -662,7 +580,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
     const int NC = (blockDim.x >> 5) - 1;          // consumer warps
     const int NCT = NC * 32;
     const int S_ = P.nstages;
-    const QGeo& Gm = P.geo[0];
+    const QGeo& Gm = P.geo;
     const int U = Gm.U;
     const int red_tile = Gm.RT * B * Gm.UP;
     const int NRED = S_ + 1;             // partial slots
@@ -869,7 +787,7 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_k
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
     const int S_ = P.nstages;
-    const int U = P.geo[0].U;
+    const int U = P.geo.U;
     Smem sm;
     size_t off = 0;
     sm.stages = smem;
@@ -879,11 +797,10 @@ __global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_k
     sm.sxs = reinterpret_cast<float*>(smem + off);
     off += (size_t)B * U * 2 * sizeof(float);
     sm.red = reinterpret_cast<float*>(smem + off);
-    off += (size_t)(S_ + 1) * P.geo[0].RT * B * P.geo[0].UP * sizeof(float);
+    off += (size_t)(S_ + 1) * P.geo.RT * B * P.geo.UP * sizeof(float);
     off = (off + 7) & ~size_t(7);
     sm.full = reinterpret_cast<uint64_t*>(smem + off);
     sm.empty = sm.full + S_;
-    sm.xfull = nullptr;
     sm.cnt = reinterpret_cast<int*>(sm.empty + S_);
     sm.abort_flag = sm.cnt + (S_ + 1);
     size_t seg_off = off + (size_t)2 * S_ * sizeof(uint64_t) + (size_t)(S_ + 2) * sizeof(int);

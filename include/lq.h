@@ -136,26 +136,6 @@ int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, co
 int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,
            const float* x, float* h, float* y, int batch, int act, lq_stream_t stream);
 
-/* lq_ffn_one_launch -- lq_ffn at batch 1 as ONE launch: every CTA runs its
- * gate/up tiles, the CTAs meet at a grid-wide barrier once h is complete,
- * then run their down tiles (h staged by bulk copies).  Results equal
- * lq_ffn's bit for bit.  Measured on GB300 at the Gemma-3-4B FFN it is not
- * faster than lq_ffn's two launches (the barrier and the distribution of h
- * to every CTA cost what the second launch did), so lq_ffn does not use it.
- * x and h 16-byte aligned (LQ_EALIGN otherwise).  Shapes and format pairs
- * the kernel cannot tile evenly (Q8_0 rows, widths without a common warp
- * count, formats other than Q4_K->Q6_K, Q4_K->Q4_K, Q6_K->Q6_K) give
- * LQ_EUNSUPPORTED before any launch.
- * sync: a device word used as the grid barrier, zero before its first use
- * (every call leaves its low 31 bits zero), or NULL for the library's own
- * word; calls that may run at the same time need distinct words.  All CTAs
- * of the launch must be resident together: if another kernel holds SMs for
- * long, the bounded waits run out (STATUS_TIMEOUT, lq_device_status) rather
- * than hang. */
-int lq_ffn_one_launch(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter,
-                      int64_t hidden, const float* x, float* h, float* y, int act, uint32_t* sync,
-                      lq_stream_t stream);
-
 /* MoE expert FFN (dotLLM MoeSwiGluMlp rule; larql Gemma 4 26B-A4B table).
  * router: [E][hidden] fp32; logits l_e = router_e . x_t, p = softmax(l),
  * top-k experts (lower index wins ties), weights p / sum of selected p;

@@ -160,25 +160,6 @@ def test_ffn_validation(lq):
     assert ffn(1, FAKE, 2, FAKE, 256, 256, FAKE, FAKE + 2, FAKE, 1, 1) == lq.LQ_EALIGN
 
 
-def test_ffn_one_launch_validation(lq):
-    """Shapes and format pairs the one-launch kernel cannot tile evenly, and
-    misaligned x / h / sync, are refused on the host (no device work).  A
-    shape fuses when some consumer-warp count tiles both matrices evenly with
-    tiles of at most 32 KB."""
-    L = lq.lib()
-    Q4, Q6, Q8 = 1, 2, 3
-    one = lambda f0, f1, inter, hidden, x=FAKE, h=FAKE, sync=None: L.lq_ffn_one_launch(
-        f0, FAKE, f1, FAKE, inter, hidden, x, h, FAKE, 1, sync, None)
-    assert one(Q4, Q4, 14336, 4096) == lq.LQ_EUNSUPPORTED     # Llama widths: no common warp count
-    assert one(Q4, Q6, 768, 2560) == lq.LQ_EUNSUPPORTED
-    assert one(Q8, Q8, 512, 512) == lq.LQ_EUNSUPPORTED        # Q8_0 rows: tiles above 32 KB
-    assert one(Q8, Q4, 512, 512) == lq.LQ_EUNSUPPORTED        # no kernel for this pair
-    assert one(Q4, Q6, 10240, 2560, x=FAKE + 4) == lq.LQ_EALIGN
-    assert one(Q4, Q6, 10240, 2560, h=FAKE + 8) == lq.LQ_EALIGN
-    assert one(Q4, Q6, 10240, 2560, sync=FAKE + 2) == lq.LQ_EALIGN
-    assert one(Q4, Q6, 0, 2560) == lq.LQ_ESHAPE
-
-
 def test_moe_validation(lq):
     L = lq.lib()
     P = C.c_void_p * 2

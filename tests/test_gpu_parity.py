@@ -91,29 +91,21 @@ def test_matvec_parity(lq, fmt, rows, cols, batch):
     assert_within(host(y), ref, oracle.matvec_bound(S), f"fmt {fmt} {rows}x{cols} b{batch}")
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
-def test_matvec_unaligned_weight_base(lq, fmt):
-    """W starting 2 bytes past a 16-byte boundary: rows are copied by the
-    threads instead of the bulk-copy engine; results identical."""
-    rows, cols = 41, 2048
-    g = synth.rng(5)
-    W = synth.weights(g, fmt, rows, cols)
-    x = synth.activations(g, 1, cols)
-    ya = empty((1, rows))
-    yb = empty((1, rows))
-    lq.lq_matvec(fmt, dev(W), rows, cols, dev(x), ya, 1)
-    keep, p = dev(W, offset_bytes=2)
-    lq.lq_matvec(fmt, p, rows, cols, dev(x), yb, 1)
-    assert np.array_equal(host(ya), host(yb))
-    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
-    assert_within(host(yb), ref, oracle.matvec_bound(S), "unaligned")
+# Which kernel a call takes (the library chooses by shape and alignment):
+#   "gv": batch 1, Q4_K alone or Q4_K with Q6_K in one launch, columns a
+#         multiple of 256, 16-row tiles of at most 48 KB, weights 4-byte
+#         aligned (the batch-1 tensor-core kernel);
+#   "tc": Q4_K with at least 2 x rows and columns a multiple of 512, Q8_0
+#         with at least 3 x rows and columns a multiple of 256 (the batched
+#         tensor-core kernel);
+#   "cc": otherwise (the CUDA-core kernel).
+# The kernels sum in different orders, so only the oracle's bound relates
+# results of different kernels; calls on the same kernel give the same bits.
+GV_TILE_MAX = 48 * 1024
 
 
-# Q4_K calls with at least 2 x rows and columns a multiple of 512, and Q8_0
-# calls with at least 3 x rows and columns a multiple of 256, run on the
-# tensor cores (a different summation order from the batch-1 kernel, so only
-# the oracle's bound relates the two).
-TC_MIN_BATCH = 2
+def _row_bytes(fmt, cols):
+    return cols // oracle.block_elems(fmt) * oracle.block_bytes(fmt)
 
 
 def _tensor_path(fmt, cols, M):
@@ -121,36 +113,136 @@ def _tensor_path(fmt, cols, M):
             (fmt == Q8_0 and cols % 256 == 0 and M >= 3))
 
 
+def _gv_path(fmts, cols, M, w_align=16):
+    fmts = set(fmts)
+    if M != 1 or cols % 256 or Q4_K not in fmts or not fmts <= {Q4_K, Q6_K} or w_align % 4:
+        return False
+    return all(_row_bytes(f, cols) % 4 == 0 and 16 * _row_bytes(f, cols) <= GV_TILE_MAX for f in fmts)
+
+
+def _kernel(fmts, cols, M, w_align=16):
+    if _gv_path(fmts, cols, M, w_align):
+        return "gv"
+    if len(set(fmts)) == 1 and _tensor_path(next(iter(fmts)), cols, M):
+        return "tc"
+    return "cc"
+
+
+@pytest.mark.parametrize("fmt,off", [(Q4_K, 4), (Q4_K, 2), (Q6_K, 2), (Q8_0, 2)])
+def test_matvec_unaligned_weight_base(lq, fmt, off):
+    """W starting `off` bytes past a 16-byte boundary: rows are copied by the
+    threads instead of the bulk-copy engine.  On the same kernel the results
+    are identical to the aligned call's; a 2-byte offset moves a Q4_K call
+    from the batch-1 tensor-core kernel to the CUDA-core one (within the
+    bound)."""
+    rows, cols = 41, 2048
+    g = synth.rng(5)
+    W = synth.weights(g, fmt, rows, cols)
+    x = synth.activations(g, 1, cols)
+    ya = empty((1, rows))
+    yb = empty((1, rows))
+    lq.lq_matvec(fmt, dev(W), rows, cols, dev(x), ya, 1)
+    keep, p = dev(W, offset_bytes=off)
+    lq.lq_matvec(fmt, p, rows, cols, dev(x), yb, 1)
+    if _kernel({fmt}, cols, 1) == _kernel({fmt}, cols, 1, w_align=off):
+        assert np.array_equal(host(ya), host(yb))
+    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    assert_within(host(yb), ref, oracle.matvec_bound(S), "unaligned")
+    assert_within(host(ya), ref, oracle.matvec_bound(S), "aligned")
+
+
 @pytest.mark.parametrize("fmt,cols", [(Q4_K, 2560), (Q6_K, 2560), (Q8_0, 4096), (Q4_K, 14336), (Q4_K, 2304),
                                       (Q6_K, 10240), (Q4_K, 8192)])
 def test_batch_invariance(lq, fmt, cols):
-    """row b of a batch-M call is bit-identical to the same x row in any other
-    call that takes the same kernel: a batch-1 call for the CUDA-core kernel,
-    the batch-8 call for the tensor-core one (each x row is its own MMA column).
-    At 8192-10240 columns each batch-1 thread stages its own x group; the
-    batch-2/4 calls stage x collectively: the same items and sums."""
+    """row b of a batch-M call is bit-identical to the same x row in every
+    other call (batch 1..8) that takes the same kernel: each x row is its own
+    MMA column on the tensor cores, and the CUDA-core kernel sums a row's
+    items in the same order at every batch width.  At 8192-10240 columns each
+    batch-1 CUDA-core thread stages its own x group; the batch-2/4 calls
+    stage x collectively: the same items and sums."""
     rows = 67
     g = synth.rng(11)
     W = synth.weights(g, fmt, rows, cols)
     X = synth.activations(g, 8, cols)
     Wd = dev(W)
-    singles = []
-    for b in range(8):
-        y1 = empty((1, rows))
-        lq.lq_matvec(fmt, Wd, rows, cols, dev(X[b:b + 1]), y1, 1)
-        singles.append(host(y1)[0])
-    y8 = empty((8, rows))
-    lq.lq_matvec(fmt, Wd, rows, cols, dev(X), y8, 8)
-    full = host(y8)
     ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
-    for M in (2, 3, 4, 5, 8):
-        yM = empty((M, rows))
-        lq.lq_matvec(fmt, Wd, rows, cols, dev(X[:M]), yM, M)
-        got = host(yM)
-        for b in range(M):
-            same = full[b] if _tensor_path(fmt, cols, M) else singles[b]
-            assert np.array_equal(got[b], same), (M, b)
-        assert_within(got, ref[:M], oracle.matvec_bound(S[:M]), f"batch {M}")
+    first = {}                       # (kernel, b) -> row of the first call seen
+    for M in (1, 2, 3, 4, 5, 8):
+        calls = [(X[b:b + 1], [b]) for b in range(8)] if M == 1 else [(X[:M], list(range(M)))]
+        for xs, bs in calls:
+            yM = empty((len(bs), rows))
+            lq.lq_matvec(fmt, Wd, rows, cols, dev(xs), yM, len(bs))
+            got = host(yM)
+            kern = _kernel({fmt}, cols, M)
+            for i, b in enumerate(bs):
+                key = (kern, b)
+                if key in first:
+                    assert np.array_equal(got[i], first[key]), (M, b, kern)
+                else:
+                    first[key] = got[i]
+            assert_within(got, ref[bs], oracle.matvec_bound(S[bs]), f"batch {M}")
+
+
+# ---------------------------------------------------------------- batch-1 tensor-core kernel
+
+@pytest.mark.parametrize("rows,cols", [(80000, 256), (50001, 512), (20000, 2304)])
+def test_gv_many_tiles_per_cta(lq, rows, cols):
+    """More row blocks per CTA than tile slots (the slots are reused), a
+    single 256-column unit per row (a unit pair with one unit), an odd unit
+    count (2304 columns), ragged last row block."""
+    assert _kernel({Q4_K}, cols, 1) == "gv"
+    g = synth.rng(rows + cols)
+    W = synth.q4k(g, rows, cols)
+    x = synth.activations(g, 1, cols)
+    y = empty((1, rows))
+    lq.lq_matvec(Q4_K, dev(W), rows, cols, dev(x), y, 1)
+    ref, S = oracle.matvec(Q4_K, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"{rows}x{cols}")
+
+
+def test_gv_rows_independent_of_partition(lq):
+    """A row's result does not depend on how the launch's row blocks are split
+    between CTAs: the first rows of a 5000-row matrix equal those of its
+    first 40 / 333 / 2000 rows (1 to 125 row blocks over up to 152 CTAs),
+    bit for bit; likewise gate/up pairs."""
+    cols = 2560
+    g = synth.rng(21)
+    W = synth.q4k(g, 5000, cols)
+    x = synth.activations(g, 1, cols)
+    Wd, xd = dev(W), dev(x)
+    yf = empty((1, 5000))
+    lq.lq_matvec(Q4_K, Wd, 5000, cols, xd, yf, 1)
+    full = host(yf)[0]
+    for n in (40, 333, 2000):
+        y = empty((1, n))
+        lq.lq_matvec(Q4_K, Wd, n, cols, xd, y, 1)
+        assert np.array_equal(host(y)[0], full[:n]), n
+    rb = lq.lq_row_bytes(Q4_K, cols)
+    Wgu = torch.empty(2 * 2000 * rb, dtype=torch.uint8, device="cuda")
+    lq.lq_pack_gate_up(Q4_K, dev(W[:2000]), dev(W[2000:4000]), 2000, cols, Wgu)
+    hf = empty((1, 2000))
+    lq.lq_ffn_gate_up_act(Q4_K, Wgu, 2000, cols, xd, hf, 1, 2)
+    for n in (8, 77, 1000):
+        h = empty((1, n))
+        lq.lq_ffn_gate_up_act(Q4_K, Wgu, n, cols, xd, h, 1, 2)     # the first n pairs of the same packing
+        assert np.array_equal(host(h)[0], host(hf)[0][:n]), n
+
+
+@pytest.mark.parametrize("cols", [512, 1536, 2560, 3584])
+def test_gv_qkv_q6k_alignments(lq, cols):
+    """Q4_K Q/K with a Q6_K V in one batch-1 launch at even super-block
+    counts (rows a multiple of 4 bytes): the Q6_K units alternate between
+    word-aligned and half-word-aligned super-blocks."""
+    nq, nk, nv = 130, 35, 45
+    assert _kernel({Q4_K, Q6_K}, cols, 1) == "gv"
+    g = synth.rng(cols)
+    Wq, Wk, Wv = synth.q4k(g, nq, cols), synth.q4k(g, nk, cols), synth.q6k(g, nv, cols)
+    x = synth.activations(g, 1, cols)
+    q, k, v = empty((1, nq)), empty((1, nk)), empty((1, nv))
+    lq.lq_qkv_mixed(Q4_K, dev(Wq), nq, Q4_K, dev(Wk), nk, Q6_K, dev(Wv), nv, cols, dev(x), q, k, v, 1)
+    for f, W, n, out in ((Q4_K, Wq, nq, q), (Q4_K, Wk, nk, k), (Q6_K, Wv, nv, v)):
+        ref, S = oracle.matvec(f, W, n, cols, x, NTH)
+        assert_within(host(out), ref, oracle.matvec_bound(S), f"qkv fmt {f} cols {cols}")
 
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
@@ -164,7 +256,12 @@ def test_one_hot_x_gives_dequant_column(lq, fmt):
         x[0, j] = 1.0
         y = empty((1, rows))
         lq.lq_matvec(fmt, Wd, rows, cols, dev(x), y, 1)
-        assert _bits_equal(host(y)[0], D[:, j])
+        if _kernel({fmt}, cols, 1) == "cc":
+            assert _bits_equal(host(y)[0], D[:, j])       # w * 1 computed as the dequantization does
+        else:
+            # the tensor-core kernel adds (q - qb) d sc and d sc qb - dmin m:
+            # the column within the bound, not bit for bit
+            assert_within(host(y)[0], D[:, j], oracle.matvec_bound(np.abs(D[:, j])), f"one-hot {j}")
 
 
 def test_q8_0_odd_block_rows(lq):
@@ -193,11 +290,12 @@ def test_matvec_zero_rows_and_zero_x(lq):
 # ---------------------------------------------------------------- final-logit soft-cap
 
 @pytest.mark.parametrize("fmt,rows,cols,batch,xscale,xoff", [
-    (Q4_K, 333, 2560, 1, 1.0, 0),      # batch-1 kernel
+    (Q4_K, 333, 2560, 1, 1.0, 0),      # batch-1 tensor-core kernel
     (Q4_K, 130, 1024, 4, 1.0, 0),      # tensor cores
     (Q8_0, 70, 1024, 4, 1.0, 0),       # tensor cores, Q8_0
     (Q6_K, 101, 2560, 3, 1.0, 0),      # CUDA cores, batch 3
-    (Q4_K, 67, 2560, 1, 1.0, 4),       # x not 16-byte aligned: the plain-load kernel
+    (Q4_K, 67, 2560, 1, 1.0, 4),       # x not 16-byte aligned: scalar x loads
+    (Q6_K, 67, 2560, 1, 1.0, 4),       # the same on the plain-load kernel
     (Q4_K, 200, 2560, 1, 3000.0, 0),   # |y| >> cap: saturation
 ])
 def test_matvec_softcap(lq, fmt, rows, cols, batch, xscale, xoff):
@@ -236,10 +334,11 @@ def test_qkv_mixed(lq, fq, fk, fv, batch):
         ref, S = oracle.matvec(f, W, n, cols, x, NTH)
         got = host(out)
         assert_within(got, ref, oracle.matvec_bound(S), f"qkv fmt {f}")
-        if not _tensor_path(f, cols, batch):
+        kq = _kernel({fq, fk, fv}, cols, batch) if batch == 1 else _kernel({f}, cols, batch)
+        if kq != "tc" and kq == _kernel({f}, cols, batch):
             single = empty((batch, n))
             lq.lq_matvec(f, dev(W), n, cols, xd, single, batch)
-            assert np.array_equal(got, host(single))    # same code path, same bits
+            assert np.array_equal(got, host(single))    # same kernel, same bits
 
 
 # ---------------------------------------------------------------- gate + up
@@ -317,59 +416,6 @@ def test_ffn(lq, f0, f1, inter, hidden, batch, act):
     h, y = empty((batch, inter)), empty((batch, hidden))
     lq.lq_ffn(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, batch, act)
     _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y)
-
-
-@pytest.mark.parametrize("f0,f1,inter,hidden,act", [
-    (Q4_K, Q6_K, 256, 512, 1),      # five tiles per phase, ragged last tiles of both
-    (Q4_K, Q6_K, 1280, 2560, 2),    # many tiles per CTA
-    (Q4_K, Q4_K, 1024, 256, 1),     # 10 gate/up tiles, 5 down tiles: CTAs with no down tile
-    (Q6_K, Q6_K, 512, 512, 2),
-    (Q4_K, Q4_K, 768, 4096, 2),     # six consumer warps; 128 gate/up tiles, 64 down tiles
-    (Q4_K, Q6_K, 10240, 2560, 1),   # the Gemma-3-4B FFN: 1280 tiles per phase over a full grid
-])
-def test_ffn_one_launch(lq, f0, f1, inter, hidden, act):
-    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, 1, 41 + inter + hidden)
-    lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
-    h, y = empty((1, inter)), empty((1, hidden))
-    lq.lq_ffn_one_launch(f0, Wgu, f1, dev(Wd), inter, hidden, dev(x), h, y, act)
-    status_clean(lq)
-    _ffn_check(lq, f0, f1, inter, hidden, 1, act, Wg, Wu, Wd, x, Wgu, h, y)
-
-
-def test_ffn_one_launch_barrier_reuse(lq):
-    """The grid-barrier word needs no reset: back-to-back calls with different
-    grids on the library's word, and on a caller word starting at zero or at
-    2^31 (the two values a completed call leaves), all give the same results."""
-    shapes = [(Q4_K, Q6_K, 256, 512), (Q4_K, Q4_K, 1024, 256), (Q4_K, Q6_K, 1280, 2560)]
-    runs = []
-    for i, (f0, f1, inter, hidden) in enumerate(shapes):
-        Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, f0, f1, inter, hidden, 1, 300 + i)
-        lq.lq_pack_gate_up(f0, dev(Wg), dev(Wu), inter, hidden, Wgu)
-        runs.append((f0, f1, inter, hidden, Wgu, dev(Wd), dev(x)))
-    ref = []
-    for f0, f1, inter, hidden, Wgu, Wd, x in runs:
-        h, y = empty((1, inter)), empty((1, hidden))
-        lq.lq_ffn(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 1, 2)
-        ref.append((host(h), host(y)))
-    word = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for start in (None, 0, -2 ** 31):
-        if start is not None:
-            word.fill_(start)
-        for rep in range(3):
-            for (f0, f1, inter, hidden, Wgu, Wd, x), (rh, ry) in zip(runs, ref):
-                h, y = empty((1, inter)), empty((1, hidden))
-                lq.lq_ffn_one_launch(f0, Wgu, f1, Wd, inter, hidden, x, h, y, 2,
-                                     sync=None if start is None else word)
-                assert _bits_equal(host(h), rh) and _bits_equal(host(y), ry), (start, rep, inter, hidden)
-    status_clean(lq)
-
-
-def test_ffn_one_launch_unsupported_raises(lq):
-    Wg, Wu, Wd, x, Wgu = _ffn_inputs(lq, Q4_K, Q6_K, 768, 2560, 1, 5)
-    h, y = empty((1, 768)), empty((1, 2560))
-    with pytest.raises(lq.LqError):
-        lq.lq_ffn_one_launch(Q4_K, Wgu, Q6_K, dev(Wd), 768, 2560, dev(x), h, y, 1)
-    assert np.isnan(host(y)).all()          # nothing launched
 
 
 # ---------------------------------------------------------------- tensor-core path
