@@ -9,15 +9,25 @@ step by step, so the weights never sit in the 129 MB L2 between uses.
 
 Headline metric: effective weight GB/s = weight-block bytes of the layer per
 second (60,518,400 B per step), with us/layer = ms_per_step * 1000.  The
-device-timed number replays the decode pass (all layer copies in one CUDA
-graph, so consecutive launches overlap) with inputs resident;
-`e2e` times the same C ABI calls with every step's x copied in from pinned
-host memory and its layer output copied back to pinned host memory, the
-copies on their own streams overlapping the kernels (double-buffered, one
-CUDA graph per step).
+device-timed number replays the decode pass (the layer copies captured in
+CUDA graphs, so consecutive launches overlap) with inputs resident; every
+graph replayed in the timed region has been replayed before it.
 
---impl reference runs the CPU oracle (fp64, all host cores) on a bounded
-sample of the same layers as the reference arm.
+`e2e` times the same C ABI calls with every step's x copied in from pinned
+host memory and its layer output copied back to pinned host memory: the
+copies on their own streams overlapping the kernels (double-buffered, one
+CUDA graph per step), and, as `e2e.direct`, the plain sequence a caller
+without graphs issues (copy in, four API calls, copy out, per step), with
+the host time spent inside the API calls.
+
+Besides the layer, the default line carries per-launch figures of the
+layer's four calls and of the other named workloads (`configs`): a 256 x 2560
+Q4_K matvec, the Llama-3-8B FFN in Q4_K and Q8_0 at batch 1, 2, 4, 8, the
+262144 x 2560 Q4_K lm_head and the Mixtral MoE FFN.
+
+--impl reference runs the CPU oracle (fp64, all host cores) on the layer:
+each step is every row of every matrix of one layer copy; the repo arm's
+`cpu_baseline` times the same sample.
 
 --workload selects one of the other named shapes instead of the layer, with
 the same JSON line: llama_ffn (SwiGLU FFN 2 x 14336 x 4096 + 4096 x 14336 at
@@ -47,11 +57,16 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-LAYER_BYTES = 6_574_080 + 2_949_120 + 29_491_200 + 21_504_000   # 60,518,400
-GATEUP_BYTES = 29_491_200
+H_, I_, NQ_, NKV_ = 2560, 10240, 2048, 1024
+CALL_WEIGHT_BYTES = {"qkv": 6_574_080, "o": 2_949_120, "gateup": 29_491_200, "down": 21_504_000}
+# fp32 activations each call reads and writes once (x in, y out)
+CALL_ACT_BYTES = {"qkv": 4 * (H_ + NQ_ + 2 * NKV_), "o": 4 * (NQ_ + H_), "gateup": 4 * (H_ + I_),
+                  "down": 4 * (I_ + H_)}
+LAYER_BYTES = sum(CALL_WEIGHT_BYTES.values())        # 60,518,400
 NLAYERS = 34
 METRIC = "effective weight GB/s per quantized matvec (decode layer, batch 1)"
 WORKLOADS = ("gemma_layer", "llama_ffn", "lm_head", "mixtral_moe", "matvec_small")
+CPU_STEPS_MAX = 272                                  # repo arm's oracle sample: layer steps
 
 
 def parse():
@@ -63,6 +78,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=NLAYERS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config figures")
     ap.add_argument("--workload", default="gemma_layer", choices=list(WORKLOADS))
     ap.add_argument("--batch", type=int, default=8, help="x rows (llama_ffn)")
     ap.add_argument("--fmt", default="q4k", choices=["q4k", "q80"], help="weight format (llama_ffn)")
@@ -74,6 +90,8 @@ def parse():
             a.steps = 2200 if a.workload == "matvec_small" else 200   # at least two passes over the copies
         if "--warmup" not in sys.argv:
             a.warmup = 20
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
     return a
 
 
@@ -81,7 +99,7 @@ def dist_setup(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if ws > 1:
+    if ws > 1 and args.impl != "reference":
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -152,14 +170,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_layers(n, dev):
-    """n Gemma-3-4B-shaped layers (seeded synthetic blocks), gate/up packed."""
+def host_layers(n):
+    """n Gemma-3-4B-shaped layers as host arrays (seeded synthetic blocks) and x."""
+    import synth
+    out = []
+    for i in range(n):
+        L, x = synth.gemma3_layer(seed=i)
+        out.append(L)
+        if i == 0:
+            x0 = x
+    return out, x0
+
+
+def make_layers(n, dev, host=None):
+    """the n layers on the device, gate/up packed (lq_pack_gate_up)."""
     import torch
     import block_quantized_weight_super_gb300 as lq
     import synth
+    if host is None:
+        host, x0 = host_layers(n)
+    else:
+        x0 = None
     layers = []
-    for i in range(n):
-        L, x = synth.gemma3_layer(seed=i)
+    for L in host:
         d = {k: torch.from_numpy(v).to(dev) for k, v in L.items()}
         rb = lq.lq_row_bytes(lq.LQ_Q4_K, synth.GEMMA3_HIDDEN)
         wgu = torch.empty(2 * synth.GEMMA3_INTER * rb, dtype=torch.uint8, device=dev)
@@ -167,8 +200,6 @@ def make_layers(n, dev):
         d["wgu"] = wgu
         del d["wg"], d["wu"]
         layers.append(d)
-        if i == 0:
-            x0 = x
     torch.cuda.synchronize()
     return layers, x0
 
@@ -178,68 +209,85 @@ class Layer:
 
     def __init__(self, dev):
         import torch
-        import synth
-        H, I, NQ, NKV = synth.GEMMA3_HIDDEN, synth.GEMMA3_INTER, synth.GEMMA3_NQ, synth.GEMMA3_NKV
         f = dict(dtype=torch.float32, device=dev)
-        self.x = torch.zeros((1, H), **f)
-        self.q = torch.empty((1, NQ), **f)
-        self.k = torch.empty((1, NKV), **f)
-        self.v = torch.empty((1, NKV), **f)
-        self.o = torch.empty((1, H), **f)
-        self.h = torch.empty((1, I), **f)
-        self.y = torch.empty((1, H), **f)
-        self.dims = (H, I, NQ, NKV)
+        self.x = torch.zeros((1, H_), **f)
+        self.q = torch.empty((1, NQ_), **f)
+        self.k = torch.empty((1, NKV_), **f)
+        self.v = torch.empty((1, NKV_), **f)
+        self.o = torch.empty((1, H_), **f)
+        self.h = torch.empty((1, I_), **f)
+        self.y = torch.empty((1, H_), **f)
 
-    def run(self, w, stream, mark=None, x=None, y=None, x_read=None):
-        """the layer's four calls; x / y override the input and output
-        buffers, and x_read (an event) is recorded once x has been read."""
+    def call(self, name, w, stream, x=None, y=None):
         import block_quantized_weight_super_gb300 as lq
-        H, I, NQ, NKV = self.dims
-        lq.lq_qkv_mixed(lq.LQ_Q4_K, w["wq"], NQ, lq.LQ_Q4_K, w["wk"], NKV, lq.LQ_Q6_K, w["wv"], NKV,
-                        H, self.x if x is None else x, self.q, self.k, self.v, 1, stream)
-        if x_read is not None:
-            x_read.record(stream)
-        lq.lq_matvec(lq.LQ_Q4_K, w["wo"], H, NQ, self.q, self.o, 1, stream)
-        if mark:
-            mark[0].record(stream)
-        lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, self.o, self.h, 1, lq.LQ_ACT_GEGLU_TANH, stream)
-        if mark:
-            mark[1].record(stream)
-        lq.lq_matvec(lq.LQ_Q6_K, w["wd"], H, I, self.h, self.y if y is None else y, 1, stream)
+        if name == "qkv":
+            lq.lq_qkv_mixed(lq.LQ_Q4_K, w["wq"], NQ_, lq.LQ_Q4_K, w["wk"], NKV_, lq.LQ_Q6_K, w["wv"], NKV_,
+                            H_, self.x if x is None else x, self.q, self.k, self.v, 1, stream)
+        elif name == "o":
+            lq.lq_matvec(lq.LQ_Q4_K, w["wo"], H_, NQ_, self.q, self.o, 1, stream)
+        elif name == "gateup":
+            lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I_, H_, self.o, self.h, 1, lq.LQ_ACT_GEGLU_TANH, stream)
+        else:
+            lq.lq_matvec(lq.LQ_Q6_K, w["wd"], H_, I_, self.h, self.y if y is None else y, 1, stream)
+
+    def run(self, w, stream, x=None, y=None):
+        """the layer's four calls; x / y override the input and output buffers."""
+        for name in ("qkv", "o", "gateup", "down"):
+            self.call(name, w, stream, x=x, y=y)
 
 
-def bench_lq(args, ws, rank, local):
+def timed_graphs(fn, items, steps, warmup, st):
+    """ms per step of fn(item, st) over the rotating items, exactly `steps`
+    steps: CUDA graphs of a full pass over the items and of the partial pass
+    that completes `steps`; both are replayed (warm) before the timed region,
+    the full one for at least `warmup` steps."""
+    import torch
+
+    def capture(cs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for w in cs:
+                fn(w, st)
+        return g
+
+    n = len(items)
+    with torch.cuda.stream(st):
+        for w in items:               # every launch once outside capture (plans, attributes)
+            fn(w, st)
+        st.synchronize()
+        full = capture(items)
+        rem = steps % n
+        part = capture(items[:rem]) if rem else None
+        for _ in range(max(1, -(-warmup // n))):
+            full.replay()
+        if part is not None:
+            part.replay()
+        st.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps // n):
+            full.replay()
+        if part is not None:
+            part.replay()
+        e1.record(st)
+        st.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_lq(args, ws, rank, local, peak):
     import torch
     import block_quantized_weight_super_gb300 as lq
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lq.lib()
-    layers, x0 = make_layers(args.layers, dev)
+    hl, x0 = host_layers(args.layers)
+    layers, _ = make_layers(args.layers, dev, host=hl)
     st = torch.cuda.Stream(device=dev)
     lay = Layer(dev)
     lay.x.copy_(torch.from_numpy(x0))
     torch.cuda.synchronize()
     rc, bits = lq.lq_device_status()
     assert rc == 0
-
-    # The decode pass: all n layer copies in one CUDA graph (a model's depth,
-    # so consecutive layers' launches overlap as in a real decode step).  K
-    # timed steps = K layers: K // n full passes plus one partial pass.
-    def capture(ws_):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=st):
-            for w in ws_:
-                lay.run(w, st)
-        return g
-
-    with torch.cuda.stream(st):
-        for w in layers:        # warm the kernels once outside capture
-            lay.run(w, st)
-        st.synchronize()
-        full = capture(layers)
-        rem = args.steps % len(layers)
-        part = capture(layers[:rem]) if rem else None
-    torch.cuda.synchronize()
     n = len(layers)
 
     def barrier():
@@ -248,21 +296,10 @@ def bench_lq(args, ws, rank, local):
             dist.barrier()
         torch.cuda.synchronize()
 
-    with torch.cuda.stream(st):
-        for _ in range(max(1, -(-args.warmup // n))):     # >= W warm-up layers
-            full.replay()
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(st):
-            e0.record(st)
-            for _ in range(args.steps // n):
-                full.replay()
-            if part is not None:
-                part.replay()
-            e1.record(st)
+        ms = timed_graphs(lay.run, layers, args.steps, args.warmup, st)
         barrier()
-    ms = e0.elapsed_time(e1) / args.steps
     ms_all = ms
     if ws > 1:
         import torch.distributed as dist
@@ -272,132 +309,162 @@ def bench_lq(args, ws, rank, local):
     rc, bits = lq.lq_device_status()
     assert rc == 0, "device status after timed region"
 
-    # dominant kernel (FFN gate+up, 29.5 MB) timed alone with CUDA events on
-    # its stream, rotating the layer copies: one graph of n launches
-    gk = torch.cuda.CUDAGraph()
+    # each of the layer's four launches alone, rotating the layer copies
+    # (one graph of n launches), CUDA events on the launching stream
+    calls = {}
+    for name in ("qkv", "o", "gateup", "down"):
+        t = timed_graphs(lambda w, s, nm=name: lay.call(nm, w, s), layers, max(n, args.steps), 3 * n, st)
+        nb = CALL_WEIGHT_BYTES[name] + CALL_ACT_BYTES[name]
+        calls[name] = {"us": t * 1e3, "alg_bytes": nb, "GB_s": nb / (t * 1e-3) / 1e9,
+                       "frac": nb / (t * 1e-3) / 1e9 / peak}
+
+    e2e = None if args.no_e2e else bench_e2e(args, ws, dev, st, lay, layers, x0, barrier)
+    return ms_all, calls, clk.summary(), e2e, hl
+
+
+def bench_e2e(args, ws, dev, st, lay, layers, x0, barrier):
+    """e2e through the C ABI: every step copies its x in from pinned host
+    memory and its layer output back to pinned host memory.
+
+    Graphed: step i's input and output live in device slots i & 1; the copies
+    run on their own streams so that they overlap the kernels: one CUDA graph
+    per layer copy c holds [copy-in of step c+1's x] || [layer c] || [copy-out
+    of step c-1's output], joined at its end.  A copy-in before the first step
+    and a copy-out after the last complete the K steps.  Every step graph is
+    replayed once before the timed region.
+
+    Direct: per step, copy x in, the four API calls, copy the output out, all
+    on one stream with no graph (what a caller without graphs pays, host work
+    of the calls included)."""
+    import torch
+    n = len(layers)
+    xh = torch.from_numpy(x0).pin_memory()
+    yh = torch.empty((1, H_), dtype=torch.float32).pin_memory()
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    xb = [torch.empty_like(lay.x) for _ in range(2)]
+    yb = [torch.empty_like(lay.y) for _ in range(2)]
+
+    def step_graph(i):                       # step i: layer copy i % n, slot i & 1
+        c, k = i % n, i & 1
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            fork = torch.cuda.Event()
+            fork.record(st)
+            cin.wait_event(fork)
+            cout.wait_event(fork)
+            with torch.cuda.stream(cin):
+                xb[k ^ 1].copy_(xh, non_blocking=True)           # the next step's slot
+            with torch.cuda.stream(cout):
+                yh.copy_(yb[k ^ 1], non_blocking=True)           # the previous step's slot
+            lay.run(layers[c], st, x=xb[k], y=yb[k])
+            st.wait_stream(cin)
+            st.wait_stream(cout)
+        return g
+
     with torch.cuda.stream(st):
-        H, I = lay.dims[0], lay.dims[1]
-        for w in layers:
-            lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, lay.o, lay.h, 1, lq.LQ_ACT_GEGLU_TANH, st)
-        st.synchronize()
-        with torch.cuda.graph(gk, stream=st):
-            for w in layers:
-                lq.lq_ffn_gate_up_act(lq.LQ_Q4_K, w["wgu"], I, H, lay.o, lay.h, 1,
-                                      lq.LQ_ACT_GEGLU_TANH, st)
-        for _ in range(3):
-            gk.replay()
-        st.synchronize()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = max(1, args.steps // n)
-        k0.record(st)
-        for _ in range(reps):
-            gk.replay()
-        k1.record(st)
-        st.synchronize()
-    gate_ms = k0.elapsed_time(k1) / (reps * n)
+        ng = n if n % 2 == 0 else 2 * n
+        sg = [step_graph(i) for i in range(ng)]
+        torch.cuda.synchronize()
 
-    # e2e through the C ABI: every step copies its x in from pinned host
-    # memory and its layer output back to pinned host memory.  Step i's
-    # input and output live in device slots i & 1; the copies run on their
-    # own streams so that they overlap the kernels: one CUDA graph per layer
-    # copy c holds [copy-in of step c+1's x] || [layer c] || [copy-out of
-    # step c-1's output], joined at its end.  A copy-in before the first step
-    # and a copy-out after the last complete the K steps.
-    e2e = None
-    if not args.no_e2e:
-        xh = torch.from_numpy(x0).pin_memory()
-        yh = torch.empty((1, lay.dims[0]), dtype=torch.float32).pin_memory()
-        cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        xb = [torch.empty_like(lay.x) for _ in range(2)]
-        yb = [torch.empty_like(lay.y) for _ in range(2)]
+        def run_steps(k):
+            xb[0].copy_(xh, non_blocking=True)
+            for i in range(k):
+                sg[i % ng].replay()
+            yh.copy_(yb[(k - 1) & 1], non_blocking=True)
 
-        def step_graph(i):                       # step i: layer copy i % n, slot i & 1
-            c, k = i % n, i & 1
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=st):
-                fork = torch.cuda.Event()
-                fork.record(st)
-                cin.wait_event(fork)
-                cout.wait_event(fork)
-                with torch.cuda.stream(cin):
-                    xb[k ^ 1].copy_(xh, non_blocking=True)           # the next step's slot
-                with torch.cuda.stream(cout):
-                    yh.copy_(yb[k ^ 1], non_blocking=True)           # the previous step's slot
-                lay.run(layers[c], st, x=xb[k], y=yb[k])
-                st.wait_stream(cin)
-                st.wait_stream(cout)
-            return g
+        run_steps(max(ng, args.warmup))             # every step graph replayed at least once
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        run_steps(args.steps)
+        torch.cuda.synchronize()
+        t_e2e = (time.perf_counter() - t0) / args.steps
 
-        with torch.cuda.stream(st):
-            ng = n if n % 2 == 0 else 2 * n
-            sg = [step_graph(i) for i in range(ng)]
-            torch.cuda.synchronize()
+        def direct_steps(k):
+            host = 0.0
+            for i in range(k):
+                lay.x.copy_(xh, non_blocking=True)
+                h0 = time.perf_counter()
+                lay.run(layers[i % n], st)
+                host += time.perf_counter() - h0
+                yh.copy_(lay.y, non_blocking=True)
+            return host
 
-            def run_steps(k):
-                xb[0].copy_(xh, non_blocking=True)
-                for i in range(k):
-                    sg[i % ng].replay()
-                yh.copy_(yb[(k - 1) & 1], non_blocking=True)
-
-            run_steps(min(args.warmup, 5) or 1)
-            torch.cuda.synchronize()
-            barrier()
-            t0 = time.perf_counter()
-            run_steps(args.steps)
-            torch.cuda.synchronize()
-            t_e2e = (time.perf_counter() - t0) / args.steps
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([t_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": ws * LAYER_BYTES / t_e2e / 1e9, "unit": "GB/s",
-               "us_per_layer": t_e2e * 1e6,
-               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4),
-               "copies": "own streams in a graph per step, overlapping the kernels (x and output double-buffered)"}
-    return ms_all, gate_ms, clk.summary(), e2e
+        direct_steps(max(n, args.warmup))
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        host = direct_steps(args.steps)
+        torch.cuda.synchronize()
+        t_dir = (time.perf_counter() - t0) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_e2e, t_dir], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e, t_dir = float(t[0].item()), float(t[1].item())
+    return {"value": ws * LAYER_BYTES / t_e2e / 1e9, "unit": "GB/s", "us_per_layer": t_e2e * 1e6,
+            "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4),
+            "copies": "own streams in a graph per step, overlapping the kernels (x and output double-buffered)",
+            "direct": {"value": ws * LAYER_BYTES / t_dir / 1e9, "unit": "GB/s", "us_per_layer": t_dir * 1e6,
+                       "host_us_per_call": host / args.steps / 4 * 1e6,
+                       "how": "no graph: per step copy x in, four API calls, copy the output out, one stream"}}
 
 
-def cpu_baseline(sample_layers=1, rows_frac=0.25):
-    """the oracle (fp64 C++, all host threads) on a bounded sample: the first
-    rows_frac of every matrix of one layer; reported as weight GB/s."""
-    import oracle
-    import synth
-    L, x = synth.gemma3_layer(seed=0)
-    H, I, NQ = synth.GEMMA3_HIDDEN, synth.GEMMA3_INTER, synth.GEMMA3_NQ
-    nth = os.cpu_count() or 1
-    jobs = [(oracle.Q4_K, L["wq"], H, x), (oracle.Q4_K, L["wk"], H, x), (oracle.Q6_K, L["wv"], H, x),
-            (oracle.Q4_K, L["wo"], NQ, np.zeros((1, NQ), np.float32)),
-            (oracle.Q4_K, L["wg"], H, x), (oracle.Q4_K, L["wu"], H, x),
-            (oracle.Q6_K, L["wd"], I, np.zeros((1, I), np.float32))]
-    nbytes = 0
-    t0 = time.perf_counter()
-    for fmt, W, cols, xin in jobs:
-        r = max(1, int(W.shape[0] * rows_frac))
-        oracle.matvec(fmt, W[:r], r, cols, xin, nth)
-        nbytes += W[:r].nbytes
-    dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
-            "sample": f"first {int(rows_frac * 100)}% of the rows of every matrix of one layer "
-                      f"({nbytes} weight bytes), fp64, {nth} threads"}
+# ---------------------------------------------------------------- the CPU oracle sample
+
+class OracleLayers:
+    """the oracle (fp64 C++, all host threads) over the layer copies: a step
+    is every row of every matrix of one layer copy (7 matvecs, 60,518,400
+    weight bytes), copies taken in turn."""
+
+    def __init__(self, hl):
+        import synth
+        g = synth.rng(1234)
+        self.hl = hl
+        self.xs = {"h": synth.activations(g, 1, H_), "q": synth.activations(g, 1, NQ_),
+                   "i": synth.activations(g, 1, I_)}
+        self.nth = os.cpu_count() or 1
+
+    def step(self, i):
+        import oracle
+        L = self.hl[i % len(self.hl)]
+        xh, xq, xi = self.xs["h"], self.xs["q"], self.xs["i"]
+        for fmt, W, cols, x in ((oracle.Q4_K, L["wq"], H_, xh), (oracle.Q4_K, L["wk"], H_, xh),
+                                (oracle.Q6_K, L["wv"], H_, xh), (oracle.Q4_K, L["wo"], NQ_, xq),
+                                (oracle.Q4_K, L["wg"], H_, xh), (oracle.Q4_K, L["wu"], H_, xh),
+                                (oracle.Q6_K, L["wd"], I_, xi)):
+            oracle.matvec(fmt, W, W.shape[0], cols, x, self.nth)
+
+    def run(self, steps, warmup):
+        for i in range(warmup):
+            self.step(i)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            self.step(warmup + i)
+        return (time.perf_counter() - t0) / steps
+
+    def describe(self, steps):
+        return {"kind": "oracle", "cores": self.nth,
+                "sample": f"{steps} layer steps: every row of every matrix of one layer copy per step "
+                          f"({LAYER_BYTES} weight bytes), copies in turn, fp64, {self.nth} threads"}
 
 
-# DRAM bytes (read + write) of one gate+up launch, from the ncu capture in
-# profiles/qmv_gate_up_and_down_dram_traffic.md, valid while the sources of
-# that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "9afbb318874b71a27d858d3c6aa7c1990a68de4051ad825eb82a1a4659cc7f17", "bytes": 29572608}
-
+# DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
+# while the sources of that kernel hash to the value they had when it was taken.
+GATEUP_TRAFFIC = {"csrc_sha256": "470ff4b1c06c41c7904872015eae99fc458400f82e6225c807d692aedf44d1bb",
+                  "bytes": 29_536_512,
+                  "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch)"}
 
 # the sources the batch-1 gate+up launch is compiled from
-QMV_SOURCES = ("lq_codec.cuh", "lq_device.cuh", "lq_group.cuh", "lq_qmv.cuh", "lq_qmv_b1.cu",
-               "lq_qmv_impl.cuh", "lq_stream.cuh")
+GV_SOURCES = ("lq_codec.cuh", "lq_device.cuh", "lq_group.cuh", "lq_gv.cu", "lq_gv.cuh", "lq_internal.h",
+              "lq_qmv.cuh", "lq_stream.cuh")
 
 
 def csrc_sha256():
     import hashlib
-    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_quantized_weight_super_gb300", "csrc")
+    d = os.path.join(ROOT, "block_quantized_weight_super_gb300", "csrc")
     h = hashlib.sha256()
-    for f in QMV_SOURCES:
+    for f in GV_SOURCES:
         h.update(f.encode())
         with open(os.path.join(d, f), "rb") as fh:
             h.update(fh.read())
@@ -413,6 +480,17 @@ def l2_bytes():
     except Exception:
         pass
     return 129_000_000
+
+
+def n_copies(nbytes):
+    """rotating copies: at least 3x the L2 size in total, one when a single copy is larger."""
+    if nbytes > l2_bytes():
+        return 1
+    return max(1, min(2048, -(-3 * l2_bytes() // max(1, nbytes))))
+
+
+def clone(d):
+    return {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone()) for k, v in d.items()}
 
 
 # ---------------------------------------------------------------- other workloads
@@ -512,18 +590,11 @@ class Workload:
                              (lq.LQ_Q4_K, W2[e0], I, np.zeros((1, I), np.float32))]
         else:
             raise ValueError(name)
-        # cold L2: copies totalling at least 3x the L2 size
-        ncopy = max(1, min(2048, -(-3 * l2_bytes() // max(1, self.bytes))))
-        if self.bytes > l2_bytes():
-            ncopy = 1
-        self.copies = [base] + [self._clone(base) for _ in range(ncopy - 1)]
+        ncopy = n_copies(self.bytes)
+        self.copies = [base] + [clone(base) for _ in range(ncopy - 1)]
         torch.cuda.synchronize()
 
-    @staticmethod
-    def _clone(d):
-        return {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone()) for k, v in d.items()}
-
-    def cpu(self, rows_frac=0.02):
+    def cpu(self, rows_frac=0.25):
         import oracle
         nth = os.cpu_count() or 1
         nbytes = 0
@@ -536,40 +607,6 @@ class Workload:
         return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": nth, "kind": "oracle",
                 "sample": f"first {rows_frac * 100:g}% of the rows of the workload's matrices "
                           f"({nbytes} weight bytes), fp64, {nth} threads"}
-
-
-def time_graph(fn, copies, steps, warmup, st):
-    """ms per step of fn over the rotating copies, exactly `steps` steps,
-    from CUDA graphs (a full pass over the copies and one partial pass)."""
-    import torch
-
-    def capture(cs):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=st):
-            for w in cs:
-                fn(w, st)
-        return g
-
-    n = len(copies)
-    with torch.cuda.stream(st):
-        for w in copies:
-            fn(w, st)
-        st.synchronize()
-        full = capture(copies)
-        rem = steps % n
-        part = capture(copies[:rem]) if rem else None
-        for _ in range(max(1, -(-warmup // n))):
-            full.replay()
-        st.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(steps // n):
-            full.replay()
-        if part is not None:
-            part.replay()
-        e1.record(st)
-        st.synchronize()
-    return e0.elapsed_time(e1) / steps
 
 
 def bench_workload(args, ws, rank, local, peak, peak_src):
@@ -587,7 +624,7 @@ def bench_workload(args, ws, rank, local, peak, peak_src):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ms = time_graph(wl.step, wl.copies, args.steps, args.warmup, st)
+        ms = timed_graphs(wl.step, wl.copies, args.steps, args.warmup, st)
         if ws > 1:
             import torch.distributed as dist
             dist.barrier()
@@ -597,7 +634,7 @@ def bench_workload(args, ws, rank, local, peak, peak_src):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_all = float(t.item())
-    dom_ms = ms if wl.dom is wl.step else time_graph(wl.dom, wl.copies, args.steps, args.warmup, st)
+    dom_ms = ms if wl.dom is wl.step else timed_graphs(wl.dom, wl.copies, args.steps, args.warmup, st)
     rc, _ = lq.lq_device_status()
     assert rc == 0, "device status after timed region"
     e2e = None
@@ -606,7 +643,7 @@ def bench_workload(args, ws, rank, local, peak, peak_src):
         yh = torch.empty(tuple(wl.y.shape), dtype=torch.float32).pin_memory()
         n = len(wl.copies)
         with torch.cuda.stream(st):
-            for i in range(min(args.warmup, 5)):
+            for i in range(max(3, min(args.warmup, n))):
                 wl.x.copy_(xh, non_blocking=True)
                 wl.step(wl.copies[i % n], st)
                 yh.copy_(wl.y, non_blocking=True)
@@ -619,7 +656,8 @@ def bench_workload(args, ws, rank, local, peak, peak_src):
             st.synchronize()
             t_e2e = (time.perf_counter() - t0) / args.steps
         e2e = {"value": ws * wl.bytes / t_e2e / 1e9, "unit": "GB/s", "us_per_call": t_e2e * 1e6,
-               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4)}
+               "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(yh.numel() * 4),
+               "how": "no graph: per step copy x in, the API call(s), copy the output out, one stream"}
     if rank != 0:
         return
     achieved = wl.dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -639,6 +677,94 @@ def bench_workload(args, ws, rank, local, peak, peak_src):
             "clocks": clk.summary(), "e2e": e2e, "gpu_launches": wl.launches * args.steps,
             "cpu_baseline": wl.cpu() if (ws == 1 and not args.no_cpu) else None}
     print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- per-config figures of the default line
+
+def config_figures(dev, peak):
+    """µs per call, GB/s and fraction of HBM for the other named workloads,
+    each timed in graphs over rotating weight copies after warm replays."""
+    import torch
+    import block_quantized_weight_super_gb300 as lq
+    import synth
+    st = torch.cuda.Stream(device=dev)
+    up = lambda a: torch.from_numpy(a).to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {}
+
+    def fig(ms, nbytes, ncopy):
+        return {"us": ms * 1e3, "weight_bytes": nbytes, "GB_s": nbytes / (ms * 1e-3) / 1e9,
+                "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "copies": ncopy}
+
+    def steps_for(ncopy):
+        return max(40, 2 * ncopy)
+
+    # config 0: Q4_K 256 x 2560, batch 1
+    W, x = synth.matvec_small(0)
+    base = {"w": up(W)}
+    cs = [base] + [clone(base) for _ in range(n_copies(W.nbytes) - 1)]
+    xd, yd = up(x), torch.empty((1, 256), **f32)
+    ms = timed_graphs(lambda w, s: lq.lq_matvec(lq.LQ_Q4_K, w["w"], 256, 2560, xd, yd, 1, s), cs,
+                      steps_for(len(cs)), len(cs), st)
+    out["matvec_small_q4k_256x2560_b1"] = fig(ms, W.nbytes, len(cs))
+    del cs, base
+
+    # config 2: Llama-3-8B FFN, Q4_K and Q8_0, batch 1, 2, 4, 8 (gate+up SwiGLU then down)
+    H, I = synth.LLAMA_HIDDEN, synth.LLAMA_INTER
+    for fmt, tag in ((lq.LQ_Q4_K, "q4k"), (lq.LQ_Q8_0, "q80")):
+        Wl, X = synth.llama_ffn(fmt, 8, seed=0)
+        wgu = torch.empty(2 * I * lq.lq_row_bytes(fmt, H), dtype=torch.uint8, device=dev)
+        lq.lq_pack_gate_up(fmt, up(Wl["wg"]), up(Wl["wu"]), I, H, wgu)
+        base = {"wgu": wgu, "wd": up(Wl["wd"])}
+        nb = wgu.numel() + base["wd"].numel()
+        cs = [base] + [clone(base) for _ in range(n_copies(nb) - 1)]
+        Xd = up(X)
+        for M in (1, 2, 4, 8):
+            h, y = torch.empty((M, I), **f32), torch.empty((M, H), **f32)
+            xm = Xd[:M]
+
+            def step(w, s, M=M, h=h, y=y, xm=xm):
+                lq.lq_ffn_gate_up_act(fmt, w["wgu"], I, H, xm, h, M, lq.LQ_ACT_SWIGLU, s)
+                lq.lq_matvec(fmt, w["wd"], H, I, h, y, M, s)
+            ms = timed_graphs(step, cs, steps_for(len(cs)), len(cs), st)
+            out[f"llama_ffn_{tag}_b{M}"] = fig(ms, nb, len(cs))
+        del cs, base, wgu
+        torch.cuda.empty_cache()
+
+    # config 3: lm_head Q4_K 262144 x 2560, batch 1 (one copy: larger than L2)
+    W, x = synth.lm_head(0)
+    wd, xd = up(W), up(x)
+    yd = torch.empty((1, W.shape[0]), **f32)
+    ms = timed_graphs(lambda w, s: lq.lq_matvec(lq.LQ_Q4_K, w, W.shape[0], 2560, xd, yd, 1, s), [wd], 40, 5, st)
+    out["lm_head_q4k_262144x2560_b1"] = fig(ms, W.nbytes, 1)
+    del wd
+    torch.cuda.empty_cache()
+
+    # config 4: Mixtral MoE FFN, 8 experts, top-2, 16 tokens, Q4_K
+    R, W1, W3, W2, X = synth.mixtral_moe(0)
+    E, Hm = R.shape
+    Im = W1[0].shape[0]
+    T, K = X.shape[0], synth.MIXTRAL_TOPK
+    w = {"d1": [up(a) for a in W1], "d3": [up(a) for a in W3], "d2": [up(a) for a in W2]}
+    Rd, Xd = up(R), up(X)
+    Y = torch.empty((T, Hm), **f32)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, K), **f32)
+    nbw = lq.lq_moe_workspace_bytes(E, K, T, Hm, Im)
+    wsp = torch.empty(nbw, dtype=torch.uint8, device=dev)
+    moe = lambda ww, s: lq.lq_moe_ffn(Rd, E, K, lq.LQ_Q4_K, ww["d1"], ww["d3"], ww["d2"], Hm, Im, Xd, Y, T,
+                                      idx, wts, wsp, nbw, s)
+    moe(w, None)
+    torch.cuda.synchronize()
+    touched = len(set(idx.cpu().numpy().ravel().tolist()))
+    ms = timed_graphs(moe, [w], 40, 5, st)
+    out["mixtral_moe_q4k_8x14336x4096_top2_t16"] = dict(
+        fig(ms, touched * (W1[0].nbytes + W3[0].nbytes + W2[0].nbytes), 1), experts_touched=touched)
+    del w
+    torch.cuda.empty_cache()
+    rc, _ = lq.lq_device_status()
+    assert rc == 0, "device status after the config figures"
+    return out
 
 
 def main():
@@ -665,37 +791,39 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        vals = []
-        for _ in range(args.warmup):
-            cpu_baseline(rows_frac=0.02)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            vals.append(cpu_baseline(rows_frac=0.02))
-        dt = (time.perf_counter() - t0) / args.steps
-        cb = vals[-1]
-        v = statistics.median(c["value"] for c in vals)
-        cb["value"] = v
+        hl, _ = host_layers(args.layers)
+        ol = OracleLayers(hl)
+        dt = ol.run(args.steps, args.warmup)
+        v = LAYER_BYTES / dt / 1e9
+        cb = dict(ol.describe(args.steps), value=v, unit="GB/s")
         line = dict(base, impl="reference", value=v, ms_per_step=dt * 1e3, n_gpus=1,
                     cpu_baseline=cb, e2e={"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                                           "d2h_bytes_per_step": 0})
         print(json.dumps(line))
         return
 
-    ms, gate_ms, clocks, e2e = bench_lq(args, ws, rank, local)
+    ms, calls, clocks, e2e, hl = bench_lq(args, ws, rank, local, peak)
+    import torch
+    configs = None if (args.no_configs or ws > 1) else config_figures(torch.device("cuda", local), peak)
     if rank != 0:
         return
     value = ws * LAYER_BYTES / (ms * 1e-3) / 1e9
-    achieved = GATEUP_BYTES / (gate_ms * 1e-3) / 1e9
-    cb = cpu_baseline() if (ws == 1 and not args.no_cpu) else None
+    g = calls["gateup"]
+    cb = None
+    if ws == 1 and not args.no_cpu:
+        ol = OracleLayers(hl)
+        k = min(args.steps, CPU_STEPS_MAX)
+        dt = ol.run(k, 1)
+        cb = dict(ol.describe(k), value=LAYER_BYTES / dt / 1e9, unit="GB/s")
+    traffic = GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["csrc_sha256"] == csrc_sha256() else None
     line = dict(base, value=value, ms_per_step=ms, us_per_layer=ms * 1e3,
                 frac_of_hbm=value / peak,
-                roofline={"bound": "hbm", "kernel": "ffn gate+up GEGLU (Q4_K 2x10240x2560)",
-                          "achieved": achieved, "peak": peak, "peak_source": peak_src,
-                          "unit": "GB/s", "frac": achieved / peak,
-                          "traffic": (GATEUP_TRAFFIC["bytes"] if csrc_sha256() == GATEUP_TRAFFIC["csrc_sha256"]
-                                      else None),
-                          "traffic_source": "profiles/qmv_gate_up_and_down_dram_traffic.md (ncu dram bytes per launch)",
-                          "us_per_launch": gate_ms * 1e3},
+                roofline={"bound": "hbm", "kernel": "ffn gate+up GEGLU (Q4_K 2x10240x2560), gv_kernel<1>",
+                          "achieved": g["GB_s"], "peak": peak, "peak_source": peak_src,
+                          "unit": "GB/s", "frac": g["frac"], "traffic": traffic,
+                          "traffic_source": GATEUP_TRAFFIC["source"],
+                          "alg_bytes_per_launch": g["alg_bytes"], "us_per_launch": g["us"]},
+                layer_calls=calls, configs=configs,
                 clocks=clocks, e2e=e2e, gpu_launches=4 * args.steps, cpu_baseline=cb)
     print(json.dumps(line))
 
