@@ -22,11 +22,13 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
            "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
-           "lq_ffn", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_static",
+           "lq_ffn", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_ex_workspace_bytes", "lq_moe_ffn_ex",
+           "lq_moe_ffn_static",
            "lq_device_status",
            "lq_set_wait_timeout_ns", "lq_probe_timeout"]
 
 LQ_MOE_STATIC_SCRATCH_BYTES = 4 << 20
+LQ_MOE_MAX_SHARED = 16
 
 
 class LqError(RuntimeError):
@@ -61,6 +63,9 @@ def lib():
             "lq_ffn": ([i32, vp, i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
             "lq_moe_workspace_bytes": ([i32, i32, i32, i64, i64], sz),
             "lq_moe_ffn": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, sz, vp], i32),
+            "lq_moe_ffn_ex_workspace_bytes": ([i32, i32, i32, i64, i64, i32, i64], sz),
+            "lq_moe_ffn_ex": ([vp, i32, i32, i32, i32, vp, vp, vp, i64, i64, i32, vp, vp, vp, i64, vp, vp, vp, i32,
+                               vp, vp, vp, sz, vp], i32),
             "lq_moe_ffn_static": ([vp, i32, i32, i32, vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp], i32),
             "lq_device_status": ([vp, C.POINTER(C.c_uint32)], i32),
             "lq_set_wait_timeout_ns": ([u64], None),
@@ -166,6 +171,23 @@ def lq_moe_ffn(router, n_experts, topk, fmt, W1, W3, W2, hidden, inter, X, Y, nt
                                    C.cast(a3, C.c_void_p), C.cast(a2, C.c_void_p), hidden, inter,
                                    _ptr(X), _ptr(Y), ntok, _ptr(topk_idx), _ptr(topk_w),
                                    _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def lq_moe_ffn_ex_workspace_bytes(n_experts, topk, ntok, hidden, inter, n_shared, inter_s) -> int:
+    return lib().lq_moe_ffn_ex_workspace_bytes(n_experts, topk, ntok, hidden, inter, n_shared, inter_s)
+
+
+def lq_moe_ffn_ex(router, n_experts, topk, norm_topk_prob, fmt, W1, W3, W2, hidden, inter, X, Y, ntok,
+                  Ws1=(), Ws3=(), Ws2=(), inter_s=0, shared_gate=None, topk_idx=None, topk_w=None,
+                  workspace=None, ws_bytes=0, stream=None):
+    a1, a3, a2 = _ptr_array(W1), _ptr_array(W3), _ptr_array(W2)
+    ns = len(Ws1)
+    s1, s3, s2 = (_ptr_array(Ws1), _ptr_array(Ws3), _ptr_array(Ws2)) if ns else (None, None, None)
+    cast = lambda a: None if a is None else C.cast(a, C.c_void_p)
+    return _check(lib().lq_moe_ffn_ex(_ptr(router), n_experts, topk, norm_topk_prob, fmt, cast(a1), cast(a3),
+                                      cast(a2), hidden, inter, ns, cast(s1), cast(s3), cast(s2), inter_s,
+                                      _ptr(shared_gate), _ptr(X), _ptr(Y), ntok, _ptr(topk_idx), _ptr(topk_w),
+                                      _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def lq_moe_ffn_static(router, n_experts, topk, fmt, W1, W3, W2, hidden, inter, X, Y, ntok,

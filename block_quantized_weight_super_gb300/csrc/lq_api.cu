@@ -59,9 +59,45 @@ struct DevInfo {
     int sms = 0;
     unsigned* status = nullptr;
     int qmm_res[2][3] = {};       // resident tensor-core CTAs / clusters of 2 / of 4 (Q4_K, Q8_0)
+    unsigned long long ctx = 0;   // id of the context these were taken in
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
+
+}  // namespace
+
+// Id of the current CUDA context (cuCtxGetId: unique for the life of the
+// process, so a context created after cudaDeviceReset has a new one); 0 when
+// no context is current.  Addresses of the library's device variables and
+// per-function attributes belong to a context: caches keyed by this id are
+// redone after a reset.  Without the driver entry points every context
+// reads as 1 (caches are then never redone).
+unsigned long long current_ctx_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static std::once_flag once;
+    static GetCurrentFn get_cur = nullptr;
+    static GetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess && a && b) {
+            get_cur = reinterpret_cast<GetCurrentFn>(a);
+            get_id = reinterpret_cast<GetIdFn>(b);
+        }
+    });
+    if (!get_cur) return 1;
+    CUcontext c = nullptr;
+    if (get_cur(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+namespace {
 
 int dev_info(DevInfo** out) {
     int dev = 0;
@@ -70,7 +106,9 @@ int dev_info(DevInfo** out) {
     if (dev < 0 || dev >= 64) return fail(LQ_EUNSUPPORTED, "device index %d", dev);
     std::lock_guard<std::mutex> lk(g_mu);
     DevInfo& d = g_dev[dev];
-    if (!d.init) {
+    const unsigned long long ctx = current_ctx_id();
+    if (!d.init || ctx == 0 || ctx != d.ctx) {
+        d.init = false;
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         void* p = nullptr;
@@ -92,6 +130,7 @@ int dev_info(DevInfo** out) {
                 if (e != cudaSuccess) return cuda_fail(e, "tensor-core matvec occupancy");
             }
         }
+        d.ctx = current_ctx_id();     // the symbol lookup made the context current
         d.init = true;
     }
     *out = &d;
@@ -568,6 +607,56 @@ int check_f32(const void* p, const char* name) {
     return LQ_OK;
 }
 
+// Everything lq_moe_ffn_ex checks before it looks at the workspace.
+int moe_validate(const float* router, int E, int topk, int norm, int fmt, const void* const* W1,
+                 const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter, int n_shared,
+                 const void* const* Ws1, const void* const* Ws3, const void* const* Ws2, int64_t inter_s,
+                 const float* shared_gate, const float* X, float* Y, int ntok, int32_t* topk_idx,
+                 float* topk_w) {
+    if (E < 1 || E > 256) return fail(LQ_EINVAL, "n_experts %d", E);
+    if (topk < 1 || topk > E) return fail(LQ_EINVAL, "topk %d with %d experts", topk, E);
+    if (norm != 0 && norm != 1) return fail(LQ_EINVAL, "norm_topk_prob %d", norm);
+    if (ntok < 0) return fail(LQ_EINVAL, "ntok %d", ntok);
+    if (n_shared < 0 || n_shared > LQ_MOE_MAX_SHARED) return fail(LQ_EINVAL, "n_shared %d", n_shared);
+    if (!W1 || !W3 || !W2) return fail(LQ_EINVAL, "expert pointer arrays are null");
+    int rc;
+    for (int e = 0; e < E; ++e) {
+        if ((rc = check_mat(fmt, W1[e], inter, hidden, "W1")) || (rc = check_mat(fmt, W3[e], inter, hidden, "W3")) ||
+            (rc = check_mat(fmt, W2[e], hidden, inter, "W2")))
+            return rc;
+        if (!W1[e] || !W3[e] || !W2[e]) return fail(LQ_EINVAL, "expert %d weights null", e);
+    }
+    if (n_shared > 0) {
+        if (!Ws1 || !Ws3 || !Ws2) return fail(LQ_EINVAL, "shared-expert pointer arrays are null");
+        for (int e = 0; e < n_shared; ++e) {
+            if ((rc = check_mat(fmt, Ws1[e], inter_s, hidden, "Ws1")) ||
+                (rc = check_mat(fmt, Ws3[e], inter_s, hidden, "Ws3")) ||
+                (rc = check_mat(fmt, Ws2[e], hidden, inter_s, "Ws2")))
+                return rc;
+            if (!Ws1[e] || !Ws3[e] || !Ws2[e]) return fail(LQ_EINVAL, "shared expert %d weights null", e);
+        }
+    } else if (shared_gate) {
+        return fail(LQ_EINVAL, "shared_gate given without shared experts");
+    }
+    if (ntok == 0) return LQ_OK;
+    if ((long long)ntok * E * 4 > 48 * 1024) return fail(LQ_ESHAPE, "ntok * n_experts too large");
+    if ((rc = check_f32(router, "router")) || (rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y"))) return rc;
+    if (shared_gate && (rc = check_f32(shared_gate, "shared_gate"))) return rc;
+    if ((topk_idx && !al(topk_idx, 4)) || (topk_w && !al(topk_w, 4)))
+        return fail(LQ_EALIGN, "topk outputs not 4-byte aligned");
+    return LQ_OK;
+}
+
+// The tensor-core kernel takes the grouped launches when every matrix of
+// the launch has a tile-multiple width and 16-byte aligned rows.
+bool moe_tc_ok(int fmt, int ntok, int64_t hidden, int64_t inter, const void* const* W1, const void* const* W3,
+               const void* const* W2, int n, const float* X) {
+    bool tc = ntok >= QMM_MOE_MIN_TOKENS && qmm_format_ok(fmt) && hidden % qmm_kc(fmt) == 0 &&
+              inter % qmm_kc(fmt) == 0 && al(X, 16);
+    for (int ex = 0; tc && ex < n; ++ex) tc = al(W1[ex], 16) && al(W3[ex], 16) && al(W2[ex], 16);
+    return tc;
+}
+
 }  // namespace
 }  // namespace lq
 
@@ -579,6 +668,7 @@ static __device__ __align__(256) uint8_t g_moe_scratch[LQ_MOE_STATIC_SCRATCH_BYT
 constexpr int kMaxDevices = 64;
 static std::mutex g_moe_scratch_mu;
 static void* g_moe_scratch_ptr[kMaxDevices] = {};
+static unsigned long long g_moe_scratch_ctx[kMaxDevices] = {};
 
 extern "C" {
 
@@ -753,36 +843,32 @@ int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t in
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-size_t lq_moe_workspace_bytes(int E, int topk, int ntok, int64_t hidden, int64_t inter) {
-    if (E < 1 || topk < 1 || ntok < 0 || hidden < 0 || inter < 0) return 0;
+size_t lq_moe_ffn_ex_workspace_bytes(int E, int topk, int ntok, int64_t hidden, int64_t inter, int n_shared,
+                                     int64_t inter_s) {
+    if (E < 1 || topk < 1 || ntok < 0 || hidden < 0 || inter < 0 || n_shared < 0 || inter_s < 0) return 0;
     const size_t ns = (size_t)ntok * topk;
-    return align256(ns * 4) * 4 + align256((size_t)E * 4) * 2 + align256(ns * inter * 4) +
-           align256(ns * hidden * 4);
+    size_t b = align256(ns * 4) * 4 + align256((size_t)E * 4) * 2 + align256(ns * inter * 4) +
+               align256(ns * hidden * 4);
+    if (n_shared > 0)
+        b += align256((size_t)ntok * 4) + align256((size_t)n_shared * ntok * inter_s * 4) +
+             align256((size_t)n_shared * ntok * hidden * 4);
+    return b;
 }
 
-int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const* W1,
-               const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
-               const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
-               void* workspace, size_t ws_bytes, lq_stream_t stream) {
+size_t lq_moe_workspace_bytes(int E, int topk, int ntok, int64_t hidden, int64_t inter) {
+    return lq_moe_ffn_ex_workspace_bytes(E, topk, ntok, hidden, inter, 0, 0);
+}
+
+int lq_moe_ffn_ex(const float* router, int E, int topk, int norm_topk_prob, int fmt, const void* const* W1,
+                  const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter, int n_shared,
+                  const void* const* Ws1, const void* const* Ws3, const void* const* Ws2, int64_t inter_s,
+                  const float* shared_gate, const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+                  void* workspace, size_t ws_bytes, lq_stream_t stream) {
     g_err[0] = 0;
-    if (E < 1 || E > 256) return fail(LQ_EINVAL, "n_experts %d", E);
-    if (topk < 1 || topk > E) return fail(LQ_EINVAL, "topk %d with %d experts", topk, E);
-    if (ntok < 0) return fail(LQ_EINVAL, "ntok %d", ntok);
-    if (!W1 || !W3 || !W2) return fail(LQ_EINVAL, "expert pointer arrays are null");
-    int rc;
-    for (int e = 0; e < E; ++e) {
-        if ((rc = check_mat(fmt, W1[e], inter, hidden, "W1")) || (rc = check_mat(fmt, W3[e], inter, hidden, "W3")) ||
-            (rc = check_mat(fmt, W2[e], hidden, inter, "W2")))
-            return rc;
-        if (!W1[e] || !W3[e] || !W2[e]) return fail(LQ_EINVAL, "expert %d weights null", e);
-    }
-    if (ntok == 0) return LQ_OK;
-    if ((long long)ntok * E * 4 > 48 * 1024) return fail(LQ_ESHAPE, "ntok * n_experts too large");
-    if ((rc = check_f32(router, "router")) || (rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y")))
-        return rc;
-    if ((topk_idx && !al(topk_idx, 4)) || (topk_w && !al(topk_w, 4)))
-        return fail(LQ_EALIGN, "topk outputs not 4-byte aligned");
-    const size_t need = lq_moe_workspace_bytes(E, topk, ntok, hidden, inter);
+    int rc = moe_validate(router, E, topk, norm_topk_prob, fmt, W1, W3, W2, hidden, inter, n_shared, Ws1, Ws3,
+                          Ws2, inter_s, shared_gate, X, Y, ntok, topk_idx, topk_w);
+    if (rc || ntok == 0) return rc;
+    const size_t need = lq_moe_ffn_ex_workspace_bytes(E, topk, ntok, hidden, inter, n_shared, inter_s);
     if (!workspace || ws_bytes < need)
         return fail(LQ_EWORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
     if (!al(workspace, 256)) return fail(LQ_EALIGN, "workspace not 256-byte aligned");
@@ -791,6 +877,7 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
     const size_t ns = (size_t)ntok * topk;
     uint8_t* p = static_cast<uint8_t*>(workspace);
     MoeWs ws;
+    memset(&ws, 0, sizeof ws);
     ws.idx = reinterpret_cast<int32_t*>(p); p += align256(ns * 4);
     ws.w = reinterpret_cast<float*>(p); p += align256(ns * 4);
     ws.tok_of = reinterpret_cast<int32_t*>(p); p += align256(ns * 4);
@@ -798,21 +885,61 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
     ws.grp_off = reinterpret_cast<int32_t*>(p); p += align256((size_t)E * 4);
     ws.grp_cnt = reinterpret_cast<int32_t*>(p); p += align256((size_t)E * 4);
     ws.hbuf = reinterpret_cast<float*>(p); p += align256(ns * inter * 4);
-    ws.ybuf = reinterpret_cast<float*>(p);
+    ws.ybuf = reinterpret_cast<float*>(p); p += align256(ns * hidden * 4);
+    if (n_shared > 0) {
+        ws.sgate = reinterpret_cast<float*>(p); p += align256((size_t)ntok * 4);
+        ws.hsh = reinterpret_cast<float*>(p); p += align256((size_t)n_shared * ntok * inter_s * 4);
+        ws.ysh = reinterpret_cast<float*>(p);
+        if (!shared_gate) ws.sgate = nullptr;
+    }
+    ws.nshared = n_shared;
+    ws.norm = norm_topk_prob;
     if (topk_idx) ws.idx = topk_idx;
     if (topk_w) ws.w = topk_w;
 
-    cudaError_t e = launch_moe_route(router, E, hidden, X, ntok, topk, ws, st);
+    cudaError_t e = launch_moe_route(router, E, hidden, X, ntok, topk, shared_gate, ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "moe route launch");
 
-    // grouped expert gate+up (+SwiGLU): segment per (expert, chunk of B rows)
-    // tensor-core path: Q4_K, both widths multiples of the tile, aligned rows
-    bool tc = ntok >= QMM_MOE_MIN_TOKENS && qmm_format_ok(fmt) && hidden % qmm_kc(fmt) == 0 &&
-              inter % qmm_kc(fmt) == 0 && al(X, 16);
-    for (int ex = 0; tc && ex < E; ++ex) tc = al(W1[ex], 16) && al(W3[ex], 16) && al(W2[ex], 16);
+    // Routed experts: one segment per (expert, chunk of B grouped rows), the
+    // row count read from the routing on the device.  Shared experts: dense
+    // segments over all tokens (chunks of B), in the same launch when they
+    // take the same kernel and (for down) the same width.
+    const bool tc = moe_tc_ok(fmt, ntok, hidden, inter, W1, W3, W2, E, X);
+    const bool tcs = n_shared > 0 && moe_tc_ok(fmt, ntok, hidden, inter_s, Ws1, Ws3, Ws2, n_shared, X);
+    auto shared_seg = [&](int ex, bool up, int b0, int nb) {
+        Seg s;
+        memset(&s, 0, sizeof s);
+        if (up) {
+            s.w = static_cast<const uint8_t*>(Ws1[ex]);
+            s.w2 = static_cast<const uint8_t*>(Ws3[ex]);
+            s.x = X;
+            s.y = ws.hsh + (int64_t)ex * ntok * inter_s;
+            s.ld_y = inter_s;
+            s.nout = (int32_t)inter_s;
+            s.mode = MODE_PAIR_TWO;
+            s.act = ACT_SWIGLU;
+        } else {
+            s.w = static_cast<const uint8_t*>(Ws2[ex]);
+            s.x = ws.hsh + (int64_t)ex * ntok * inter_s;
+            s.y = ws.ysh + (int64_t)ex * ntok * hidden;
+            s.ld_y = hidden;
+            s.nout = (int32_t)hidden;
+            s.mode = MODE_PLAIN;
+        }
+        s.fmt = fmt;
+        s.b0 = b0;
+        s.nbatch = nb;
+        return s;
+    };
+    auto run = [&](std::vector<Seg>& segs, bool t, int B, int64_t cols) {
+        if (segs.empty()) return (int)LQ_OK;
+        return t ? run_qmm(segs, cols, st) : run_segments(segs, B, cols, st);
+    };
+    // grouped expert gate+up (+SwiGLU)
     {
         const int B = tc ? QMM_NT : batch_width(hidden, ntok, {fmt}, true);
-        std::vector<Seg> segs;
+        const int Bs = tcs ? QMM_NT : batch_width(hidden, ntok, {fmt}, true);
+        std::vector<Seg> segs, ssegs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {
                 Seg s;
@@ -832,13 +959,16 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
                 s.b0 = c * B;
                 segs.push_back(s);
             }
-        rc = tc ? run_qmm(segs, hidden, st) : run_segments(segs, B, hidden, st);
-        if (rc) return rc;
+        std::vector<Seg>& dst = (tcs == tc && Bs == B) ? segs : ssegs;
+        for (int c = 0; c * Bs < ntok; ++c)
+            for (int ex = 0; ex < n_shared; ++ex) dst.push_back(shared_seg(ex, true, c * Bs, std::min(Bs, ntok - c * Bs)));
+        if ((rc = run(segs, tc, B, hidden)) || (rc = run(ssegs, tcs, Bs, hidden))) return rc;
     }
     // grouped expert down: x rows are the grouped hidden activations
     {
         const int B = tc ? QMM_NT : batch_width(inter, ntok, {fmt}, false);
-        std::vector<Seg> segs;
+        const int Bs = tcs ? QMM_NT : batch_width(inter_s, ntok, {fmt}, false);
+        std::vector<Seg> segs, ssegs;
         for (int c = 0; c * B < ntok; ++c)
             for (int ex = 0; ex < E; ++ex) {
                 Seg s;
@@ -855,20 +985,39 @@ int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const*
                 s.b0 = c * B;
                 segs.push_back(s);
             }
-        rc = tc ? run_qmm(segs, inter, st) : run_segments(segs, B, inter, st);
-        if (rc) return rc;
+        std::vector<Seg>& dst = (tcs == tc && Bs == B && inter_s == inter) ? segs : ssegs;
+        for (int c = 0; c * Bs < ntok; ++c)
+            for (int ex = 0; ex < n_shared; ++ex) dst.push_back(shared_seg(ex, false, c * Bs, std::min(Bs, ntok - c * Bs)));
+        if ((rc = run(segs, tc, B, inter)) || (rc = run(ssegs, tcs, Bs, inter_s))) return rc;
     }
     e = launch_moe_combine(ws.ybuf, hidden, ntok, topk, ws, Y, st);
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "moe combine launch");
 }
 
+int lq_moe_ffn(const float* router, int E, int topk, int fmt, const void* const* W1,
+               const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
+               const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
+               void* workspace, size_t ws_bytes, lq_stream_t stream) {
+    return lq_moe_ffn_ex(router, E, topk, 1, fmt, W1, W3, W2, hidden, inter, 0, nullptr, nullptr, nullptr, 0,
+                         nullptr, X, Y, ntok, topk_idx, topk_w, workspace, ws_bytes, stream);
+}
+
 // No-allocation variant: the scratch is a static device array of this
-// module, its address looked up once per device (with that device current).
+// module, its address looked up per device and context (with that device
+// current), again after a context change such as cudaDeviceReset.
 int lq_moe_ffn_static(const float* router, int E, int topk, int fmt, const void* const* W1,
                       const void* const* W3, const void* const* W2, int64_t hidden, int64_t inter,
                       const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
                       lq_stream_t stream) {
     g_err[0] = 0;
+    int rc = moe_validate(router, E, topk, 1, fmt, W1, W3, W2, hidden, inter, 0, nullptr, nullptr, nullptr, 0,
+                          nullptr, X, Y, ntok, topk_idx, topk_w);
+    if (rc) return rc;
+    const size_t need = lq_moe_workspace_bytes(E, topk, ntok, hidden, inter);
+    if (need > (size_t)LQ_MOE_STATIC_SCRATCH_BYTES)
+        return fail(LQ_EWORKSPACE, "MoE needs %zu bytes of scratch; the static scratch holds %zu", need,
+                    (size_t)LQ_MOE_STATIC_SCRATCH_BYTES);
+    if (ntok == 0) return LQ_OK;
     int d = 0;
     cudaError_t e = cudaGetDevice(&d);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -876,18 +1025,16 @@ int lq_moe_ffn_static(const float* router, int E, int topk, int fmt, const void*
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_moe_scratch_mu);
-        if (!g_moe_scratch_ptr[d]) {
+        const unsigned long long ctx = current_ctx_id();
+        if (!g_moe_scratch_ptr[d] || ctx == 0 || ctx != g_moe_scratch_ctx[d]) {
             void* ptr = nullptr;
             e = cudaGetSymbolAddress(&ptr, g_moe_scratch);
             if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static MoE scratch)");
             g_moe_scratch_ptr[d] = ptr;
+            g_moe_scratch_ctx[d] = current_ctx_id();
         }
         scratch = g_moe_scratch_ptr[d];
     }
-    const size_t need = lq_moe_workspace_bytes(E, topk, ntok, hidden, inter);
-    if (need > (size_t)LQ_MOE_STATIC_SCRATCH_BYTES)
-        return fail(LQ_EWORKSPACE, "MoE needs %zu bytes of scratch; the static scratch holds %zu", need,
-                    (size_t)LQ_MOE_STATIC_SCRATCH_BYTES);
     return lq_moe_ffn(router, E, topk, fmt, W1, W3, W2, hidden, inter, X, Y, ntok, topk_idx, topk_w,
                       scratch, (size_t)LQ_MOE_STATIC_SCRATCH_BYTES, stream);
 }
@@ -897,8 +1044,9 @@ int lq_device_status(lq_stream_t stream, uint32_t* bits) {
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    (void)stream;
+    cudaError_t e = cudaDeviceSynchronize();     // the word is shared by every stream's launches
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     unsigned v = 0;
     e = cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "read status");

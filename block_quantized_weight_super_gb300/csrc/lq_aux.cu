@@ -197,22 +197,36 @@ __global__ void direct_mv_kernel(Seg S, int64_t cols, int maxb) {
 // One CTA: router logits (one warp per (token, expert) dot product,
 // deterministic), softmax over the experts, top-k by repeated maximum with
 // the lower index winning ties, weights renormalised by the selected sum
-// (dotLLM PR #320, MoE commit).  Then groups the (token, slot) pairs by
-// expert in token order.
+// (dotLLM PR #320, MoE commit) or, with ws.norm = 0, the selected softmax
+// probabilities as they are (norm_topk_prob = false, the Qwen-MoE commit).
+// With a shared-expert gate vector g, also sgate[t] = sigmoid(g . x_t), one
+// warp per token.  Then groups the (token, slot) pairs by expert in token
+// order.
+__device__ __forceinline__ float warp_dot(const float* __restrict__ a, const float* __restrict__ b, int64_t n,
+                                          int lane) {
+    float acc = 0.f;
+    for (int64_t j = lane; j < n; j += 32) acc = fmaf(__ldg(a + j), __ldg(b + j), acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    return acc;
+}
+
 __global__ void moe_route_kernel(const float* __restrict__ R, int E, int64_t hidden,
-                                 const float* __restrict__ X, int ntok, int topk, MoeWs ws) {
+                                 const float* __restrict__ X, int ntok, int topk,
+                                 const float* __restrict__ gvec, MoeWs ws) {
     extern __shared__ float sh[];
     float* logits = sh;                          // ntok * E
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int p = warp; p < ntok * E; p += nw) {
         const int t = p / E, e = p % E;
-        const float* xr = X + (int64_t)t * hidden;
-        const float* rr = R + (int64_t)e * hidden;
-        float acc = 0.f;
-        for (int64_t j = lane; j < hidden; j += 32) acc = fmaf(__ldg(rr + j), __ldg(xr + j), acc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        const float acc = warp_dot(R + (int64_t)e * hidden, X + (int64_t)t * hidden, hidden, lane);
         if (lane == 0) logits[p] = acc;
+    }
+    if (gvec) {
+        for (int t = warp; t < ntok; t += nw) {
+            const float z = warp_dot(gvec, X + (int64_t)t * hidden, hidden, lane);
+            if (lane == 0) ws.sgate[t] = 1.0f / (1.0f + expf(-z));
+        }
     }
     __syncthreads();
     for (int t = threadIdx.x; t < ntok; t += blockDim.x) {
@@ -239,7 +253,8 @@ __global__ void moe_route_kernel(const float* __restrict__ R, int E, int64_t hid
             ws.w[t * topk + k] = bp;
             sel += bp;
         }
-        for (int k = 0; k < topk; ++k) ws.w[t * topk + k] = ws.w[t * topk + k] / sel;
+        if (ws.norm)
+            for (int k = 0; k < topk; ++k) ws.w[t * topk + k] = ws.w[t * topk + k] / sel;
     }
     __syncthreads();
     // grouping: expert e's slots in token order (single thread: ntok*topk small)
@@ -260,9 +275,11 @@ __global__ void moe_route_kernel(const float* __restrict__ R, int E, int64_t hid
     }
 }
 
-// Y[t] = sum_k w[t][k] * ye[row of (t,k)], k in order.
+// Y[t] = sum_k w[t][k] * ye[row of (t,k)], k in order, plus the shared
+// experts' outputs summed in expert order and scaled by the gate (sgate[t],
+// or 1 without a gate vector).
 __global__ void moe_combine_kernel(const float* __restrict__ ye, int64_t hidden, int ntok,
-                                   int topk, MoeWs ws, float* __restrict__ Y) {
+                                   int topk, MoeWs ws, bool gated, float* __restrict__ Y) {
     const int64_t total = (int64_t)ntok * hidden;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -272,6 +289,11 @@ __global__ void moe_combine_kernel(const float* __restrict__ ye, int64_t hidden,
         for (int k = 0; k < topk; ++k) {
             const int s = t * topk + k;
             acc = fmaf(ws.w[s], ye[(int64_t)ws.slot_row[s] * hidden + o], acc);
+        }
+        if (ws.nshared > 0) {
+            float sum = 0.f;
+            for (int e = 0; e < ws.nshared; ++e) sum += ws.ysh[((int64_t)e * ntok + t) * hidden + o];
+            acc = gated ? fmaf(ws.sgate[t], sum, acc) : acc + sum;
         }
         Y[i] = acc;
     }
@@ -323,9 +345,9 @@ cudaError_t launch_direct(const Seg& S, int64_t cols, int maxb, cudaStream_t st)
 }
 
 cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float* X, int ntok,
-                             int topk, const MoeWs& ws, cudaStream_t st) {
+                             int topk, const float* sgate_vec, const MoeWs& ws, cudaStream_t st) {
     const size_t smem = (size_t)ntok * E * sizeof(float);
-    moe_route_kernel<<<1, 1024, smem, st>>>(R, E, hidden, X, ntok, topk, ws);
+    moe_route_kernel<<<1, 1024, smem, st>>>(R, E, hidden, X, ntok, topk, sgate_vec, ws);
     return cudaGetLastError();
 }
 
@@ -334,7 +356,7 @@ cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int to
     const int64_t n = (int64_t)ntok * hidden;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    moe_combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(ye, hidden, ntok, topk, ws, Y);
+    moe_combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(ye, hidden, ntok, topk, ws, ws.sgate != nullptr, Y);
     return cudaGetLastError();
 }
 

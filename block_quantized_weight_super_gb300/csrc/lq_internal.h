@@ -18,6 +18,11 @@ struct MoeWs {
     int32_t* grp_cnt;    // [E] grouped rows of each expert
     float* hbuf;         // [ntok*topk][inter] expert hidden activations
     float* ybuf;         // [ntok*topk][hidden] expert outputs
+    float* sgate;        // [ntok] shared-expert gate sigmoid(g . x_t) (when a gate vector is given)
+    float* hsh;          // [nshared][ntok][inter_s] shared-expert hidden activations
+    float* ysh;          // [nshared][ntok][hidden] shared-expert outputs
+    int32_t nshared;
+    int32_t norm;        // 1: weights renormalised by the selected sum; 0: raw softmax probabilities
 };
 
 // tensor-core matvec for up to QMM_NT x rows of Q4_K or Q8_0 (lq_qmm.cu):
@@ -120,7 +125,7 @@ cudaError_t launch_interleave(const uint8_t* Wg, const uint8_t* Wu, int64_t rows
                               uint8_t* out, cudaStream_t st);
 cudaError_t launch_direct(const Seg& S, int64_t cols, int maxb, cudaStream_t st);
 cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float* X, int ntok,
-                             int topk, const MoeWs& ws, cudaStream_t st);
+                             int topk, const float* sgate_vec, const MoeWs& ws, cudaStream_t st);
 cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int topk,
                                const MoeWs& ws, float* Y, cudaStream_t st);
 cudaError_t launch_timeout_probe(uint64_t timeout_ns, unsigned* status, cudaStream_t st);

@@ -151,6 +151,35 @@ int lq_moe_ffn(const float* router, int n_experts, int topk, int fmt, const void
                const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
                void* workspace, size_t ws_bytes, lq_stream_t stream);
 
+/* lq_moe_ffn_ex -- lq_moe_ffn with the MoE variants of dotLLM PR #320 (the
+ * Qwen-MoE commit and its N-shared-experts follow-up):
+ *   norm_topk_prob: 1 renormalises the selected weights by their sum (the
+ *     lq_moe_ffn rule); 0 keeps the selected softmax probabilities p_e as
+ *     they are (norm_topk_prob = false).
+ *   n_shared (0..LQ_MOE_MAX_SHARED) shared experts, dense SwiGLU FFNs that
+ *     every token passes through: Ws1 (gate), Ws3 (up): inter_s x hidden,
+ *     Ws2 (down): hidden x inter_s, format fmt; HOST arrays of n_shared device
+ *     pointers (NULL when n_shared == 0).  Their outputs are summed in expert
+ *     order and added to the routed sum:
+ *       Y_t = sum_k w_tk * E_k(x_t) + gate_t * sum_s S_s(x_t)
+ *   shared_gate: optional [hidden] fp32 vector g; gate_t = sigmoid(g . x_t)
+ *     scales the sum of the shared experts (NULL: gate_t = 1).  A gate
+ *     without shared experts -> LQ_EINVAL.
+ * The shared experts run as extra dense segments of the grouped gate/up and
+ * down launches (in the same launch when they take the same kernel and, for
+ * down, the same width); the gate is computed in the routing launch and
+ * applied in the combine.  workspace: lq_moe_ffn_ex_workspace_bytes bytes,
+ * 256-byte aligned.  Other arguments, outputs and errors as lq_moe_ffn. */
+#define LQ_MOE_MAX_SHARED 16
+size_t lq_moe_ffn_ex_workspace_bytes(int n_experts, int topk, int ntok, int64_t hidden, int64_t inter,
+                                     int n_shared, int64_t inter_s);
+int lq_moe_ffn_ex(const float* router, int n_experts, int topk, int norm_topk_prob, int fmt,
+                  const void* const* W1, const void* const* W3, const void* const* W2, int64_t hidden,
+                  int64_t inter, int n_shared, const void* const* Ws1, const void* const* Ws3,
+                  const void* const* Ws2, int64_t inter_s, const float* shared_gate, const float* X, float* Y,
+                  int ntok, int32_t* topk_idx, float* topk_w, void* workspace, size_t ws_bytes,
+                  lq_stream_t stream);
+
 /* lq_moe_ffn_static -- lq_moe_ffn without a caller-supplied workspace: the
  * scratch is a static device array of LQ_MOE_STATIC_SCRATCH_BYTES (4 MiB)
  * inside the library, one per device, and the call allocates no device
@@ -165,7 +194,10 @@ int lq_moe_ffn(const float* router, int n_experts, int topk, int fmt, const void
  * hidden 4096, inter 14336 fit up to ntok * topk = 56).
  *   The first call on a device does the set-up (looks up the scratch
  * address with that device current) and returns LQ_ECUDA if that fails;
- * make it before any stream capture.  No part of the scratch needs to start
+ * make it before any stream capture.  The address is kept per device and
+ * CUDA context: after cudaDeviceReset the next call looks it up again.
+ * Arguments are validated before the size check (LQ_EINVAL, LQ_ESHAPE,
+ * LQ_EALIGN come before LQ_EWORKSPACE).  No part of the scratch needs to start
  * at zero: every word a call reads was written earlier in the same call.
  * All calls on a device share the one scratch: calls that overlap in time
  * (on different streams, or from different host threads without ordering)
@@ -176,10 +208,13 @@ int lq_moe_ffn_static(const float* router, int n_experts, int topk, int fmt, con
                       const float* X, float* Y, int ntok, int32_t* topk_idx, float* topk_w,
                       lq_stream_t stream);
 
-/* lq_device_status -- synchronises `stream`, then reads and clears the
- * device status word that kernels set when a bounded wait runs out.
- * *bits = the word (0 = clean).  Returns LQ_ETIMEOUT if the timeout bit was
- * set, LQ_OK otherwise (LQ_ECUDA on a CUDA error). */
+/* lq_device_status -- waits for all work on the current device (every
+ * stream: the status word is one per device, shared by every launch of the
+ * library, so a bit set by a launch on another stream is reported here
+ * too), then reads and clears the word that kernels set when a bounded wait
+ * runs out.  *bits = the word (0 = clean).  Returns LQ_ETIMEOUT if the
+ * timeout bit was set, LQ_OK otherwise (LQ_ECUDA on a CUDA error).  `stream`
+ * is accepted for symmetry with the other calls; the wait covers it. */
 int lq_device_status(lq_stream_t stream, uint32_t* bits);
 
 /* lq_set_wait_timeout_ns -- wall-time limit of every bounded wait in later

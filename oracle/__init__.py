@@ -299,7 +299,7 @@ def gate_up_bound(g, u, Sg, Su, act: int):
 
 
 def moe_check(fmt: int, W1, W3, W2, hidden: int, inter: int, X, logits, labs, idx_gpu,
-              nthreads: int = 1):
+              nthreads: int = 1, norm: bool = True):
     """Oracle result and per-element bound for the MoE evaluated on the GPU's
     expert selection idx_gpu [ntok][topk].
 
@@ -307,7 +307,11 @@ def moe_check(fmt: int, W1, W3, W2, hidden: int, inter: int, X, logits, labs, id
     admissible (bool per token: the selection is a valid top-k within the
     logits' error e_l = 1e-5*sum|R x| + 1e-6).
     Bound per output: sum_k w_k B_y,k + |y_k| (2 w_k e_lmax + 8 u32 w_k), with
-    B_y = 1e-5 Sy + 1e-6 + sum_j |w2_ij| B_h,j and B_h the gate/up bound."""
+    B_y = 1e-5 Sy + 1e-6 + sum_j |w2_ij| B_h,j and B_h the gate/up bound.
+    norm: renormalised weights (True) or the raw selected softmax
+    probabilities (False); either way log w_k moves by at most 2 e_lmax when
+    the logits move by e_l (|d log p_k| <= |d l_k| + max |d l|), so the
+    same bound holds."""
     idx_gpu = np.ascontiguousarray(idx_gpu, dtype=np.int32)
     ntok, topk = idx_gpu.shape
     E = logits.shape[1]
@@ -320,7 +324,7 @@ def moe_check(fmt: int, W1, W3, W2, hidden: int, inter: int, X, logits, labs, id
         rest = [e for e in range(E) if e not in sel]
         ok = all(logits[t, a] + el[t, a] >= logits[t, b] - el[t, b] for a in sel for b in rest)
         adm[t] = ok
-    w = moe_weights(logits, idx_gpu)
+    w = moe_weights(logits, idx_gpu, norm)
     out = moe_ffn(fmt, W1, W3, W2, hidden, inter, X, idx_gpu, w, nthreads)
     Bh = gate_up_bound(out["g"], out["u"], out["Sg"], out["Su"], ACT_SWIGLU)
     bound = np.zeros((ntok, hidden))

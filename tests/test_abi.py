@@ -176,3 +176,49 @@ def test_moe_validation(lq):
     assert args(2, 1, 4, None, need) == lq.LQ_EWORKSPACE
     assert args(2, 1, 4, FAKE + 16, need) == lq.LQ_EALIGN    # workspace 256-aligned
     assert args(2, 1, 0, FAKE, need) == lq.LQ_OK            # no tokens: no launch
+
+
+def test_moe_ex_validation(lq):
+    """The MoE variants' arguments are checked on the host before the
+    workspace: shared-expert arrays, their width, the gate without shared
+    experts, the weighting flag."""
+    L = lq.lib()
+    P = C.c_void_p * 2
+    w = P(FAKE, FAKE)
+    wp = C.cast(w, C.c_void_p)
+    need = lq.lq_moe_ffn_ex_workspace_bytes(2, 1, 4, 256, 256, 2, 512)
+    assert need > lq.lq_moe_workspace_bytes(2, 1, 4, 256, 256)
+    assert lq.lq_moe_ffn_ex_workspace_bytes(2, 1, 4, 256, 256, 0, 0) == lq.lq_moe_workspace_bytes(2, 1, 4, 256, 256)
+    assert lq.lq_moe_ffn_ex_workspace_bytes(2, 1, 4, 256, 256, -1, 0) == 0
+
+    def ex(norm=1, ns=2, s1=wp, s3=wp, s2=wp, inter_s=512, gate=FAKE, ws=FAKE, wsb=need, ntok=4):
+        return L.lq_moe_ffn_ex(FAKE, 2, 1, norm, 1, wp, wp, wp, 256, 256, ns, s1, s3, s2, inter_s, gate,
+                               FAKE, FAKE, ntok, None, None, ws, wsb, None)
+    assert ex(norm=2) == lq.LQ_EINVAL
+    assert ex(ns=-1) == lq.LQ_EINVAL
+    assert ex(ns=lq.LQ_MOE_MAX_SHARED + 1) == lq.LQ_EINVAL
+    assert ex(s1=None) == lq.LQ_EINVAL
+    assert ex(s2=None) == lq.LQ_EINVAL
+    assert ex(inter_s=500) == lq.LQ_ESHAPE              # not a multiple of the Q4_K block
+    assert ex(ns=0, gate=FAKE) == lq.LQ_EINVAL          # a gate without shared experts
+    assert ex(gate=FAKE + 2) == lq.LQ_EALIGN
+    assert ex(wsb=need - 1) == lq.LQ_EWORKSPACE
+    assert ex(ws=FAKE + 16) == lq.LQ_EALIGN
+    assert ex(ntok=0, ws=None, wsb=0) == lq.LQ_OK        # no tokens: nothing checked past the shapes, no launch
+
+
+def test_moe_static_validates_before_the_scratch_size(lq):
+    """Invalid arguments are reported as such even when the shape would also
+    exceed the static scratch (argument errors come first)."""
+    L = lq.lib()
+    P = C.c_void_p * 2
+    w = P(FAKE, FAKE)
+    wp = C.cast(w, C.c_void_p)
+    st = lambda E, k, fmt, hidden, inter, ntok, x=FAKE: L.lq_moe_ffn_static(
+        FAKE, E, k, fmt, wp, wp, wp, hidden, inter, x, FAKE, ntok, None, None, None)
+    big = 4096                                          # 2 experts x 4096 tokens: far over 4 MiB
+    assert st(2, 3, 1, 4096, 14336, big) == lq.LQ_EINVAL     # topk > n_experts
+    assert st(2, 1, 9, 4096, 14336, big) == lq.LQ_EINVAL     # unknown format
+    assert st(2, 1, 1, 4096, 14300, big) == lq.LQ_ESHAPE     # inter not a block multiple
+    assert st(2, 1, 1, 4096, 14336, 8, x=FAKE + 2) == lq.LQ_EALIGN
+    assert st(2, 1, 1, 4096, 14336, 1000) == lq.LQ_EWORKSPACE

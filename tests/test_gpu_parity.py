@@ -572,6 +572,103 @@ def test_moe_one_hot_router_is_single_expert(lq):
     assert_within(Y, ref, chk["bound"], "one-hot router")
 
 
+# ---------------------------------------------------------------- MoE variants
+
+def _shared_check(fmt, Ws1, Ws3, Ws2, hidden, inter_s, X, gvec):
+    """The oracle's shared-expert branch gate_t * sum_s S_s(x_t) and a
+    per-element bound for the GPU's: each expert carries the composite
+    down-after-activation bound (as a routed expert with weight 1); the gate
+    sigmoid(g . x) moves by at most 1/4 of its argument's matvec bound plus
+    fp32 rounding; the fp32 sum over n experts and the final fma add
+    (n + 8) u32 of the magnitudes."""
+    n, ntok = len(Ws1), X.shape[0]
+    idx = np.tile(np.arange(n, dtype=np.int32), (ntok, 1))
+    out = oracle.moe_ffn(fmt, Ws1, Ws3, Ws2, hidden, inter_s, X, idx, np.ones((ntok, n)), NTH)
+    S, gs = oracle.moe_shared(fmt, Ws1, Ws3, Ws2, hidden, inter_s, X, gate=gvec, nthreads=NTH)
+    # the two oracle routines agree: the shared branch is the gate times the
+    # sum of the experts taken with weight 1
+    assert np.allclose(S, gs[:, None] * out["Y"], rtol=1e-12, atol=1e-300)
+    Bh = oracle.gate_up_bound(out["g"], out["u"], out["Sg"], out["Su"], oracle.ACT_SWIGLU)
+    B = np.zeros((ntok, hidden))
+    for t in range(ntok):
+        for e in range(n):
+            sl = t * n + e
+            B[t] += 1e-5 * out["Sy"][sl] + 1e-6 + oracle.abs_matvec(fmt, Ws2[e], hidden, inter_s, Bh[sl], NTH)
+    if gvec is None:
+        eg = np.zeros(ntok)
+    else:
+        Sz = np.abs(X.astype(np.float64)) @ np.abs(gvec.astype(np.float64))
+        eg = 0.25 * oracle.matvec_bound(Sz) + 4 * oracle.U32 * gs
+    mag = np.abs(out["ye"]).reshape(ntok, n, hidden).sum(axis=1) + B
+    bound = gs[:, None] * B + eg[:, None] * mag + (n + 8) * oracle.U32 * gs[:, None] * mag
+    return S, bound
+
+
+@pytest.mark.parametrize("E,topk,ntok,norm,nsh,inter_s,gate,ident,fmt,hidden,inter", [
+    (4, 2, 5, 0, 0, 0, None, False, Q4_K, 256, 512),        # raw softmax weights only
+    (8, 2, 16, 0, 1, 1024, "rand", False, Q4_K, 512, 1024),  # raw + one gated shared expert (tensor cores)
+    (4, 2, 6, 1, 2, 1024, "rand", False, Q4_K, 512, 1024),   # two shared, down in the routed launch
+    (4, 2, 6, 1, 2, 512, "rand", True, Q4_K, 256, 512),      # two identical shared experts
+    (4, 2, 6, 1, 2, 768, "zero", False, Q4_K, 256, 512),     # zero gate vector: gate 1/2
+    (6, 3, 9, 1, 2, 768, None, False, Q4_K, 256, 512),       # shared experts without a gate
+    (4, 1, 1, 0, 1, 512, "rand", False, Q4_K, 256, 512),     # one token (batch-1 kernels)
+    (4, 2, 10, 1, 1, 1024, "rand", False, Q8_0, 512, 1024),  # Q8_0
+    (4, 2, 7, 1, 2, 512, "neg", False, Q4_K, 256, 512),      # gate driven to 0: the routed sum alone
+])
+def test_moe_variants(lq, E, topk, ntok, norm, nsh, inter_s, gate, ident, fmt, hidden, inter):
+    """lq_moe_ffn_ex against the oracle: routed part by moe_check (raw or
+    renormalised weights), shared part by moe_shared, bounds added."""
+    seed = E * 100 + ntok * 7 + nsh
+    R, W1, W3, W2, X = _moe_inputs(E, hidden, inter, ntok, seed=seed)
+    g = synth.rng(seed + 1)
+    if fmt != Q4_K:
+        W1 = [synth.weights(g, fmt, inter, hidden) for _ in range(E)]
+        W3 = [synth.weights(g, fmt, inter, hidden) for _ in range(E)]
+        W2 = [synth.weights(g, fmt, hidden, inter) for _ in range(E)]
+    Ws1 = [synth.weights(g, fmt, inter_s, hidden) for _ in range(nsh)]
+    Ws3 = [synth.weights(g, fmt, inter_s, hidden) for _ in range(nsh)]
+    Ws2 = [synth.weights(g, fmt, hidden, inter_s) for _ in range(nsh)]
+    if ident:
+        Ws1, Ws3, Ws2 = [Ws1[0]] * nsh, [Ws3[0]] * nsh, [Ws2[0]] * nsh
+    gvec = None
+    if gate == "rand":
+        gvec = synth.router(g, 1, hidden, std=0.05)[0]
+    elif gate == "zero":
+        gvec = np.zeros(hidden, np.float32)
+    elif gate == "neg":
+        # g . x_t = -200 for every token (least-norm solution): sigmoid -> 0
+        X64 = X.astype(np.float64)
+        gvec = (X64.T @ np.linalg.solve(X64 @ X64.T, np.full(ntok, -200.0))).astype(np.float32)
+        assert (X64 @ gvec.astype(np.float64) < -150).all()
+    Y = empty((ntok, hidden))
+    idx = torch.full((ntok, topk), -1, dtype=torch.int32, device="cuda")
+    w = empty((ntok, topk))
+    nb = lq.lq_moe_ffn_ex_workspace_bytes(E, topk, ntok, hidden, inter, nsh, inter_s)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    lq.lq_moe_ffn_ex(dev(R), E, topk, norm, fmt, [dev(a) for a in W1], [dev(a) for a in W3], [dev(a) for a in W2],
+                     hidden, inter, dev(X), Y, ntok, Ws1=[dev(a) for a in Ws1], Ws3=[dev(a) for a in Ws3],
+                     Ws2=[dev(a) for a in Ws2], inter_s=inter_s, shared_gate=None if gvec is None else dev(gvec),
+                     topk_idx=idx, topk_w=w, workspace=ws, ws_bytes=nb)
+    Yg, ig, wg = host(Y), host(idx), host(w)
+    _, _, lg, labs = oracle.moe_route(R, X, topk)
+    chk = oracle.moe_check(fmt, W1, W3, W2, hidden, inter, X, lg, labs, ig, NTH, norm=bool(norm))
+    assert chk["admissible"].all()
+    elmax = chk["el"].max(axis=1, keepdims=True)
+    assert_within(wg, chk["w"], 2 * chk["w"] * elmax + 8 * oracle.U32, "moe weights")
+    if not norm:
+        assert (wg.sum(axis=1) < 1 + 1e-6).all()          # raw probabilities of a subset
+    ref, bound = chk["Y"], chk["bound"]
+    if nsh:
+        S, sb = _shared_check(fmt, Ws1, Ws3, Ws2, hidden, inter_s, X, gvec)
+        if gate == "zero":
+            assert np.array_equal(oracle.moe_shared(fmt, Ws1[:1], Ws3[:1], Ws2[:1], hidden, inter_s, X[:1],
+                                                    gate=gvec)[1], [0.5])
+        if gate == "neg":
+            assert np.abs(S).max() < 1e-30
+        ref, bound = ref + S, bound + sb
+    assert_within(Yg, ref, bound, "moe variant Y")
+
+
 # ---------------------------------------------------------------- failure detection
 
 def test_bounded_wait_times_out_and_reports(lq):

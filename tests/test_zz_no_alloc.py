@@ -81,3 +81,91 @@ def test_static_scratch_rejects_oversized_shapes(lq):
         lq.lq_moe_ffn_static(R, E, topk, Q4_K, W, W, W2, hidden, inter, X, Y, ntok)
     assert ei.value.status == lq.LQ_EWORKSPACE
     assert "static scratch" in lq.lq_last_error()
+
+
+def _static_args(lq, case, topk, E, hidden, inter):
+    R, W1, W3, W2, X = case
+    ntok = X.shape[0]
+    d = {"R": dev(R), "W1": [dev(a) for a in W1], "W3": [dev(a) for a in W3], "W2": [dev(a) for a in W2],
+         "X": dev(X), "Y": empty((ntok, hidden)), "idx": torch.full((ntok, topk), -1, dtype=torch.int32, device="cuda"),
+         "w": empty((ntok, topk)), "ntok": ntok}
+    return d
+
+
+def _static(lq, d, topk, E, hidden, inter, stream=None):
+    lq.lq_moe_ffn_static(d["R"], E, topk, Q4_K, d["W1"], d["W3"], d["W2"], hidden, inter, d["X"], d["Y"],
+                         d["ntok"], d["idx"], d["w"], stream=stream)
+
+
+def _workspace(lq, d, topk, E, hidden, inter):
+    nbytes = lq.lq_moe_workspace_bytes(E, topk, d["ntok"], hidden, inter)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    Y = empty((d["ntok"], hidden))
+    lq.lq_moe_ffn(d["R"], E, topk, Q4_K, d["W1"], d["W3"], d["W2"], hidden, inter, d["X"], Y, d["ntok"], None, None,
+                  ws, nbytes)
+    return host(Y)
+
+
+def test_static_back_to_back_shapes_one_stream(lq):
+    """Two static calls of different shapes queued on one stream with no
+    synchronisation between them (the scratch is reused in stream order),
+    each equal to the workspace entry point's result bit for bit (same
+    kernels, same scratch layout)."""
+    E, topk, hidden, inter = 8, 2, 256, 512
+    a = _static_args(lq, _case(81, E, topk, 6, hidden, inter), topk, E, hidden, inter)
+    b = _static_args(lq, _case(82, E, topk, 13, hidden, inter), topk, E, hidden, inter)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        _static(lq, a, topk, E, hidden, inter, st)
+        _static(lq, b, topk, E, hidden, inter, st)
+    st.synchronize()
+    for d in (a, b):
+        assert np.array_equal(host(d["Y"]), _workspace(lq, d, topk, E, hidden, inter))
+
+
+def test_static_near_the_scratch_limit(lq):
+    """hidden 4096, inter 14336 at 56 routed rows (two experts, top-2, 28
+    tokens): 4,130,304 of the 4,194,304 scratch bytes.  Equal to the
+    workspace entry point bit for bit; three tokens checked against the
+    oracle."""
+    E, topk, ntok, hidden, inter = 2, 2, 28, 4096, 14336
+    need = lq.lq_moe_workspace_bytes(E, topk, ntok, hidden, inter)
+    assert lq.LQ_MOE_STATIC_SCRATCH_BYTES - 65536 < need <= lq.LQ_MOE_STATIC_SCRATCH_BYTES
+    case = _case(83, E, topk, ntok, hidden, inter)
+    d = _static_args(lq, case, topk, E, hidden, inter)
+    _static(lq, d, topk, E, hidden, inter)
+    Ys = host(d["Y"])
+    assert np.array_equal(Ys, _workspace(lq, d, topk, E, hidden, inter))
+    R, W1, W3, W2, X = case
+    for t in (0, 13, ntok - 1):
+        _, _, lg, labs = oracle.moe_route(R, X[t:t + 1], topk)
+        chk = oracle.moe_check(Q4_K, W1, W3, W2, hidden, inter, X[t:t + 1], lg, labs, host(d["idx"])[t:t + 1], NTH)
+        assert_within(Ys[t:t + 1], chk["Y"], chk["bound"], f"near-limit token {t}")
+
+
+def test_static_call_captures_in_a_graph_without_allocating(lq):
+    """After a first (set-up) call, a static call captures into a CUDA graph
+    under the global capture mode (any allocation during capture would fail
+    the capture) and an eager static call leaves the device's free memory
+    unchanged; the graph's replay equals the eager result bit for bit."""
+    E, topk, hidden, inter = 4, 2, 256, 512
+    d = _static_args(lq, _case(84, E, topk, 9, hidden, inter), topk, E, hidden, inter)
+    _static(lq, d, topk, E, hidden, inter)          # set-up call
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    _static(lq, d, topk, E, hidden, inter)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    ref = host(d["Y"]).copy()
+    d["Y"].fill_(float("nan"))
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st, capture_error_mode="global"):
+        _static(lq, d, topk, E, hidden, inter, st)
+    torch.cuda.synchronize()
+    assert np.isnan(host(d["Y"])).all()              # capture ran nothing
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host(d["Y"]), ref)
