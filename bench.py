@@ -23,7 +23,9 @@ the host time spent inside the API calls.
 Besides the layer, the default line carries per-launch figures of the
 layer's four calls and of the other named workloads (`configs`): a 256 x 2560
 Q4_K matvec, the Llama-3-8B FFN in Q4_K and Q8_0 at batch 1, 2, 4, 8, the
-262144 x 2560 Q4_K lm_head and the Mixtral MoE FFN.
+262144 x 2560 Q4_K lm_head with its fp16 / fp32 fallbacks, and the Mixtral
+MoE FFN; `fusions` compares the fused input norm and activated down input
+with the same work unfused.
 
 --impl reference runs the CPU oracle (fp64, all host cores) on the layer:
 each step is every row of every matrix of one layer copy; the repo arm's
@@ -318,8 +320,50 @@ def bench_lq(args, ws, rank, local, peak):
         calls[name] = {"us": t * 1e3, "alg_bytes": nb, "GB_s": nb / (t * 1e-3) / 1e9,
                        "frac": nb / (t * 1e-3) / 1e9 / peak}
 
+    fusions = None if args.no_configs else fusion_figures(lay, layers, max(n, args.steps), 3 * n, st, dev)
     e2e = None if args.no_e2e else bench_e2e(args, ws, dev, st, lay, layers, x0, barrier)
-    return ms_all, calls, clk.summary(), e2e, hl
+    return ms_all, calls, fusions, clk.summary(), e2e, hl
+
+
+def fusion_figures(lay, layers, steps, warmup, st, dev):
+    """us per layer copy of the fused input norm and activated down input
+    against the same work unfused, on the layer's shapes (rotating copies):
+    qkv_rmsnorm: lq_qkv_mixed_rmsnorm vs lq_rmsnorm + lq_qkv_mixed;
+    ffn_act: lq_matvec over the packed gate/up rows + lq_matvec_act (the
+    activation on down's x-load) vs lq_ffn_gate_up_act + lq_matvec (the
+    activation in gate+up's store, the layer's form)."""
+    import torch
+    import block_quantized_weight_super_gb300 as lq
+    import synth
+    g = synth.rng(99)
+    nw = torch.from_numpy((1.0 + 0.25 * g.standard_normal(H_)).astype(np.float32)).to(dev)
+    xn = torch.empty((1, H_), dtype=torch.float32, device=dev)
+    gu = torch.empty((1, 2 * I_), dtype=torch.float32, device=dev)
+    eps = 1e-6
+
+    def qkv_fused(w, s):
+        lq.lq_qkv_mixed_rmsnorm(lq.LQ_Q4_K, w["wq"], NQ_, lq.LQ_Q4_K, w["wk"], NKV_, lq.LQ_Q6_K, w["wv"], NKV_, H_,
+                                lay.x, nw, eps, xn, lay.q, lay.k, lay.v, 1, s)
+
+    def qkv_unfused(w, s):
+        lq.lq_rmsnorm(lay.x, nw, eps, xn, 1, H_, s)
+        lay.call("qkv", w, s, x=xn)
+
+    def ffn_act_down(w, s):
+        lq.lq_matvec(lq.LQ_Q4_K, w["wgu"], 2 * I_, H_, lay.o, gu, 1, s)
+        lq.lq_matvec_act(lq.LQ_Q6_K, w["wd"], H_, I_, gu, lay.h, lay.y, 1, lq.LQ_ACT_GEGLU_TANH, s)
+
+    def ffn_act_gateup(w, s):
+        lay.call("gateup", w, s)
+        lay.call("down", w, s)
+
+    out = {}
+    for name, fn in (("qkv_rmsnorm_fused", qkv_fused), ("qkv_rmsnorm_unfused", qkv_unfused),
+                     ("ffn_act_on_down_load", ffn_act_down), ("ffn_act_in_gate_up", ffn_act_gateup)):
+        out[name] = {"us": timed_graphs(fn, layers, steps, warmup, st) * 1e3}
+    out["launches"] = {"qkv_rmsnorm_fused": 1, "qkv_rmsnorm_unfused": 2, "ffn_act_on_down_load": 2,
+                       "ffn_act_in_gate_up": 2}
+    return out
 
 
 def bench_e2e(args, ws, dev, st, lay, layers, x0, barrier):
@@ -739,6 +783,16 @@ def config_figures(dev, peak):
     out["lm_head_q4k_262144x2560_b1"] = fig(ms, W.nbytes, 1)
     del wd
     torch.cuda.empty_cache()
+    # the non-quantized lm_head fallbacks of the same shape (fp16, fp32 weights;
+    # seeded device-side draws: the values do not change the time)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    for dt, name, f in ((torch.float16, "f16", lq.lq_gemv_f16), (torch.float32, "f32", lq.lq_gemv_f32)):
+        Wt = (0.05 * torch.randn((W.shape[0], 2560), generator=gen, device=dev, dtype=torch.float32)).to(dt)
+        ms = timed_graphs(lambda w, s, f=f: f(w, w.shape[0], 2560, xd, yd, 1, s), [Wt], 40, 5, st)
+        out[f"lm_head_{name}_262144x2560_b1"] = fig(ms, Wt.numel() * Wt.element_size(), 1)
+        del Wt
+        torch.cuda.empty_cache()
 
     # config 4: Mixtral MoE FFN, 8 experts, top-2, 16 tokens, Q4_K
     R, W1, W3, W2, X = synth.mixtral_moe(0)
@@ -802,7 +856,7 @@ def main():
         print(json.dumps(line))
         return
 
-    ms, calls, clocks, e2e, hl = bench_lq(args, ws, rank, local, peak)
+    ms, calls, fusions, clocks, e2e, hl = bench_lq(args, ws, rank, local, peak)
     import torch
     configs = None if (args.no_configs or ws > 1) else config_figures(torch.device("cuda", local), peak)
     if rank != 0:
@@ -823,7 +877,7 @@ def main():
                           "unit": "GB/s", "frac": g["frac"], "traffic": traffic,
                           "traffic_source": GATEUP_TRAFFIC["source"],
                           "alg_bytes_per_launch": g["alg_bytes"], "us_per_launch": g["us"]},
-                layer_calls=calls, configs=configs,
+                layer_calls=calls, fusions=fusions, configs=configs,
                 clocks=clocks, e2e=e2e, gpu_launches=4 * args.steps, cpu_baseline=cb)
     print(json.dumps(line))
 

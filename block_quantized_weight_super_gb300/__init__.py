@@ -21,7 +21,8 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
  LQ_EUNSUPPORTED) = range(8)
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
-           "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_qkv_mixed", "lq_pack_gate_up", "lq_ffn_gate_up_act",
+           "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_matvec_act", "lq_gemv_f16", "lq_gemv_f32", "lq_rmsnorm", "lq_qkv_mixed",
+           "lq_qkv_mixed_rmsnorm", "lq_pack_gate_up", "lq_ffn_gate_up_act", "lq_ffn_gate_up_act_rmsnorm",
            "lq_ffn", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_ex_workspace_bytes", "lq_moe_ffn_ex",
            "lq_moe_ffn_static",
            "lq_device_status",
@@ -57,7 +58,14 @@ def lib():
             "lq_dequant": ([i32, vp, i64, i64, vp, vp], i32),
             "lq_matvec": ([i32, vp, i64, i64, vp, vp, i32, vp], i32),
             "lq_matvec_softcap": ([i32, vp, i64, i64, vp, vp, i32, C.c_float, vp], i32),
+            "lq_matvec_act": ([i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
+            "lq_gemv_f16": ([vp, i64, i64, vp, vp, i32, vp], i32),
+            "lq_gemv_f32": ([vp, i64, i64, vp, vp, i32, vp], i32),
+            "lq_rmsnorm": ([vp, vp, C.c_float, vp, i32, i64, vp], i32),
             "lq_qkv_mixed": ([i32, vp, i64, i32, vp, i64, i32, vp, i64, i64, vp, vp, vp, vp, i32, vp], i32),
+            "lq_qkv_mixed_rmsnorm": ([i32, vp, i64, i32, vp, i64, i32, vp, i64, i64, vp, vp, C.c_float, vp, vp, vp,
+                                      vp, i32, vp], i32),
+            "lq_ffn_gate_up_act_rmsnorm": ([i32, vp, i64, i64, vp, vp, C.c_float, vp, vp, i32, i32, vp], i32),
             "lq_pack_gate_up": ([i32, vp, vp, i64, i64, vp, vp], i32),
             "lq_ffn_gate_up_act": ([i32, vp, i64, i64, vp, vp, i32, i32, vp], i32),
             "lq_ffn": ([i32, vp, i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
@@ -133,6 +141,35 @@ def lq_matvec(fmt, W, rows, cols, x, y, batch, stream=None):
 def lq_matvec_softcap(fmt, W, rows, cols, x, y, batch, cap, stream=None):
     return _check(lib().lq_matvec_softcap(fmt, _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, float(cap),
                                           _stream(stream)))
+
+
+def lq_matvec_act(fmt, W, rows, cols, gu, h, y, batch, act, stream=None):
+    return _check(lib().lq_matvec_act(fmt, _ptr(W), rows, cols, _ptr(gu), _ptr(h), _ptr(y), batch, act,
+                                      _stream(stream)))
+
+
+def lq_gemv_f16(W, rows, cols, x, y, batch, stream=None):
+    return _check(lib().lq_gemv_f16(_ptr(W), rows, cols, _ptr(x), _ptr(y), batch, _stream(stream)))
+
+
+def lq_gemv_f32(W, rows, cols, x, y, batch, stream=None):
+    return _check(lib().lq_gemv_f32(_ptr(W), rows, cols, _ptr(x), _ptr(y), batch, _stream(stream)))
+
+
+def lq_rmsnorm(x, w, eps, out, ntok, n, stream=None):
+    return _check(lib().lq_rmsnorm(_ptr(x), _ptr(w), float(eps), _ptr(out), ntok, n, _stream(stream)))
+
+
+def lq_qkv_mixed_rmsnorm(fq, Wq, nq, fk, Wk, nk, fv, Wv, nv, cols, x, norm_w, eps, xn, q, k, v, batch,
+                         stream=None):
+    return _check(lib().lq_qkv_mixed_rmsnorm(fq, _ptr(Wq), nq, fk, _ptr(Wk), nk, fv, _ptr(Wv), nv, cols, _ptr(x),
+                                             _ptr(norm_w), float(eps), _ptr(xn), _ptr(q), _ptr(k), _ptr(v), batch,
+                                             _stream(stream)))
+
+
+def lq_ffn_gate_up_act_rmsnorm(fmt, Wgu, inter, cols, x, norm_w, eps, xn, h, batch, act, stream=None):
+    return _check(lib().lq_ffn_gate_up_act_rmsnorm(fmt, _ptr(Wgu), inter, cols, _ptr(x), _ptr(norm_w), float(eps),
+                                                   _ptr(xn), _ptr(h), batch, act, _stream(stream)))
 
 
 def lq_qkv_mixed(fq, Wq, nq, fk, Wk, nk, fv, Wv, nv, cols, x, q, k, v, batch, stream=None):

@@ -205,18 +205,43 @@ bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPl
 }
 
 constexpr int GV_NOT_ELIGIBLE = -1;
-int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st);
+constexpr int NEEDS_PREPASS = -2;
+
+// A transform of the launch's x rows made before the matvec (GV_X_NORM:
+// the RMS-norm of each row with weight nw and epsilon eps; GV_X_ACT: x rows
+// of (g, u) pairs, the value act(g) * u).  The transformed rows
+// ([batch][cols]) are written to `out` by whichever path runs.
+struct XPre {
+    int kind = GV_X_PLAIN;
+    const float* nw = nullptr;
+    float eps = 0.f;
+    int act = ACT_NONE;
+    float* out = nullptr;
+};
+
+int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* pre);
 
 // Run the segments (all sharing cols and the batch width B): at batch 1 the
 // tensor-core kernel when it can take them, else the quantized matvec
-// kernel when it can take the shape, else the plain-load kernel.
-int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
+// kernel when it can take the shape, else the plain-load kernel.  With a
+// transform `pre`: fused where the chosen kernel has it (the batch-1
+// tensor-core kernel: both; the quantized matvec kernel: the activation);
+// otherwise NEEDS_PREPASS, before anything is launched.
+int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, const XPre* pre = nullptr) {
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
     if (B == 1) {
-        rc = run_gv(segs, cols, st);
+        rc = run_gv(segs, cols, st, pre);
         if (rc != GV_NOT_ELIGIBLE) return rc;
+    }
+    if (pre && pre->kind == GV_X_NORM) return NEEDS_PREPASS;
+    if (pre && pre->kind == GV_X_ACT) {
+        if (!al(pre->out, 16)) return NEEDS_PREPASS;
+        for (auto& s : segs) {
+            s.xact = pre->act;
+            s.xout = pre->out;
+        }
     }
     // formats in order of first appearance (at most two per launch)
     std::vector<int> fmts;
@@ -231,6 +256,7 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st) {
     for (auto& s : segs) rows += (s.mode == MODE_PLAIN ? 1 : 2) * (int64_t)s.nout;
     QPlan pl;
     if (fmts.size() > 2 || !xal || !plan_qmv(B, cols, fmts, pairs, pl, rows, 2 * dev->sms)) {
+        if (pre) return NEEDS_PREPASS;          // the plain-load kernel reads x as it is
         for (auto& s : segs) {
             if (s.nout <= 0) continue;
             cudaError_t e = launch_direct(s, cols, B, st);
@@ -376,8 +402,10 @@ int tensor_map(CUtensorMap* out, const void* base, int64_t rows, int64_t rowbyte
 // Plan: one CTA per SM; the row blocks are split into contiguous ranges of
 // nearly equal weight bytes, one per CTA; tiles land in a ring of up to
 // GV_MAX_INFLIGHT slots, as many as shared memory holds.
-int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
+int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* xp) {
     if (segs.empty() || segs.size() > (size_t)GV_MAX_SEG || cols % 256 != 0 || cols > (1 << 20))
+        return GV_NOT_ELIGIBLE;
+    if (xp && xp->kind != GV_X_PLAIN && (!al(xp->out, 16) || (xp->kind == GV_X_NORM && !al(xp->nw, 16))))
         return GV_NOT_ELIGIBLE;
     int mask = 0;
     for (auto& s : segs) {
@@ -447,7 +475,7 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
     // keep HBM busy, few enough that they land one after another and the
     // warps compute each as it arrives
     int ns = std::min(GV_MAX_INFLIGHT, std::max(2, mxt));
-    while (ns >= 2 && gv_layout(mask, ns, slot, mxt, nsb).total > GV_SMEM_MAX) --ns;
+    while (ns >= 2 && gv_layout(mask, ns, slot, mxt, nsb, ns).total > GV_SMEM_MAX) --ns;
     if (ns < 2) return GV_NOT_ELIGIBLE;
     P.nseg = n;
     P.x = segs[0].x;
@@ -458,8 +486,15 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st) {
     P.slot_bytes = slot;
     P.maxtiles = mxt;
     P.x16 = al(segs[0].x, 16) ? 1 : 0;
+    if (xp) {
+        P.xpre = xp->kind;
+        P.act = xp->act;
+        P.nw = xp->nw;
+        P.eps = xp->eps;
+        P.xout = xp->kind != GV_X_PLAIN ? xp->out : nullptr;
+    }
     for (int k = 0; k <= ncta; ++k) P.cta_rb[k] = b[k];
-    const size_t smem = gv_layout(mask, ns, slot, mxt, nsb).total;
+    const size_t smem = gv_layout(mask, ns, slot, mxt, nsb, ns).total;
     cudaError_t e = gv_launch(mask, P, ncta, smem, st);
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "batch-1 tensor-core matvec launch");
 }
@@ -708,21 +743,50 @@ int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, l
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "dequant launch");
 }
 
-// y = W.x, each output stored through seg_out (cap 0: as computed)
+// The transform `pre` as its own launch: the rows written to pre.out.
+static int prepass(const XPre& pre, const float* x, int batch, int64_t cols, cudaStream_t st) {
+    cudaError_t e = pre.kind == GV_X_NORM ? launch_rmsnorm(x, pre.nw, pre.eps, pre.out, batch, cols, st)
+                                          : launch_act_pairs(x, pre.out, (int64_t)batch * cols, pre.act, st);
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "x transform launch");
+}
+
+// run_segments with an optional transform of x: fused when the kernel that
+// runs has it, else the transform first (into pre.out) and the segments
+// reading that.
+static int run_pre(std::vector<Seg>& segs, int B, int64_t cols, int batch, cudaStream_t st, const XPre* pre,
+                   const float* x) {
+    if (!pre) return run_segments(segs, B, cols, st);
+    int rc = run_segments(segs, B, cols, st, pre);
+    if (rc != NEEDS_PREPASS) return rc;
+    if ((rc = prepass(*pre, x, batch, cols, st))) return rc;
+    for (auto& s : segs) {
+        s.x = pre->out;
+        s.xact = ACT_NONE;
+        s.xout = nullptr;
+    }
+    return run_segments(segs, B, cols, st);
+}
+
+// y = W.x, each output stored through seg_out (cap 0: as computed); x
+// transformed first by pre (if given)
 static int matvec_impl(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
-                       float cap, lq_stream_t stream) {
+                       float cap, lq_stream_t stream, const XPre* pre = nullptr) {
     int rc = check_mat(fmt, W, rows, cols, "W");
     if (rc) return rc;
     if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
     if (rows == 0) return LQ_OK;
     if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (batch >= qmm_min_batch(fmt)) {
         std::vector<Seg> segs;
         for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
-            segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(QMM_NT, batch - b0)));
+            segs.push_back(plain_seg(fmt, W, rows, pre ? pre->out : x, y, rows, b0, std::min(QMM_NT, batch - b0)));
             segs.back().cap = cap;
         }
-        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
+        if (qmm_eligible(segs, cols)) {
+            if (pre && (rc = prepass(*pre, x, batch, cols, st))) return rc;
+            return run_qmm(segs, cols, st);
+        }
     }
     const int B = batch_width(cols, batch, {fmt}, false);
     std::vector<Seg> segs;
@@ -730,7 +794,95 @@ static int matvec_impl(int fmt, const void* W, int64_t rows, int64_t cols, const
         segs.push_back(plain_seg(fmt, W, rows, x, y, rows, b0, std::min(B, batch - b0)));
         segs.back().cap = cap;
     }
-    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+    return run_pre(segs, B, cols, batch, st, pre, x);
+}
+
+static int qkv_impl(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv, const void* Wv,
+                    int64_t nv, int64_t cols, const float* x, float* q, float* k, float* v, int batch,
+                    lq_stream_t stream, const XPre* pre = nullptr) {
+    int rc;
+    if ((rc = check_mat(fq, Wq, nq, cols, "Wq")) || (rc = check_mat(fk, Wk, nk, cols, "Wk")) ||
+        (rc = check_mat(fv, Wv, nv, cols, "Wv")))
+        return rc;
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (nq + nk + nv == 0) return LQ_OK;
+    if ((rc = check_f32(x, "x"))) return rc;
+    if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
+        (nv && (rc = check_f32(v, "v"))))
+        return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (batch >= qmm_min_batch(fq)) {
+        const float* xq = pre ? pre->out : x;
+        std::vector<Seg> segs;
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
+            const int nb = std::min(QMM_NT, batch - b0);
+            if (nq) segs.push_back(plain_seg(fq, Wq, nq, xq, q, nq, b0, nb));
+            if (nk) segs.push_back(plain_seg(fk, Wk, nk, xq, k, nk, b0, nb));
+            if (nv) segs.push_back(plain_seg(fv, Wv, nv, xq, v, nv, b0, nb));
+        }
+        if (qmm_eligible(segs, cols)) {
+            if (pre && (rc = prepass(*pre, x, batch, cols, st))) return rc;
+            return run_qmm(segs, cols, st);
+        }
+    }
+    const int B = batch_width(cols, batch, {fq, fk, fv}, false);
+    std::vector<Seg> segs;
+    for (int b0 = 0; b0 < batch; b0 += B) {
+        const int nb = std::min(B, batch - b0);
+        if (nq) segs.push_back(plain_seg(fq, Wq, nq, x, q, nq, b0, nb));
+        if (nk) segs.push_back(plain_seg(fk, Wk, nk, x, k, nk, b0, nb));
+        if (nv) segs.push_back(plain_seg(fv, Wv, nv, x, v, nv, b0, nb));
+    }
+    return run_pre(segs, B, cols, batch, st, pre, x);
+}
+
+static int gate_up_impl(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x, float* h, int batch,
+                        int act, lq_stream_t stream, const XPre* pre = nullptr) {
+    int rc = check_mat(fmt, Wgu, 2 * inter, cols, "Wgu");
+    if (rc) return rc;
+    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    if (inter == 0) return LQ_OK;
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (batch >= qmm_min_batch(fmt)) {
+        std::vector<Seg> segs;
+        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
+            Seg s = plain_seg(fmt, Wgu, inter, pre ? pre->out : x, h, inter, b0, std::min(QMM_NT, batch - b0));
+            s.mode = MODE_PAIR_INTERLEAVED;
+            s.act = act;
+            segs.push_back(s);
+        }
+        if (qmm_eligible(segs, cols)) {
+            if (pre && (rc = prepass(*pre, x, batch, cols, st))) return rc;
+            return run_qmm(segs, cols, st);
+        }
+    }
+    const int B = batch_width(cols, batch, {fmt}, true);
+    std::vector<Seg> segs;
+    for (int b0 = 0; b0 < batch; b0 += B) {
+        Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(B, batch - b0));
+        s.mode = MODE_PAIR_INTERLEAVED;
+        s.act = act;
+        segs.push_back(s);
+    }
+    return run_pre(segs, B, cols, batch, st, pre, x);
+}
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+// Arguments of the fused input norm: weight, epsilon, the normalised rows'
+// buffer (not overlapping x: the fused kernel stores it while others read x).
+static int check_norm(const float* x, const float* nw, float eps, const float* xn, int batch, int64_t cols) {
+    int rc;
+    if ((rc = check_f32(nw, "norm_w")) || (rc = check_f32(xn, "xn"))) return rc;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(LQ_EINVAL, "eps %g", (double)eps);
+    if (x && batch > 0 && cols > 0 && overlaps(x, (size_t)batch * cols * 4, xn, (size_t)batch * cols * 4))
+        return fail(LQ_EINVAL, "xn overlaps x");
+    return LQ_OK;
 }
 
 int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
@@ -746,39 +898,80 @@ int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const 
     return matvec_impl(fmt, W, rows, cols, x, y, batch, cap, stream);
 }
 
+int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const float* gu, float* h, float* y, int batch,
+                  int act, lq_stream_t stream) {
+    g_err[0] = 0;
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    int rc;
+    if ((rc = check_f32(h, "h"))) return rc;
+    if (gu && batch > 0 && cols > 0 && overlaps(gu, (size_t)batch * cols * 8, h, (size_t)batch * cols * 4))
+        return fail(LQ_EINVAL, "h overlaps gu");
+    XPre pre;
+    pre.kind = GV_X_ACT;
+    pre.act = act;
+    pre.out = h;
+    return matvec_impl(fmt, W, rows, cols, gu, y, batch, 0.f, stream, &pre);
+}
+
+static int gemv_dense(bool f16, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
+                      lq_stream_t stream) {
+    const int epc = f16 ? 8 : 4;
+    if (rows < 0 || rows > (int64_t)1 << 30 || cols <= 0 || cols % epc)
+        return fail(LQ_ESHAPE, "rows %lld cols %lld (cols a multiple of %d)", (long long)rows, (long long)cols, epc);
+    if (batch < 1 || batch > 8) return fail(LQ_EINVAL, "batch %d (1..8)", batch);
+    if ((int64_t)batch * cols * 4 > 200 * 1024) return fail(LQ_ESHAPE, "batch * cols too large for the x staging");
+    if (rows == 0) return LQ_OK;
+    if (!W) return fail(LQ_EINVAL, "W is null");
+    int rc;
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(y, "y"))) return rc;
+    if (!al(W, 16) || !al(x, 16)) return fail(LQ_EALIGN, "W and x must be 16-byte aligned");
+    DevInfo* dev = nullptr;
+    if ((rc = dev_info(&dev))) return rc;
+    cudaError_t e = dense_gemv_launch(f16, W, rows, (int)cols, x, y, batch, dev->sms,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "dense gemv launch");
+}
+
+int lq_gemv_f16(const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    return gemv_dense(true, W, rows, cols, x, y, batch, stream);
+}
+
+int lq_gemv_f32(const float* W, int64_t rows, int64_t cols, const float* x, float* y, int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    return gemv_dense(false, W, rows, cols, x, y, batch, stream);
+}
+
+int lq_rmsnorm(const float* x, const float* w, float eps, float* out, int ntok, int64_t n, lq_stream_t stream) {
+    g_err[0] = 0;
+    if (ntok < 0 || n <= 0 || n > (int64_t)1 << 20) return fail(LQ_ESHAPE, "ntok %d n %lld", ntok, (long long)n);
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(LQ_EINVAL, "eps %g", (double)eps);
+    int rc;
+    if ((rc = check_f32(x, "x")) || (rc = check_f32(w, "w")) || (rc = check_f32(out, "out"))) return rc;
+    if (ntok == 0) return LQ_OK;
+    cudaError_t e = launch_rmsnorm(x, w, eps, out, ntok, n, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "rmsnorm launch");
+}
+
 int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
                  const void* Wv, int64_t nv, int64_t cols, const float* x, float* q, float* k,
                  float* v, int batch, lq_stream_t stream) {
     g_err[0] = 0;
-    int rc;
-    if ((rc = check_mat(fq, Wq, nq, cols, "Wq")) || (rc = check_mat(fk, Wk, nk, cols, "Wk")) ||
-        (rc = check_mat(fv, Wv, nv, cols, "Wv")))
-        return rc;
-    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
-    if (nq + nk + nv == 0) return LQ_OK;
-    if ((rc = check_f32(x, "x"))) return rc;
-    if ((nq && (rc = check_f32(q, "q"))) || (nk && (rc = check_f32(k, "k"))) ||
-        (nv && (rc = check_f32(v, "v"))))
-        return rc;
-    if (batch >= qmm_min_batch(fq)) {
-        std::vector<Seg> segs;
-        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
-            const int nb = std::min(QMM_NT, batch - b0);
-            if (nq) segs.push_back(plain_seg(fq, Wq, nq, x, q, nq, b0, nb));
-            if (nk) segs.push_back(plain_seg(fk, Wk, nk, x, k, nk, b0, nb));
-            if (nv) segs.push_back(plain_seg(fv, Wv, nv, x, v, nv, b0, nb));
-        }
-        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
-    }
-    const int B = batch_width(cols, batch, {fq, fk, fv}, false);
-    std::vector<Seg> segs;
-    for (int b0 = 0; b0 < batch; b0 += B) {
-        const int nb = std::min(B, batch - b0);
-        if (nq) segs.push_back(plain_seg(fq, Wq, nq, x, q, nq, b0, nb));
-        if (nk) segs.push_back(plain_seg(fk, Wk, nk, x, k, nk, b0, nb));
-        if (nv) segs.push_back(plain_seg(fv, Wv, nv, x, v, nv, b0, nb));
-    }
-    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+    return qkv_impl(fq, Wq, nq, fk, Wk, nk, fv, Wv, nv, cols, x, q, k, v, batch, stream);
+}
+
+int lq_qkv_mixed_rmsnorm(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
+                         const void* Wv, int64_t nv, int64_t cols, const float* x, const float* norm_w, float eps,
+                         float* xn, float* q, float* k, float* v, int batch, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_norm(x, norm_w, eps, xn, batch, cols);
+    if (rc) return rc;
+    XPre pre;
+    pre.kind = GV_X_NORM;
+    pre.nw = norm_w;
+    pre.eps = eps;
+    pre.out = xn;
+    return qkv_impl(fq, Wq, nq, fk, Wk, nk, fv, Wv, nv, cols, x, q, k, v, batch, stream, &pre);
 }
 
 int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int64_t cols,
@@ -799,31 +992,21 @@ int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int6
 int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
                        float* h, int batch, int act, lq_stream_t stream) {
     g_err[0] = 0;
-    int rc = check_mat(fmt, Wgu, 2 * inter, cols, "Wgu");
+    return gate_up_impl(fmt, Wgu, inter, cols, x, h, batch, act, stream);
+}
+
+int lq_ffn_gate_up_act_rmsnorm(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
+                               const float* norm_w, float eps, float* xn, float* h, int batch, int act,
+                               lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_norm(x, norm_w, eps, xn, batch, cols);
     if (rc) return rc;
-    if (batch < 1) return fail(LQ_EINVAL, "batch %d < 1", batch);
-    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
-    if (inter == 0) return LQ_OK;
-    if ((rc = check_f32(x, "x")) || (rc = check_f32(h, "h"))) return rc;
-    if (batch >= qmm_min_batch(fmt)) {
-        std::vector<Seg> segs;
-        for (int b0 = 0; b0 < batch; b0 += QMM_NT) {
-            Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(QMM_NT, batch - b0));
-            s.mode = MODE_PAIR_INTERLEAVED;
-            s.act = act;
-            segs.push_back(s);
-        }
-        if (qmm_eligible(segs, cols)) return run_qmm(segs, cols, reinterpret_cast<cudaStream_t>(stream));
-    }
-    const int B = batch_width(cols, batch, {fmt}, true);
-    std::vector<Seg> segs;
-    for (int b0 = 0; b0 < batch; b0 += B) {
-        Seg s = plain_seg(fmt, Wgu, inter, x, h, inter, b0, std::min(B, batch - b0));
-        s.mode = MODE_PAIR_INTERLEAVED;
-        s.act = act;
-        segs.push_back(s);
-    }
-    return run_segments(segs, B, cols, reinterpret_cast<cudaStream_t>(stream));
+    XPre pre;
+    pre.kind = GV_X_NORM;
+    pre.nw = norm_w;
+    pre.eps = eps;
+    pre.out = xn;
+    return gate_up_impl(fmt, Wgu, inter, cols, x, h, batch, act, stream, &pre);
 }
 
 int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t inter, int64_t hidden,

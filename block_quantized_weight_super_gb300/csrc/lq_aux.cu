@@ -159,14 +159,6 @@ __device__ float direct_row(int fmt, const uint8_t* row, int64_t cols, const flo
     return acc;
 }
 
-__device__ __forceinline__ float act_apply_d(int act, float g) {
-    if (act == ACT_GEGLU_TANH) {
-        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
-        return g / (1.0f + expf(-2.0f * z));
-    }
-    return g / (1.0f + expf(-g));
-}
-
 __global__ void direct_mv_kernel(Seg S, int64_t cols, int maxb) {
     const int warp = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
@@ -187,10 +179,38 @@ __global__ void direct_mv_kernel(Seg S, int64_t cols, int maxb) {
             const uint8_t* ru = S.mode == MODE_PAIR_INTERLEAVED ? rg + rb : S.w2 + (int64_t)warp * rb;
             const float g = direct_row(S.fmt, rg, cols, xrow, lane);
             const float u = direct_row(S.fmt, ru, cols, xrow, lane);
-            v = act_apply_d(S.act, g) * u;
+            v = act_eval(S.act, g) * u;
         }
         if (lane == 0) S.y[(int64_t)rho * S.ld_y + warp] = v;
     }
+}
+
+// ---------------------------------------------------------------- x transforms
+// RMS-norm of one row per CTA (256 threads): out = (x * r) * w with
+// r = 1 / sqrt(mean(x^2) + eps), the sum of squares in a fixed order (per
+// thread over its columns, a butterfly over the warp, the warps in order).
+// out may be x itself: every thread reads its own columns again after the
+// barrier that ends the sum, then writes them.
+__global__ void rmsnorm_kernel(const float* x, const float* __restrict__ w, float eps, float* out, int64_t n) {
+    __shared__ float red[8];
+    const float* xr = x + (int64_t)blockIdx.x * n;
+    float* orow = out + (int64_t)blockIdx.x * n;
+    float ss = 0.f;
+    for (int64_t j = threadIdx.x; j < n; j += 256) ss = fmaf(xr[j], xr[j], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += red[i];
+    const float r = 1.0f / sqrtf(t / (float)n + eps);
+    for (int64_t j = threadIdx.x; j < n; j += 256) orow[j] = (xr[j] * r) * __ldg(w + j);
+}
+
+// h[i] = act(g_i) * u_i of n (g, u) pairs.
+__global__ void act_pairs_kernel(const float* __restrict__ gu, float* __restrict__ h, int64_t n, int act) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        h[i] = act_eval(act, gu[2 * i]) * gu[2 * i + 1];
 }
 
 // ---------------------------------------------------------------- MoE routing
@@ -341,6 +361,19 @@ cudaError_t launch_direct(const Seg& S, int64_t cols, int maxb, cudaStream_t st)
     const int64_t threads = (int64_t)S.nout * 32;
     const int tpb = 256;
     direct_mv_kernel<<<(unsigned)((threads + tpb - 1) / tpb), tpb, 0, st>>>(S, cols, maxb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, float* out, int rows, int64_t n,
+                           cudaStream_t st) {
+    rmsnorm_kernel<<<(unsigned)rows, 256, 0, st>>>(x, w, eps, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_pairs(const float* gu, float* h, int64_t n, int act, cudaStream_t st) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    act_pairs_kernel<<<(unsigned)blocks, 256, 0, st>>>(gu, h, n, act);
     return cudaGetLastError();
 }
 

@@ -21,7 +21,10 @@
 //    units to the warps, round robin, so all warps work on each tile as it
 //    lands and no tile's last units wait on one warp.
 //  * x (the preceding kernel's output) is read once per CTA after
-//    griddepcontrol.wait and turned into the MMA B images.
+//    griddepcontrol.wait and turned into the MMA B images, optionally
+//    RMS-normalised first (the input norm fused in front of QKV or gate+up)
+//    or formed as act(g) * u from (g, u) pairs (the activation fused into
+//    the down projection's x-load); CTA 0 stores the resulting row.
 //  * Sums: a lane adds its rows' parts of a pair's units in order, the lane
 //    quad adds in a fixed butterfly, and the warp that completes a tile adds
 //    the tile's pair sums in column order and stores them: every order is
@@ -65,14 +68,6 @@ __device__ __forceinline__ uint32_t h2pack(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
-__device__ __forceinline__ float gv_act(int act, float g) {
-    if (act == ACT_GEGLU_TANH) {
-        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
-        return g / (1.0f + expf(-2.0f * z));
-    }
-    return g / (1.0f + expf(-g));
-}
-
 // the segment of row block rb (segs: the shared copy of the table)
 __device__ __forceinline__ const GvSeg& gv_seg(const GvSeg* segs, int nseg, int rb) {
     int i = 0;
@@ -90,8 +85,126 @@ __device__ __forceinline__ void gv_store(const GvSeg& G, int rb, int r, float v0
         if (o + 8 < G.nout) G.y[o + 8] = seg_out(G.cap, v1);
     } else {
         const int o = 8 * lrb + r;
-        if (o < G.nout) G.y[o] = gv_act(G.act, v0) * v1;
+        if (o < G.nout) G.y[o] = act_eval(G.act, v0) * v1;
     }
+}
+
+// Four consecutive values of the launch's x row from column c, as the
+// matvec sees them before any norm: the row itself, or act(g) * u of its
+// (g, u) pairs (GV_X_ACT).
+__device__ __forceinline__ float4 gv_x4(const GvParams& P, int c) {
+    if (P.xpre == GV_X_ACT) {
+        const float* p = P.x + 2 * (int64_t)c;
+        float4 a, b;
+        if (P.x16) {
+            a = __ldcg(reinterpret_cast<const float4*>(p));
+            b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+        } else {
+            a = make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+            b = make_float4(__ldcg(p + 4), __ldcg(p + 5), __ldcg(p + 6), __ldcg(p + 7));
+        }
+        return make_float4(act_eval(P.act, a.x) * a.y, act_eval(P.act, a.z) * a.w, act_eval(P.act, b.x) * b.y,
+                           act_eval(P.act, b.z) * b.w);
+    }
+    const float* p = P.x + c;
+    if (P.x16) return __ldcg(reinterpret_cast<const float4*>(p));
+    return make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+}
+
+constexpr uint32_t GV_RED_OFF = 384;      // in the parameter area: the warps' sums of squares
+static_assert(GV_MAX_SEG * sizeof(GvSeg) + 8 <= GV_RED_OFF && GV_RED_OFF + 4 * GV_NW <= GV_PRM_BYTES,
+              "parameter area layout");
+
+// The MMA B images and x tables of the launch's x row (eight threads per
+// 32-column block; every thread of the CTA takes part), after the optional
+// RMS-norm or activation of x; CTA 0 stores the resulting row to P.xout.
+template <int MASK>
+__device__ __forceinline__ void gv_images(const GvParams& P, const GvLayout& L, uint8_t* smem, int nsb, int tid,
+                                          int warp, int lane) {
+    const int nblk = 8 * nsb;
+    // RMS-norm: every CTA sums the squares in the same fixed order (per
+    // thread over its columns, a butterfly over the warp, then the warps
+    // in order), so every CTA scales by the same r
+    float rn = 1.0f;
+    if (P.xpre == GV_X_NORM) {
+        float ss = 0.f;
+        for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
+            const int bi = bw + (lane >> 3);
+            if (bi < nblk) {
+                const float4 v = gv_x4(P, 32 * bi + 4 * (lane & 7));
+                ss = fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, ss))));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        float* red = reinterpret_cast<float*>(smem + L.prm + GV_RED_OFF);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float t = 0.f;
+        for (int w = 0; w < GV_NW; ++w) t += red[w];
+        rn = 1.0f / sqrtf(t / (float)(256 * nsb) + P.eps);
+    }
+    for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
+        const int bi = bw + (lane >> 3), j = lane & 7;
+        const bool valid = bi < nblk;
+        const int sb = bi >> 3, blk = bi & 7;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            const int c = 32 * bi + 4 * j;
+            v = gv_x4(P, c);
+            if (P.xpre == GV_X_NORM) {
+                const float4 w = __ldg(reinterpret_cast<const float4*>(P.nw + c));
+                v = make_float4((v.x * rn) * w.x, (v.y * rn) * w.y, (v.z * rn) * w.z, (v.w * rn) * w.w);
+            }
+            if (P.xout && blockIdx.x == 0) *reinterpret_cast<float4*>(P.xout + c) = v;
+        }
+        float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+        const int es = max(1, E - 14);                                  // s = 2^(es - 127): |x / s| < 2^15
+        const float inv = __uint_as_float((uint32_t)(254 - es) << 23);  // 1 / s, exact
+        const float sc = __uint_as_float((uint32_t)es << 23);
+        const float a[4] = {v.x * inv, v.y * inv, v.z * inv, v.w * inv};
+        __half hi[4], lo[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            hi[c] = __float2half_rn(a[c]);
+            lo[c] = __float2half_rn(a[c] - __half2float(hi[c]));
+        }
+        const uint2 ph = make_uint2(h2pack(hi[0], hi[2]), h2pack(hi[1], hi[3]));
+        const uint2 pl = make_uint2(h2pack(lo[0], lo[2]), h2pack(lo[1], lo[3]));
+        float sum = (v.x + v.y) + (v.z + v.w);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+        if (valid && (MASK & 1)) {
+            const int tq = blk >> 1, hf = blk & 1, mm = 8 * hf + j;
+            uint8_t* im = smem + L.img4 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+            *reinterpret_cast<uint2*>(im) = ph;
+            *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+            if (j == 0) {
+                float* tb = reinterpret_cast<float*>(smem + L.tab4) + (sb * 4 + tq) * 4;
+                tb[hf] = sum;
+                tb[2 + hf] = sc;
+            }
+        }
+        if (valid && (MASK & 2)) {
+            const int h = blk >> 2, q = blk & 3, s6 = j >> 2, i = j & 3;
+            const int tq = 2 * h + s6, mm = 4 * q + i;
+            uint8_t* im = smem + L.img6 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+            *reinterpret_cast<uint2*>(im) = ph;
+            *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+            if (j == 0) {
+                float* tb = reinterpret_cast<float*>(smem + L.tab6) + (sb * 4 + 2 * h) * 4;
+                const float sq = q >= 2 ? sc * 0.0625f : sc;      // quarters 2, 3 arrive as 16 code
+                tb[q] = sq;
+                tb[4 + q] = sq;
+            }
+        }
+    }
+    if (tid < 32) reinterpret_cast<uint32_t*>(smem + L.zero)[tid] = 0u;
 }
 
 template <int MASK>
@@ -101,7 +214,7 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NS = P.nslots, nsb = P.nsb;
     const uint32_t SLOT = P.slot_bytes;
-    const GvLayout L = gv_layout(MASK, NS, SLOT, P.maxtiles, nsb);
+    const GvLayout L = gv_layout(MASK, NS, SLOT, P.maxtiles, nsb, NS);
     const uint32_t sbase = smem_u32(smem);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [tile] its copy has landed
     int* done = reinterpret_cast<int*>(smem + L.done);          // [tile] units done
@@ -163,67 +276,7 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
     for (int i = warp; i < min(ntile, NS); i += GV_NW) issue_tile(i);
     pdl_wait();
 
-    // ---- x images: eight threads per 32-column block
-    {
-        const int nblk = 8 * nsb;
-        for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
-            const int bi = bw + (lane >> 3), j = lane & 7;
-            const bool valid = bi < nblk;
-            const int sb = bi >> 3, blk = bi & 7;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid) {
-                const float* xp = P.x + (int64_t)sb * 256 + 32 * blk + 4 * j;
-                if (P.x16) v = __ldcg(reinterpret_cast<const float4*>(xp));
-                else v = make_float4(__ldcg(xp), __ldcg(xp + 1), __ldcg(xp + 2), __ldcg(xp + 3));
-            }
-            float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-            const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu);
-            const int es = max(1, E - 14);                                  // s = 2^(es - 127): |x / s| < 2^15
-            const float inv = __uint_as_float((uint32_t)(254 - es) << 23);  // 1 / s, exact
-            const float sc = __uint_as_float((uint32_t)es << 23);
-            const float a[4] = {v.x * inv, v.y * inv, v.z * inv, v.w * inv};
-            __half hi[4], lo[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                hi[c] = __float2half_rn(a[c]);
-                lo[c] = __float2half_rn(a[c] - __half2float(hi[c]));
-            }
-            const uint2 ph = make_uint2(h2pack(hi[0], hi[2]), h2pack(hi[1], hi[3]));
-            const uint2 pl = make_uint2(h2pack(lo[0], lo[2]), h2pack(lo[1], lo[3]));
-            float sum = (v.x + v.y) + (v.z + v.w);
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
-            if (valid && (MASK & 1)) {
-                const int tq = blk >> 1, hf = blk & 1, mm = 8 * hf + j;
-                uint8_t* im = smem + L.img4 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
-                *reinterpret_cast<uint2*>(im) = ph;
-                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
-                if (j == 0) {
-                    float* tb = reinterpret_cast<float*>(smem + L.tab4) + (sb * 4 + tq) * 4;
-                    tb[hf] = sum;
-                    tb[2 + hf] = sc;
-                }
-            }
-            if (valid && (MASK & 2)) {
-                const int h = blk >> 2, q = blk & 3, s6 = j >> 2, i = j & 3;
-                const int tq = 2 * h + s6, mm = 4 * q + i;
-                uint8_t* im = smem + L.img6 + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
-                *reinterpret_cast<uint2*>(im) = ph;
-                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
-                if (j == 0) {
-                    float* tb = reinterpret_cast<float*>(smem + L.tab6) + (sb * 4 + 2 * h) * 4;
-                    const float sq = q >= 2 ? sc * 0.0625f : sc;      // quarters 2, 3 arrive as 16 code
-                    tb[q] = sq;
-                    tb[4 + q] = sq;
-                }
-            }
-        }
-        if (tid < 32) reinterpret_cast<uint32_t*>(smem + L.zero)[tid] = 0u;
-    }
+    gv_images<MASK>(P, L, smem, nsb, tid, warp, lane);
     __syncthreads();
 
     // ---- the units: warp w takes the unit pairs v = w, w + GV_NW, ...; pair

@@ -92,17 +92,18 @@ constexpr int GV_BIMG = 8 * GV_BSLOT;     // bytes per super-block
 constexpr int GV_NW = 16;                 // warps per CTA (one CTA per SM)
 constexpr uint32_t GV_SMEM_MAX = 227u * 1024u;
 
-// Shared memory of a CTA: the tile slots, one mbarrier and two counters per
-// tile (single use: a slot's next tile waits on a fresh barrier, so no phase
-// can be mistaken for another), the shared copy of the parameters, the x
-// images and per-block x tables (layout "4": Q4_K, layout "6": Q6_K) of the
-// nsb super-blocks, a zero B slot, and per slot the 16 row sums of each unit
-// pair of the tile.
+// Shared memory of a CTA: the weight slots (whole tiles, or the warps'
+// unit-pair stages), one mbarrier and two counters per tile (single use: a
+// slot's next tile waits on a fresh barrier, so no phase can be mistaken for
+// another), the shared copy of the parameters, the x images and per-block x
+// tables (layout "4": Q4_K, layout "6": Q6_K) of the nsb super-blocks, a
+// zero B slot, and for npart tiles the 16 row sums of each unit pair.
 struct GvLayout {
     uint32_t slots, bars, done, prm, img4, img6, zero, tab4, tab6, part, total;
 };
 constexpr uint32_t GV_PRM_BYTES = 512;     // shared copy of the segment table and the CTA's row-block range
-__host__ __device__ inline GvLayout gv_layout(int mask, int nslots, uint32_t slot_bytes, int maxtiles, int nsb) {
+__host__ __device__ inline GvLayout gv_layout(int mask, int nslots, uint32_t slot_bytes, int maxtiles, int nsb,
+                                              int npart) {
     GvLayout L;
     uint32_t o = 0;
     L.slots = o;
@@ -126,7 +127,7 @@ __host__ __device__ inline GvLayout gv_layout(int mask, int nslots, uint32_t slo
     L.tab6 = o;
     if (mask & 2) o += (uint32_t)nsb * 64u;
     L.part = o;
-    o += (uint32_t)(nslots * ((nsb + 1) / 2)) * 64u;
+    o += (uint32_t)(npart * ((nsb + 1) / 2)) * 64u;
     L.total = o;
     return L;
 }

@@ -102,8 +102,18 @@ struct GvParams {
     uint32_t slot_bytes;
     int32_t maxtiles;        // most tiles (row blocks) of one CTA
     int32_t x16;             // x is 16-byte aligned
+    // what the kernel makes of x before the matvec (GV_X_*), and where CTA 0
+    // stores the resulting x row (xout, cols floats; null: not stored)
+    int32_t xpre;
+    int32_t act;             // GV_X_ACT: the activation of the (g, u) pairs
+    const float* nw;         // GV_X_NORM: the norm weight [cols]
+    float eps;               // GV_X_NORM: epsilon
+    float* xout;
     int32_t cta_rb[GV_MAX_CTA + 1];
 };
+// GV_X_NORM: x * nw / sqrt(mean(x^2) + eps) (RMS-norm of the row);
+// GV_X_ACT: x holds (g, u) pairs (2 cols floats), the value is act(g) * u.
+enum { GV_X_PLAIN = 0, GV_X_NORM = 1, GV_X_ACT = 2 };
 cudaError_t gv_set_smem(int bytes);
 cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st);
 
@@ -124,10 +134,17 @@ cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols
 cudaError_t launch_interleave(const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t rb,
                               uint8_t* out, cudaStream_t st);
 cudaError_t launch_direct(const Seg& S, int64_t cols, int maxb, cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, float* out, int rows, int64_t n,
+                           cudaStream_t st);
+cudaError_t launch_act_pairs(const float* gu, float* h, int64_t n, int act, cudaStream_t st);
 cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float* X, int ntok,
                              int topk, const float* sgate_vec, const MoeWs& ws, cudaStream_t st);
 cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int topk,
                                const MoeWs& ws, float* Y, cudaStream_t st);
+// non-quantized GEMV (lq_dense.cu): fp16 (f16) or fp32 W [rows][cols], x
+// [batch][cols] 16-byte aligned, y [batch][rows]; batch 1..8
+cudaError_t dense_gemv_launch(bool f16, const void* W, int64_t rows, int cols, const float* x, float* y, int batch,
+                              int sms, cudaStream_t st);
 cudaError_t launch_timeout_probe(uint64_t timeout_ns, unsigned* status, cudaStream_t st);
 
 }  // namespace lq

@@ -244,14 +244,6 @@ __device__ __forceinline__ uint64_t u64_of(uint32_t lo, uint32_t hi) {
     return r;
 }
 
-__device__ __forceinline__ float act_f(int act, float g) {
-    if (act == ACT_GEGLU_TANH) {
-        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
-        return g / (1.0f + expf(-2.0f * z));
-    }
-    return g / (1.0f + expf(-g));
-}
-
 __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
 }
@@ -733,7 +725,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_kernel(const __grid_cons
                         for (int i = 0; i < 2; ++i) {
                             const int tok = 2 * cq + i;
                             if (out < S.nout && tok < nval)
-                                S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_f(S.act, v[i]) * v[2 + i];
+                                S.y[(int64_t)(boff + tok) * S.ld_y + out] = act_eval(S.act, v[i]) * v[2 + i];
                         }
                     }
                 }

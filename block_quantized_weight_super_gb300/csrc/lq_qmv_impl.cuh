@@ -140,14 +140,6 @@ __device__ __forceinline__ void consumer_sync(int nct) {
 
 __device__ __forceinline__ float4 lds_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-__device__ __forceinline__ float act_q(int act, float g) {
-    if (act == ACT_GEGLU_TANH) {
-        const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
-        return g / (1.0f + expf(-2.0f * z));
-    }
-    return g / (1.0f + expf(-g));
-}
-
 // ---------------------------------------------------------------- x staging
 
 // column of x value i (0..63) of group G in the format's group order
@@ -170,13 +162,15 @@ __device__ __forceinline__ int qxcol(int G, int i) {
 // the caller brackets it with one before.  COHERENT: x was written by other
 // CTAs of this kernel, so it is read through L2 (no read-only path).  NU:
 // units each thread loads before storing (all in flight at once).
-template <int FMT, int B, bool COHERENT = false, int NU = 2>
-__device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int ct, int nct) {
+template <int FMT, int B, bool COHERENT, int NU, bool XACT>
+__device__ __forceinline__ void stage_x_body(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int ct, int nct,
+                                             bool wout) {
     const int U = Gm.U;
     const int nval = qseg_nval(S, B);
     const int boff = qseg_boff(S);
     const int units = B * U * 4;
     const int wbase = ct & ~31;                  // loop bound uniform over the warp
+    const int64_t xstride = (int64_t)Gm.cols * (XACT ? 2 : 1);
     for (int e0 = ct, w0 = wbase; w0 < units; e0 += NU * nct, w0 += NU * nct) {
         float4 v[NU][4];
 #pragma unroll
@@ -185,10 +179,10 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
             const int b = e / (U * 4), r = e % (U * 4), G = r >> 2, q = r & 3;
             if (e < units && b < nval) {
                 const int rho = boff + b;
-                const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * Gm.cols;
-                const float4* src = reinterpret_cast<const float4*>(xrow + qxcol<FMT>(G, 16 * q));
+                const float* xrow = S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * xstride;
+                const int c0 = qxcol<FMT>(G, 16 * q);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[h][k] = COHERENT ? __ldcg(src + k) : __ldg(src + k);
+                for (int k = 0; k < 4; ++k) v[h][k] = load_x4<COHERENT>(xrow, c0 + 4 * k, XACT ? S.xact : 0);
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[h][k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -202,6 +196,11 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
                 float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dst[k] = v[h][k];
+                if (XACT && wout && b < nval) {
+                    float* o = S.xout + (int64_t)(boff + b) * Gm.cols + qxcol<FMT>(G, 16 * q);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(o + 4 * k) = v[h][k];
+                }
             }
             if (FMT == FMT_Q4_K) {
                 float s16 = 0.f;
@@ -212,13 +211,23 @@ __device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int
             }
         }
     }
+}
+
+// With S.xact the staged values are act(g) * u of x's (g, u) pairs (one
+// unit per thread in flight: the pairs take twice the registers), and when
+// wout is set (the CTA staging for the segment's first tile) they are also
+// stored to S.xout.
+template <int FMT, int B, bool COHERENT = false, int NU = 2>
+__device__ void stage_x(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int ct, int nct, bool wout = false) {
+    if (S.xact) stage_x_body<FMT, B, COHERENT, 1, true>(Gm, S, xs, sxs, ct, nct, wout);
+    else stage_x_body<FMT, B, COHERENT, NU, false>(Gm, S, xs, sxs, ct, nct, false);
     consumer_sync(nct);
 }
 
 // Segments reading the same x rows (QKV: Q and K) need no second staging.
 __device__ __forceinline__ bool same_xsrc(const Seg& a, const Seg& b) {
     return a.x == b.x && a.xmap == b.xmap && a.boff == b.boff && a.bcnt == b.bcnt && a.b0 == b.b0 &&
-           a.nbatch == b.nbatch;
+           a.nbatch == b.nbatch && a.xact == b.xact;
 }
 
 // Stage group G of the B x rows of segment S for the calling thread alone.
@@ -229,10 +238,48 @@ __device__ __forceinline__ bool same_xsrc(const Seg& a, const Seg& b) {
 // whole CTA's x (the L2 bandwidth of all CTAs together) has arrived.  The
 // values and the sub-block sums (same order of additions) equal stage_x's.
 template <int FMT, int B, bool COHERENT = false>
-__device__ __forceinline__ void stage_x_own(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int G) {
+__device__ __forceinline__ void stage_x_own(const QGeo& Gm, const Seg& S, float* xs, float* sxs, int G,
+                                            bool wout = false) {
     const int U = Gm.U;
     const int nval = qseg_nval(S, B);
     const int boff = qseg_boff(S);
+    if (S.xact) {
+        // act(g) * u of (g, u) pairs, one 16-column quarter at a time (the
+        // pairs take twice the registers); the same values and sums
+#pragma unroll 1
+        for (int b = 0; b < B; ++b) {
+            const int rho = boff + b;
+            const float* xrow = b < nval ? S.x + (int64_t)(S.xmap ? S.xmap[rho] : rho) * (2 * (int64_t)Gm.cols)
+                                         : nullptr;
+            float slo = 0.f, shi = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                const int c0 = qxcol<FMT>(G, 16 * q);
+                float4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[k] = xrow ? load_x4<COHERENT>(xrow, c0 + 4 * k, S.xact) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float4* dst = reinterpret_cast<float4*>(xs + (b * U + G) * XS_STRIDE + 16 * q);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                if (wout && xrow) {
+                    float* o = S.xout + (int64_t)rho * Gm.cols + c0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(o + 4 * k) = v[k];
+                }
+                float s16 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s16 = ((s16 + v[k].x) + v[k].y) + v[k].z + v[k].w;
+                if (q < 2) slo += s16;
+                else shi += s16;
+            }
+            if (FMT == FMT_Q4_K) {
+                sxs[(b * U + G) * 2] = slo;
+                sxs[(b * U + G) * 2 + 1] = shi;
+            }
+        }
+        return;
+    }
 #pragma unroll 1
     for (int b = 0; b < B; ++b) {
         float4 v[4][4];
@@ -553,7 +600,7 @@ __device__ __forceinline__ void reduce_tile(const QGeo& Gm, const Seg& S, int t,
             vg += __shfl_xor_sync(0xFFFFFFFFu, vg, m);
             vu += __shfl_xor_sync(0xFFFFFFFFu, vu, m);
         }
-        const float v = pair ? act_q(S.act, vg) * vu : seg_out(S.cap, vg);
+        const float v = pair ? act_eval(S.act, vg) * vu : seg_out(S.cap, vg);
         const int pi = oo / B, b = oo % B;
         if (live && j == 0 && b < nval) y[(int64_t)(boff + b) * ldy + o0 + pi] = v;
     }
@@ -693,10 +740,10 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
             if (cur_seg >= 0 && same_xsrc(sm.segs[cur_seg], S)) {
                 // the staged x serves this segment too
             } else if (NCT == U) {
-                stage_x_own<FMT, B>(Gm, S, sm.xs, sm.sxs, G_first);
+                stage_x_own<FMT, B>(Gm, S, sm.xs, sm.sxs, G_first, S.xout && w.t == S.tile0);
             } else {
                 consumer_sync(NCT);      // every consumer is done with the previous x
-                stage_x<FMT, B>(Gm, S, sm.xs, sm.sxs, tid, NCT);
+                stage_x<FMT, B>(Gm, S, sm.xs, sm.sxs, tid, NCT, S.xout && w.t == S.tile0);
             }
             cur_seg = w.hint;
         }

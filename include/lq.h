@@ -102,6 +102,36 @@ int lq_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const float* x
 int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y,
                       int batch, float cap, lq_stream_t stream);
 
+/* lq_matvec_act -- y[b][r] = sum_j w_rj h[b][j] with h[b][j] = act(g_j) * u_j
+ * formed as the matvec loads its input: the activation fused into the down
+ * projection's x-load (larql "Architecture -> Metal shader map", Gemma 4
+ * 26B-A4B section, Expert FFN row: q4k_ffn_gate_up followed by
+ * q4k_geglu_down).  gu: [batch][2 cols] (g, u) pairs, g at even positions:
+ * the output of lq_matvec over an interleaved Wgu (lq_pack_gate_up).
+ * h: [batch][cols] (written: the activated input, not overlapping gu),
+ * y: [batch][rows].  act as lq_ffn_gate_up_act.  Where the kernel that runs
+ * cannot form h while loading (the batched tensor-core kernel, the
+ * plain-load kernel), h is formed by a separate launch first; the results
+ * are the same within the matvec bound.  rows == 0: nothing is launched. */
+int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const float* gu, float* h, float* y,
+                  int batch, int act, lq_stream_t stream);
+
+/* lq_gemv_f16, lq_gemv_f32 -- y[b][r] = sum_j W[r][j] x[b][j] for a
+ * non-quantized W, fp16 or fp32, [rows][cols] row-major, 16-byte aligned:
+ * the lm_head fallbacks for a tied embedding that is not block-quantized
+ * (larql Gemma 3 table, lm_head row: the f16_gemv / f32_gemv fallback
+ * chain).  fp32 accumulation; the results are within the matvec bound.
+ * cols a multiple of 8 (fp16) or 4 (fp32); batch 1..8 with batch * cols *
+ * 4 <= 200 KB (LQ_ESHAPE / LQ_EINVAL otherwise); x 16-byte aligned. */
+int lq_gemv_f16(const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch, lq_stream_t stream);
+int lq_gemv_f32(const float* W, int64_t rows, int64_t cols, const float* x, float* y, int batch, lq_stream_t stream);
+
+/* lq_rmsnorm -- out[t][j] = x[t][j] * w[j] / sqrt(mean_j(x[t][j]^2) + eps)
+ * for ntok rows of n values (larql Gemma 3 table, "Input RMS-norm" row;
+ * the stored weight already carries any offset, eps from the model config).
+ * fp32, the sum of squares in a fixed order; out may equal x. */
+int lq_rmsnorm(const float* x, const float* w, float eps, float* out, int ntok, int64_t n, lq_stream_t stream);
+
 /* lq_qkv_mixed -- q = Wq.x, k = Wk.x, v = Wv.x in ONE launch over a shared
  * x (larql q4k_q6k_qkv_proj: Q/K Q4_K and V Q6_K, or uniform formats).
  * Each matrix has its own format and row count; all share cols.
@@ -109,6 +139,18 @@ int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const 
 int lq_qkv_mixed(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
                  const void* Wv, int64_t nv, int64_t cols, const float* x, float* q, float* k,
                  float* v, int batch, lq_stream_t stream);
+
+/* lq_qkv_mixed_rmsnorm -- lq_qkv_mixed of the RMS-normed input:
+ * xn = lq_rmsnorm(x, norm_w, eps), then q, k, v from xn (larql Gemma 3
+ * table, "Input RMS-norm" and "QKV projection" rows: the opt-in variant
+ * that fuses the norm into the projection).  At batch 1 on the tensor-core
+ * kernel every CTA computes the row's norm while it builds its x operand
+ * (one launch) and CTA 0 stores xn; elsewhere the norm is a launch of its
+ * own.  xn: [batch][cols] (written; must not overlap x), norm_w: [cols],
+ * eps finite and >= 0 (LQ_EINVAL otherwise). */
+int lq_qkv_mixed_rmsnorm(int fq, const void* Wq, int64_t nq, int fk, const void* Wk, int64_t nk, int fv,
+                         const void* Wv, int64_t nv, int64_t cols, const float* x, const float* norm_w, float eps,
+                         float* xn, float* q, float* k, float* v, int batch, lq_stream_t stream);
 
 /* lq_pack_gate_up -- one-time repack of separate gate and up matrices
  * (inter x cols each, same format) into the interleaved layout the fused
@@ -124,6 +166,14 @@ int lq_pack_gate_up(int fmt, const void* Wg, const void* Wu, int64_t inter, int6
  * (g / (1 + exp(-g))).  larql q4k_ffn_gate_up_8sg + geglu.  h: [batch][inter]. */
 int lq_ffn_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
                        float* h, int batch, int act, lq_stream_t stream);
+
+/* lq_ffn_gate_up_act_rmsnorm -- lq_ffn_gate_up_act of the RMS-normed input
+ * (the pre-FFN norm), fused as lq_qkv_mixed_rmsnorm fuses the input norm;
+ * xn, norm_w, eps as there.  The pages fuse the norm only in front of QKV;
+ * this applies the same fusion to the FFN's own input norm. */
+int lq_ffn_gate_up_act_rmsnorm(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* x,
+                               const float* norm_w, float eps, float* xn, float* h, int batch, int act,
+                               lq_stream_t stream);
 
 /* lq_ffn -- the dense FFN of a decode step: h = act(Wg.x) * (Wu.x) by
  * lq_ffn_gate_up_act (interleaved Wgu, format fmt_gu, inter pairs x hidden

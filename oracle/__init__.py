@@ -247,6 +247,18 @@ def moe_ffn(fmt: int, W1, W3, W2, hidden: int, inter: int, X, idx, w, nthreads: 
     return out
 
 
+def dense_matvec(W, x):
+    """y = W . x for a non-quantized W (fp16 or fp32 [rows][cols], each value
+    taken exactly in fp64) and x [batch][cols] fp32; returns (y, S) with
+    S = sum_j |w_ij x_j|, both [batch][rows] fp64 (larql Gemma 3 table,
+    lm_head row: the f16_gemv / f32_gemv fallbacks).  A library matmul in
+    fp64 is the step: every product of two fp16/fp32 values is exact in
+    fp64, and its sums carry ~1e-16 relative error."""
+    W64 = np.asarray(W).astype(np.float64)
+    x64 = np.atleast_2d(np.asarray(x, dtype=np.float32)).astype(np.float64)
+    return x64 @ W64.T, np.abs(x64) @ np.abs(W64).T
+
+
 def abs_matvec(fmt: int, W, rows: int, cols: int, v, nthreads: int = 1) -> np.ndarray:
     """sum_j |w_ij| v_j for each row (carries an input bound through a matvec)."""
     W = _u8(W)

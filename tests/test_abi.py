@@ -222,3 +222,48 @@ def test_moe_static_validates_before_the_scratch_size(lq):
     assert st(2, 1, 1, 4096, 14300, big) == lq.LQ_ESHAPE     # inter not a block multiple
     assert st(2, 1, 1, 4096, 14336, 8, x=FAKE + 2) == lq.LQ_EALIGN
     assert st(2, 1, 1, 4096, 14336, 1000) == lq.LQ_EWORKSPACE
+
+
+def test_fused_norm_and_act_validation(lq):
+    """The input-norm and activated-input entry points check epsilon, the
+    norm weight, and that the written intermediate does not overlap the
+    input, before any launch."""
+    L = lq.lib()
+    n, cols = 64, 512
+    qkv = lambda x=FAKE, w=FAKE, eps=1e-6, xn=FAKE + (1 << 20): L.lq_qkv_mixed_rmsnorm(
+        1, FAKE, n, 1, FAKE, n, 2, FAKE, n, cols, x, w, eps, xn, FAKE, FAKE, FAKE, 1, None)
+    assert qkv(eps=-1.0) == lq.LQ_EINVAL
+    assert qkv(eps=float("nan")) == lq.LQ_EINVAL
+    assert qkv(w=None) == lq.LQ_EINVAL
+    assert qkv(xn=None) == lq.LQ_EINVAL
+    assert qkv(xn=FAKE + 1024) == lq.LQ_EINVAL              # overlaps x (512 floats = 2048 bytes)
+    assert qkv(xn=FAKE + 2) == lq.LQ_EALIGN
+    gu = lambda eps=1e-6, xn=FAKE + (1 << 20), act=1: L.lq_ffn_gate_up_act_rmsnorm(
+        1, FAKE, n, cols, FAKE, FAKE, eps, xn, FAKE, 1, act, None)
+    assert gu(eps=float("inf")) == lq.LQ_EINVAL
+    assert gu(xn=FAKE) == lq.LQ_EINVAL
+    assert gu(act=3) == lq.LQ_EINVAL
+    act = lambda h=FAKE + (1 << 20), a=1, gup=FAKE: L.lq_matvec_act(2, FAKE, n, cols, gup, h, FAKE, 1, a, None)
+    assert act(a=0) == lq.LQ_EINVAL
+    assert act(h=None) == lq.LQ_EINVAL
+    assert act(h=FAKE + 4096 - 4) == lq.LQ_EINVAL           # overlaps the 1024-float pair row
+    assert act(gup=None) == lq.LQ_EINVAL
+    rn = lambda ntok=1, nn=cols, eps=1e-6: L.lq_rmsnorm(FAKE, FAKE, eps, FAKE, ntok, nn, None)
+    assert rn(nn=0) == lq.LQ_ESHAPE
+    assert rn(ntok=-1) == lq.LQ_ESHAPE
+    assert rn(eps=-1e-3) == lq.LQ_EINVAL
+    assert rn(ntok=0) == lq.LQ_OK
+
+
+def test_dense_gemv_validation(lq):
+    L = lq.lib()
+    f16 = lambda rows=16, cols=64, b=1, W=FAKE, x=FAKE: L.lq_gemv_f16(W, rows, cols, x, FAKE, b, None)
+    assert f16(cols=60) == lq.LQ_ESHAPE            # not a multiple of 8 halves
+    assert f16(b=0) == lq.LQ_EINVAL
+    assert f16(b=9) == lq.LQ_EINVAL
+    assert f16(cols=8192, b=8) == lq.LQ_ESHAPE     # x staging over 200 KB
+    assert f16(W=None) == lq.LQ_EINVAL
+    assert f16(W=FAKE + 8) == lq.LQ_EALIGN
+    assert f16(x=FAKE + 4) == lq.LQ_EALIGN
+    assert f16(rows=0) == lq.LQ_OK
+    assert L.lq_gemv_f32(FAKE, 16, 62, FAKE, FAKE, 1, None) == lq.LQ_ESHAPE

@@ -418,6 +418,148 @@ def test_ffn(lq, f0, f1, inter, hidden, batch, act):
     _ffn_check(lq, f0, f1, inter, hidden, batch, act, Wg, Wu, Wd, x, Wgu, h, y)
 
 
+# ---------------------------------------------------------------- fused input norm, activated input
+
+def _norm_inputs(g, batch, cols):
+    x = (synth.activations(g, batch, cols) * np.float32(3.0)).astype(np.float32)
+    w = (1.0 + 0.25 * g.standard_normal(cols)).astype(np.float32)
+    return x, w
+
+
+def _check_xn(xn, x, w, eps):
+    """the GPU's normalised rows against the oracle's (fp32 sum of squares:
+    a few u32 relative through the square root, two roundings in the
+    product)."""
+    ref = oracle.rmsnorm(x, w, eps)
+    assert_within(xn, ref, 32 * oracle.U32 * np.abs(ref) + 1e-30, "xn")
+    return ref
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+@pytest.mark.parametrize("fv", [Q6_K, Q4_K])
+def test_qkv_rmsnorm(lq, batch, fv):
+    """q, k, v of the RMS-normed x (Gemma-3-4B widths): xn against the
+    oracle's norm; q, k, v bit for bit those of lq_qkv_mixed on the written
+    xn (the fused kernel multiplies exactly the values it stores), and
+    within the matvec bound of the oracle's matvec of its own norm (plus the
+    norm's rounding carried through |W|)."""
+    cols, nq, nk, nv, eps = 2560, 2048, 1024, 1024, 1e-6
+    g = synth.rng(600 + batch + fv)
+    Wq, Wk, Wv = synth.q4k(g, nq, cols), synth.q4k(g, nk, cols), synth.weights(g, fv, nv, cols)
+    x, w = _norm_inputs(g, batch, cols)
+    xd, wd = dev(x), dev(w)
+    xn = empty((batch, cols))
+    q, k, v = empty((batch, nq)), empty((batch, nk)), empty((batch, nv))
+    Wqd, Wkd, Wvd = dev(Wq), dev(Wk), dev(Wv)
+    lq.lq_qkv_mixed_rmsnorm(Q4_K, Wqd, nq, Q4_K, Wkd, nk, fv, Wvd, nv, cols, xd, wd, eps, xn, q, k, v, batch)
+    xng = host(xn)
+    ref_xn = _check_xn(xng, x, w, eps)
+    q2, k2, v2 = empty((batch, nq)), empty((batch, nk)), empty((batch, nv))
+    lq.lq_qkv_mixed(Q4_K, Wqd, nq, Q4_K, Wkd, nk, fv, Wvd, nv, cols, xn, q2, k2, v2, batch)
+    for a, b in ((q, q2), (k, k2), (v, v2)):
+        assert np.array_equal(host(a), host(b))
+    for f, W, n, out in ((Q4_K, Wq, nq, q), (Q4_K, Wk, nk, k), (fv, Wv, nv, v)):
+        ref, S = oracle.matvec(f, W, n, cols, ref_xn, NTH)
+        assert_within(host(out), ref, oracle.matvec_bound(S) + 32 * oracle.U32 * S, f"qkv rmsnorm fmt {f}")
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_gate_up_rmsnorm(lq, batch):
+    """gate+up with the pre-FFN norm fused (GEGLU, Gemma-3-4B widths at a
+    reduced inter): h bit for bit lq_ffn_gate_up_act on the written xn, and
+    within the composite bound of the oracle's gate/up of its own norm."""
+    cols, inter, eps = 2560, 1280, 1e-6
+    g = synth.rng(700 + batch)
+    Wg, Wu = synth.q4k(g, inter, cols), synth.q4k(g, inter, cols)
+    x, w = _norm_inputs(g, batch, cols)
+    Wgu = torch.empty(2 * inter * lq.lq_row_bytes(Q4_K, cols), dtype=torch.uint8, device="cuda")
+    lq.lq_pack_gate_up(Q4_K, dev(Wg), dev(Wu), inter, cols, Wgu)
+    xn, h, h2 = empty((batch, cols)), empty((batch, inter)), empty((batch, inter))
+    lq.lq_ffn_gate_up_act_rmsnorm(Q4_K, Wgu, inter, cols, dev(x), dev(w), eps, xn, h, batch, lq.LQ_ACT_GEGLU_TANH)
+    ref_xn = _check_xn(host(xn), x, w, eps)
+    lq.lq_ffn_gate_up_act(Q4_K, Wgu, inter, cols, xn, h2, batch, lq.LQ_ACT_GEGLU_TANH)
+    assert np.array_equal(host(h), host(h2))
+    o = oracle.ffn_gate_up(Q4_K, Wg, Wu, inter, cols, ref_xn, oracle.ACT_GEGLU_TANH, NTH)
+    # the norm's rounding (32 u32 of each |w x| term) joins the matvec bound
+    # of g and u by widening their sums: 1e-5 (widen S) = 1e-5 S + 32 u32 S
+    widen = 1 + 32 * oracle.U32 / 1e-5
+    bound = oracle.gate_up_bound(o["g"], o["u"], o["Sg"] * widen, o["Su"] * widen, oracle.ACT_GEGLU_TANH)
+    assert_within(host(h), o["h"], bound, "gate_up rmsnorm")
+
+
+def test_rmsnorm_standalone_and_in_place(lq):
+    g = synth.rng(710)
+    x, w = _norm_inputs(g, 5, 4096)
+    out = empty((5, 4096))
+    lq.lq_rmsnorm(dev(x), dev(w), 1e-5, out, 5, 4096)
+    _check_xn(host(out), x, w, 1e-5)
+    xd = dev(x)
+    lq.lq_rmsnorm(xd, dev(w), 1e-5, xd, 5, 4096)          # in place
+    assert np.array_equal(host(xd), host(out))
+
+
+def _act_inputs(g, batch, cols):
+    return (synth.activations(g, batch, 2 * cols) * np.float32(2.0)).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt,rows,cols,batch,act,gu_off", [
+    (Q6_K, 2560, 10240, 1, 1, 0),      # the Gemma-3-4B down: CUDA-core kernel, one thread per group
+    (Q4_K, 512, 2560, 1, 1, 0),        # batch-1 tensor-core kernel
+    (Q4_K, 333, 2560, 1, 2, 0),
+    (Q8_0, 300, 4096, 1, 2, 0),        # CUDA-core kernel, collective staging
+    (Q6_K, 300, 2560, 2, 1, 0),        # batch 2 and 4 on the CUDA-core kernel
+    (Q6_K, 300, 2560, 4, 2, 0),
+    (Q4_K, 300, 2048, 8, 2, 0),        # batch 8 on the tensor cores: the activation as its own launch
+    (Q6_K, 200, 2560, 1, 1, 8),        # gu not 16-byte aligned: its own launch, then the matvec
+])
+def test_matvec_act(lq, fmt, rows, cols, batch, act, gu_off):
+    """y = W (act(g) * u) with the activation formed on the x-load: h against
+    the oracle's activation of the same (g, u) (fp32 evaluation); y bit for
+    bit lq_matvec on the written h; y within the matvec bound of the oracle's
+    matvec of its own h plus h's rounding carried through |W|."""
+    g = synth.rng(800 + rows + batch + act)
+    W = synth.weights(g, fmt, rows, cols)
+    gu = _act_inputs(g, batch, cols)
+    if gu_off:
+        keep, gup = dev(gu, offset_bytes=gu_off)
+    else:
+        keep = gup = dev(gu)
+    h, y, y2 = empty((batch, cols)), empty((batch, rows)), empty((batch, rows))
+    Wd = dev(W)
+    lq.lq_matvec_act(fmt, Wd, rows, cols, gup, h, y, batch, act)
+    gg, uu = gu[:, 0::2].astype(np.float64), gu[:, 1::2].astype(np.float64)
+    a = oracle.act_abs(gg, act) * np.sign(gg)
+    href = a * uu
+    hb = 16 * oracle.U32 * np.abs(href) + 4 * oracle.U32 * np.abs(gg * uu) + 1e-30
+    hg = host(h)
+    assert_within(hg, href, hb, "h")
+    lq.lq_matvec(fmt, Wd, rows, cols, h, y2, batch)
+    assert np.array_equal(host(y), host(y2))
+    ref, S = oracle.matvec(fmt, W, rows, cols, href, NTH)
+    carry = np.stack([oracle.abs_matvec(fmt, W, rows, cols, hb[b], NTH) for b in range(batch)])
+    assert_within(host(y), ref, oracle.matvec_bound(S) + carry, "y")
+
+
+# ---------------------------------------------------------------- non-quantized lm_head fallbacks
+
+@pytest.mark.parametrize("dt", ["f16", "f32"])
+@pytest.mark.parametrize("rows,cols,batch", [(3001, 2560, 1), (1000, 2560, 3), (517, 4096, 8), (33, 8, 2),
+                                             (1, 2560, 1)])
+def test_dense_gemv(lq, dt, rows, cols, batch):
+    """lq_gemv_f16 / lq_gemv_f32 against the oracle's fp64 matvec of the same
+    values, within the matvec bound; ragged row counts, the narrowest rows."""
+    if dt == "f32" and cols % 4:
+        pytest.skip("cols")
+    g = synth.rng(rows + cols + batch)
+    W = (0.05 * g.standard_normal((rows, cols))).astype(np.float16 if dt == "f16" else np.float32)
+    x = synth.activations(g, batch, cols)
+    y = empty((batch, rows))
+    f = lq.lq_gemv_f16 if dt == "f16" else lq.lq_gemv_f32
+    f(dev(W), rows, cols, dev(x), y, batch)
+    ref, S = oracle.dense_matvec(W, x)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"gemv {dt} {rows}x{cols} b{batch}")
+
+
 # ---------------------------------------------------------------- tensor-core path
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q8_0])

@@ -454,3 +454,24 @@ def test_moe_weights_of_selection(orc):
     wo = orc.moe_weights(lg, other)
     for t in range(6):
         assert abs(wo[t, 0] - 1 / (1 + math.exp(lg[t, 1] - lg[t, 3]))) < 1e-14
+
+
+def test_dense_matvec_pins():
+    """dense_matvec against closed forms: the identity returns x, an all-ones
+    fp16 matrix returns each row's sum of x, a one-hot row picks one column,
+    and fp16 values go in exactly (2^-24 survives where an fp16-rounded x
+    product would not)."""
+    import oracle
+    g = np.random.default_rng(5)
+    x = g.standard_normal((2, 64)).astype(np.float32)
+    y, S = oracle.dense_matvec(np.eye(64, dtype=np.float32), x)
+    assert np.array_equal(y, x.astype(np.float64)) and np.array_equal(S, np.abs(x.astype(np.float64)))
+    y, _ = oracle.dense_matvec(np.ones((3, 64), np.float16), x)
+    assert np.allclose(y, np.repeat(x.astype(np.float64).sum(axis=1, keepdims=True), 3, axis=1), rtol=0, atol=1e-12)
+    W = np.zeros((5, 64), np.float16)
+    W[2, 17] = np.float16(-2.5)
+    y, _ = oracle.dense_matvec(W, x)
+    assert y[0, 2] == -2.5 * float(x[0, 17]) and (np.delete(y[0], 2) == 0).all()
+    W = np.full((1, 4), np.float16(2.0 ** -24))          # the smallest fp16 subnormal
+    y, _ = oracle.dense_matvec(W, np.ones((1, 4), np.float32))
+    assert y[0, 0] == 4 * 2.0 ** -24
