@@ -775,6 +775,36 @@ def config_figures(dev, peak):
         del cs, base, wgu
         torch.cuda.empty_cache()
 
+    # prefill: the Llama-3-8B FFN's gate (14336 x 4096) and down (4096 x 14336)
+    # as GEMMs over M x rows (one weight copy each: the x rows re-use it)
+    for fmt, tag in ((lq.LQ_Q4_K, "q4k"), (lq.LQ_Q8_0, "q80")):
+        Wl, _ = synth.llama_ffn(fmt, 1, seed=1)
+        wg, wd = up(Wl["wg"]), up(Wl["wd"])
+        nbw = wg.numel() + wd.numel()
+        for M in (64, 128, 512):
+            Xg = torch.randn((M, H), generator=torch.Generator(device=dev).manual_seed(M), device=dev)
+            Xd = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(M + 1), device=dev)
+            Yg, Yd = torch.empty((M, I), **f32), torch.empty((M, H), **f32)
+            nws = max(lq.lq_gemm_workspace_bytes(M, H), lq.lq_gemm_workspace_bytes(M, I))
+            wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+            def step(w, s, M=M, Xg=Xg, Xd=Xd, Yg=Yg, Yd=Yd, wsp=wsp, nws=nws):
+                lq.lq_gemm(fmt, wg, I, H, Xg, Yg, M, wsp, nws, s)
+                lq.lq_gemm(fmt, wd, H, I, Xd, Yd, M, wsp, nws, s)
+            ms = timed_graphs(step, [None], 20, 3, st)
+            out[f"prefill_gemm_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=4.0 * M * H * I / (ms * 1e-3) / 1e12,
+                                                    what="gate 14336x4096 + down 4096x14336, lq_gemm")
+            if M == 512 and tag == "q4k":
+                def step_mv(w, s, M=M, Xg=Xg, Xd=Xd, Yg=Yg, Yd=Yd):
+                    lq.lq_matvec(fmt, wg, I, H, Xg, Yg, M, s)
+                    lq.lq_matvec(fmt, wd, H, I, Xd, Yd, M, s)
+                ms = timed_graphs(step_mv, [None], 10, 3, st)
+                out[f"prefill_matvec_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=4.0 * M * H * I / (ms * 1e-3) / 1e12,
+                                                          what="the same through lq_matvec (8 x rows per pass)")
+            del Xg, Xd, Yg, Yd, wsp
+        del wg, wd
+        torch.cuda.empty_cache()
+
     # config 3: lm_head Q4_K 262144 x 2560, batch 1 (one copy: larger than L2)
     W, x = synth.lm_head(0)
     wd, xd = up(W), up(x)

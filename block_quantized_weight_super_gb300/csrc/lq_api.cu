@@ -121,6 +121,7 @@ int dev_info(DevInfo** out) {
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
         if (e == cudaSuccess) e = gv_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = gemm_set_smem();
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         for (int f = 0; f < 2; ++f) {
             const int fmt = f ? FMT_Q8_0 : FMT_Q4_K;
@@ -743,6 +744,8 @@ int lq_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, l
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "dequant launch");
 }
 
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
 // The transform `pre` as its own launch: the rows written to pre.out.
 static int prepass(const XPre& pre, const float* x, int batch, int64_t cols, cudaStream_t st) {
     cudaError_t e = pre.kind == GV_X_NORM ? launch_rmsnorm(x, pre.nw, pre.eps, pre.out, batch, cols, st)
@@ -913,6 +916,54 @@ int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const floa
     return matvec_impl(fmt, W, rows, cols, gu, y, batch, 0.f, stream, &pre);
 }
 
+size_t lq_gemm_workspace_bytes(int64_t M, int64_t cols) {
+    if (M < 0 || cols < 0) return 0;
+    return align256((size_t)M * cols * 2) * 2 + align256((size_t)M * (cols / 32) * 4) + align256((size_t)M * 4);
+}
+
+int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
+            void* workspace, size_t ws_bytes, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_mat(fmt, W, rows, cols, "W");
+    if (rc) return rc;
+    if (M < 1 || M > (int64_t)1 << 24) return fail(LQ_EINVAL, "M %lld", (long long)M);
+    if (rows == 0) return LQ_OK;
+    if ((rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y"))) return rc;
+    const bool tiled = (fmt == FMT_Q4_K || fmt == FMT_Q8_0) && cols % 256 == 0 && M >= LQ_GEMM_MIN_M &&
+                       al(W, 16) && al(X, 16) && rowbytes(fmt, cols) % 16 == 0;
+    if (!tiled) {
+        // the batched matvec (a pass over the weights per 8 x rows)
+        for (int64_t b0 = 0; b0 < M; b0 += 1 << 20) {
+            const int nb = (int)std::min<int64_t>(1 << 20, M - b0);
+            if ((rc = matvec_impl(fmt, W, rows, cols, X + b0 * cols, Y + b0 * rows, nb, 0.f, stream))) return rc;
+        }
+        return LQ_OK;
+    }
+    const size_t need = lq_gemm_workspace_bytes(M, cols);
+    if (!workspace || ws_bytes < need) return fail(LQ_EWORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    if (!al(workspace, 256)) return fail(LQ_EALIGN, "workspace not 256-byte aligned");
+    DevInfo* dev = nullptr;
+    if ((rc = dev_info(&dev))) return rc;
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    GemmParams P;
+    memset(&P, 0, sizeof P);
+    P.W = static_cast<const uint8_t*>(W);
+    P.rows = rows;
+    P.cols = cols;
+    P.rowbytes = rowbytes(fmt, cols);
+    P.M = M;
+    P.ld_y = rows;
+    P.xh = reinterpret_cast<uint16_t*>(p); p += align256((size_t)M * cols * 2);
+    P.xl = reinterpret_cast<uint16_t*>(p); p += align256((size_t)M * cols * 2);
+    P.xs = reinterpret_cast<float*>(p); p += align256((size_t)M * (cols / 32) * 4);
+    P.sn = reinterpret_cast<float*>(p);
+    P.Y = Y;
+    P.nmt = (int32_t)((M + GEMM_XN - 1) / GEMM_XN);
+    if ((rows + GEMM_WR - 1) / GEMM_WR * P.nmt > INT32_MAX) return fail(LQ_ESHAPE, "too many tiles");
+    cudaError_t e = gemm_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "gemm launch");
+}
+
 static int gemv_dense(bool f16, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,
                       lq_stream_t stream) {
     const int epc = f16 ? 8 : 4;
@@ -1023,8 +1074,6 @@ int lq_ffn(int fmt_gu, const void* Wgu, int fmt_down, const void* Wd, int64_t in
     if ((rc = lq_ffn_gate_up_act(fmt_gu, Wgu, inter, hidden, x, h, batch, act, stream))) return rc;
     return lq_matvec(fmt_down, Wd, hidden, inter, h, y, batch, stream);
 }
-
-static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
 size_t lq_moe_ffn_ex_workspace_bytes(int E, int topk, int ntok, int64_t hidden, int64_t inter, int n_shared,
                                      int64_t inter_s) {

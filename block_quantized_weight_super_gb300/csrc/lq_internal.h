@@ -141,6 +141,27 @@ cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float*
                              int topk, const float* sgate_vec, const MoeWs& ws, cudaStream_t st);
 cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int topk,
                                const MoeWs& ws, float* Y, cudaStream_t st);
+// prefill GEMM (lq_gemm.cu): Y[n][r] = sum_j w_rj X[n][j], Q4_K or Q8_0 W
+// with rows 16-byte aligned and cols a multiple of 256; CTA tiles of GEMM_WR
+// weight rows x GEMM_XN x rows (nmt x-row tiles, the fastest-varying).  The
+// x pieces (xh, xl: [M][cols] fp16 bits), block sums (xs: [M][cols / 32])
+// and row scales (sn: [M]) are workspace written by the launch itself.
+constexpr int GEMM_WR = 128;
+constexpr int GEMM_XN = 64;
+struct GemmParams {
+    const uint8_t* W;
+    int64_t rows, cols, rowbytes, M, ld_y;
+    uint16_t* xh;
+    uint16_t* xl;
+    float* xs;
+    float* sn;
+    float* Y;
+    int32_t nmt;
+};
+size_t gemm_smem_bytes(int fmt);
+cudaError_t gemm_set_smem();
+cudaError_t gemm_launch(int fmt, const GemmParams& P, const float* X, cudaStream_t st);
+
 // non-quantized GEMV (lq_dense.cu): fp16 (f16) or fp32 W [rows][cols], x
 // [batch][cols] 16-byte aligned, y [batch][rows]; batch 1..8
 cudaError_t dense_gemv_launch(bool f16, const void* W, int64_t rows, int cols, const float* x, float* y, int batch,

@@ -116,6 +116,23 @@ int lq_matvec_softcap(int fmt, const void* W, int64_t rows, int64_t cols, const 
 int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const float* gu, float* h, float* y,
                   int batch, int act, lq_stream_t stream);
 
+/* lq_gemm -- the prefill GEMM: Y[n][r] = sum_j w_rj X[n][j] for M x rows
+ * (X: [M][cols] fp32, Y: [M][rows] fp32), the same values as lq_matvec
+ * within the same bound.  dotLLM PR #320: the tiled matmul_q8_0_gemm for
+ * many tokens (parity over a grid of (M, K, N)) and ForwardBatch's batched
+ * GEMMs; Q4_K weights as in the larql tables.  Q4_K and Q8_0 weights with
+ * cols a multiple of 256, 16-byte aligned W and X, and M >= LQ_GEMM_MIN_M
+ * run on the tiled tensor-core kernel: each weight tile is read once per 64
+ * x rows.  Other calls run lq_matvec's batched kernels (a pass over the
+ * weights per 8 x rows) and leave the workspace untouched.
+ * workspace: lq_gemm_workspace_bytes(M, cols) bytes, 256-byte aligned
+ * (LQ_EWORKSPACE / LQ_EALIGN otherwise, checked when the tiled kernel
+ * runs): the fp16 pieces of x that the kernel reads. */
+#define LQ_GEMM_MIN_M 32
+size_t lq_gemm_workspace_bytes(int64_t M, int64_t cols);
+int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
+            void* workspace, size_t ws_bytes, lq_stream_t stream);
+
 /* lq_gemv_f16, lq_gemv_f32 -- y[b][r] = sum_j W[r][j] x[b][j] for a
  * non-quantized W, fp16 or fp32, [rows][cols] row-major, 16-byte aligned:
  * the lm_head fallbacks for a tied embedding that is not block-quantized

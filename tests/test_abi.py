@@ -53,7 +53,7 @@ def _declared_params():
 
 def _ctype_class(c_param):
     """the ctypes type a C parameter must be passed as"""
-    t = re.sub(r"\b[a-z_0-9]+$", "", c_param).strip()       # drop the parameter name
+    t = re.sub(r"\b[A-Za-z_0-9]+$", "", c_param).strip()   # drop the parameter name
     if "*" in t or t == "lq_stream_t":
         return "pointer"
     return {"int": C.c_int, "int64_t": C.c_int64, "uint64_t": C.c_uint64, "size_t": C.c_size_t,
@@ -267,3 +267,17 @@ def test_dense_gemv_validation(lq):
     assert f16(x=FAKE + 4) == lq.LQ_EALIGN
     assert f16(rows=0) == lq.LQ_OK
     assert L.lq_gemv_f32(FAKE, 16, 62, FAKE, FAKE, 1, None) == lq.LQ_ESHAPE
+
+
+def test_gemm_validation(lq):
+    L = lq.lib()
+    need = lq.lq_gemm_workspace_bytes(64, 2560)
+    assert need >= 64 * 2560 * 4
+    gm = lambda fmt=1, M=64, cols=2560, ws=FAKE, wsb=need, W=FAKE: L.lq_gemm(fmt, W, 128, cols, FAKE, FAKE, M, ws,
+                                                                           wsb, None)
+    assert gm(M=0) == lq.LQ_EINVAL
+    assert gm(fmt=7) == lq.LQ_EINVAL
+    assert gm(cols=2500) == lq.LQ_ESHAPE
+    assert gm(wsb=need - 1) == lq.LQ_EWORKSPACE
+    assert gm(ws=None) == lq.LQ_EWORKSPACE
+    assert gm(ws=FAKE + 16) == lq.LQ_EALIGN

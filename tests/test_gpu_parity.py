@@ -540,6 +540,84 @@ def test_matvec_act(lq, fmt, rows, cols, batch, act, gu_off):
     assert_within(host(y), ref, oracle.matvec_bound(S) + carry, "y")
 
 
+# ---------------------------------------------------------------- prefill GEMM
+
+def _gemm(lq, fmt, W, rows, cols, X, w_off=0):
+    M = X.shape[0]
+    Y = empty((M, rows))
+    nb = lq.lq_gemm_workspace_bytes(M, cols)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    if w_off:
+        keep, wp = dev(W, offset_bytes=w_off)
+    else:
+        wp = dev(W)
+    lq.lq_gemm(fmt, wp, rows, cols, dev(X), Y, M, ws, nb)
+    return host(Y)
+
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
+@pytest.mark.parametrize("M,cols,rows", [
+    (32, 256, 1), (33, 512, 127), (64, 256, 128), (65, 1024, 129), (100, 4096, 300), (130, 2560, 64),
+    (256, 512, 257), (64, 14336, 40),
+])
+def test_gemm_parity(lq, fmt, M, cols, rows):
+    """lq_gemm on the tiled kernel over a grid of (M, K, N): ragged x-row and
+    weight-row tiles, one to 56 K steps, against the oracle's matvec of
+    every x row."""
+    g = synth.rng(M * 7 + cols + rows + fmt)
+    W = synth.weights(g, fmt, rows, cols)
+    X = synth.activations(g, M, cols)
+    got = _gemm(lq, fmt, W, rows, cols, X)
+    ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
+    assert_within(got, ref, oracle.matvec_bound(S), f"gemm fmt {fmt} M {M} K {cols} N {rows}")
+
+
+def test_gemm_rows_independent_and_deterministic(lq):
+    """A row's result does not depend on the other x rows of the call or on
+    its position in the x-row tile (MMA columns are independent and the sum
+    order is fixed by the shape); two calls give the same bits."""
+    fmt, cols, rows = Q4_K, 2560, 200
+    g = synth.rng(901)
+    W = synth.q4k(g, rows, cols)
+    X = synth.activations(g, 150, cols)
+    a = _gemm(lq, fmt, W, rows, cols, X)
+    b = _gemm(lq, fmt, W, rows, cols, X)
+    assert np.array_equal(a, b)
+    c = _gemm(lq, fmt, W, rows, cols, X[37:37 + 70])       # rows 37.. land at other tile positions
+    assert np.array_equal(c, a[37:37 + 70])
+
+
+def test_gemm_x_scale_extremes(lq):
+    """x rows of very different magnitudes (per-row scale), a zero row, a row
+    with one huge entry (small values far below it in the same row)."""
+    fmt, cols, rows = Q8_0, 1024, 96
+    g = synth.rng(902)
+    W = synth.q8_0(g, rows, cols)
+    X = synth.activations(g, 40, cols)
+    X[0] *= np.float32(1e-30)
+    X[1] *= np.float32(1e25)
+    X[2] = 0
+    X[3, 17] = np.float32(3e4)
+    got = _gemm(lq, fmt, W, rows, cols, X)
+    ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
+    assert_within(got, ref, oracle.matvec_bound(S), "gemm scales")
+    assert (got[2] == 0).all()
+
+
+@pytest.mark.parametrize("fmt,M,cols,w_off", [(Q6_K, 64, 2560, 0), (Q4_K, 16, 2560, 0), (Q4_K, 64, 2560, 4),
+                                               (Q8_0, 64, 2080, 0)])
+def test_gemm_untiled_calls(lq, fmt, M, cols, w_off):
+    """Calls the tiled kernel does not take (Q6_K, M below the minimum, W not
+    16-byte aligned, cols not a multiple of 256) run the batched matvec."""
+    rows = 70
+    g = synth.rng(M + cols + w_off)
+    W = synth.weights(g, fmt, rows, cols)
+    X = synth.activations(g, M, cols)
+    got = _gemm(lq, fmt, W, rows, cols, X, w_off)
+    ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
+    assert_within(got, ref, oracle.matvec_bound(S), "untiled gemm")
+
+
 # ---------------------------------------------------------------- non-quantized lm_head fallbacks
 
 @pytest.mark.parametrize("dt", ["f16", "f32"])
