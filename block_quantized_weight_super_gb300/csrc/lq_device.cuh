@@ -211,11 +211,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Hint: bring `bytes` (multiple of 16) at a 16-byte aligned address into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, unsigned bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void record_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }

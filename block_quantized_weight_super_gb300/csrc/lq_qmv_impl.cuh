@@ -927,8 +927,10 @@ struct QmvTable {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, get(mask), nt, smem);
     }
     // Launched with programmatic stream serialization: the kernel may start
-    // while the preceding kernel of the stream finishes; it reads x, device
-    // row counts and (after an L2 prefetch hint) W only after griddepcontrol.wait.
+    // while the preceding kernel of the stream finishes.  x and device row
+    // counts are read only after griddepcontrol.wait; the producer copies its
+    // first S weight tiles before that wait (weights do not depend on the
+    // preceding kernel) unless the row counts come from the device.
     static cudaError_t launch(int mask, const QmvParams& P, int grid, int nt, size_t smem,
                               cudaStream_t st) {
         const GroupConsts K = group_consts();

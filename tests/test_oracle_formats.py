@@ -96,6 +96,32 @@ def test_q4k_positions_raw_bytes(orc):
         assert np.count_nonzero(w) == 2
 
 
+def test_q4k_high_scale_fields_hand_typed(orc):
+    """A Q4_K block typed byte by byte (no packer): d = dmin = 1.0 (fp16
+    0x3C00), the twelve scale bytes below, and in every sub-block quants 0 in
+    the first 16 weights and 2 in the last 16, so a sub-block decodes to -m
+    and then 2 sc - m.  Sub-blocks 0..3 take sc, m from the low six bits of
+    bytes 0..3 and 4..7; sub-blocks 4..7 take the low four bits from bytes
+    8..11 (sc: low nibble, m: high nibble) and the top two bits from the top
+    bits of bytes 0..3 (sc) and 4..7 (m).  The expected fields are worked
+    out by hand in the comments."""
+    scales = bytes([0xC1, 0x82, 0x43, 0x04,     # sc0..3 = 1, 2, 3, 4; top bits 3, 2, 1, 0
+                    0x85, 0x46, 0xC7, 0x08,     # m0..3 = 5, 6, 7, 8; top bits 2, 1, 3, 0
+                    0x9A, 0x3B, 0xFC, 0x0D])    # sc4..7 low 10, 11, 12, 13; m4..7 low 9, 3, 15, 0
+    expect = {0: (1, 5), 1: (2, 6), 2: (3, 7), 3: (4, 8),
+              4: (10 + 16 * 3, 9 + 16 * 2),     # (58, 41)
+              5: (11 + 16 * 2, 3 + 16 * 1),     # (43, 19)
+              6: (12 + 16 * 1, 15 + 16 * 3),    # (28, 63)
+              7: (13 + 16 * 0, 0 + 16 * 0)}     # (13, 0)
+    qs = bytes(([0x00] * 16 + [0x22] * 16) * 4)   # byte 32g + l: low nibble sub-block 2g, high 2g + 1
+    blk = np.frombuffer(bytes([0x00, 0x3C, 0x00, 0x3C]) + scales + qs, dtype=np.uint8)
+    assert blk.size == 144
+    w = _dq(orc, Q4_K, blk)
+    for j, (sc, m) in expect.items():
+        assert (w[32 * j:32 * j + 16] == -m).all(), j
+        assert (w[32 * j + 16:32 * j + 32] == 2 * sc - m).all(), j
+
+
 def test_q4k_scale_min_roundtrip(orc):
     """random and exhaustive 6-bit scales/mins, recovered through two blocks:
     all q = 0 gives w = -dmin*m, all q = 1 gives w = d*sc - dmin*m."""
