@@ -67,7 +67,7 @@ CALL_ACT_BYTES = {"qkv": 4 * (H_ + NQ_ + 2 * NKV_), "o": 4 * (NQ_ + H_), "gateup
 LAYER_BYTES = sum(CALL_WEIGHT_BYTES.values())        # 60,518,400
 NLAYERS = 34
 METRIC = "effective weight GB/s per quantized matvec (decode layer, batch 1)"
-WORKLOADS = ("gemma_layer", "llama_ffn", "lm_head", "mixtral_moe", "matvec_small")
+WORKLOADS = ("gemma_layer", "llama_ffn", "lm_head", "mixtral_moe", "matvec_small", "prefill_gemm")
 CPU_STEPS_MAX = 272                                  # repo arm's oracle sample: layer steps
 
 
@@ -82,8 +82,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config figures")
     ap.add_argument("--workload", default="gemma_layer", choices=list(WORKLOADS))
-    ap.add_argument("--batch", type=int, default=8, help="x rows (llama_ffn)")
-    ap.add_argument("--fmt", default="q4k", choices=["q4k", "q80"], help="weight format (llama_ffn)")
+    ap.add_argument("--batch", type=int, default=8, help="x rows (llama_ffn, prefill_gemm)")
+    ap.add_argument("--fmt", default="q4k", choices=["q4k", "q80"], help="weight format (llama_ffn, prefill_gemm)")
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="final-logit soft-cap fused into the store (lm_head; 0 = none)")
     a = ap.parse_args()
@@ -495,8 +495,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "470ff4b1c06c41c7904872015eae99fc458400f82e6225c807d692aedf44d1bb",
-                  "bytes": 29_536_512,
+GATEUP_TRAFFIC = {"csrc_sha256": "f360fd6cf27d730faecb3133b4a2f93524811164a05b330dfd21ff5bbb443edb",
+                  "bytes": 29_547_264,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch)"}
 
 # the sources the batch-1 gate+up launch is compiled from
@@ -576,6 +576,28 @@ class Workload:
             self.step = lambda w, st: (self._gu(w, st), self._down(w, st))
             self.dom = self._gu
             self.cpu_jobs = [(fmt, W["wg"], H, X), (fmt, W["wu"], H, X), (fmt, W["wd"], I, np.zeros((M, I), np.float32))]
+        elif name == "prefill_gemm":
+            fmt = lq.LQ_Q4_K if args.fmt == "q4k" else lq.LQ_Q8_0
+            M = args.batch
+            W, X = synth.llama_ffn(fmt, M, seed=0)
+            H, I = synth.LLAMA_HIDDEN, synth.LLAMA_INTER
+            base = {"wg": up(W["wg"]), "wd": up(W["wd"])}
+            self.bytes = self.dom_bytes = base["wg"].numel() + base["wd"].numel()
+            self.x_host = X
+            self.x = up(X)
+            self.h = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(5), device=dev)
+            self.y = torch.empty((M, H), **f32)
+            self.g = torch.empty((M, I), **f32)
+            nws = max(lq.lq_gemm_workspace_bytes(M, H), lq.lq_gemm_workspace_bytes(M, I))
+            self.ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+            self.desc = (f"prefill GEMMs of the Llama-3-8B FFN, {M} x rows, {args.fmt.upper()}: gate 14336x4096 "
+                         f"and down 4096x14336 through lq_gemm")
+            self.dom_name = f"prefill GEMM ({args.fmt.upper()}, M {M})"
+            self.launches = 4
+            self.step = lambda w, st: (lq.lq_gemm(fmt, w["wg"], I, H, self.x, self.g, M, self.ws, nws, st),
+                                       lq.lq_gemm(fmt, w["wd"], H, I, self.h, self.y, M, self.ws, nws, st))
+            self.dom = self.step
+            self.cpu_jobs = [(fmt, W["wg"], H, X[:1]), (fmt, W["wd"], I, np.zeros((1, I), np.float32))]
         elif name in ("lm_head", "matvec_small"):
             if name == "lm_head":
                 Wn, x = synth.lm_head(0)
