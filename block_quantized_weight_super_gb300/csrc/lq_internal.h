@@ -76,7 +76,7 @@ cudaError_t qmm_launch(int fmt, const QmmParams& P, int grid, size_t smem, cudaS
 // mask: bit 0 Q4_K, bit 1 Q6_K; masks 1 (Q4_K) and 3 (both) are built.
 constexpr int GV_MAX_SEG = 4;
 constexpr int GV_MAX_CTA = 160;
-constexpr int GV_MAX_INFLIGHT = 16;    // tiles in flight per CTA
+constexpr int GV_MAX_INFLIGHT = 6;     // tiles in flight per CTA (more delays the first tile)
 constexpr int GV_MAX_TILES = 512;
 constexpr int GV_MAX_TILE_BYTES = 48 * 1024;
 enum { GV_COPY_TILE = 0, GV_COPY_CPA = 1 };
