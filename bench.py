@@ -495,9 +495,9 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "f360fd6cf27d730faecb3133b4a2f93524811164a05b330dfd21ff5bbb443edb",
-                  "bytes": 29_547_264,
-                  "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch)"}
+GATEUP_TRAFFIC = {"csrc_sha256": "04ea4795dbdc1d3463a085ae9cd86f001605ec1e209e0afcbaccd8bc566f72bf",
+                  "bytes": 29_548_544,
+                  "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from
 GV_SOURCES = ("lq_codec.cuh", "lq_device.cuh", "lq_group.cuh", "lq_gv.cu", "lq_gv.cuh", "lq_internal.h",
