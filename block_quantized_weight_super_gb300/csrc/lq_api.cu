@@ -959,7 +959,7 @@ int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, 
     P.xs = reinterpret_cast<float*>(p); p += align256((size_t)M * (cols / 32) * 4);
     P.sn = reinterpret_cast<float*>(p);
     P.Y = Y;
-    P.nmt = (int32_t)((M + GEMM_XN - 1) / GEMM_XN);
+    P.nmt = (int32_t)((M + gemm_xn(fmt) - 1) / gemm_xn(fmt));
     if ((rows + GEMM_WR - 1) / GEMM_WR * P.nmt > INT32_MAX) return fail(LQ_ESHAPE, "too many tiles");
     cudaError_t e = gemm_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "gemm launch");

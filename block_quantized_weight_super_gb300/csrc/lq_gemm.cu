@@ -46,14 +46,16 @@ namespace {
 constexpr int GM_THREADS = 256;
 constexpr int GM_XP = 528;                 // shared pitch of an x piece row (256 halves + 16 bytes)
 
-template <int FMT>
+// Stage layout for XN x rows per CTA (8 or 4 n-tiles of 8 per warp).
+template <int FMT, int XN>
 struct GmF {
     static constexpr int WB = FMT == FMT_Q4_K ? 144 : 272;     // weight bytes of a row per stage
+    static constexpr int NTL = XN / 8;                         // n-tiles per warp
     static constexpr uint32_t W_OFF = 0;
     static constexpr uint32_t XH_OFF = GEMM_WR * WB;
-    static constexpr uint32_t XL_OFF = XH_OFF + GEMM_XN * GM_XP;
-    static constexpr uint32_t XS_OFF = XL_OFF + GEMM_XN * GM_XP;
-    static constexpr uint32_t STAGE = XS_OFF + (FMT == FMT_Q4_K ? GEMM_XN * 8 * 4 : 0);
+    static constexpr uint32_t XL_OFF = XH_OFF + XN * GM_XP;
+    static constexpr uint32_t XS_OFF = XL_OFF + XN * GM_XP;
+    static constexpr uint32_t STAGE = XS_OFF + (FMT == FMT_Q4_K ? XN * 8 * 4 : 0);
 };
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
@@ -138,18 +140,19 @@ __global__ void __launch_bounds__(GM_THREADS) gemm_xprep_kernel(const float* __r
     }
 }
 
-// 16 rows x 32 columns of one (sub-)block against the 64 x rows of the
+// 16 rows x 32 columns of one (sub-)block against the NTL x 8 x rows of the
 // stage: P[jn] (n-tile jn: x rows 8 jn .. 8 jn + 7) += A . (hi + lo).
 // a[h][0..3]: the A registers of the two 16-column halves.
+template <int NTL>
 __device__ __forceinline__ void gm_block(const uint32_t (&a)[2][4], uint32_t xh_base, uint32_t xl_base, int blk,
-                                         int lane, float (&P)[8][4]) {
+                                         int lane, float (&P)[NTL][4]) {
     const int mi = lane >> 3, r8 = lane & 7;
     // lane's ldmatrix row: n-tile (jn + (mi >> 1)), row r8, k half (mi & 1)
     const uint32_t roff = (uint32_t)((8 * (mi >> 1) + r8) * GM_XP + 2 * (32 * blk + 8 * (mi & 1)));
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int jn = 0; jn < 8; jn += 2) {
+        for (int jn = 0; jn < NTL; jn += 2) {
             const uint32_t off = roff + (uint32_t)(8 * jn * GM_XP + 2 * 16 * h);
             uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
             ldsm4(xh_base + off, b0, b1, b2, b3);
@@ -162,14 +165,15 @@ __device__ __forceinline__ void gm_block(const uint32_t (&a)[2][4], uint32_t xh_
     }
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
-    using F = GmF<FMT>;
+template <int FMT, int XN>
+__global__ void __launch_bounds__(GM_THREADS, XN == 32 ? 2 : 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+    using F = GmF<FMT, XN>;
+    constexpr int NTL = F::NTL;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int mt = blockIdx.x % P.nmt, wt = blockIdx.x / P.nmt;
-    const int64_t r0 = (int64_t)wt * GEMM_WR, n0 = (int64_t)mt * GEMM_XN;
+    const int64_t r0 = (int64_t)wt * GEMM_WR, n0 = (int64_t)mt * XN;
     const int64_t K = P.cols;
     const int nk = (int)(K / 256);
     const uint32_t sbase = smem_u32(smem);
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
                 cp16(st + F::W_OFF + (uint32_t)(rr * F::WB + 16 * q),
                      P.W + (r0 + rr) * P.rowbytes + (int64_t)kk * F::WB + 16 * q);
         }
-        for (int p = tid; p < GEMM_XN * 32; p += GM_THREADS) {
+        for (int p = tid; p < XN * 32; p += GM_THREADS) {
             const int nn = p >> 5, q = p & 31;
             if (n0 + nn < P.M) {
                 const int64_t src = (n0 + nn) * K + (int64_t)kk * 256 + 8 * q;
@@ -192,16 +196,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
             }
         }
         if (FMT == FMT_Q4_K) {
-            for (int p = tid; p < GEMM_XN * 2; p += GM_THREADS) {
+            for (int p = tid; p < XN * 2; p += GM_THREADS) {
                 const int nn = p >> 1, q = p & 1;
                 if (n0 + nn < P.M) cp16(st + F::XS_OFF + (uint32_t)(nn * 32 + 16 * q), P.xs + (n0 + nn) * (K / 32) + kk * 8 + 4 * q);
             }
         }
     };
 
-    float acc[8][4];
+    float acc[NTL][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int j = 0; j < NTL; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     const GvK KC = gv_consts();
 
     load_stage(0, 0);
@@ -239,16 +243,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
                         a[h][2] = hsub2_u32(lop_and_or(wA >> 8, KC.m4lo, KC.magic), sA);
                         a[h][3] = hsub2_u32(lop_and_or(wB >> 8, KC.m4lo, KC.magic), sB);
                     }
-                    float Pp[8][4];
+                    float Pp[NTL][4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) Pp[j][0] = Pp[j][1] = Pp[j][2] = Pp[j][3] = 0.f;
+                    for (int j = 0; j < NTL; ++j) Pp[j][0] = Pp[j][1] = Pp[j][2] = Pp[j][3] = 0.f;
                     const int blk = 2 * jq + nib;
-                    gm_block(a, xhb, xlb, blk, lane, Pp);
+                    gm_block<NTL>(a, xhb, xlb, blk, lane, Pp);
                     const float dA = nib ? cA.dsc1 : cA.dsc0, dB = nib ? cB.dsc1 : cB.dsc0;
                     const float eA = nib ? cA.e1 : cA.e0, eB = nib ? cB.e1 : cB.e0;
                     const float* xsb = reinterpret_cast<const float*>(smem + (kk & 1) * F::STAGE + F::XS_OFF);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < NTL; ++j) {
                         const int nl = 8 * j + 2 * t;
                         const float s0 = xsb[nl * 8 + blk], s1 = xsb[(nl + 1) * 8 + blk];
                         acc[j][0] = fmaf(dA, Pp[j][0], fmaf(eA, s0, acc[j][0]));
@@ -281,12 +285,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
                     a[h][2] = hsub2_u32(lop_and_xor(wA >> 8, KC.m8, KC.x8), KC.s8);
                     a[h][3] = hsub2_u32(lop_and_xor(wB >> 8, KC.m8, KC.x8), KC.s8);
                 }
-                float Pp[8][4];
+                float Pp[NTL][4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) Pp[j][0] = Pp[j][1] = Pp[j][2] = Pp[j][3] = 0.f;
-                gm_block(a, xhb, xlb, blk, lane, Pp);
+                for (int j = 0; j < NTL; ++j) Pp[j][0] = Pp[j][1] = Pp[j][2] = Pp[j][3] = 0.f;
+                gm_block<NTL>(a, xhb, xlb, blk, lane, Pp);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < NTL; ++j) {
                     acc[j][0] = fmaf(dA, Pp[j][0], acc[j][0]);
                     acc[j][1] = fmaf(dA, Pp[j][1], acc[j][1]);
                     acc[j][2] = fmaf(dB, Pp[j][2], acc[j][2]);
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
     // y[n][r] = s_n * acc; lane holds rows g, g + 8 and x rows 8 j + 2 t, + 1
     const int64_t ra = r0 + 16 * warp + g, rb = ra + 8;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < NTL; ++j) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int64_t n = n0 + 8 * j + 2 * t + e;
@@ -314,15 +318,17 @@ __global__ void __launch_bounds__(GM_THREADS, 1) gemm_kernel(const __grid_consta
 
 }  // namespace
 
+int gemm_xn(int fmt) { return fmt == FMT_Q4_K ? GEMM_XN_Q4K : GEMM_XN_Q80; }
+
 size_t gemm_smem_bytes(int fmt) {
-    return 2 * (size_t)(fmt == FMT_Q4_K ? GmF<FMT_Q4_K>::STAGE : GmF<FMT_Q8_0>::STAGE);
+    return 2 * (size_t)(fmt == FMT_Q4_K ? GmF<FMT_Q4_K, GEMM_XN_Q4K>::STAGE : GmF<FMT_Q8_0, GEMM_XN_Q80>::STAGE);
 }
 
 cudaError_t gemm_set_smem() {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT_Q4_K, GEMM_XN_Q4K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)gemm_smem_bytes(FMT_Q4_K));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_kernel<FMT_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_kernel<FMT_Q8_0, GEMM_XN_Q80>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)gemm_smem_bytes(FMT_Q8_0));
 }
 
@@ -334,9 +340,9 @@ cudaError_t gemm_launch(int fmt, const GemmParams& P, const float* X, cudaStream
     const int64_t nwt = (P.rows + GEMM_WR - 1) / GEMM_WR;
     const int grid = (int)(nwt * P.nmt);
     if (fmt == FMT_Q4_K)
-        gemm_kernel<FMT_Q4_K><<<grid, GM_THREADS, gemm_smem_bytes(fmt), st>>>(P);
+        gemm_kernel<FMT_Q4_K, GEMM_XN_Q4K><<<grid, GM_THREADS, gemm_smem_bytes(fmt), st>>>(P);
     else
-        gemm_kernel<FMT_Q8_0><<<grid, GM_THREADS, gemm_smem_bytes(fmt), st>>>(P);
+        gemm_kernel<FMT_Q8_0, GEMM_XN_Q80><<<grid, GM_THREADS, gemm_smem_bytes(fmt), st>>>(P);
     return cudaGetLastError();
 }
 

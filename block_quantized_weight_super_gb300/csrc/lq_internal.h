@@ -143,11 +143,12 @@ cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int to
                                const MoeWs& ws, float* Y, cudaStream_t st);
 // prefill GEMM (lq_gemm.cu): Y[n][r] = sum_j w_rj X[n][j], Q4_K or Q8_0 W
 // with rows 16-byte aligned and cols a multiple of 256; CTA tiles of GEMM_WR
-// weight rows x GEMM_XN x rows (nmt x-row tiles, the fastest-varying).  The
+// weight rows x gemm_xn(fmt) x rows (nmt x-row tiles, the fastest-varying).  The
 // x pieces (xh, xl: [M][cols] fp16 bits), block sums (xs: [M][cols / 32])
 // and row scales (sn: [M]) are workspace written by the launch itself.
 constexpr int GEMM_WR = 128;
-constexpr int GEMM_XN = 64;
+constexpr int GEMM_XN_Q4K = 32;        // x rows per CTA tile: Q4_K two CTAs per SM
+constexpr int GEMM_XN_Q80 = 64;        // Q8_0 (its 34 KB weight stages leave room for one)
 struct GemmParams {
     const uint8_t* W;
     int64_t rows, cols, rowbytes, M, ld_y;
@@ -158,6 +159,7 @@ struct GemmParams {
     float* Y;
     int32_t nmt;
 };
+int gemm_xn(int fmt);
 size_t gemm_smem_bytes(int fmt);
 cudaError_t gemm_set_smem();
 cudaError_t gemm_launch(int fmt, const GemmParams& P, const float* X, cudaStream_t st);
