@@ -588,7 +588,7 @@ class Workload:
             self.h = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(5), device=dev)
             self.y = torch.empty((M, H), **f32)
             self.g = torch.empty((M, I), **f32)
-            nws = max(lq.lq_gemm_workspace_bytes(M, H), lq.lq_gemm_workspace_bytes(M, I))
+            nws = max(lq.lq_gemm_workspace_bytes(M, I, H), lq.lq_gemm_workspace_bytes(M, H, I))
             self.ws = torch.empty(nws, dtype=torch.uint8, device=dev)
             self.desc = (f"prefill GEMMs of the Llama-3-8B FFN, {M} x rows, {args.fmt.upper()}: gate 14336x4096 "
                          f"and down 4096x14336 through lq_gemm")
@@ -807,7 +807,7 @@ def config_figures(dev, peak):
             Xg = torch.randn((M, H), generator=torch.Generator(device=dev).manual_seed(M), device=dev)
             Xd = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(M + 1), device=dev)
             Yg, Yd = torch.empty((M, I), **f32), torch.empty((M, H), **f32)
-            nws = max(lq.lq_gemm_workspace_bytes(M, H), lq.lq_gemm_workspace_bytes(M, I))
+            nws = max(lq.lq_gemm_workspace_bytes(M, I, H), lq.lq_gemm_workspace_bytes(M, H, I))
             wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
 
             def step(w, s, M=M, Xg=Xg, Xd=Xd, Yg=Yg, Yd=Yd, wsp=wsp, nws=nws):

@@ -31,6 +31,7 @@ EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", 
 LQ_MOE_STATIC_SCRATCH_BYTES = 4 << 20
 LQ_MOE_MAX_SHARED = 16
 LQ_GEMM_MIN_M = 32
+LQ_GEMM_TC_MIN_M = 128
 
 
 class LqError(RuntimeError):
@@ -60,7 +61,7 @@ def lib():
             "lq_matvec": ([i32, vp, i64, i64, vp, vp, i32, vp], i32),
             "lq_matvec_softcap": ([i32, vp, i64, i64, vp, vp, i32, C.c_float, vp], i32),
             "lq_matvec_act": ([i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
-            "lq_gemm_workspace_bytes": ([i64, i64], sz),
+            "lq_gemm_workspace_bytes": ([i64, i64, i64], sz),
             "lq_gemm": ([i32, vp, i64, i64, vp, vp, i64, vp, sz, vp], i32),
             "lq_gemv_f16": ([vp, i64, i64, vp, vp, i32, vp], i32),
             "lq_gemv_f32": ([vp, i64, i64, vp, vp, i32, vp], i32),
@@ -151,8 +152,8 @@ def lq_matvec_act(fmt, W, rows, cols, gu, h, y, batch, act, stream=None):
                                       _stream(stream)))
 
 
-def lq_gemm_workspace_bytes(M, cols) -> int:
-    return lib().lq_gemm_workspace_bytes(M, cols)
+def lq_gemm_workspace_bytes(M, rows, cols) -> int:
+    return lib().lq_gemm_workspace_bytes(M, rows, cols)
 
 
 def lq_gemm(fmt, W, rows, cols, X, Y, M, workspace=None, ws_bytes=0, stream=None):

@@ -158,11 +158,31 @@ struct GemmParams {
     float* sn;
     float* Y;
     int32_t nmt;
+    // tcgen05 kernel: a tensor map over W (uint32 elements, boxes of one
+    // 256-column chunk x GEMM_TC_WR rows), the x image (pieces in the MMA
+    // operand layout), 1 / t_r per weight row, the bound on its waits and the
+    // status word
+    CUtensorMap tmw;
+    uint8_t* ximg;
+    float* tinv;
+    float* part;             // split-K partial sums [ksplit][M][rows] (ksplit > 1)
+    int32_t ksplit;          // K ranges per output tile
+    uint64_t timeout_ns;
+    unsigned* status;
 };
 int gemm_xn(int fmt);
 size_t gemm_smem_bytes(int fmt);
 cudaError_t gemm_set_smem();
 cudaError_t gemm_launch(int fmt, const GemmParams& P, const float* X, cudaStream_t st);
+// the same on tcgen05 (lq_gemm.cu): CTA tiles of GEMM_TC_WR weight rows x
+// GEMM_TC_XN x rows; the x image is padded to a multiple of GEMM_TC_XN rows
+constexpr int GEMM_TC_WR = 128;
+constexpr int GEMM_TC_XN = 128;
+// K ranges per output tile for a weight matrix of this shape (a function of
+// the weight shape alone, so a row's result does not depend on M)
+int gemm_tc_ksplit(int64_t rows, int64_t cols);
+size_t gemm_tc_smem_bytes(int fmt);
+cudaError_t gemm_tc_launch(int fmt, const GemmParams& P, const float* X, cudaStream_t st);
 
 // non-quantized GEMV (lq_dense.cu): fp16 (f16) or fp32 W [rows][cols], x
 // [batch][cols] 16-byte aligned, y [batch][rows]; batch 1..8

@@ -271,8 +271,11 @@ def test_dense_gemv_validation(lq):
 
 def test_gemm_validation(lq):
     L = lq.lib()
-    need = lq.lq_gemm_workspace_bytes(64, 2560)
+    need = lq.lq_gemm_workspace_bytes(64, 128, 2560)
     assert need >= 64 * 2560 * 4
+    # the tcgen05 kernel's x image is padded to whole 128-row tiles, plus s_n and a scale per weight row
+    assert lq.lq_gemm_workspace_bytes(129, 300, 256) >= 256 * 256 * 4 + 256 * 4 + 300 * 4
+    assert lq.lq_gemm_workspace_bytes(-1, 300, 256) == 0
     gm = lambda fmt=1, M=64, cols=2560, ws=FAKE, wsb=need, W=FAKE: L.lq_gemm(fmt, W, 128, cols, FAKE, FAKE, M, ws,
                                                                            wsb, None)
     assert gm(M=0) == lq.LQ_EINVAL

@@ -545,7 +545,7 @@ def test_matvec_act(lq, fmt, rows, cols, batch, act, gu_off):
 def _gemm(lq, fmt, W, rows, cols, X, w_off=0):
     M = X.shape[0]
     Y = empty((M, rows))
-    nb = lq.lq_gemm_workspace_bytes(M, cols)
+    nb = lq.lq_gemm_workspace_bytes(M, rows, cols)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     if w_off:
         keep, wp = dev(W, offset_bytes=w_off)
@@ -557,13 +557,15 @@ def _gemm(lq, fmt, W, rows, cols, X, w_off=0):
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
 @pytest.mark.parametrize("M,cols,rows", [
-    (32, 256, 1), (33, 512, 127), (64, 256, 128), (65, 1024, 129), (100, 4096, 300), (130, 2560, 64),
-    (256, 512, 257), (64, 14336, 40),
+    (32, 256, 1), (33, 512, 127), (64, 256, 128), (65, 1024, 129), (100, 4096, 300), (64, 14336, 40),
+    (128, 256, 64), (130, 2560, 65), (256, 512, 257), (200, 14336, 33), (384, 4096, 130),
 ])
 def test_gemm_parity(lq, fmt, M, cols, rows):
-    """lq_gemm on the tiled kernel over a grid of (M, K, N): ragged x-row and
-    weight-row tiles, one to 56 K steps, against the oracle's matvec of
-    every x row."""
+    """lq_gemm on the tiled kernels over a grid of (M, K, N): below 128 x rows
+    the mma.sync kernel, from 128 the tcgen05 one; ragged x-row and
+    weight-row tiles, one to 56 super-blocks per row (the tcgen05 kernel
+    accumulates a whole row in tensor memory), against the oracle's matvec
+    of every x row."""
     g = synth.rng(M * 7 + cols + rows + fmt)
     W = synth.weights(g, fmt, rows, cols)
     X = synth.activations(g, M, cols)
@@ -572,28 +574,33 @@ def test_gemm_parity(lq, fmt, M, cols, rows):
     assert_within(got, ref, oracle.matvec_bound(S), f"gemm fmt {fmt} M {M} K {cols} N {rows}")
 
 
-def test_gemm_rows_independent_and_deterministic(lq):
+@pytest.mark.parametrize("fmt,M,sub", [(Q4_K, 100, 70), (Q4_K, 300, 150), (Q8_0, 300, 131)])
+def test_gemm_rows_independent_and_deterministic(lq, fmt, M, sub):
     """A row's result does not depend on the other x rows of the call or on
     its position in the x-row tile (MMA columns are independent and the sum
-    order is fixed by the shape); two calls give the same bits."""
-    fmt, cols, rows = Q4_K, 2560, 200
-    g = synth.rng(901)
-    W = synth.q4k(g, rows, cols)
-    X = synth.activations(g, 150, cols)
+    order is fixed by the shape); two calls give the same bits.  The sub-call
+    takes the same kernel as the full one (both below or both from 128 x
+    rows)."""
+    cols, rows = 2560, 200
+    g = synth.rng(901 + M)
+    W = synth.weights(g, fmt, rows, cols)
+    X = synth.activations(g, M, cols)
     a = _gemm(lq, fmt, W, rows, cols, X)
     b = _gemm(lq, fmt, W, rows, cols, X)
     assert np.array_equal(a, b)
-    c = _gemm(lq, fmt, W, rows, cols, X[37:37 + 70])       # rows 37.. land at other tile positions
-    assert np.array_equal(c, a[37:37 + 70])
+    c = _gemm(lq, fmt, W, rows, cols, X[37:37 + sub])       # rows 37.. land at other tile positions
+    assert np.array_equal(c, a[37:37 + sub])
 
 
-def test_gemm_x_scale_extremes(lq):
+@pytest.mark.parametrize("M", [40, 140])
+def test_gemm_x_scale_extremes(lq, M):
     """x rows of very different magnitudes (per-row scale), a zero row, a row
-    with one huge entry (small values far below it in the same row)."""
+    with one huge entry (small values far below it in the same row); both
+    tiled kernels."""
     fmt, cols, rows = Q8_0, 1024, 96
     g = synth.rng(902)
     W = synth.q8_0(g, rows, cols)
-    X = synth.activations(g, 40, cols)
+    X = synth.activations(g, M, cols)
     X[0] *= np.float32(1e-30)
     X[1] *= np.float32(1e25)
     X[2] = 0
@@ -602,6 +609,33 @@ def test_gemm_x_scale_extremes(lq):
     ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
     assert_within(got, ref, oracle.matvec_bound(S), "gemm scales")
     assert (got[2] == 0).all()
+
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
+def test_gemm_weight_scale_extremes(lq, fmt):
+    """The tcgen05 kernel scales each weight row by a power of two taken from
+    its block scales: rows whose scales are the smallest fp16 subnormal, rows
+    near the fp16 maximum, an all-zero row, and rows whose super-blocks mix
+    scales 2^20 apart, against the oracle."""
+    M, cols, rows = 130, 1024, 70
+    g = synth.rng(903 + fmt)
+    W = synth.weights(g, fmt, rows, cols)
+    bb, be = (144, 256) if fmt == Q4_K else (34, 32)
+    nblk = cols // be
+    def set_d(r, blk, bits):                                    # fp16 d (Q4_K: and dmin) of one block
+        W[r, bb * blk:bb * blk + 2] = np.frombuffer(np.uint16(bits).tobytes(), np.uint8)
+        if fmt == Q4_K:
+            W[r, bb * blk + 2:bb * blk + 4] = np.frombuffer(np.uint16(bits).tobytes(), np.uint8)
+    for blk in range(nblk):
+        set_d(0, blk, 0x0001)                                   # 2^-24
+        set_d(1, blk, 0x7BFF)                                   # 65504
+        set_d(2, blk, 0x0000)
+        set_d(3, blk, 0x3C00 if blk % 2 else 0x0C00)            # 1 and 2^-12 alternating
+    X = synth.activations(g, M, cols)
+    got = _gemm(lq, fmt, W, rows, cols, X)
+    ref, S = oracle.matvec(fmt, W, rows, cols, X, NTH)
+    assert_within(got, ref, oracle.matvec_bound(S), "gemm weight scales")
+    assert (got[:, 2] == 0).all()
 
 
 @pytest.mark.parametrize("fmt,M,cols,w_off", [(Q6_K, 64, 2560, 0), (Q4_K, 16, 2560, 0), (Q4_K, 64, 2560, 4),
