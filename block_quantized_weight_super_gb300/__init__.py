@@ -31,7 +31,6 @@ EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", 
 LQ_MOE_STATIC_SCRATCH_BYTES = 4 << 20
 LQ_MOE_MAX_SHARED = 16
 LQ_GEMM_MIN_M = 32
-LQ_GEMM_TC_MIN_M = 128
 
 
 class LqError(RuntimeError):

@@ -919,15 +919,12 @@ int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const floa
 
 size_t lq_gemm_workspace_bytes(int64_t M, int64_t rows, int64_t cols) {
     if (M < 0 || rows < 0 || cols < 0) return 0;
-    if (M >= LQ_GEMM_TC_MIN_M) {
-        // the x image (hi and lo pieces, M padded to whole x tiles), s_n,
-        // 1 / t_r and, when K is split, the partial sums
-        const size_t mp = (size_t)((M + GEMM_TC_XN - 1) / GEMM_TC_XN) * GEMM_TC_XN;
-        const int ks = gemm_tc_ksplit(rows, cols);
-        return align256(mp * cols * 4) + align256(mp * 4) + align256((size_t)rows * 4) +
-               (ks > 1 ? align256((size_t)ks * M * rows * 4) : 0);
-    }
-    return align256((size_t)M * cols * 2) * 2 + align256((size_t)M * (cols / 32) * 4) + align256((size_t)M * 4);
+    // the x image (hi and lo pieces, M padded to whole x tiles), s_n, 1 / t_r
+    // and, when K is split, the partial sums
+    const size_t mp = (size_t)((M + GEMM_TC_XN - 1) / GEMM_TC_XN) * GEMM_TC_XN;
+    const int ks = gemm_tc_ksplit(rows, cols);
+    return align256(mp * cols * 4) + align256(mp * 4) + align256((size_t)rows * 4) +
+           (ks > 1 ? align256((size_t)ks * M * rows * 4) : 0);
 }
 
 int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
@@ -962,31 +959,19 @@ int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, 
     P.rowbytes = rowbytes(fmt, cols);
     P.M = M;
     P.ld_y = rows;
-    const bool tc = M >= LQ_GEMM_TC_MIN_M;
-    const int xn = tc ? GEMM_TC_XN : gemm_xn(fmt);
-    P.nmt = (int32_t)((M + xn - 1) / xn);
-    if (tc) {
-        if ((rc = tensor_map(&P.tmw, W, rows, P.rowbytes, P.rowbytes, (int)(P.rowbytes / (cols / 256) / 4),
-                             GEMM_TC_WR)))
-            return rc;
-        const size_t mp = (size_t)P.nmt * GEMM_TC_XN;
-        P.ximg = p; p += align256(mp * cols * 4);
-        P.sn = reinterpret_cast<float*>(p); p += align256(mp * 4);
-        P.tinv = reinterpret_cast<float*>(p); p += align256((size_t)rows * 4);
-        P.ksplit = gemm_tc_ksplit(rows, cols);
-        P.part = P.ksplit > 1 ? reinterpret_cast<float*>(p) : nullptr;
-    } else {
-        P.xh = reinterpret_cast<uint16_t*>(p); p += align256((size_t)M * cols * 2);
-        P.xl = reinterpret_cast<uint16_t*>(p); p += align256((size_t)M * cols * 2);
-        P.xs = reinterpret_cast<float*>(p); p += align256((size_t)M * (cols / 32) * 4);
-        P.sn = reinterpret_cast<float*>(p);
-    }
+    P.nmt = (int32_t)((M + GEMM_TC_XN - 1) / GEMM_TC_XN);
+    if ((rc = tensor_map(&P.tmw, W, rows, P.rowbytes, P.rowbytes, (int)(P.rowbytes / (cols / 256) / 4), GEMM_TC_WR)))
+        return rc;
+    const size_t mp = (size_t)P.nmt * GEMM_TC_XN;
+    P.ximg = p; p += align256(mp * cols * 4);
+    P.sn = reinterpret_cast<float*>(p); p += align256(mp * 4);
+    P.tinv = reinterpret_cast<float*>(p); p += align256((size_t)rows * 4);
+    P.ksplit = gemm_tc_ksplit(rows, cols);
+    P.part = P.ksplit > 1 ? reinterpret_cast<float*>(p) : nullptr;
     P.Y = Y;
     P.timeout_ns = g_timeout_ns.load();
     P.status = dev->status;
-    if ((rows + 63) / 64 * P.nmt > INT32_MAX) return fail(LQ_ESHAPE, "too many tiles");
-    cudaError_t e = tc ? gemm_tc_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream))
-                       : gemm_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = gemm_tc_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "gemm launch");
 }
 

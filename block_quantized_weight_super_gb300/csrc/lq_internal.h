@@ -142,42 +142,27 @@ cudaError_t launch_moe_route(const float* R, int E, int64_t hidden, const float*
 cudaError_t launch_moe_combine(const float* ye, int64_t hidden, int ntok, int topk,
                                const MoeWs& ws, float* Y, cudaStream_t st);
 // prefill GEMM (lq_gemm.cu): Y[n][r] = sum_j w_rj X[n][j], Q4_K or Q8_0 W
-// with rows 16-byte aligned and cols a multiple of 256; CTA tiles of GEMM_WR
-// weight rows x gemm_xn(fmt) x rows (nmt x-row tiles, the fastest-varying).  The
-// x pieces (xh, xl: [M][cols] fp16 bits), block sums (xs: [M][cols / 32])
-// and row scales (sn: [M]) are workspace written by the launch itself.
-constexpr int GEMM_WR = 128;
-constexpr int GEMM_XN_Q4K = 32;        // x rows per CTA tile: Q4_K two CTAs per SM
-constexpr int GEMM_XN_Q80 = 64;        // Q8_0 (its 34 KB weight stages leave room for one)
+// with rows 16-byte aligned and cols a multiple of 256, on tcgen05: CTA
+// tiles of GEMM_TC_WR weight rows x one or two x tiles of GEMM_TC_XN rows
+// (nmt x tiles).  The x image, s_n, 1 / t_r and the split-K partial sums are
+// workspace written by the launch itself.
+constexpr int GEMM_TC_WR = 128;
+constexpr int GEMM_TC_XN = 128;
 struct GemmParams {
     const uint8_t* W;
     int64_t rows, cols, rowbytes, M, ld_y;
-    uint16_t* xh;
-    uint16_t* xl;
-    float* xs;
-    float* sn;
+    float* sn;               // [nmt * GEMM_TC_XN] x row scales
     float* Y;
     int32_t nmt;
-    // tcgen05 kernel: a tensor map over W (uint32 elements, boxes of one
-    // 256-column chunk x GEMM_TC_WR rows), the x image (pieces in the MMA
-    // operand layout), 1 / t_r per weight row, the bound on its waits and the
-    // status word
-    CUtensorMap tmw;
-    uint8_t* ximg;
-    float* tinv;
+    CUtensorMap tmw;         // W as uint32 elements, boxes of one 256-column chunk x GEMM_TC_WR rows
+    uint8_t* ximg;           // the x pieces in the MMA operand layout
+    float* tinv;             // [rows] 1 / t_r
     float* part;             // split-K partial sums [ksplit][M][rows] (ksplit > 1)
     int32_t ksplit;          // K ranges per output tile
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;     // bound on every wait
     unsigned* status;
 };
-int gemm_xn(int fmt);
-size_t gemm_smem_bytes(int fmt);
 cudaError_t gemm_set_smem();
-cudaError_t gemm_launch(int fmt, const GemmParams& P, const float* X, cudaStream_t st);
-// the same on tcgen05 (lq_gemm.cu): CTA tiles of GEMM_TC_WR weight rows x
-// GEMM_TC_XN x rows; the x image is padded to a multiple of GEMM_TC_XN rows
-constexpr int GEMM_TC_WR = 128;
-constexpr int GEMM_TC_XN = 128;
 // K ranges per output tile for a weight matrix of this shape (a function of
 // the weight shape alone, so a row's result does not depend on M)
 int gemm_tc_ksplit(int64_t rows, int64_t cols);

@@ -122,17 +122,17 @@ int lq_matvec_act(int fmt, const void* W, int64_t rows, int64_t cols, const floa
  * many tokens (parity over a grid of (M, K, N)) and ForwardBatch's batched
  * GEMMs; Q4_K weights as in the larql tables.  Q4_K and Q8_0 weights with
  * cols a multiple of 256, 16-byte aligned W and X, and M >= LQ_GEMM_MIN_M
- * run on a tiled tensor-core kernel: from LQ_GEMM_TC_MIN_M x rows on the
- * tcgen05 one (each weight tile read once per 128 x rows), below that an
- * mma.sync one (once per 32 or 64 x rows).  Other calls run lq_matvec's
- * batched kernels (a pass over the weights per 8 x rows) and leave the
- * workspace untouched.
+ * run on the tcgen05 tensor-core kernel (each weight tile read once per 128
+ * or 256 x rows); a row's result depends only on the row, W and its shape,
+ * not on M or on the other rows.  Other calls run lq_matvec's batched
+ * kernels (a pass over the weights per 8 x rows) and leave the workspace
+ * untouched.
  * workspace: lq_gemm_workspace_bytes(M, rows, cols) bytes, 256-byte
- * aligned (LQ_EWORKSPACE / LQ_EALIGN otherwise, checked when a tiled kernel
- * runs): the fp16 pieces of x that the kernel reads and, for the tcgen05
- * kernel, a scale per weight row.  Sizes < 0 give 0. */
+ * aligned (LQ_EWORKSPACE / LQ_EALIGN otherwise, checked when the tiled
+ * kernel runs): the fp16 pieces of x that the kernel reads, a scale per
+ * weight row and, for matrices of few rows, partial sums over K ranges.
+ * Sizes < 0 give 0. */
 #define LQ_GEMM_MIN_M 32
-#define LQ_GEMM_TC_MIN_M 128
 size_t lq_gemm_workspace_bytes(int64_t M, int64_t rows, int64_t cols);
 int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
             void* workspace, size_t ws_bytes, lq_stream_t stream);

@@ -561,8 +561,8 @@ def _gemm(lq, fmt, W, rows, cols, X, w_off=0):
     (128, 256, 64), (130, 2560, 65), (256, 512, 257), (200, 14336, 33), (384, 4096, 130),
 ])
 def test_gemm_parity(lq, fmt, M, cols, rows):
-    """lq_gemm on the tiled kernels over a grid of (M, K, N): below 128 x rows
-    the mma.sync kernel, from 128 the tcgen05 one; ragged x-row and
+    """lq_gemm on the tcgen05 kernel over a grid of (M, K, N): one and two x
+    tiles per CTA, K split into ranges for narrow matrices; ragged x-row and
     weight-row tiles, one to 56 super-blocks per row (the tcgen05 kernel
     accumulates a whole row in tensor memory), against the oracle's matvec
     of every x row."""
@@ -574,13 +574,13 @@ def test_gemm_parity(lq, fmt, M, cols, rows):
     assert_within(got, ref, oracle.matvec_bound(S), f"gemm fmt {fmt} M {M} K {cols} N {rows}")
 
 
-@pytest.mark.parametrize("fmt,M,sub", [(Q4_K, 100, 70), (Q4_K, 300, 150), (Q8_0, 300, 131)])
+@pytest.mark.parametrize("fmt,M,sub", [(Q4_K, 100, 70), (Q4_K, 300, 150), (Q8_0, 300, 131), (Q4_K, 300, 40)])
 def test_gemm_rows_independent_and_deterministic(lq, fmt, M, sub):
-    """A row's result does not depend on the other x rows of the call or on
-    its position in the x-row tile (MMA columns are independent and the sum
-    order is fixed by the shape); two calls give the same bits.  The sub-call
-    takes the same kernel as the full one (both below or both from 128 x
-    rows)."""
+    """A row's result does not depend on the other x rows of the call, on M
+    or on its position in the x-row tile (MMA columns are independent, the
+    sum order and any split of K are fixed by the weight shape); two calls
+    give the same bits.  M 300 takes two x tiles per CTA, the sub-calls one
+    or two; cols 2560 / rows 200 split K into five ranges."""
     cols, rows = 2560, 200
     g = synth.rng(901 + M)
     W = synth.weights(g, fmt, rows, cols)
@@ -595,8 +595,8 @@ def test_gemm_rows_independent_and_deterministic(lq, fmt, M, sub):
 @pytest.mark.parametrize("M", [40, 140])
 def test_gemm_x_scale_extremes(lq, M):
     """x rows of very different magnitudes (per-row scale), a zero row, a row
-    with one huge entry (small values far below it in the same row); both
-    tiled kernels."""
+    with one huge entry (small values far below it in the same row); one x
+    tile (M 40) and two per CTA (M 140)."""
     fmt, cols, rows = Q8_0, 1024, 96
     g = synth.rng(902)
     W = synth.q8_0(g, rows, cols)
