@@ -126,9 +126,14 @@ __device__ __forceinline__ bool gt_wait1(uint64_t* bar, uint32_t parity, uint64_
     return mbar_wait_bounded(bar, parity, timeout_ns);
 }
 
-// Warp-uniform bounded wait (every lane polls).
+// Warp-uniform bounded wait: lane 0 polls (32 lanes polling one barrier
+// serialize on it), then the warp synchronizes, which orders the other
+// lanes' later accesses after lane 0's observation of the phase.
 __device__ __forceinline__ bool gt_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-    return __all_sync(0xFFFFFFFFu, gt_wait1(bar, parity, timeout_ns));
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = gt_wait1(bar, parity, timeout_ns);
+    __syncwarp();
+    return __shfl_sync(0xFFFFFFFFu, ok, 0);
 }
 
 __device__ __forceinline__ uint32_t h2pk(float2 v) {
