@@ -505,8 +505,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "04ea4795dbdc1d3463a085ae9cd86f001605ec1e209e0afcbaccd8bc566f72bf",
-                  "bytes": 29_548_544,
+GATEUP_TRAFFIC = {"csrc_sha256": "bb3d24bb69f5ba480f66e9245f6fc9e501ebe303e069f5e41b77b0a2874486b7",
+                  "bytes": 29_548_032,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from

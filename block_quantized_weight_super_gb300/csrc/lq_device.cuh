@@ -86,6 +86,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     }
 }
 
+// Bound for the waits that let a CTA's own copies (or MMAs) in flight finish
+// before it exits or frees memory they write: at least 10 ms whatever the
+// configured limit, so a very short limit cannot end a CTA with a copy still
+// landing in its shared memory.
+constexpr uint64_t DRAIN_MIN_NS = 10000000ull;
+__device__ __forceinline__ uint64_t drain_bound(uint64_t timeout_ns) {
+    return timeout_ns > DRAIN_MIN_NS ? timeout_ns : DRAIN_MIN_NS;
+}
+
 // ---- thread-block clusters (distributed shared memory)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

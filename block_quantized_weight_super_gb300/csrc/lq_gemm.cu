@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_tc_kernel(const __grid_con
         }
         // the last copy of each stage has landed before the CTA may exit
         for (int s = max(0, issued - NSB); s < issued; ++s)
-            gt_wait(&bfull[s % NSB], (uint32_t)((s / NSB) & 1), P.timeout_ns);
+            gt_wait(&bfull[s % NSB], (uint32_t)((s / NSB) & 1), drain_bound(P.timeout_ns));
     } else if (warp == GT_WLOAD_WARP) {
         // ---- weight bytes: one tensor copy per 256-column chunk (128 rows,
         // rows past the matrix zero-filled)
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_tc_kernel(const __grid_con
             issued = c + 1;
         }
         for (int c = max(0, issued - 2); c < issued; ++c)
-            gt_wait(&wfull[c & 1], (uint32_t)((c / 2) & 1), P.timeout_ns);
+            gt_wait(&wfull[c & 1], (uint32_t)((c / 2) & 1), drain_bound(P.timeout_ns));
     } else if (warp == GT_MMA_WARP) {
         // ---- MMA issue (one thread).  Per tile and 16-column half: A_hi
         // against B (256 rows, hi then lo), then A_lo against B's hi rows.
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_tc_kernel(const __grid_con
                 gt_commit(&aempty[sa]);
             }
             gt_commit(dfull);                              // completes once every MMA issued above has
-            if (!gt_wait1(dfull, 0, P.timeout_ns)) ok = false;
+            if (!gt_wait1(dfull, 0, drain_bound(P.timeout_ns))) ok = false;   // before the memory is freed
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     } else if (bi >= 0) {

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
         // no copy may still be in flight when the CTA exits (every request was
         // waited for unless a warp gave up): wait, bounded, for each requested tile
         for (int i = 0; i < ntile; ++i)
-            if (reqd[i]) mbar_wait_bounded(&full[i], 0u, P.timeout_ns);
+            if (reqd[i]) mbar_wait_bounded(&full[i], 0u, drain_bound(P.timeout_ns));
     }
 }
 

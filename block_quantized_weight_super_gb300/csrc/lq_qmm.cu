@@ -396,8 +396,9 @@ __global__ void __launch_bounds__(32 * (NW + 1), 2) qmm_kernel(const __grid_cons
         // no copy may still be in flight when the CTA exits
         if (lane == 0) {
             for (int s2 = 0; s2 < S_; ++s2)
-                if (last_use[s2] >= 0) mbar_wait_bounded(&full[s2], (uint32_t)last_use[s2] & 1u, P.timeout_ns);
-            if (xn > 0) mbar_wait_bounded(xfull, (uint32_t)(xn - 1) & 1u, P.timeout_ns);
+                if (last_use[s2] >= 0)
+                    mbar_wait_bounded(&full[s2], (uint32_t)last_use[s2] & 1u, drain_bound(P.timeout_ns));
+            if (xn > 0) mbar_wait_bounded(xfull, (uint32_t)(xn - 1) & 1u, drain_bound(P.timeout_ns));
         }
         __syncwarp();
         if (cs > 1) {                            // no CTA leaves while a peer may address it

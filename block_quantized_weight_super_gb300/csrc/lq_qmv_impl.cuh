@@ -710,7 +710,7 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
         if (lane == 0) {
             for (int s2 = 0; s2 < S_; ++s2)
                 if (last_use[s2] >= 0)
-                    mbar_wait_bounded(&sm.full[s2], (uint32_t)last_use[s2] & 1u, P.timeout_ns);
+                    mbar_wait_bounded(&sm.full[s2], (uint32_t)last_use[s2] & 1u, drain_bound(P.timeout_ns));
         }
         return;
     }

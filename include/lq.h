@@ -289,7 +289,9 @@ int lq_moe_ffn_static(const float* router, int n_experts, int topk, int fmt, con
 int lq_device_status(lq_stream_t stream, uint32_t* bits);
 
 /* lq_set_wait_timeout_ns -- wall-time limit of every bounded wait in later
- * launches (default 1e9 ns).  Process-wide. */
+ * launches (default 1e9 ns).  Process-wide.  The waits with which a CTA lets
+ * its own copies and MMAs in flight finish before it exits use at least
+ * 10 ms whatever this limit. */
 void lq_set_wait_timeout_ns(uint64_t ns);
 
 /* lq_probe_timeout -- failure-detection check: launches a kernel that waits,
