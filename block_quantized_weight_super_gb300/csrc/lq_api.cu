@@ -221,6 +221,113 @@ struct XPre {
     float* out = nullptr;
 };
 
+// ---------------------------------------------------------------- launch plans
+// Plans of recent launches, keyed by everything that shapes them: the
+// segments (matrices, buffers, shapes, modes), cols, the batch width, the x
+// transform and the context.  A decode loop repeats the same calls on the
+// same buffers, and a plan (CTA partition, tile ring, occupancy) costs
+// several microseconds of host time, more than the launch itself.  Keys are
+// compared byte for byte (every key is zeroed before it is filled); on a hit
+// only the wait limit and the status word are refreshed.
+constexpr int PLAN_SEGS = 8;
+constexpr int PLAN_ENTRIES = 512;          // a model's layers x calls per layer
+struct PlanKey {
+    unsigned long long ctx;
+    int64_t cols;
+    int32_t B, nseg, xkind, xact;
+    float eps;
+    int32_t pad;
+    const float* xout;
+    const float* xnw;
+    Seg seg[PLAN_SEGS];
+};
+static_assert(sizeof(PlanKey) % 8 == 0, "plan keys are hashed as 64-bit words");
+
+static bool plan_key(PlanKey& k, unsigned long long ctx, const std::vector<Seg>& segs, int64_t cols, int B,
+                     const XPre* xp) {
+    if (segs.size() > (size_t)PLAN_SEGS) return false;
+    memset(&k, 0, sizeof k);
+    k.ctx = ctx;
+    k.cols = cols;
+    k.B = B;
+    k.nseg = (int32_t)segs.size();
+    if (xp) {
+        k.xkind = xp->kind;
+        k.xact = xp->act;
+        k.eps = xp->eps;
+        k.xout = xp->out;
+        k.xnw = xp->nw;
+    } else {
+        k.xkind = -1;
+    }
+    for (size_t i = 0; i < segs.size(); ++i) memcpy(&k.seg[i], &segs[i], sizeof(Seg));
+    return true;
+}
+
+static uint64_t plan_hash(const PlanKey& k) {
+    uint64_t w[sizeof(PlanKey) / 8];
+    memcpy(w, &k, sizeof k);
+    uint64_t h = 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : w) {
+        h ^= v;
+        h *= 0xBF58476D1CE4E5B9ull;
+        h ^= h >> 31;
+    }
+    return h;
+}
+
+// A fixed ring of entries with a hash index; a hit is confirmed by
+// comparing the whole key, and the oldest entry gives way to a new one.
+template <class V>
+struct PlanCache {
+    std::mutex mu;
+    std::vector<PlanKey> key;
+    std::vector<V> val;
+    std::vector<uint64_t> hash;
+    std::unordered_map<uint64_t, int> index;
+    int n = 0, next = 0;
+    bool find(const PlanKey& k, V& v) {
+        const uint64_t h = plan_hash(k);
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = index.find(h);
+        if (it == index.end() || memcmp(&key[it->second], &k, sizeof k) != 0) return false;
+        v = val[it->second];
+        return true;
+    }
+    void put(const PlanKey& k, const V& v) {
+        const uint64_t h = plan_hash(k);
+        std::lock_guard<std::mutex> lk(mu);
+        if (key.empty()) {
+            key.resize(PLAN_ENTRIES);
+            val.resize(PLAN_ENTRIES);
+            hash.resize(PLAN_ENTRIES);
+        }
+        if (n == PLAN_ENTRIES) {
+            auto it = index.find(hash[next]);
+            if (it != index.end() && it->second == next) index.erase(it);
+        }
+        key[next] = k;
+        val[next] = v;
+        hash[next] = h;
+        index[h] = next;
+        next = (next + 1) % PLAN_ENTRIES;
+        n = std::min(n + 1, PLAN_ENTRIES);
+    }
+};
+
+struct GvPlan {
+    GvParams P;
+    int mask, ncta;
+    size_t smem;
+};
+struct QmvPlan {
+    QmvParams P;
+    int mask, B, grid, nt;
+    size_t smem;
+};
+static PlanCache<GvPlan> g_gv_plans;
+static PlanCache<QmvPlan> g_qmv_plans;
+
 int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* pre);
 
 // Run the segments (all sharing cols and the batch width B): at batch 1 the
@@ -244,6 +351,17 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
             s.xact = pre->act;
             s.xout = pre->out;
         }
+    }
+    PlanKey key;
+    const bool keyed = plan_key(key, dev->ctx, segs, cols, B, nullptr);
+    QmvPlan qp;
+    if (keyed && g_qmv_plans.find(key, qp)) {
+        qp.P.timeout_ns = g_timeout_ns.load();
+        qp.P.status = dev->status;
+        cudaError_t e = qp.B == 1 ? qmv1_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st)
+                      : qp.B == 2 ? qmv2_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st)
+                                  : qmv4_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st);
+        return e == cudaSuccess ? LQ_OK : cuda_fail(e, "qmv launch");
     }
     // formats in order of first appearance (at most two per launch)
     std::vector<int> fmts;
@@ -326,6 +444,15 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
           : B == 2 ? qmv2_launch(mask, P, grid, nt, pl.smem, st)
                    : qmv4_launch(mask, P, grid, nt, pl.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "qmv launch");
+        if (keyed && order.size() <= (size_t)MAX_SEG) {
+            qp.P = P;
+            qp.mask = mask;
+            qp.B = B;
+            qp.grid = grid;
+            qp.nt = nt;
+            qp.smem = pl.smem;
+            g_qmv_plans.put(key, qp);
+        }
     }
     return LQ_OK;
 }
@@ -420,6 +547,15 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XP
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
+    PlanKey key;
+    const bool keyed = plan_key(key, dev->ctx, segs, cols, 1, xp ? xp : nullptr);
+    GvPlan gp;
+    if (keyed && g_gv_plans.find(key, gp)) {
+        gp.P.timeout_ns = g_timeout_ns.load();
+        gp.P.status = dev->status;
+        cudaError_t e = gv_launch(gp.mask, gp.P, gp.ncta, gp.smem, st);
+        return e == cudaSuccess ? LQ_OK : cuda_fail(e, "batch-1 tensor-core matvec launch");
+    }
     const int nsb = (int)(cols / 256);
     GvParams P;
     memset(&P, 0, sizeof P);
@@ -498,7 +634,15 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XP
     for (int k = 0; k <= ncta; ++k) P.cta_rb[k] = b[k];
     const size_t smem = gv_layout(mask, ns, slot, mxt, nsb, ns).total;
     cudaError_t e = gv_launch(mask, P, ncta, smem, st);
-    return e == cudaSuccess ? LQ_OK : cuda_fail(e, "batch-1 tensor-core matvec launch");
+    if (e != cudaSuccess) return cuda_fail(e, "batch-1 tensor-core matvec launch");
+    if (keyed) {
+        gp.P = P;
+        gp.mask = mask;
+        gp.ncta = ncta;
+        gp.smem = smem;
+        g_gv_plans.put(key, gp);
+    }
+    return LQ_OK;
 }
 
 // ---------------------------------------------------------------- tensor-core path

@@ -91,6 +91,38 @@ def test_matvec_parity(lq, fmt, rows, cols, batch):
     assert_within(host(y), ref, oracle.matvec_bound(S), f"fmt {fmt} {rows}x{cols} b{batch}")
 
 
+def test_repeated_calls_reuse_plans(lq):
+    """The library keeps the launch plans of recent calls (keyed by every
+    pointer, shape and option of the call): repeated calls on the same
+    buffers with new contents, the same weights into a new output buffer, a
+    changed wait limit, and calls alternating between the batch-1 kernels,
+    each against the oracle, and a repeat of a call gives the same bits."""
+    cases = [(Q4_K, 300, 2560), (Q6_K, 260, 10240), (Q8_0, 70, 4096)]
+    data = []
+    for fmt, rows, cols in cases:
+        g = synth.rng(4242 + fmt)
+        W = synth.weights(g, fmt, rows, cols)
+        data.append((fmt, rows, cols, W, dev(W), torch.empty((1, cols), device="cuda"), empty((1, rows))))
+    try:
+        for it in range(3):
+            for fmt, rows, cols, W, Wd, xd, yd in data:
+                x = synth.activations(synth.rng(777 + 10 * it + fmt), 1, cols)
+                xd.copy_(torch.from_numpy(x))
+                if it == 1:
+                    lq.lq_set_wait_timeout_ns(2_000_000_000)
+                lq.lq_matvec(fmt, Wd, rows, cols, xd, yd, 1)
+                got = host(yd)
+                ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+                assert_within(got, ref, oracle.matvec_bound(S), f"repeat {it} fmt {fmt}")
+                lq.lq_matvec(fmt, Wd, rows, cols, xd, yd, 1)
+                assert np.array_equal(host(yd), got)
+                y2 = empty((1, rows))                     # same weights and x, another output buffer
+                lq.lq_matvec(fmt, Wd, rows, cols, xd, y2, 1)
+                assert np.array_equal(host(y2), got)
+    finally:
+        lq.lq_set_wait_timeout_ns(1_000_000_000)
+
+
 # Which kernel a call takes (the library chooses by shape and alignment):
 #   "gv": batch 1, Q4_K alone or Q4_K with Q6_K in one launch, columns a
 #         multiple of 256, 16-row tiles of at most 48 KB, weights 4-byte
