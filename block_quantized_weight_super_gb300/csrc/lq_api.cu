@@ -544,6 +544,9 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XP
         mask |= s.fmt == FMT_Q4_K ? 1 : 2;
     }
     if (!(mask & 1)) return GV_NOT_ELIGIBLE;
+    // the kernel instances are gv_kernel<1> (Q4_K) and gv_kernel<3> (both
+    // formats): the shared-memory layout is sized for the instance launched
+    mask = mask == 1 ? 1 : 3;
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
