@@ -591,25 +591,29 @@ class Workload:
             M = args.batch
             W, X = synth.llama_ffn(fmt, M, seed=0)
             H, I = synth.LLAMA_HIDDEN, synth.LLAMA_INTER
-            base = {"wg": up(W["wg"]), "wd": up(W["wd"])}
-            self.bytes = self.dom_bytes = base["wg"].numel() + base["wd"].numel()
+            rb = lq.lq_row_bytes(fmt, H)
+            wgu = torch.empty(2 * I * rb, dtype=torch.uint8, device=dev)
+            lq.lq_pack_gate_up(fmt, up(W["wg"]), up(W["wu"]), I, H, wgu)
+            base = {"wgu": wgu, "wd": up(W["wd"])}
+            self.bytes = self.dom_bytes = wgu.numel() + base["wd"].numel()
             self.x_host = X
             self.x = up(X)
-            self.h = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(5), device=dev)
+            self.h = torch.empty((M, I), **f32)
             self.y = torch.empty((M, H), **f32)
-            self.g = torch.empty((M, I), **f32)
-            nws = max(lq.lq_gemm_workspace_bytes(M, I, H), lq.lq_gemm_workspace_bytes(M, H, I))
+            nws = max(lq.lq_gemm_workspace_bytes(M, 2 * I, H), lq.lq_gemm_workspace_bytes(M, H, I))
             self.ws = torch.empty(nws, dtype=torch.uint8, device=dev)
-            self.desc = (f"prefill GEMMs of the Llama-3-8B FFN, {M} x rows, {args.fmt.upper()}: gate 14336x4096 "
-                         f"and down 4096x14336 through lq_gemm")
-            self.dom_name = f"prefill GEMM ({args.fmt.upper()}, M {M}), gemm_tc_kernel"
-            self.dom_flops = 2.0 * M * H * I * 2                   # gate and down, useful multiply-adds x 2
+            self.desc = (f"prefill of the Llama-3-8B SwiGLU FFN, {M} x rows, {args.fmt.upper()}: gate+up 2x14336x4096 "
+                         f"fused with SwiGLU (lq_gemm_gate_up_act), down 4096x14336 (lq_gemm)")
+            self.dom_name = f"prefill FFN ({args.fmt.upper()}, M {M}), gemm_tc_kernel"
+            self.dom_flops = 2.0 * M * H * I * 3                   # gate, up, down: useful multiply-adds x 2
             # per call: scale pre-pass, x image, GEMM; the down projection (4096 rows) adds the split-K sum
             self.launches = 7
-            self.step = lambda w, st: (lq.lq_gemm(fmt, w["wg"], I, H, self.x, self.g, M, self.ws, nws, st),
+            self.step = lambda w, st: (lq.lq_gemm_gate_up_act(fmt, w["wgu"], I, H, self.x, self.h, M, lq.LQ_ACT_SWIGLU,
+                                                              self.ws, nws, st),
                                        lq.lq_gemm(fmt, w["wd"], H, I, self.h, self.y, M, self.ws, nws, st))
             self.dom = self.step
-            self.cpu_jobs = [(fmt, W["wg"], H, X[:1]), (fmt, W["wd"], I, np.zeros((1, I), np.float32))]
+            self.cpu_jobs = [(fmt, W["wg"], H, X[:1]), (fmt, W["wu"], H, X[:1]),
+                             (fmt, W["wd"], I, np.zeros((1, I), np.float32))]
         elif name in ("lm_head", "matvec_small"):
             if name == "lm_head":
                 Wn, x = synth.lm_head(0)
@@ -815,34 +819,38 @@ def config_figures(dev, peak):
         del cs, base, wgu
         torch.cuda.empty_cache()
 
-    # prefill: the Llama-3-8B FFN's gate (14336 x 4096) and down (4096 x 14336)
-    # as GEMMs over M x rows (one weight copy each: the x rows re-use it)
+    # prefill: the Llama-3-8B SwiGLU FFN as GEMMs over M x rows: gate+up
+    # (2 x 14336 x 4096, packed pairs) with the activation fused, then down
+    # (4096 x 14336); one weight copy each (the x rows re-use it)
     for fmt, tag in ((lq.LQ_Q4_K, "q4k"), (lq.LQ_Q8_0, "q80")):
         Wl, _ = synth.llama_ffn(fmt, 1, seed=1)
-        wg, wd = up(Wl["wg"]), up(Wl["wd"])
-        nbw = wg.numel() + wd.numel()
+        wgu = torch.empty(2 * I * lq.lq_row_bytes(fmt, H), dtype=torch.uint8, device=dev)
+        lq.lq_pack_gate_up(fmt, up(Wl["wg"]), up(Wl["wu"]), I, H, wgu)
+        wd = up(Wl["wd"])
+        nbw = wgu.numel() + wd.numel()
         for M in (64, 128, 512):
             Xg = torch.randn((M, H), generator=torch.Generator(device=dev).manual_seed(M), device=dev)
-            Xd = torch.randn((M, I), generator=torch.Generator(device=dev).manual_seed(M + 1), device=dev)
-            Yg, Yd = torch.empty((M, I), **f32), torch.empty((M, H), **f32)
-            nws = max(lq.lq_gemm_workspace_bytes(M, I, H), lq.lq_gemm_workspace_bytes(M, H, I))
+            Hh, Yd = torch.empty((M, I), **f32), torch.empty((M, H), **f32)
+            nws = max(lq.lq_gemm_workspace_bytes(M, 2 * I, H), lq.lq_gemm_workspace_bytes(M, H, I))
             wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
 
-            def step(w, s, M=M, Xg=Xg, Xd=Xd, Yg=Yg, Yd=Yd, wsp=wsp, nws=nws):
-                lq.lq_gemm(fmt, wg, I, H, Xg, Yg, M, wsp, nws, s)
-                lq.lq_gemm(fmt, wd, H, I, Xd, Yd, M, wsp, nws, s)
+            def step(w, s, M=M, Xg=Xg, Hh=Hh, Yd=Yd, wsp=wsp, nws=nws):
+                lq.lq_gemm_gate_up_act(fmt, wgu, I, H, Xg, Hh, M, lq.LQ_ACT_SWIGLU, wsp, nws, s)
+                lq.lq_gemm(fmt, wd, H, I, Hh, Yd, M, wsp, nws, s)
             ms = timed_graphs(step, [None], 20, 3, st)
-            out[f"prefill_gemm_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=4.0 * M * H * I / (ms * 1e-3) / 1e12,
-                                                    what="gate 14336x4096 + down 4096x14336, lq_gemm")
+            out[f"prefill_ffn_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=6.0 * M * H * I / (ms * 1e-3) / 1e12,
+                                                   what="gate+up 2x14336x4096 with SwiGLU (lq_gemm_gate_up_act) "
+                                                        "+ down 4096x14336 (lq_gemm)")
             if M == 512 and tag == "q4k":
-                def step_mv(w, s, M=M, Xg=Xg, Xd=Xd, Yg=Yg, Yd=Yd):
-                    lq.lq_matvec(fmt, wg, I, H, Xg, Yg, M, s)
-                    lq.lq_matvec(fmt, wd, H, I, Xd, Yd, M, s)
+                def step_mv(w, s, M=M, Xg=Xg, Hh=Hh, Yd=Yd):
+                    lq.lq_ffn_gate_up_act(fmt, wgu, I, H, Xg, Hh, M, lq.LQ_ACT_SWIGLU, s)
+                    lq.lq_matvec(fmt, wd, H, I, Hh, Yd, M, s)
                 ms = timed_graphs(step_mv, [None], 10, 3, st)
-                out[f"prefill_matvec_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=4.0 * M * H * I / (ms * 1e-3) / 1e12,
-                                                          what="the same through lq_matvec (8 x rows per pass)")
-            del Xg, Xd, Yg, Yd, wsp
-        del wg, wd
+                out[f"prefill_ffn_batched_{tag}_M{M}"] = dict(fig(ms, nbw, 1), tflops=6.0 * M * H * I / (ms * 1e-3) / 1e12,
+                                                               what="the same through lq_ffn_gate_up_act + lq_matvec "
+                                                                    "(8 x rows per pass)")
+            del Xg, Hh, Yd, wsp
+        del wgu, wd
         torch.cuda.empty_cache()
 
     # config 3: lm_head Q4_K 262144 x 2560, batch 1 (one copy: larger than L2)

@@ -21,7 +21,7 @@ LQ_ACT_GEGLU_TANH, LQ_ACT_SWIGLU = 1, 2
  LQ_EUNSUPPORTED) = range(8)
 
 EXPORTS = ["lq_block_bytes", "lq_block_elems", "lq_row_bytes", "lq_status_str", "lq_last_error",
-           "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_matvec_act", "lq_gemm_workspace_bytes", "lq_gemm", "lq_gemv_f16", "lq_gemv_f32", "lq_rmsnorm", "lq_qkv_mixed",
+           "lq_dequant", "lq_matvec", "lq_matvec_softcap", "lq_matvec_act", "lq_gemm_workspace_bytes", "lq_gemm", "lq_gemm_gate_up_act", "lq_gemv_f16", "lq_gemv_f32", "lq_rmsnorm", "lq_qkv_mixed",
            "lq_qkv_mixed_rmsnorm", "lq_pack_gate_up", "lq_ffn_gate_up_act", "lq_ffn_gate_up_act_rmsnorm",
            "lq_ffn", "lq_moe_workspace_bytes", "lq_moe_ffn", "lq_moe_ffn_ex_workspace_bytes", "lq_moe_ffn_ex",
            "lq_moe_ffn_static",
@@ -62,6 +62,7 @@ def lib():
             "lq_matvec_act": ([i32, vp, i64, i64, vp, vp, vp, i32, i32, vp], i32),
             "lq_gemm_workspace_bytes": ([i64, i64, i64], sz),
             "lq_gemm": ([i32, vp, i64, i64, vp, vp, i64, vp, sz, vp], i32),
+            "lq_gemm_gate_up_act": ([i32, vp, i64, i64, vp, vp, i64, i32, vp, sz, vp], i32),
             "lq_gemv_f16": ([vp, i64, i64, vp, vp, i32, vp], i32),
             "lq_gemv_f32": ([vp, i64, i64, vp, vp, i32, vp], i32),
             "lq_rmsnorm": ([vp, vp, C.c_float, vp, i32, i64, vp], i32),
@@ -158,6 +159,11 @@ def lq_gemm_workspace_bytes(M, rows, cols) -> int:
 def lq_gemm(fmt, W, rows, cols, X, Y, M, workspace=None, ws_bytes=0, stream=None):
     return _check(lib().lq_gemm(fmt, _ptr(W), rows, cols, _ptr(X), _ptr(Y), M, _ptr(workspace), ws_bytes,
                                 _stream(stream)))
+
+
+def lq_gemm_gate_up_act(fmt, Wgu, inter, cols, X, H, M, act, workspace=None, ws_bytes=0, stream=None):
+    return _check(lib().lq_gemm_gate_up_act(fmt, _ptr(Wgu), inter, cols, _ptr(X), _ptr(H), M, act, _ptr(workspace),
+                                            ws_bytes, _stream(stream)))
 
 
 def lq_gemv_f16(W, rows, cols, x, y, batch, stream=None):

@@ -1074,29 +1074,16 @@ size_t lq_gemm_workspace_bytes(int64_t M, int64_t rows, int64_t cols) {
            (ks > 1 ? align256((size_t)ks * M * rows * 4) : 0);
 }
 
-int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
-            void* workspace, size_t ws_bytes, lq_stream_t stream) {
-    g_err[0] = 0;
-    int rc = check_mat(fmt, W, rows, cols, "W");
-    if (rc) return rc;
-    if (M < 1 || M > (int64_t)1 << 24) return fail(LQ_EINVAL, "M %lld", (long long)M);
-    if (rows == 0) return LQ_OK;
-    if ((rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y"))) return rc;
-    const bool tiled = (fmt == FMT_Q4_K || fmt == FMT_Q8_0) && cols % 256 == 0 && M >= LQ_GEMM_MIN_M &&
-                       al(W, 16) && al(X, 16) && rowbytes(fmt, cols) % 16 == 0;
-    if (!tiled) {
-        // the batched matvec (a pass over the weights per 8 x rows)
-        for (int64_t b0 = 0; b0 < M; b0 += 1 << 20) {
-            const int nb = (int)std::min<int64_t>(1 << 20, M - b0);
-            if ((rc = matvec_impl(fmt, W, rows, cols, X + b0 * cols, Y + b0 * rows, nb, 0.f, stream))) return rc;
-        }
-        return LQ_OK;
-    }
+// The tiled GEMM of lq_gemm and lq_gemm_gate_up_act: Y[n][r] (plain) or
+// Y[n][i] = act(row 2i) * row 2i + 1 (pairs), W of `rows` rows.
+static int gemm_tiled(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t ld_y,
+                      int64_t M, int pairs, int act, void* workspace, size_t ws_bytes, lq_stream_t stream) {
     const size_t need = lq_gemm_workspace_bytes(M, rows, cols);
     if (!workspace || ws_bytes < need) return fail(LQ_EWORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
     if (!al(workspace, 256)) return fail(LQ_EALIGN, "workspace not 256-byte aligned");
     DevInfo* dev = nullptr;
-    if ((rc = dev_info(&dev))) return rc;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
     uint8_t* p = static_cast<uint8_t*>(workspace);
     GemmParams P;
     memset(&P, 0, sizeof P);
@@ -1105,7 +1092,9 @@ int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, 
     P.cols = cols;
     P.rowbytes = rowbytes(fmt, cols);
     P.M = M;
-    P.ld_y = rows;
+    P.ld_y = ld_y;
+    P.pairs = pairs;
+    P.act = act;
     P.nmt = (int32_t)((M + GEMM_TC_XN - 1) / GEMM_TC_XN);
     if ((rc = tensor_map(&P.tmw, W, rows, P.rowbytes, P.rowbytes, (int)(P.rowbytes / (cols / 256) / 4), GEMM_TC_WR)))
         return rc;
@@ -1120,6 +1109,51 @@ int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, 
     P.status = dev->status;
     cudaError_t e = gemm_tc_launch(fmt, P, X, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LQ_OK : cuda_fail(e, "gemm launch");
+}
+
+static bool gemm_is_tiled(int fmt, const void* W, int64_t cols, const float* X, int64_t M) {
+    return (fmt == FMT_Q4_K || fmt == FMT_Q8_0) && cols % 256 == 0 && M >= LQ_GEMM_MIN_M && al(W, 16) && al(X, 16) &&
+           rowbytes(fmt, cols) % 16 == 0;
+}
+
+int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
+            void* workspace, size_t ws_bytes, lq_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_mat(fmt, W, rows, cols, "W");
+    if (rc) return rc;
+    if (M < 1 || M > (int64_t)1 << 24) return fail(LQ_EINVAL, "M %lld", (long long)M);
+    if (rows == 0) return LQ_OK;
+    if ((rc = check_f32(X, "X")) || (rc = check_f32(Y, "Y"))) return rc;
+    if (!gemm_is_tiled(fmt, W, cols, X, M)) {
+        // the batched matvec (a pass over the weights per 8 x rows)
+        for (int64_t b0 = 0; b0 < M; b0 += 1 << 20) {
+            const int nb = (int)std::min<int64_t>(1 << 20, M - b0);
+            if ((rc = matvec_impl(fmt, W, rows, cols, X + b0 * cols, Y + b0 * rows, nb, 0.f, stream))) return rc;
+        }
+        return LQ_OK;
+    }
+    return gemm_tiled(fmt, W, rows, cols, X, Y, rows, M, 0, 0, workspace, ws_bytes, stream);
+}
+
+int lq_gemm_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* X, float* H, int64_t M,
+                        int act, void* workspace, size_t ws_bytes, lq_stream_t stream) {
+    g_err[0] = 0;
+    if (act != LQ_ACT_GEGLU_TANH && act != LQ_ACT_SWIGLU) return fail(LQ_EINVAL, "act %d", act);
+    if (inter < 0 || inter > (int64_t)1 << 29) return fail(LQ_ESHAPE, "inter %lld", (long long)inter);
+    int rc = check_mat(fmt, Wgu, 2 * inter, cols, "Wgu");
+    if (rc) return rc;
+    if (M < 1 || M > (int64_t)1 << 24) return fail(LQ_EINVAL, "M %lld", (long long)M);
+    if (inter == 0) return LQ_OK;
+    if ((rc = check_f32(X, "X")) || (rc = check_f32(H, "H"))) return rc;
+    if (!gemm_is_tiled(fmt, Wgu, cols, X, M)) {
+        // the batched gate+up kernels (a pass over the weights per 8 x rows)
+        for (int64_t b0 = 0; b0 < M; b0 += 1 << 20) {
+            const int nb = (int)std::min<int64_t>(1 << 20, M - b0);
+            if ((rc = gate_up_impl(fmt, Wgu, inter, cols, X + b0 * cols, H + b0 * inter, nb, act, stream))) return rc;
+        }
+        return LQ_OK;
+    }
+    return gemm_tiled(fmt, Wgu, 2 * inter, cols, X, H, inter, M, 1, act, workspace, ws_bytes, stream);
 }
 
 static int gemv_dense(bool f16, const void* W, int64_t rows, int64_t cols, const float* x, float* y, int batch,

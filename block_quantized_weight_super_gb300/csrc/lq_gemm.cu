@@ -34,6 +34,11 @@
 // accumulator sees the same sequence either way, so a row's result does not
 // depend on NX.
 //
+// Gate / up pairs (the packed matrix of lq_pack_gate_up, rows 2i and 2i + 1
+// the gate and up rows of output i): the epilogue scales both sums, the odd
+// lane hands its up value to the even one by a shuffle, and the even lane
+// stores act(g) * u.
+//
 // Split K: where the weight matrix has few 128-row tiles the row is cut
 // into ksplit ranges of whole 256-column chunks (gemm_tc_ksplit, a
 // function of the weight shape alone); each CTA stores its raw partial sums
@@ -290,6 +295,26 @@ __global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const float* __rest
     }
 }
 
+// The same for gate / up pairs: H[n][i] = act(g) * u with g, u the scaled
+// sums of rows 2i and 2i + 1; a thread per output
+__global__ void __launch_bounds__(256) gemm_tc_reduce_pairs_kernel(const float* __restrict__ part, int ksplit,
+                                                                   int64_t M, int64_t rows, const float* __restrict__ tinv,
+                                                                   const float* __restrict__ sn, int act,
+                                                                   float* __restrict__ H) {
+    const int64_t n = blockIdx.x, i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x, inter = rows / 2;
+    if (i >= inter) return;
+    const int64_t total = M * rows, o = n * rows + 2 * i;
+    float g = part[o], u = part[o + 1];
+    for (int k = 1; k < ksplit; ++k) {
+        g += part[(int64_t)k * total + o];
+        u += part[(int64_t)k * total + o + 1];
+    }
+    const float s = __ldg(sn + n);
+    g = (g * (1.0f / tinv[2 * i])) * s;
+    u = (u * (1.0f / tinv[2 * i + 1])) * s;
+    H[n * inter + i] = act_eval(act, g) * u;
+}
+
 template <int FMT, int NX>
 __global__ void __launch_bounds__(GT_THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams P) {
     using F = GtF<FMT, NX>;
@@ -497,22 +522,27 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemm_tc_kernel(const __grid_con
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16) + 256u * (uint32_t)t + (uint32_t)cb;
         if (ok && t < ntile) {
             const float tr = r < P.rows ? 1.0f / P.tinv[r] : 0.f;           // exact: a power of two
-            float* part = P.ksplit > 1 ? P.part + (int64_t)ks * P.M * P.ld_y : nullptr;
+            float* part = P.ksplit > 1 ? P.part + (int64_t)ks * P.M * P.rows : nullptr;
 #pragma unroll 1
             for (int c = 0; c < cn; c += 16) {
                 uint32_t x0[16], x1[16];
                 tmem_ld16(tl + (uint32_t)c, x0);
                 tmem_ld16(tl + 128u + (uint32_t)c, x1);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (live) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int64_t n = nb + c + e;
-                        if (n < P.M) {
-                            const float v = __uint_as_float(x0[e]) + __uint_as_float(x1[e]);
-                            if (part) part[n * P.ld_y + r] = v;
-                            else P.Y[n * P.ld_y + r] = (v * tr) * __ldg(P.sn + n);
-                        }
+                for (int e = 0; e < 16; ++e) {
+                    const int64_t n = nb + c + e;
+                    const bool on = live && n < P.M;
+                    const float v = __uint_as_float(x0[e]) + __uint_as_float(x1[e]);
+                    if (part) {
+                        if (on) part[n * P.rows + r] = v;
+                    } else if (!P.pairs) {
+                        if (on) P.Y[n * P.ld_y + r] = (v * tr) * __ldg(P.sn + n);
+                    } else {
+                        // gate in the even lane, up in the odd one (rows 2i, 2i + 1)
+                        const float sv = on ? (v * tr) * __ldg(P.sn + n) : 0.f;
+                        const float up = __shfl_xor_sync(0xFFFFFFFFu, sv, 1);
+                        if (on && (lane & 1) == 0) P.Y[n * P.ld_y + (r >> 1)] = act_eval(P.act, sv) * up;
                     }
                 }
             }
@@ -580,8 +610,14 @@ cudaError_t gemm_tc_launch(int fmt, const GemmParams& P, const float* X, cudaStr
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (P.ksplit > 1) {
         if ((P.rows + 1023) / 1024 > 65535) return cudaErrorInvalidValue;
-        const dim3 rgrid((unsigned)P.M, (unsigned)((P.rows + 1023) / 1024));
-        gemm_tc_reduce_kernel<<<rgrid, 256, 0, st>>>(P.part, P.ksplit, P.M, P.rows, P.tinv, P.sn, P.Y);
+        if (P.pairs) {
+            const dim3 rgrid((unsigned)P.M, (unsigned)((P.rows / 2 + 255) / 256));
+            gemm_tc_reduce_pairs_kernel<<<rgrid, 256, 0, st>>>(P.part, P.ksplit, P.M, P.rows, P.tinv, P.sn, P.act,
+                                                               P.Y);
+        } else {
+            const dim3 rgrid((unsigned)P.M, (unsigned)((P.rows + 1023) / 1024));
+            gemm_tc_reduce_kernel<<<rgrid, 256, 0, st>>>(P.part, P.ksplit, P.M, P.rows, P.tinv, P.sn, P.Y);
+        }
         e = cudaGetLastError();
     }
     return e;

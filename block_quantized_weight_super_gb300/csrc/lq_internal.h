@@ -159,6 +159,8 @@ struct GemmParams {
     float* tinv;             // [rows] 1 / t_r
     float* part;             // split-K partial sums [ksplit][M][rows] (ksplit > 1)
     int32_t ksplit;          // K ranges per output tile
+    int32_t pairs;           // rows 2i, 2i + 1 are gate / up: Y[n][i] = act(gate) * up
+    int32_t act;             // with pairs: ACT_GEGLU_TANH or ACT_SWIGLU
     uint64_t timeout_ns;     // bound on every wait
     unsigned* status;
 };

@@ -137,6 +137,21 @@ size_t lq_gemm_workspace_bytes(int64_t M, int64_t rows, int64_t cols);
 int lq_gemm(int fmt, const void* W, int64_t rows, int64_t cols, const float* X, float* Y, int64_t M,
             void* workspace, size_t ws_bytes, lq_stream_t stream);
 
+/* lq_gemm_gate_up_act -- the prefill FFN's gate and up GEMMs with the
+ * activation fused before the store: H[n][i] = act(g_i . X[n]) * (u_i . X[n])
+ * over the packed matrix Wgu of lq_pack_gate_up (rows 2i, 2i + 1 the gate
+ * and up rows of output i; [2 inter][cols]) for M x rows (X: [M][cols],
+ * H: [M][inter] fp32).  The prefill counterpart of lq_ffn_gate_up_act
+ * (larql Gemma 3 table, FFN gate+up row; dotLLM PR #320 ForwardBatch for
+ * the many-token form): the same kernel and conditions as lq_gemm, with the
+ * x pieces built once for both matrices; other calls run the batched
+ * lq_ffn_gate_up_act kernels.  act as lq_ffn_gate_up_act (LQ_EINVAL
+ * otherwise).  workspace: lq_gemm_workspace_bytes(M, 2 * inter, cols)
+ * bytes, 256-byte aligned.  Each output is within the bound the oracle's
+ * gate_up check states for the matvec bounds of g and u. */
+int lq_gemm_gate_up_act(int fmt, const void* Wgu, int64_t inter, int64_t cols, const float* X, float* H, int64_t M,
+                        int act, void* workspace, size_t ws_bytes, lq_stream_t stream);
+
 /* lq_gemv_f16, lq_gemv_f32 -- y[b][r] = sum_j W[r][j] x[b][j] for a
  * non-quantized W, fp16 or fp32, [rows][cols] row-major, 16-byte aligned:
  * the lm_head fallbacks for a tied embedding that is not block-quantized

@@ -284,3 +284,18 @@ def test_gemm_validation(lq):
     assert gm(wsb=need - 1) == lq.LQ_EWORKSPACE
     assert gm(ws=None) == lq.LQ_EWORKSPACE
     assert gm(ws=FAKE + 16) == lq.LQ_EALIGN
+
+
+def test_gemm_gate_up_validation(lq):
+    L = lq.lib()
+    need = lq.lq_gemm_workspace_bytes(64, 256, 2560)
+    gu = lambda fmt=1, inter=128, M=64, act=1, ws=FAKE, wsb=need: L.lq_gemm_gate_up_act(fmt, FAKE, inter, 2560, FAKE,
+                                                                                        FAKE, M, act, ws, wsb, None)
+    assert gu(act=0) == lq.LQ_EINVAL
+    assert gu(act=3) == lq.LQ_EINVAL
+    assert gu(M=0) == lq.LQ_EINVAL
+    assert gu(fmt=7) == lq.LQ_EINVAL
+    assert gu(inter=-1) == lq.LQ_ESHAPE
+    assert gu(inter=0) == lq.LQ_OK
+    assert gu(wsb=need - 1) == lq.LQ_EWORKSPACE
+    assert gu(ws=FAKE + 16) == lq.LQ_EALIGN

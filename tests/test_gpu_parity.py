@@ -670,6 +670,54 @@ def test_gemm_weight_scale_extremes(lq, fmt):
     assert (got[:, 2] == 0).all()
 
 
+def _gemm_gate_up(lq, fmt, Wg, Wu, inter, cols, X, act):
+    M = X.shape[0]
+    rb = lq.lq_row_bytes(fmt, cols)
+    Wgu = torch.empty(2 * inter * rb, dtype=torch.uint8, device="cuda")
+    lq.lq_pack_gate_up(fmt, dev(Wg), dev(Wu), inter, cols, Wgu)
+    H = empty((M, inter))
+    nb = lq.lq_gemm_workspace_bytes(M, 2 * inter, cols)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    lq.lq_gemm_gate_up_act(fmt, Wgu, inter, cols, dev(X), H, M, act, ws, nb)
+    return host(H)
+
+
+@pytest.mark.parametrize("fmt,inter,cols,M,act", [
+    (Q4_K, 100, 512, 40, 1),        # one x tile, K not split
+    (Q4_K, 300, 2560, 140, 2),      # two x tiles per CTA, K split into 5 ranges
+    (Q8_0, 129, 1024, 33, 1),       # K split into 2, ragged weight tile
+    (Q4_K, 4900, 512, 64, 2),       # 77 weight tiles: K not split
+    (Q4_K, 64, 2560, 16, 1),        # M below the tiled minimum: the batched gate+up kernels
+    (Q6_K, 96, 1024, 40, 2),        # Q6_K: the batched gate+up kernels
+])
+def test_gemm_gate_up_act(lq, fmt, inter, cols, M, act):
+    """The prefill gate+up GEMM with the activation fused before the store,
+    over the packed gate/up matrix, against the oracle's gate/up check (the
+    matvec bounds of g and u carried through the activation)."""
+    g = synth.rng(31 * inter + M + fmt)
+    Wg, Wu = synth.weights(g, fmt, inter, cols), synth.weights(g, fmt, inter, cols)
+    X = synth.activations(g, M, cols)
+    got = _gemm_gate_up(lq, fmt, Wg, Wu, inter, cols, X, act)
+    o = oracle.ffn_gate_up(fmt, Wg, Wu, inter, cols, X, act, NTH)
+    assert_within(got, o["h"], oracle.gate_up_bound(o["g"], o["u"], o["Sg"], o["Su"], act),
+                  f"gemm gate_up fmt {fmt} inter {inter} K {cols} M {M}")
+
+
+def test_gemm_gate_up_act_rows_independent(lq):
+    """A row's h does not depend on M or on the other x rows (the split of K
+    is fixed by the weight shape), and equals the separate GEMMs' act(g) * u
+    within the activation's rounding."""
+    fmt, inter, cols, act = Q4_K, 300, 2560, 1
+    g = synth.rng(9090)
+    Wg, Wu = synth.weights(g, fmt, inter, cols), synth.weights(g, fmt, inter, cols)
+    X = synth.activations(g, 200, cols)
+    a = _gemm_gate_up(lq, fmt, Wg, Wu, inter, cols, X, act)
+    b = _gemm_gate_up(lq, fmt, Wg, Wu, inter, cols, X[50:90], act)
+    assert np.array_equal(b, a[50:90])
+    o = oracle.ffn_gate_up(fmt, Wg, Wu, inter, cols, X[:8], act, NTH)
+    assert_within(a[:8], o["h"], oracle.gate_up_bound(o["g"], o["u"], o["Sg"], o["Su"], act), "first rows")
+
+
 @pytest.mark.parametrize("fmt,M,cols,w_off", [(Q6_K, 64, 2560, 0), (Q4_K, 16, 2560, 0), (Q4_K, 64, 2560, 4),
                                                (Q8_0, 64, 2080, 0)])
 def test_gemm_untiled_calls(lq, fmt, M, cols, w_off):
