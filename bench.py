@@ -505,8 +505,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "bb3d24bb69f5ba480f66e9245f6fc9e501ebe303e069f5e41b77b0a2874486b7",
-                  "bytes": 29_548_032,
+GATEUP_TRAFFIC = {"csrc_sha256": "0c054740ec3b2f0687c8d1fa003e11752ecfbe4b5b0c0f453f41b828db4f7587",
+                  "bytes": 29_548_288,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from
