@@ -60,6 +60,14 @@ struct DevInfo {
     unsigned* status = nullptr;
     int qmm_res[2][3] = {};       // resident tensor-core CTAs / clusters of 2 / of 4 (Q4_K, Q8_0)
     unsigned long long ctx = 0;   // id of the context these were taken in
+    // scratch sets of the column-chunked batch-1 kernel, and the stream that
+    // holds each (a set is bound to the first stream that needs it, for the
+    // life of the context: launches on one stream run in order, so they can
+    // share a set; launches on different streams must not)
+    unsigned* gvw_cnt = nullptr;
+    float* gvw_part = nullptr;
+    cudaStream_t gvw_stream[GVW_SLOTS] = {};
+    bool gvw_bound[GVW_SLOTS] = {};
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -121,6 +129,11 @@ int dev_info(DevInfo** out) {
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
         if (e == cudaSuccess) e = gv_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = gvw_scratch(&d.gvw_cnt, &d.gvw_part);
+        for (int k = 0; k < GVW_SLOTS; ++k) {
+            d.gvw_stream[k] = nullptr;
+            d.gvw_bound[k] = false;
+        }
         if (e == cudaSuccess) e = gemm_set_smem();
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         for (int f = 0; f < 2; ++f) {
@@ -329,6 +342,7 @@ static PlanCache<GvPlan> g_gv_plans;
 static PlanCache<QmvPlan> g_qmv_plans;
 
 int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* pre);
+int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* pre);
 
 // Run the segments (all sharing cols and the batch width B): at batch 1 the
 // tensor-core kernel when it can take them, else the quantized matvec
@@ -342,6 +356,8 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
     if (rc) return rc;
     if (B == 1) {
         rc = run_gv(segs, cols, st, pre);
+        if (rc != GV_NOT_ELIGIBLE) return rc;
+        rc = run_gvw(segs, cols, st, pre);
         if (rc != GV_NOT_ELIGIBLE) return rc;
     }
     if (pre && pre->kind == GV_X_NORM) return NEEDS_PREPASS;
@@ -560,6 +576,7 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XP
         return e == cudaSuccess ? LQ_OK : cuda_fail(e, "batch-1 tensor-core matvec launch");
     }
     const int nsb = (int)(cols / 256);
+    if (nsb > GV_MAX_NSB) return GV_NOT_ELIGIBLE;
     GvParams P;
     memset(&P, 0, sizeof P);
     std::vector<double> rbcost;            // weight bytes of a row block, in Q4_K super-blocks
@@ -645,6 +662,121 @@ int run_gv(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XP
         gp.smem = smem;
         g_gv_plans.put(key, gp);
     }
+    return LQ_OK;
+}
+
+// The scratch set of stream st for the column-chunked kernel: the set bound
+// to st, else a free one (bound now); -1 when every set is bound to another
+// stream.
+static int gvw_slot(DevInfo* dev, cudaStream_t st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int k = 0; k < GVW_SLOTS; ++k)
+        if (dev->gvw_bound[k] && dev->gvw_stream[k] == st) return k;
+    for (int k = 0; k < GVW_SLOTS; ++k)
+        if (!dev->gvw_bound[k]) {
+            dev->gvw_bound[k] = true;
+            dev->gvw_stream[k] = st;
+            return k;
+        }
+    return -1;
+}
+
+struct GvwPlan {
+    GvwParams P;
+    int fmt = 0, ncta = 0;
+    size_t smem = 0;
+};
+static PlanCache<GvwPlan> g_gvw_plans;
+
+// One plain Q4_K or Q6_K matrix at batch 1 that the whole-row kernel does not
+// take (rows too wide for a tile, or Q6_K alone), on the column-chunked
+// kernel: items of 16 rows x ch super-blocks (ch = 7 for Q4_K, 8 for Q6_K:
+// a row piece of 1008 or 1680 bytes, an odd multiple of 16, so the rows a
+// quarter-warp reads fall in distinct banks), spread evenly over one CTA per
+// SM in column-major order.  Needs W 16-byte aligned with rows a multiple of
+// 16 bytes (every row piece one bulk copy) and no input norm (it needs
+// whole rows).
+int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* xp) {
+    if (segs.size() != 1 || cols % 256 != 0 || cols > (1 << 20)) return GV_NOT_ELIGIBLE;
+    const Seg& s = segs[0];
+    if (s.nbatch != 1 || s.b0 != 0 || s.xmap || s.boff || s.bcnt || s.mode != MODE_PLAIN) return GV_NOT_ELIGIBLE;
+    if (s.fmt != FMT_Q4_K && s.fmt != FMT_Q6_K) return GV_NOT_ELIGIBLE;
+    if (xp && (xp->kind == GV_X_NORM || (xp->kind == GV_X_ACT && !al(xp->out, 16)))) return GV_NOT_ELIGIBLE;
+    const int64_t rb = rowbytes(s.fmt, cols);
+    if (!al(s.w, 16) || rb % 16 != 0 || s.nout <= 0) return GV_NOT_ELIGIBLE;
+    DevInfo* dev = nullptr;
+    int rc = dev_info(&dev);
+    if (rc) return rc;
+    PlanKey key;
+    const bool keyed = plan_key(key, dev->ctx, segs, cols, 1, xp ? xp : nullptr);
+    GvwPlan gp;
+    const bool cached = keyed && g_gvw_plans.find(key, gp);
+    if (!cached) {
+        const int span = s.fmt == FMT_Q4_K ? 144 : 210;
+        const int ch = s.fmt == FMT_Q4_K ? 7 : 8;
+        const int nsb = (int)(cols / 256);
+        const int nch = (nsb + ch - 1) / ch;
+        const int64_t nrb = (s.nout + GV_ROWS - 1) / GV_ROWS;
+        // with many row blocks the CUDA-core kernel's row partition is even
+        // already and the cross-CTA chunk sums only cost (measured: Q4_K
+        // 14336 x 8192, 5.9 row blocks per SM, 28.2 us here against 27.3)
+        if (nch > 1 && nrb >= (int64_t)GVW_MAX_RB_PER_SM * dev->sms) return GV_NOT_ELIGIBLE;
+        if (nch > 1 && (nrb > GVW_MAX_RB || (int64_t)nch * nrb * GV_ROWS > GVW_MAX_PART)) return GV_NOT_ELIGIBLE;
+        const int64_t nitems = (int64_t)nch * nrb;
+        if (nitems > (int64_t)GV_MAX_TILES * GV_MAX_CTA) return GV_NOT_ELIGIBLE;
+        const int ncta = (int)std::min<int64_t>(std::min(dev->sms, GV_MAX_CTA), nitems);
+        GvwParams& P = gp.P;
+        memset(&P, 0, sizeof P);
+        int maxtiles = 0, winsb = 0;
+        for (int k = 0; k <= ncta; ++k) P.cta_j[k] = (int32_t)(nitems * k / ncta);
+        for (int k = 0; k < ncta; ++k) {
+            const int64_t jA = P.cta_j[k], jB = P.cta_j[k + 1];
+            maxtiles = std::max(maxtiles, (int)(jB - jA));
+            const int cA = (int)(jA / nrb), cB = (int)((jB - 1) / nrb);
+            winsb = std::max(winsb, std::min(nsb, (cB + 1) * ch) - cA * ch);
+        }
+        if (maxtiles > GV_MAX_TILES || winsb > GV_MAX_NSB) return GV_NOT_ELIGIBLE;
+        const uint32_t slot = ((uint32_t)(GV_ROWS * ch * span) + 127u) & ~127u;
+        int ns = std::min(GV_MAX_INFLIGHT, std::max(2, maxtiles));
+        while (ns >= 2 && gvw_smem_bytes(s.fmt, ns, slot, maxtiles, winsb, ch) > GV_SMEM_MAX) --ns;
+        if (ns < 2) return GV_NOT_ELIGIBLE;
+        P.w = s.w;
+        P.y = s.y;
+        P.x = s.x;
+        P.rowbytes = rb;
+        P.rows = s.nout;
+        P.nsb = nsb;
+        P.ch = ch;
+        P.nch = nch;
+        P.nrb = (int32_t)nrb;
+        P.pitch = ch * span;
+        P.slot_bytes = slot;
+        P.nslots = ns;
+        P.maxtiles = maxtiles;
+        P.winsb = winsb;
+        P.x16 = al(s.x, 16) ? 1 : 0;
+        P.cap = s.cap;
+        if (xp) {
+            P.xpre = xp->kind;
+            P.act = xp->act;
+            P.xout = xp->kind != GV_X_PLAIN ? xp->out : nullptr;
+        }
+        gp.fmt = s.fmt;
+        gp.ncta = ncta;
+        gp.smem = gvw_smem_bytes(s.fmt, ns, slot, maxtiles, winsb, ch);
+    }
+    GvwParams P = gp.P;
+    if (P.nch > 1) {
+        const int k = gvw_slot(dev, st);
+        if (k < 0) return GV_NOT_ELIGIBLE;
+        P.cnt = dev->gvw_cnt + (size_t)k * GVW_MAX_RB;
+        P.part = dev->gvw_part + (size_t)k * GVW_MAX_PART;
+    }
+    P.timeout_ns = g_timeout_ns.load();
+    P.status = dev->status;
+    cudaError_t e = gvw_launch(gp.fmt, P, gp.ncta, gp.smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "batch-1 column-chunked matvec launch");
+    if (keyed && !cached) g_gvw_plans.put(key, gp);
     return LQ_OK;
 }
 

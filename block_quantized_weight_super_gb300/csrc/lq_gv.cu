@@ -17,9 +17,10 @@
 //    mbarrier.  Every tile that has a slot is requested at kernel entry,
 //    before griddepcontrol.wait (weights never depend on the preceding
 //    kernel); a slot is requested again once every unit of its tile is done.
-//  * A tile's units (16 rows x 256 columns) are dealt in pairs of consecutive
-//    units to the warps, round robin, so all warps work on each tile as it
-//    lands and no tile's last units wait on one warp.
+//  * A tile's units (16 rows x 256 columns) go to the warps in pairs of
+//    consecutive units, in order, so all warps work on each tile as it
+//    lands: round robin when a CTA has a few pairs per warp, else from a
+//    shared counter, so that a warp held up takes fewer pairs.
 //  * x (the preceding kernel's output) is read once per CTA after
 //    griddepcontrol.wait and turned into the MMA B images, optionally
 //    RMS-normalised first (the input norm fused in front of QKV or gate+up)
@@ -64,6 +65,22 @@ __device__ __forceinline__ int atom_add_acqrel_cta(int* p, int v) {
     return old;
 }
 
+// Device-scope wrap-around count (atom.inc: the value returned is the count
+// before this arrival; reaching lim + 1 leaves 0), acquire-release.
+__device__ __forceinline__ unsigned atom_inc_acqrel_gpu(unsigned* p, unsigned lim) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(lim) : "memory");
+    return old;
+}
+__device__ __forceinline__ void st_relaxed_gpu(float* p, float v) {
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_relaxed_gpu(const float* p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t h2pack(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
@@ -89,51 +106,99 @@ __device__ __forceinline__ void gv_store(const GvSeg& G, int rb, int r, float v0
     }
 }
 
-// Four consecutive values of the launch's x row from column c, as the
-// matvec sees them before any norm: the row itself, or act(g) * u of its
-// (g, u) pairs (GV_X_ACT).
-__device__ __forceinline__ float4 gv_x4(const GvParams& P, int c) {
+// x chunks per thread in the image build: 32-column blocks bi = 64 it +
+// 4 warp + lane / 8 (it < GV_XIT), so rows of up to 24 super-blocks
+constexpr int GV_XIT = 3;
+static_assert(GV_XIT * GV_NW * 4 * 32 >= GV_MAX_NSB * 256, "image build covers the widest row");
+
+// The raw loads behind four consecutive values of the launch's x row from
+// column c: four floats, or with GV_X_ACT the four (g, u) pairs (a, b).
+struct GvXRaw {
+    float4 a, b;
+};
+template <class XP>
+__device__ __forceinline__ GvXRaw gv_xload(const XP& P, int c) {
+    GvXRaw r;
     if (P.xpre == GV_X_ACT) {
         const float* p = P.x + 2 * (int64_t)c;
-        float4 a, b;
         if (P.x16) {
-            a = __ldcg(reinterpret_cast<const float4*>(p));
-            b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+            r.a = __ldcg(reinterpret_cast<const float4*>(p));
+            r.b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
         } else {
-            a = make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
-            b = make_float4(__ldcg(p + 4), __ldcg(p + 5), __ldcg(p + 6), __ldcg(p + 7));
+            r.a = make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+            r.b = make_float4(__ldcg(p + 4), __ldcg(p + 5), __ldcg(p + 6), __ldcg(p + 7));
         }
-        return make_float4(act_eval(P.act, a.x) * a.y, act_eval(P.act, a.z) * a.w, act_eval(P.act, b.x) * b.y,
-                           act_eval(P.act, b.z) * b.w);
+        return r;
     }
     const float* p = P.x + c;
-    if (P.x16) return __ldcg(reinterpret_cast<const float4*>(p));
-    return make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+    r.a = P.x16 ? __ldcg(reinterpret_cast<const float4*>(p)) : make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+    r.b = make_float4(0.f, 0.f, 0.f, 0.f);
+    return r;
+}
+
+// The four values as the matvec sees them before any norm: the row itself,
+// or act(g) * u of its (g, u) pairs (GV_X_ACT).
+template <class XP>
+__device__ __forceinline__ float4 gv_xval(const XP& P, const GvXRaw& r) {
+    if (P.xpre == GV_X_ACT)
+        return make_float4(act_eval(P.act, r.a.x) * r.a.y, act_eval(P.act, r.a.z) * r.a.w, act_eval(P.act, r.b.x) * r.b.y,
+                           act_eval(P.act, r.b.z) * r.b.w);
+    return r.a;
+}
+
+// The norm weights of this thread's x chunks (GV_X_NORM).  They never
+// depend on the preceding kernel, so they are read before griddepcontrol.wait.
+__device__ __forceinline__ void gv_load_nw(const GvParams& P, int nsb, int warp, int lane, float4 (&nwv)[GV_XIT]) {
+#pragma unroll
+    for (int it = 0; it < GV_XIT; ++it) {
+        const int bi = 64 * it + 4 * warp + (lane >> 3);
+        nwv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (P.xpre == GV_X_NORM && bi < 8 * nsb) nwv[it] = __ldg(reinterpret_cast<const float4*>(P.nw + 32 * bi + 4 * (lane & 7)));
+    }
 }
 
 constexpr uint32_t GV_RED_OFF = 384;      // in the parameter area: the warps' sums of squares
-static_assert(GV_MAX_SEG * sizeof(GvSeg) + 8 <= GV_RED_OFF && GV_RED_OFF + 4 * GV_NW <= GV_PRM_BYTES,
+constexpr uint32_t GV_NEXT_OFF = GV_RED_OFF + 4 * GV_NW;   // the unit counter
+constexpr int GV_DYN_PAIRS = 4 * GV_NW;   // unit pairs of a CTA from which they are handed out by the counter
+static_assert(GV_MAX_SEG * sizeof(GvSeg) + 8 <= GV_RED_OFF && GV_NEXT_OFF + 4 <= GV_PRM_BYTES,
               "parameter area layout");
 
 // The MMA B images and x tables of the launch's x row (eight threads per
 // 32-column block; every thread of the CTA takes part), after the optional
 // RMS-norm or activation of x; CTA 0 stores the resulting row to P.xout.
-template <int MASK>
-__device__ __forceinline__ void gv_images(const GvParams& P, const GvLayout& L, uint8_t* smem, int nsb, int tid,
-                                          int warp, int lane) {
+// x is read once, all of a thread's chunks at the same time (one L2 round
+// trip after griddepcontrol.wait); nwv holds the norm weights of the chunks.
+//   The images cover the nsb super-blocks from super-block sbA of the row
+// (the whole row, or the column window of a CTA's chunks); the super-blocks
+// [st_lo, st_hi) of the window are also stored to P.xout.  The RMS-norm needs
+// the whole row (sbA = 0, nsb = the row's super-blocks).
+template <int MASK, class XP>
+__device__ __forceinline__ void gv_images(const XP& P, const GvLayout& L, uint8_t* smem, int sbA, int nsb, int st_lo,
+                                          int st_hi, int tid, int warp, int lane, const float4 (&nwv)[GV_XIT]) {
     const int nblk = 8 * nsb;
+    const int c0 = 256 * sbA;
+    GvXRaw raw[GV_XIT];
+#pragma unroll
+    for (int it = 0; it < GV_XIT; ++it) {
+        const int bi = 64 * it + 4 * warp + (lane >> 3);
+        if (bi < nblk) raw[it] = gv_xload(P, c0 + 32 * bi + 4 * (lane & 7));
+    }
+    float4 xv[GV_XIT];
+#pragma unroll
+    for (int it = 0; it < GV_XIT; ++it) {
+        const int bi = 64 * it + 4 * warp + (lane >> 3);
+        xv[it] = bi < nblk ? gv_xval(P, raw[it]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     // RMS-norm: every CTA sums the squares in the same fixed order (per
     // thread over its columns, a butterfly over the warp, then the warps
     // in order), so every CTA scales by the same r
     float rn = 1.0f;
     if (P.xpre == GV_X_NORM) {
         float ss = 0.f;
-        for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
-            const int bi = bw + (lane >> 3);
-            if (bi < nblk) {
-                const float4 v = gv_x4(P, 32 * bi + 4 * (lane & 7));
-                ss = fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, ss))));
-            }
+#pragma unroll
+        for (int it = 0; it < GV_XIT; ++it) {
+            const float4 v = xv[it];
+            ss = fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, ss))));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
@@ -144,19 +209,19 @@ __device__ __forceinline__ void gv_images(const GvParams& P, const GvLayout& L, 
         for (int w = 0; w < GV_NW; ++w) t += red[w];
         rn = 1.0f / sqrtf(t / (float)(256 * nsb) + P.eps);
     }
-    for (int bw = warp * 4; bw < nblk; bw += GV_NW * 4) {
-        const int bi = bw + (lane >> 3), j = lane & 7;
+#pragma unroll
+    for (int it = 0; it < GV_XIT; ++it) {
+        const int bi = 64 * it + 4 * warp + (lane >> 3), j = lane & 7;
+        if (64 * it + 4 * warp >= nblk) break;          // warp-uniform: no block of this warp is left
         const bool valid = bi < nblk;
         const int sb = bi >> 3, blk = bi & 7;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = xv[it];
         if (valid) {
-            const int c = 32 * bi + 4 * j;
-            v = gv_x4(P, c);
             if (P.xpre == GV_X_NORM) {
-                const float4 w = __ldg(reinterpret_cast<const float4*>(P.nw + c));
+                const float4 w = nwv[it];
                 v = make_float4((v.x * rn) * w.x, (v.y * rn) * w.y, (v.z * rn) * w.z, (v.w * rn) * w.w);
             }
-            if (P.xout && blockIdx.x == 0) *reinterpret_cast<float4*>(P.xout + c) = v;
+            if (P.xout && sb >= st_lo && sb < st_hi) *reinterpret_cast<float4*>(P.xout + c0 + 32 * bi + 4 * j) = v;
         }
         float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
@@ -224,10 +289,12 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
     // range are copied to shared memory with one round of parallel loads
     GvSeg* segs = reinterpret_cast<GvSeg*>(smem + L.prm);
     int* crng = reinterpret_cast<int*>(smem + L.prm + GV_MAX_SEG * sizeof(GvSeg));
+    int* nextv = reinterpret_cast<int*>(smem + L.prm + GV_NEXT_OFF);   // the next unit pair to hand out
     {
         const int nw = P.nseg * (int)(sizeof(GvSeg) / 4);
         if (tid < nw) reinterpret_cast<uint32_t*>(segs)[tid] = reinterpret_cast<const uint32_t*>(P.seg)[tid];
         if (tid >= 64 && tid < 66) crng[tid - 64] = P.cta_rb[blockIdx.x + tid - 64];
+        if (tid == 96) *nextv = GV_NW;
         for (int i = tid; i < P.maxtiles; i += GV_NW * 32) {
             done[i] = 0;
             reqd[i] = 0;
@@ -274,14 +341,20 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
 
     // every tile that has a slot is requested at entry (warp w: tiles w, w + GV_NW, ...)
     for (int i = warp; i < min(ntile, NS); i += GV_NW) issue_tile(i);
+    float4 nwv[GV_XIT];
+    gv_load_nw(P, nsb, warp, lane, nwv);
     pdl_wait();
 
-    gv_images<MASK>(P, L, smem, nsb, tid, warp, lane);
+    gv_images<MASK>(P, L, smem, 0, nsb, 0, blockIdx.x == 0 ? nsb : 0, tid, warp, lane, nwv);
     __syncthreads();
 
-    // ---- the units: warp w takes the unit pairs v = w, w + GV_NW, ...; pair
-    // v is units 2 (v % hp) and 2 (v % hp) + 1 of tile v / hp (hp pairs per
-    // tile; the last pair of a tile with an odd unit count has one unit)
+    // ---- the units: unit pairs v = 0, 1, ... in order; pair v is units
+    // 2 (v % hp) and 2 (v % hp) + 1 of tile v / hp (hp pairs per tile; the
+    // last pair of a tile with an odd unit count has one unit).  Warp w starts
+    // with pair w.  A CTA with many pairs hands out the next pair from a
+    // shared counter, so a warp held up (waiting for a tile, completing one)
+    // takes fewer; one with a few per warp deals them round robin (v + GV_NW),
+    // which measured faster for the short launches.
     const GvK K = gv_consts();
     const int g = lane >> 2, t = lane & 3;
     const bool bact = (g >> 1) == t;                       // lanes holding B values
@@ -294,7 +367,8 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
     const int hp = (nsb + 1) / 2;
     int waited = -1;
     bool aborted = false;
-    for (int v = warp; v < ntile * hp; v += GV_NW) {
+    const bool dyn = ntile * hp >= GV_DYN_PAIRS;
+    for (int v = warp; v < ntile * hp;) {
         const int i = v / hp, sb0 = 2 * (v % hp);
         const int nun = min(2, nsb - sb0);
         if (i != waited && !aborted) {
@@ -364,6 +438,13 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
                 issue_tile(i + NS);
             }
         }
+        if (dyn) {
+            int vn = 0;
+            if (lane == 0) vn = atomicAdd(nextv, 1);
+            v = __shfl_sync(0xFFFFFFFFu, vn, 0);
+        } else {
+            v += GV_NW;
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -371,6 +452,221 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
         // waited for unless a warp gave up): wait, bounded, for each requested tile
         for (int i = 0; i < ntile; ++i)
             if (reqd[i]) mbar_wait_bounded(&full[i], 0u, drain_bound(P.timeout_ns));
+    }
+}
+
+// ---------------------------------------------------------------- column chunks
+// gvw_kernel: one plain matrix whose items are (column chunk, row block)
+// pieces (the parameter struct describes the numbering).  The structure is
+// gv_kernel's with two changes: a tile is an item (16 rows of ch
+// super-blocks, one bulk copy per row), and the CTA stages x only for the
+// column window of its chunks.
+
+// Shared memory of a gvw_kernel CTA: the tile slots, one mbarrier and two
+// counters per tile, the parameter area (the RMS-norm's scratch in
+// gv_images, unused here), the x image and table of the window's
+// super-blocks (one format), a zero B slot, and per slot the 16 row sums of
+// each of its unit pairs (at most ch).
+__host__ __device__ inline GvLayout gvw_layout(int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch) {
+    GvLayout L;
+    uint32_t o = 0;
+    L.slots = o;
+    o += (uint32_t)nslots * slot_bytes;
+    o = (o + 127u) & ~127u;
+    L.bars = o;
+    o += (uint32_t)maxtiles * 8u;
+    L.done = o;
+    o += (uint32_t)maxtiles * 8u;
+    o = (o + 15u) & ~15u;
+    L.prm = o;
+    o += GV_PRM_BYTES;
+    L.img4 = L.img6 = o;
+    o += (uint32_t)winsb * GV_BIMG;
+    L.zero = o;
+    o += 128u;
+    L.tab4 = L.tab6 = o;
+    o += (uint32_t)winsb * 64u;
+    L.part = o;
+    o += (uint32_t)(nslots * ch) * 64u;
+    L.total = o;
+    return L;
+}
+
+// MASK 1: Q4_K, 2: Q6_K.
+template <int MASK>
+__global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constant__ GvwParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();
+    constexpr int SPAN = MASK == 1 ? 144 : 210;      // bytes of a super-block row
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NS = P.nslots, ch = P.ch, nrb = P.nrb, nsb = P.nsb;
+    const uint32_t SLOT = P.slot_bytes;
+    const GvLayout L = gvw_layout(NS, SLOT, P.maxtiles, P.winsb, ch);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [tile] its copies have landed
+    int* done = reinterpret_cast<int*>(smem + L.done);          // [tile] units done
+    int* reqd = done + P.maxtiles;                               // [tile] requested
+    int* nextu = reinterpret_cast<int*>(smem + L.prm);          // the next unit to hand out
+    const int jA = P.cta_j[blockIdx.x], jB = P.cta_j[blockIdx.x + 1], ntile = jB - jA;
+    for (int i = tid; i < P.maxtiles; i += GV_NW * 32) {
+        done[i] = 0;
+        reqd[i] = 0;
+        mbar_init(&full[i], 1);
+    }
+    if (tid == 0) *nextu = GV_NW;
+    fence_mbar_init();
+    __syncthreads();
+    const uint64_t policy = policy_evict_first();
+
+    // Request tile i (item jA + i) into slot i % NS: row r of the item (16
+    // row-block rows, fewer in a ragged last block) lands at r * pitch.
+    auto issue_tile = [&](int i) {
+        const int j = jA + i, c = j / nrb, rb = j - c * nrb;
+        const int row0 = GV_ROWS * rb, nval = min(GV_ROWS, P.rows - row0);
+        const uint32_t len = (uint32_t)(min(ch, nsb - c * ch) * SPAN);
+        const uint32_t dst = sbase + L.slots + (uint32_t)(i % NS) * SLOT;
+        uint64_t* bar = &full[i];
+        if (lane == 0) {
+            reqd[i] = 1;
+            mbar_arrive_expect_tx(bar, len * (uint32_t)nval);
+        }
+        __syncwarp();
+        if (lane < nval)
+            bulk_s(dst + (uint32_t)(lane * P.pitch), P.w + (int64_t)(row0 + lane) * P.rowbytes + (int64_t)c * ch * SPAN,
+                   len, bar, policy);
+        __syncwarp();
+    };
+
+    for (int i = warp; i < min(ntile, NS); i += GV_NW) issue_tile(i);
+    float4 nwv[GV_XIT];
+#pragma unroll
+    for (int it = 0; it < GV_XIT; ++it) nwv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pdl_wait();
+
+    // the column window: chunks cA .. cB; x is stored for the chunks whose
+    // first item (row block 0) is this CTA's
+    const int cA = jA / nrb, cB = (jB - 1) / nrb, sbA = cA * ch;
+    const int nsbw = min(nsb, (cB + 1) * ch) - sbA;
+    const int cs0 = (jA + nrb - 1) / nrb, cs1 = (jB + nrb - 1) / nrb;
+    gv_images<MASK>(P, L, smem, sbA, nsbw, cs0 * ch - sbA, min(nsb, cs1 * ch) - sbA, tid, warp, lane, nwv);
+    __syncthreads();
+
+    // ---- the unit pairs v = 0, 1, ... of the CTA's tiles in order (hpc
+    // pairs per tile: pair v is units 2 (v % hpc) and 2 (v % hpc) + 1 of tile
+    // v / hpc; the last pair of a chunk with an odd unit count has one unit,
+    // and pairs past a ragged last chunk's end are skipped).  Warp w starts
+    // with pair w and then takes the next pair from a shared counter, so a
+    // warp held up (by a tile's completion) takes fewer.
+    const GvK K = gv_consts();
+    const int g = lane >> 2, t = lane & 3;
+    const bool bact = (g >> 1) == t;                       // lanes holding B values
+    const uint32_t bslot = (uint32_t)(2 * t + (g & 1)) * GV_BSLOT;
+    const uint32_t bimg = bact ? sbase + L.img4 + bslot : sbase + L.zero;
+    const uint32_t bstr = bact ? GV_BIMG : 0u;
+    const Q4Sel sel4 = q4_sel(t);
+    float* part = reinterpret_cast<float*>(smem + L.part);   // [slot][pair][16]
+    const int hpc = (ch + 1) / 2;
+    int i = warp / hpc, pr = warp - i * hpc;
+    int ti = -1, c = 0, rb = 0, ncb = 0, waited = -1;
+    bool aborted = false;
+    while (i < ntile) {
+        if (i != ti) {
+            ti = i;
+            const int j = jA + i;
+            c = j / nrb;
+            rb = j - c * nrb;
+            ncb = min(ch, nsb - c * ch);
+        }
+        const int u0 = 2 * pr, nun = min(2, ncb - u0);
+        if (nun > 0) {
+            if (i != waited && !aborted) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&full[i], 0u, P.timeout_ns);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+                if (!ok) {
+                    aborted = true;
+                    if (lane == 0) record_status(P.status, STATUS_TIMEOUT);
+                }
+                waited = i;
+            }
+            float y0 = 0.f, y1 = 0.f;
+            if (!aborted) {
+                for (int uu = 0; uu < nun; ++uu) {
+                    const int u = u0 + uu;
+                    const uint32_t r0 = sbase + L.slots + (uint32_t)(i % NS) * SLOT + (uint32_t)(g * P.pitch + u * SPAN);
+                    const uint32_t r1 = r0 + (uint32_t)(8 * P.pitch);
+                    const int sbl = c * ch + u - sbA;             // the unit's super-block in the window
+                    const float4 xs = lds128f(sbase + L.tab4 + (uint32_t)(sbl * 4 + t) * 16);
+                    const uint32_t bb = bimg + (uint32_t)sbl * bstr;
+                    if constexpr (MASK == 1) {
+                        q4k_unit(r0, r1, t, sel4, bb, xs, K, y0, y1);
+                    } else {
+                        // rows start on 4-byte boundaries (pitch 16 ch), so the
+                        // unit is half-word aligned exactly when 210 u = 2 (mod 4)
+                        if ((SPAN * u) & 2) q6k_unit<true>(r0, r1, t, bb, xs, K, y0, y1);
+                        else q6k_unit<false>(r0, r1, t, bb, xs, K, y0, y1);
+                    }
+                }
+            }
+            y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 1);
+            y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 2);
+            y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
+            y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 2);
+            float* pu = part + ((i % NS) * hpc + pr) * 16;
+            if (t == 0) {
+                pu[g] = y0;
+                pu[g + 8] = y1;
+            }
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = atom_add_acqrel_cta(&done[i], nun) + nun == ncb;
+            if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                // the item's sums, its pairs in column order
+                const float* pt = part + (i % NS) * hpc * 16;
+                float v = 0.f;
+                if (lane < 16)
+                    for (int k = 0; k < (ncb + 1) / 2; ++k) v += pt[k * 16 + lane];
+                // the slot's next tile first (its reads of the slot are done)
+                if (i + NS < ntile && !aborted) {
+                    __syncwarp();
+                    if (lane == 0) fence_proxy_async_smem();   // every warp's reads of the slot come first
+                    __syncwarp();
+                    issue_tile(i + NS);
+                }
+                const int row = GV_ROWS * rb + lane;
+                if (P.nch == 1) {
+                    if (lane < 16 && row < P.rows) P.y[row] = seg_out(P.cap, v);
+                } else {
+                    // publish the item's sums (the warp's stores, then one
+                    // lane's acquire-release count: the release covers the
+                    // stores the warp barrier ordered before it); the warp
+                    // whose item completes the row block adds the chunks in
+                    // order
+                    if (lane < 16) st_relaxed_gpu(P.part + (int64_t)(c * nrb + rb) * 16 + lane, v);
+                    __syncwarp();
+                    unsigned before = 0;
+                    if (lane == 0) before = atom_inc_acqrel_gpu(P.cnt + rb, (unsigned)(P.nch - 1));
+                    before = __shfl_sync(0xFFFFFFFFu, before, 0);
+                    if (before == (unsigned)(P.nch - 1)) {
+                        __syncwarp();                      // lane 0's acquire before every lane's loads
+                        float sum = 0.f;
+                        if (lane < 16)
+                            for (int cc = 0; cc < P.nch; ++cc) sum += ld_relaxed_gpu(P.part + (int64_t)(cc * nrb + rb) * 16 + lane);
+                        if (lane < 16 && row < P.rows) P.y[row] = seg_out(P.cap, sum);
+                    }
+                }
+            }
+        }
+        int vn = 0;
+        if (lane == 0) vn = atomicAdd(nextu, 1);
+        vn = __shfl_sync(0xFFFFFFFFu, vn, 0);
+        i = vn / hpc;
+        pr = vn - i * hpc;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int k = 0; k < ntile; ++k)
+            if (reqd[k]) mbar_wait_bounded(&full[k], 0u, drain_bound(P.timeout_ns));
     }
 }
 
@@ -385,7 +681,49 @@ cudaError_t gv_set_smem(int bytes) {
         cudaError_t e = cudaFuncSetAttribute(gv_get(m), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
     }
+    for (void* f : {reinterpret_cast<void*>(gvw_kernel<1>), reinterpret_cast<void*>(gvw_kernel<2>)}) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
+}
+
+size_t gvw_smem_bytes(int fmt, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch) {
+    (void)fmt;
+    return gvw_layout(nslots, slot_bytes, maxtiles, winsb, ch).total;
+}
+
+// The scratch sets of the column-chunked kernel: item sums and row-block
+// counters.  Device globals start at zero and every launch leaves each
+// counter at zero (a wrapping count), so no set needs clearing.
+__device__ unsigned g_gvw_cnt[GVW_SLOTS][GVW_MAX_RB];
+__device__ float g_gvw_part[GVW_SLOTS][GVW_MAX_PART];
+
+cudaError_t gvw_scratch(unsigned** cnt, float** part) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_gvw_cnt);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&b, g_gvw_part);
+    if (e != cudaSuccess) return e;
+    *cnt = static_cast<unsigned*>(a);
+    *part = static_cast<float*>(b);
+    return cudaSuccess;
+}
+
+cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaStream_t st) {
+    void* args[1] = {const_cast<GvwParams*>(&P)};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(GV_NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* f = fmt == FMT_Q4_K ? reinterpret_cast<void*>(gvw_kernel<1>) : reinterpret_cast<void*>(gvw_kernel<2>);
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st) {

@@ -79,6 +79,7 @@ constexpr int GV_MAX_CTA = 160;
 constexpr int GV_MAX_INFLIGHT = 6;     // tiles in flight per CTA (more delays the first tile)
 constexpr int GV_MAX_TILES = 512;
 constexpr int GV_MAX_TILE_BYTES = 48 * 1024;
+constexpr int GV_MAX_NSB = 24;          // 256-column units per row (the x image build's reach)
 enum { GV_COPY_TILE = 0, GV_COPY_CPA = 1 };
 struct GvSeg {
     const uint8_t* w;        // plain matrix or interleaved gate/up pairs (row 2i gate, 2i+1 up)
@@ -91,6 +92,9 @@ struct GvSeg {
     int32_t pitch;           // shared row pitch of GV_COPY_CPA tiles
     float cap;               // > 0: plain outputs are cap * tanh(y / cap)
 };
+// GV_X_NORM: x * nw / sqrt(mean(x^2) + eps) (RMS-norm of the row);
+// GV_X_ACT: x holds (g, u) pairs (2 cols floats), the value is act(g) * u.
+enum { GV_X_PLAIN = 0, GV_X_NORM = 1, GV_X_ACT = 2 };
 struct GvParams {
     GvSeg seg[GV_MAX_SEG];
     const float* x;
@@ -111,11 +115,47 @@ struct GvParams {
     float* xout;
     int32_t cta_rb[GV_MAX_CTA + 1];
 };
-// GV_X_NORM: x * nw / sqrt(mean(x^2) + eps) (RMS-norm of the row);
-// GV_X_ACT: x holds (g, u) pairs (2 cols floats), the value is act(g) * u.
-enum { GV_X_PLAIN = 0, GV_X_NORM = 1, GV_X_ACT = 2 };
 cudaError_t gv_set_smem(int bytes);
 cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st);
+
+// batch-1 tensor-core matvec over column chunks (lq_gv.cu, gvw_kernel): one
+// plain Q4_K or Q6_K matrix whose rows are too wide for whole-row tiles, or
+// Q6_K alone.  Work items are (column chunk c, row block rb) = 16 rows x ch
+// super-blocks, numbered j = c * nrb + rb (column-major, so a CTA's items span
+// few chunks and it stages x for those only); CTA k takes items
+// [cta_j[k], cta_j[k+1]).  Each row is 16-byte aligned and a multiple of
+// 16 bytes, so every row of an item comes in by one bulk copy.  With nch > 1
+// a row block's chunks are summed across CTAs: each item's 16 sums go to
+// part[j][16], the counter cnt[rb] counts the items done (wrapping to 0), and
+// the CTA that completes the row block adds the chunks in order c = 0, 1, ...
+constexpr int GVW_SLOTS = 4;                 // scratch sets (one per stream in use)
+constexpr int GVW_MAX_PART = 1 << 17;        // floats of item sums per scratch set
+constexpr int GVW_MAX_RB = 1 << 13;          // row-block counters per scratch set
+constexpr int GVW_MAX_RB_PER_SM = 4;         // with nch > 1: fewer row blocks than this per SM
+struct GvwParams {
+    const uint8_t* w;
+    float* y;
+    const float* x;
+    float* part;             // nch > 1: [nch * nrb][16] item sums
+    unsigned* cnt;           // nch > 1: [nrb] items done (every entry 0 between launches)
+    uint64_t timeout_ns;
+    unsigned* status;
+    int64_t rowbytes;
+    int32_t rows, nsb, ch, nch, nrb;
+    int32_t pitch;           // shared row pitch of a tile: ch super-blocks
+    uint32_t slot_bytes;
+    int32_t nslots, maxtiles;
+    int32_t winsb;           // super-blocks of the widest CTA's column window
+    int32_t x16, xpre, act;  // xpre: GV_X_PLAIN or GV_X_ACT
+    const float* nw;         // unused (the RMS-norm needs whole rows)
+    float eps;
+    float* xout;
+    float cap;
+    int32_t cta_j[GV_MAX_CTA + 1];
+};
+cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaStream_t st);
+size_t gvw_smem_bytes(int fmt, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch);
+cudaError_t gvw_scratch(unsigned** cnt, float** part);   // the GVW_SLOTS scratch sets of the current device
 
 // quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
 cudaError_t qmv1_set_smem(int bytes);

@@ -33,16 +33,31 @@
  *    d*sc*q - dmin*m; Q6_K, Q8_0: exact); dot products accumulate in fp32
  *    with short fixed-order chains; each output is within
  *    1e-5 * sum_j |w_ij x_j| + 1e-6 of the exact value.  Results are
- *    deterministic.  Q4_K calls with batch >= 2 and Q8_0 calls with
- *    batch >= 3 whose cols are a multiple of 512 (Q4_K) or 256 (Q8_0), with
- *    W and x 16-byte aligned, run on the tensor cores (exact bf16 / fp16
- *    codes times x split into two pieces, fp32 sums); every other call runs
- *    the CUDA-core matvec kernel, or, when x is not 16-byte aligned or the
- *    width cannot be tiled, a plain-load kernel.  Within one kernel row b
- *    of a batch call equals, bit for bit, the same x row in any other
+ *    deterministic.  Kernel choice (by shape and alignment only):
+ *    batch-1 calls with Q4_K weights (alone, or with Q6_K in one QKV
+ *    launch), cols a multiple of 256 and 16-row tiles of at most 48 KB run
+ *    on the batch-1 tensor-core kernel; batch-1 calls of one Q4_K or Q6_K
+ *    matrix that it does not take, with W 16-byte aligned and rows a
+ *    multiple of 16 bytes, run on its column-chunked form (16-row x 7 or 8
+ *    super-block items spread evenly over the SMs; a matrix with several
+ *    chunks per row and at least 4 row blocks per SM stays on the CUDA-core
+ *    kernel); Q4_K calls with batch >= 2 and Q8_0 calls with batch >= 3
+ *    whose cols are a multiple of 512 (Q4_K) or 256 (Q8_0), with W and x
+ *    16-byte aligned, run on the batched tensor-core kernel (exact bf16 /
+ *    fp16 codes times x split into two pieces, fp32 sums); every other call
+ *    runs the CUDA-core matvec kernel, or, when x is not 16-byte aligned or
+ *    the width cannot be tiled, a plain-load kernel.  Within one kernel row
+ *    b of a batch call equals, bit for bit, the same x row in any other
  *    batch width; across kernels results differ only by rounding (all
- *    within the bound).  The grouped MoE expert FFN uses the tensor
- *    cores for Q4_K / Q8_0 when ntok >= 2.
+ *    within the bound).  The grouped MoE expert FFN uses the tensor cores for
+ *    Q4_K / Q8_0 when ntok >= 2.
+ *  - Streams: calls on different streams may run concurrently.  The
+ *    column-chunked batch-1 kernel adds the chunk sums of a row through one
+ *    of 4 scratch sets inside the library (static device memory, no
+ *    allocation), each bound to the first stream that needs it for the
+ *    life of the CUDA context; a call on a fifth stream runs on the CUDA-core
+ *    kernel instead.  A captured graph holding such a call must not run
+ *    concurrently with other work of the stream it was captured on.
  *  - Pointers are device pointers unless stated; the caller owns all memory.
  *  - stream may be NULL (the legacy default stream).
  */

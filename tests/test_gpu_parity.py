@@ -130,6 +130,10 @@ def test_repeated_calls_reuse_plans(lq):
 #   "tc": Q4_K with at least 2 x rows and columns a multiple of 512, Q8_0
 #         with at least 3 x rows and columns a multiple of 256 (the batched
 #         tensor-core kernel);
+#   "gvw": batch 1, one plain Q4_K or Q6_K matrix that "gv" does not take
+#         (rows too wide for a tile, or Q6_K alone), weights 16-byte aligned
+#         with rows a multiple of 16 bytes (the column-chunked batch-1
+#         tensor-core kernel);
 #   "cc": otherwise (the CUDA-core kernel).
 # The kernels sum in different orders, so only the oracle's bound relates
 # results of different kernels; calls on the same kernel give the same bits.
@@ -152,9 +156,22 @@ def _gv_path(fmts, cols, M, w_align=16):
     return all(_row_bytes(f, cols) % 4 == 0 and 16 * _row_bytes(f, cols) <= GV_TILE_MAX for f in fmts)
 
 
-def _kernel(fmts, cols, M, w_align=16):
+def _gvw_path(fmts, cols, M, w_align=16, rows=1):
+    fmts = set(fmts)
+    if M != 1 or cols % 256 or len(fmts) != 1 or not fmts <= {Q4_K, Q6_K} or w_align % 16:
+        return False
+    fmt = next(iter(fmts))
+    nch = -(-(cols // 256) // (7 if fmt == Q4_K else 8))
+    if nch > 1 and -(-rows // 16) >= 4 * torch.cuda.get_device_properties(0).multi_processor_count:
+        return False                 # many row blocks: the CUDA-core kernel
+    return _row_bytes(fmt, cols) % 16 == 0
+
+
+def _kernel(fmts, cols, M, w_align=16, rows=1):
     if _gv_path(fmts, cols, M, w_align):
         return "gv"
+    if _gvw_path(fmts, cols, M, w_align, rows):
+        return "gvw"
     if len(set(fmts)) == 1 and _tensor_path(next(iter(fmts)), cols, M):
         return "tc"
     return "cc"
@@ -260,6 +277,82 @@ def test_gv_rows_independent_of_partition(lq):
         assert np.array_equal(host(h)[0], host(hf)[0][:n]), n
 
 
+# ---------------------------------------------------------------- column-chunked batch-1 kernel
+
+GVW_CASES = [
+    (Q6_K, 2560, 10240),    # the Gemma-3-4B down: 5 chunks of 8 super-blocks, 800 items
+    (Q6_K, 45, 10240),      # few row blocks: 15 items, ragged last row block
+    (Q6_K, 1, 10240),       # one row
+    (Q6_K, 100, 2048),      # one chunk: every item completes its row block
+    (Q6_K, 20000, 2048),    # one chunk, more items per CTA than tile slots
+    (Q6_K, 333, 4096),      # 2 chunks
+    (Q6_K, 37, 6144),       # 3 chunks, windows of up to 3 chunks
+    (Q4_K, 4096, 14336),    # the Llama-3-8B down: 8 chunks of 7 super-blocks
+    (Q4_K, 300, 6400),      # a ragged last chunk (4 super-blocks)
+    (Q4_K, 17, 14336),      # 2 row blocks x 8 chunks: one item per CTA
+]
+
+
+@pytest.mark.parametrize("fmt,rows,cols", GVW_CASES)
+def test_gvw_parity(lq, fmt, rows, cols):
+    """Batch-1 matvecs on the column-chunked kernel against the oracle; a
+    repeat gives the same bits (the row-block counters are left at zero)."""
+    assert _kernel({fmt}, cols, 1, rows=rows) == "gvw"
+    g = synth.rng(rows * 3 + cols + fmt)
+    W = synth.weights(g, fmt, rows, cols)
+    x = synth.activations(g, 1, cols)
+    Wd, xd = dev(W), dev(x)
+    y = empty((1, rows))
+    lq.lq_matvec(fmt, Wd, rows, cols, xd, y, 1)
+    ref, S = oracle.matvec(fmt, W, rows, cols, x, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"gvw fmt {fmt} {rows}x{cols}")
+    y2 = empty((1, rows))
+    lq.lq_matvec(fmt, Wd, rows, cols, xd, y2, 1)
+    assert np.array_equal(host(y2), host(y))
+
+
+@pytest.mark.parametrize("fmt,cols", [(Q6_K, 10240), (Q4_K, 14336)])
+def test_gvw_rows_independent_of_partition(lq, fmt, cols):
+    """A row's chunk sums are added in chunk order whichever CTAs computed
+    them: the first rows of a 2560-row matrix equal those of its first 16 /
+    100 / 1000 rows (items spread differently over the CTAs), bit for bit."""
+    g = synth.rng(31 + fmt)
+    W = synth.weights(g, fmt, 2560, cols)
+    x = synth.activations(g, 1, cols)
+    Wd, xd = dev(W), dev(x)
+    yf = empty((1, 2560))
+    lq.lq_matvec(fmt, Wd, 2560, cols, xd, yf, 1)
+    full = host(yf)[0]
+    for n in (16, 100, 1000):
+        y = empty((1, n))
+        lq.lq_matvec(fmt, Wd, n, cols, xd, y, 1)
+        assert np.array_equal(host(y)[0], full[:n]), n
+
+
+def test_gvw_streams(lq):
+    """Calls on six streams at once: the column-chunked kernel has four
+    scratch sets, each bound to the first stream that needs it (the default
+    stream has one from the earlier tests); calls on streams without a set
+    run on the CUDA-core kernel.  Every result against the oracle."""
+    rows, cols = 700, 10240
+    g = synth.rng(77)
+    W = synth.q6k(g, rows, cols)
+    Wd = dev(W)
+    xs = [synth.activations(synth.rng(900 + k), 1, cols) for k in range(6)]
+    xds = [dev(x) for x in xs]
+    ys = [empty((1, rows)) for _ in range(6)]
+    streams = [torch.cuda.Stream() for _ in range(6)]
+    torch.cuda.synchronize()
+    for it in range(3):
+        for k in range(6):
+            with torch.cuda.stream(streams[k]):
+                lq.lq_matvec(Q6_K, Wd, rows, cols, xds[k], ys[k], 1, streams[k].cuda_stream)
+        torch.cuda.synchronize()
+        for k in range(6):
+            ref, S = oracle.matvec(Q6_K, W, rows, cols, xs[k], NTH)
+            assert_within(host(ys[k]), ref, oracle.matvec_bound(S), f"stream {k} pass {it}")
+
+
 @pytest.mark.parametrize("cols", [512, 1536, 2560, 3584])
 def test_gv_qkv_q6k_alignments(lq, cols):
     """Q4_K Q/K with a Q6_K V in one batch-1 launch at even super-block
@@ -328,6 +421,8 @@ def test_matvec_zero_rows_and_zero_x(lq):
     (Q6_K, 101, 2560, 3, 1.0, 0),      # CUDA cores, batch 3
     (Q4_K, 67, 2560, 1, 1.0, 4),       # x not 16-byte aligned: scalar x loads
     (Q6_K, 67, 2560, 1, 1.0, 4),       # the same on the plain-load kernel
+    (Q6_K, 300, 10240, 1, 1.0, 0),     # column-chunked kernel: the cap after the chunk sum
+    (Q6_K, 300, 10240, 1, 1.0, 4),     # the same with x not 16-byte aligned
     (Q4_K, 200, 2560, 1, 3000.0, 0),   # |y| >> cap: saturation
 ])
 def test_matvec_softcap(lq, fmt, rows, cols, batch, xscale, xoff):
@@ -535,7 +630,8 @@ def _act_inputs(g, batch, cols):
 
 
 @pytest.mark.parametrize("fmt,rows,cols,batch,act,gu_off", [
-    (Q6_K, 2560, 10240, 1, 1, 0),      # the Gemma-3-4B down: CUDA-core kernel, one thread per group
+    (Q6_K, 2560, 10240, 1, 1, 0),      # the Gemma-3-4B down: column-chunked tensor-core kernel
+    (Q4_K, 400, 14336, 1, 2, 0),       # the same, Q4_K with 8 chunks
     (Q4_K, 512, 2560, 1, 1, 0),        # batch-1 tensor-core kernel
     (Q4_K, 333, 2560, 1, 2, 0),
     (Q8_0, 300, 4096, 1, 2, 0),        # CUDA-core kernel, collective staging
