@@ -505,8 +505,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "0c054740ec3b2f0687c8d1fa003e11752ecfbe4b5b0c0f453f41b828db4f7587",
-                  "bytes": 29_548_288,
+GATEUP_TRAFFIC = {"csrc_sha256": "48a094dc3f736ae2d9eb3931e3a2c34ed1411e64c5b530ab772738b0e640a678",
+                  "bytes": 29_558_528,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from
