@@ -126,6 +126,7 @@ int dev_info(DevInfo** out) {
         e = qmv1_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv2_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmv4_set_smem(227 * 1024);
+        if (e == cudaSuccess) e = qmv8_set_smem(227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q4_K, 227 * 1024);
         if (e == cudaSuccess) e = qmm_set_smem(FMT_Q8_0, 227 * 1024);
         if (e == cudaSuccess) e = gv_set_smem(227 * 1024);
@@ -217,6 +218,13 @@ bool plan_qmv(int B, int64_t cols, const std::vector<int>& fmts, bool pairs, QPl
     p.nstages = 2;
     p.smem = qmv_smem_bytes(B, (int)U, p.RT, p.nstages, p.stage_bytes);
     return p.smem <= 227 * 1024;
+}
+
+cudaError_t qmv_launch_b(int B, int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st) {
+    return B == 1 ? qmv1_launch(mask, P, grid, nt, smem, st)
+         : B == 2 ? qmv2_launch(mask, P, grid, nt, smem, st)
+         : B == 4 ? qmv4_launch(mask, P, grid, nt, smem, st)
+                  : qmv8_launch(mask, P, grid, nt, smem, st);
 }
 
 constexpr int GV_NOT_ELIGIBLE = -1;
@@ -374,9 +382,7 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
     if (keyed && g_qmv_plans.find(key, qp)) {
         qp.P.timeout_ns = g_timeout_ns.load();
         qp.P.status = dev->status;
-        cudaError_t e = qp.B == 1 ? qmv1_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st)
-                      : qp.B == 2 ? qmv2_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st)
-                                  : qmv4_launch(qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st);
+        cudaError_t e = qmv_launch_b(qp.B, qp.mask, qp.P, qp.grid, qp.nt, qp.smem, st);
         return e == cudaSuccess ? LQ_OK : cuda_fail(e, "qmv launch");
     }
     // formats in order of first appearance (at most two per launch)
@@ -410,7 +416,8 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
     int per_sm = 0;
     cudaError_t e = B == 1 ? qmv1_occupancy(mask, nt, pl.smem, &per_sm)
                   : B == 2 ? qmv2_occupancy(mask, nt, pl.smem, &per_sm)
-                           : qmv4_occupancy(mask, nt, pl.smem, &per_sm);
+                  : B == 4 ? qmv4_occupancy(mask, nt, pl.smem, &per_sm)
+                           : qmv8_occupancy(mask, nt, pl.smem, &per_sm);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy");
     if (per_sm < 1) per_sm = 1;
     for (size_t s0 = 0; s0 < order.size(); s0 += MAX_SEG) {
@@ -456,9 +463,7 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
             g0 = std::max(1, std::min(grid - 1, g0));
             P.cta_split = g0;
         }
-        e = B == 1 ? qmv1_launch(mask, P, grid, nt, pl.smem, st)
-          : B == 2 ? qmv2_launch(mask, P, grid, nt, pl.smem, st)
-                   : qmv4_launch(mask, P, grid, nt, pl.smem, st);
+        e = qmv_launch_b(B, mask, P, grid, nt, pl.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "qmv launch");
         if (keyed && order.size() <= (size_t)MAX_SEG) {
             qp.P = P;
@@ -882,8 +887,11 @@ int qmm_min_batch(int fmt) {
 
 // Widest batch width (4, 2 or 1) the quantized matvec kernel can plan for
 // these columns and formats (x for B rows must fit in shared memory).
+// x rows per pass of the quantized matvec kernel: 8 for batches of 5 or
+// more (the weights read once for up to 8 rows), 4 for 3 or 4, else the
+// batch; narrower when the plan does not fit (x staged for B rows).
 int batch_width(int64_t cols, int batch, const std::vector<int>& fmts, bool pairs) {
-    int B = batch >= 3 ? 4 : batch;
+    int B = batch >= 5 ? 8 : batch >= 3 ? 4 : batch;
     QPlan pl;
     while (B > 1 && !plan_qmv(B, cols, fmts, pairs, pl)) B /= 2;
     return B;

@@ -157,16 +157,19 @@ cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaS
 size_t gvw_smem_bytes(int fmt, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch);
 cudaError_t gvw_scratch(unsigned** cnt, float** part);   // the GVW_SLOTS scratch sets of the current device
 
-// quantized matvec kernel (lq_qmv_b{1,2,4}.cu); mask = block formats present
+// quantized matvec kernel (lq_qmv_b{1,2,4,8}.cu); mask = block formats present
 cudaError_t qmv1_set_smem(int bytes);
 cudaError_t qmv2_set_smem(int bytes);
 cudaError_t qmv4_set_smem(int bytes);
+cudaError_t qmv8_set_smem(int bytes);
 cudaError_t qmv1_occupancy(int mask, int nt, size_t smem, int* per_sm);
 cudaError_t qmv2_occupancy(int mask, int nt, size_t smem, int* per_sm);
 cudaError_t qmv4_occupancy(int mask, int nt, size_t smem, int* per_sm);
+cudaError_t qmv8_occupancy(int mask, int nt, size_t smem, int* per_sm);
 cudaError_t qmv1_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 cudaError_t qmv2_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 cudaError_t qmv4_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
+cudaError_t qmv8_launch(int mask, const QmvParams& P, int grid, int nt, size_t smem, cudaStream_t st);
 
 
 cudaError_t launch_dequant(int fmt, const uint8_t* W, int64_t rows, int64_t cols, float* out,

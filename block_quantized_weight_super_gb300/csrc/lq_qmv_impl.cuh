@@ -829,8 +829,8 @@ __device__ void qmv_cta(const QmvParams& P, const GroupConsts& K, const Smem& sm
 // Kernel: B x rows, R rows per work item, MASK = block formats compiled in
 // (bit 0 Q4_K, bit 1 Q6_K, bit 2 Q8_0).
 template <int B, int R, int MASK>
-__global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), 2) qmv_kernel(const __grid_constant__ QmvParams P,
-                                                      const GroupConsts K) {
+__global__ void __launch_bounds__(32 * (qmv_max_consumer_warps(R) + 1), B >= 8 ? 1 : 2)
+    qmv_kernel(const __grid_constant__ QmvParams P, const GroupConsts K) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
     const int S_ = P.nstages;
