@@ -365,6 +365,8 @@ int run_segments(std::vector<Seg>& segs, int B, int64_t cols, cudaStream_t st, c
     if (B == 1) {
         rc = run_gv(segs, cols, st, pre);
         if (rc != GV_NOT_ELIGIBLE) return rc;
+    }
+    if (B <= GVW_MAX_X) {
         rc = run_gvw(segs, cols, st, pre);
         if (rc != GV_NOT_ELIGIBLE) return rc;
     }
@@ -688,32 +690,35 @@ static int gvw_slot(DevInfo* dev, cudaStream_t st) {
 
 struct GvwPlan {
     GvwParams P;
-    int fmt = 0, ncta = 0;
+    int fmt = 0, nm = 1, ncta = 0;
     size_t smem = 0;
 };
 static PlanCache<GvwPlan> g_gvw_plans;
 
 // One plain Q4_K or Q6_K matrix at batch 1 that the whole-row kernel does not
-// take (rows too wide for a tile, or Q6_K alone), on the column-chunked
-// kernel: items of 16 rows x ch super-blocks (ch = 7 for Q4_K, 8 for Q6_K:
-// a row piece of 1008 or 1680 bytes, an odd multiple of 16, so the rows a
-// quarter-warp reads fall in distinct banks), spread evenly over one CTA per
-// SM in column-major order.  Needs W 16-byte aligned with rows a multiple of
-// 16 bytes (every row piece one bulk copy) and no input norm (it needs
-// whole rows).
+// take (rows too wide for a tile, or Q6_K alone), or a Q6_K matrix against 2
+// to 8 plain x rows, on the column-chunked kernel: items of 16 rows x ch
+// super-blocks (ch = 7 for Q4_K, 8 for Q6_K: a row piece of 1008 or 1680
+// bytes, an odd multiple of 16, so the rows a quarter-warp reads fall in
+// distinct banks), spread evenly over one CTA per SM in column-major order.
+// Needs W 16-byte aligned with rows a multiple of 16 bytes (every row piece
+// one bulk copy) and no input norm (it needs whole rows).
 int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const XPre* xp) {
     if (segs.size() != 1 || cols % 256 != 0 || cols > (1 << 20)) return GV_NOT_ELIGIBLE;
     const Seg& s = segs[0];
-    if (s.nbatch != 1 || s.b0 != 0 || s.xmap || s.boff || s.bcnt || s.mode != MODE_PLAIN) return GV_NOT_ELIGIBLE;
+    const int M = s.nbatch;
+    if (M < 1 || M > GVW_MAX_X || s.xmap || s.boff || s.bcnt || s.mode != MODE_PLAIN) return GV_NOT_ELIGIBLE;
     if (s.fmt != FMT_Q4_K && s.fmt != FMT_Q6_K) return GV_NOT_ELIGIBLE;
+    if (M > 1 && (s.fmt != FMT_Q6_K || (xp && xp->kind != GV_X_PLAIN))) return GV_NOT_ELIGIBLE;
     if (xp && (xp->kind == GV_X_NORM || (xp->kind == GV_X_ACT && !al(xp->out, 16)))) return GV_NOT_ELIGIBLE;
+    const int nm = M == 1 ? 1 : M <= 4 ? 4 : 8;           // the kernel instance's x rows
     const int64_t rb = rowbytes(s.fmt, cols);
     if (!al(s.w, 16) || rb % 16 != 0 || s.nout <= 0) return GV_NOT_ELIGIBLE;
     DevInfo* dev = nullptr;
     int rc = dev_info(&dev);
     if (rc) return rc;
     PlanKey key;
-    const bool keyed = plan_key(key, dev->ctx, segs, cols, 1, xp ? xp : nullptr);
+    const bool keyed = plan_key(key, dev->ctx, segs, cols, M, xp ? xp : nullptr);
     GvwPlan gp;
     const bool cached = keyed && g_gvw_plans.find(key, gp);
     if (!cached) {
@@ -722,11 +727,16 @@ int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const X
         const int nsb = (int)(cols / 256);
         const int nch = (nsb + ch - 1) / ch;
         const int64_t nrb = (s.nout + GV_ROWS - 1) / GV_ROWS;
+        // several x rows pay off against the CUDA-core kernel from 3 rows of
+        // several chunks (Q6_K 2560 x 10240: 8 rows 38.4 us against 62.4, 5
+        // rows 33.4 against 46.6, 2 rows 18.3 against 18.6; 1024 x 2048, one
+        // chunk, 8 rows: 10.5 against 8.6)
+        if (M > 1 && (M < 3 || nch < 2)) return GV_NOT_ELIGIBLE;
         // with many row blocks the CUDA-core kernel's row partition is even
         // already and the cross-CTA chunk sums only cost (measured: Q4_K
         // 14336 x 8192, 5.9 row blocks per SM, 28.2 us here against 27.3)
         if (nch > 1 && nrb >= (int64_t)GVW_MAX_RB_PER_SM * dev->sms) return GV_NOT_ELIGIBLE;
-        if (nch > 1 && (nrb > GVW_MAX_RB || (int64_t)nch * nrb * GV_ROWS > GVW_MAX_PART)) return GV_NOT_ELIGIBLE;
+        if (nch > 1 && (nrb > GVW_MAX_RB || (int64_t)nch * nrb * GV_ROWS * nm > GVW_MAX_PART)) return GV_NOT_ELIGIBLE;
         const int64_t nitems = (int64_t)nch * nrb;
         if (nitems > (int64_t)GV_MAX_TILES * GV_MAX_CTA) return GV_NOT_ELIGIBLE;
         const int ncta = (int)std::min<int64_t>(std::min(dev->sms, GV_MAX_CTA), nitems);
@@ -743,11 +753,14 @@ int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const X
         if (maxtiles > GV_MAX_TILES || winsb > GV_MAX_NSB) return GV_NOT_ELIGIBLE;
         const uint32_t slot = ((uint32_t)(GV_ROWS * ch * span) + 127u) & ~127u;
         int ns = std::min(GV_MAX_INFLIGHT, std::max(2, maxtiles));
-        while (ns >= 2 && gvw_smem_bytes(s.fmt, ns, slot, maxtiles, winsb, ch) > GV_SMEM_MAX) --ns;
+        while (ns >= 2 && gvw_smem_bytes(nm, ns, slot, maxtiles, winsb, ch) > GV_SMEM_MAX) --ns;
         if (ns < 2) return GV_NOT_ELIGIBLE;
         P.w = s.w;
-        P.y = s.y;
-        P.x = s.x;
+        P.y = s.y + (int64_t)s.b0 * s.ld_y;
+        P.x = s.x + (int64_t)s.b0 * cols;
+        P.nx = M;
+        P.ld_x = cols;
+        P.ld_y = s.ld_y;
         P.rowbytes = rb;
         P.rows = s.nout;
         P.nsb = nsb;
@@ -759,7 +772,7 @@ int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const X
         P.nslots = ns;
         P.maxtiles = maxtiles;
         P.winsb = winsb;
-        P.x16 = al(s.x, 16) ? 1 : 0;
+        P.x16 = al(P.x, 16) ? 1 : 0;
         P.cap = s.cap;
         if (xp) {
             P.xpre = xp->kind;
@@ -767,8 +780,9 @@ int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const X
             P.xout = xp->kind != GV_X_PLAIN ? xp->out : nullptr;
         }
         gp.fmt = s.fmt;
+        gp.nm = nm;
         gp.ncta = ncta;
-        gp.smem = gvw_smem_bytes(s.fmt, ns, slot, maxtiles, winsb, ch);
+        gp.smem = gvw_smem_bytes(nm, ns, slot, maxtiles, winsb, ch);
     }
     GvwParams P = gp.P;
     if (P.nch > 1) {
@@ -779,8 +793,8 @@ int run_gvw(const std::vector<Seg>& segs, int64_t cols, cudaStream_t st, const X
     }
     P.timeout_ns = g_timeout_ns.load();
     P.status = dev->status;
-    cudaError_t e = gvw_launch(gp.fmt, P, gp.ncta, gp.smem, st);
-    if (e != cudaSuccess) return cuda_fail(e, "batch-1 column-chunked matvec launch");
+    cudaError_t e = gvw_launch(gp.fmt, gp.nm, P, gp.ncta, gp.smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "column-chunked tensor-core matvec launch");
     if (keyed && !cached) g_gvw_plans.put(key, gp);
     return LQ_OK;
 }
@@ -1078,6 +1092,14 @@ static int matvec_impl(int fmt, const void* W, int64_t rows, int64_t cols, const
             if (pre && (rc = prepass(*pre, x, batch, cols, st))) return rc;
             return run_qmm(segs, cols, st);
         }
+    }
+    if (batch > 1 && batch <= GVW_MAX_X && !pre) {
+        // all x rows in one pass of the column-chunked tensor-core kernel
+        // (Q6_K), whatever width the CUDA-core kernel would take
+        std::vector<Seg> one{plain_seg(fmt, W, rows, x, y, rows, 0, batch)};
+        one.back().cap = cap;
+        rc = run_gvw(one, cols, st, nullptr);
+        if (rc != GV_NOT_ELIGIBLE) return rc;
     }
     const int B = batch_width(cols, batch, {fmt}, false);
     std::vector<Seg> segs;

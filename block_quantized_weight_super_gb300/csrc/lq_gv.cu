@@ -478,10 +478,12 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
 
 // Shared memory of a gvw_kernel CTA: the tile slots, one mbarrier and two
 // counters per tile, the parameter area (the RMS-norm's scratch in
-// gv_images, unused here), the x image and table of the window's
-// super-blocks (one format), a zero B slot, and per slot the 16 row sums of
-// each of its unit pairs (at most ch).
-__host__ __device__ inline GvLayout gvw_layout(int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch) {
+// gv_images, unused here), for each of nm x rows the x image and table of
+// the window's super-blocks (one format; row m at m * winsb super-blocks), a
+// zero B slot, and per slot the 16 row sums of each of its unit pairs (at
+// most ch) for each x row.
+__host__ __device__ inline GvLayout gvw_layout(int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch,
+                                               int nm) {
     GvLayout L;
     uint32_t o = 0;
     L.slots = o;
@@ -495,19 +497,103 @@ __host__ __device__ inline GvLayout gvw_layout(int nslots, uint32_t slot_bytes, 
     L.prm = o;
     o += GV_PRM_BYTES;
     L.img4 = L.img6 = o;
-    o += (uint32_t)winsb * GV_BIMG;
+    o += (uint32_t)(nm * winsb) * GV_BIMG;
     L.zero = o;
     o += 128u;
     L.tab4 = L.tab6 = o;
-    o += (uint32_t)winsb * 64u;
+    o += (uint32_t)(nm * winsb) * 64u;
     L.part = o;
-    o += (uint32_t)(nslots * ch) * 64u;
+    o += (uint32_t)(nslots * ch * nm) * 64u;
     L.total = o;
     return L;
 }
 
-// MASK 1: Q4_K, 2: Q6_K.
-template <int MASK>
+// The B images and x tables of M x rows (M > 1, x plain) over the column
+// window of nsb super-blocks from sbA: gv_images' arithmetic, with the
+// 32-column blocks of all rows numbered together (block vb: row vb / (8 nsb))
+// and loaded three per thread at a time.
+template <int MASK, class F>
+__device__ __forceinline__ void gvw_images_m(const GvwParams& P, const GvLayout& L, uint8_t* smem, int sbA, int nsb,
+                                             int M, int tid, int warp, int lane, F&& issued) {
+    const int nblk = 8 * nsb, nvb = M * nblk;
+    const uint32_t imgrow = (uint32_t)P.winsb * GV_BIMG, tabrow = (uint32_t)P.winsb * 64u;
+    const int j = lane & 7;
+    for (int base = 0; base < nvb; base += 64 * GV_XIT) {
+        float4 xv[GV_XIT];
+#pragma unroll
+        for (int it = 0; it < GV_XIT; ++it) {
+            const int vb = base + 64 * it + 4 * warp + (lane >> 3);
+            xv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (vb < nvb) {
+                const int m = vb / nblk, bi = vb - m * nblk;
+                const float* p = P.x + (int64_t)m * P.ld_x + 256 * sbA + 32 * bi + 4 * j;
+                xv[it] = P.x16 ? __ldcg(reinterpret_cast<const float4*>(p))
+                               : make_float4(__ldcg(p), __ldcg(p + 1), __ldcg(p + 2), __ldcg(p + 3));
+            }
+        }
+        if (base == 0) issued();
+#pragma unroll
+        for (int it = 0; it < GV_XIT; ++it) {
+            const int vb0 = base + 64 * it + 4 * warp;
+            if (vb0 >= nvb) break;                         // warp-uniform: no block of this warp is left
+            const int vb = vb0 + (lane >> 3);
+            const bool valid = vb < nvb;
+            const int m = valid ? vb / nblk : 0, bi = valid ? vb - m * nblk : 0;
+            const int sb = bi >> 3, blk = bi & 7;
+            const float4 v = xv[it];
+            float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+            const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+            const int es = max(1, E - 14);                                  // s = 2^(es - 127): |x / s| < 2^15
+            const float inv = __uint_as_float((uint32_t)(254 - es) << 23);  // 1 / s, exact
+            const float sc = __uint_as_float((uint32_t)es << 23);
+            const float a[4] = {v.x * inv, v.y * inv, v.z * inv, v.w * inv};
+            __half hi[4], lo[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                hi[c] = __float2half_rn(a[c]);
+                lo[c] = __float2half_rn(a[c] - __half2float(hi[c]));
+            }
+            const uint2 ph = make_uint2(h2pack(hi[0], hi[2]), h2pack(hi[1], hi[3]));
+            const uint2 pl = make_uint2(h2pack(lo[0], lo[2]), h2pack(lo[1], lo[3]));
+            float sum = (v.x + v.y) + (v.z + v.w);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+            if (valid && (MASK & 1)) {
+                const int tq = blk >> 1, hf = blk & 1, mm = 8 * hf + j;
+                uint8_t* im = smem + L.img4 + m * imgrow + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+                *reinterpret_cast<uint2*>(im) = ph;
+                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+                if (j == 0) {
+                    float* tb = reinterpret_cast<float*>(smem + L.tab4 + m * tabrow) + (sb * 4 + tq) * 4;
+                    tb[hf] = sum;
+                    tb[2 + hf] = sc;
+                }
+            }
+            if (valid && (MASK & 2)) {
+                const int h = blk >> 2, q = blk & 3, s6 = j >> 2, i = j & 3;
+                const int tq = 2 * h + s6, mm = 4 * q + i;
+                uint8_t* im = smem + L.img6 + m * imgrow + sb * GV_BIMG + (2 * tq) * GV_BSLOT + mm * 8;
+                *reinterpret_cast<uint2*>(im) = ph;
+                *reinterpret_cast<uint2*>(im + GV_BSLOT) = pl;
+                if (j == 0) {
+                    float* tb = reinterpret_cast<float*>(smem + L.tab6 + m * tabrow) + (sb * 4 + 2 * h) * 4;
+                    const float sq = q >= 2 ? sc * 0.0625f : sc;      // quarters 2, 3 arrive as 16 code
+                    tb[q] = sq;
+                    tb[4 + q] = sq;
+                }
+            }
+        }
+    }
+    if (tid < 32) reinterpret_cast<uint32_t*>(smem + L.zero)[tid] = 0u;
+}
+
+// MASK 1: Q4_K, 2: Q6_K; NM: x rows the kernel is built for (1, or 4 and
+// 8 for Q6_K with P.nx <= NM rows; absent rows read the zero slot).
+template <int MASK, int NM>
 __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constant__ GvwParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();
@@ -515,7 +601,8 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NS = P.nslots, ch = P.ch, nrb = P.nrb, nsb = P.nsb;
     const uint32_t SLOT = P.slot_bytes;
-    const GvLayout L = gvw_layout(NS, SLOT, P.maxtiles, P.winsb, ch);
+    const GvLayout L = gvw_layout(NS, SLOT, P.maxtiles, P.winsb, ch, NM);
+    const int M = NM == 1 ? 1 : P.nx;
     const uint32_t sbase = smem_u32(smem);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);  // [tile] its copies have landed
     int* done = reinterpret_cast<int*>(smem + L.done);          // [tile] units done
@@ -563,9 +650,14 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
     const int cA = jA / nrb, cB = (jB - 1) / nrb, sbA = cA * ch;
     const int nsbw = min(nsb, (cB + 1) * ch) - sbA;
     const int cs0 = (jA + nrb - 1) / nrb, cs1 = (jB + nrb - 1) / nrb;
-    gv_images<MASK>(P, L, smem, sbA, nsbw, cs0 * ch - sbA, min(nsb, cs1 * ch) - sbA, tid, warp, lane, nwv, [&] {
+    auto issue_rest = [&] {
         for (int i = early + warp; i < min(ntile, NS); i += GV_NW) issue_tile(i);
-    });
+    };
+    if constexpr (NM == 1)
+        gv_images<MASK>(P, L, smem, sbA, nsbw, cs0 * ch - sbA, min(nsb, cs1 * ch) - sbA, tid, warp, lane, nwv,
+                        issue_rest);
+    else
+        gvw_images_m<MASK>(P, L, smem, sbA, nsbw, M, tid, warp, lane, issue_rest);
     __syncthreads();
 
     // ---- the unit pairs v = 0, 1, ... of the CTA's tiles in order (hpc
@@ -578,11 +670,14 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
     const int g = lane >> 2, t = lane & 3;
     const bool bact = (g >> 1) == t;                       // lanes holding B values
     const uint32_t bslot = (uint32_t)(2 * t + (g & 1)) * GV_BSLOT;
+    // x row m's images and tables are imgrow / tabrow bytes after row 0's
+    const uint32_t imgrow = (uint32_t)P.winsb * GV_BIMG, tabrow = (uint32_t)P.winsb * 64u;
     const uint32_t bimg = bact ? sbase + L.img4 + bslot : sbase + L.zero;
     const uint32_t bstr = bact ? GV_BIMG : 0u;
     const Q4Sel sel4 = q4_sel(t);
-    float* part = reinterpret_cast<float*>(smem + L.part);   // [slot][pair][16]
-    const int hpc = (ch + 1) / 2;
+    float* part = reinterpret_cast<float*>(smem + L.part);   // [slot][pair][x row][16]
+    constexpr int UT = NM == 1 ? 2 : 1;                    // units per take: pairs, one with several x rows
+    const int hpc = (ch + UT - 1) / UT;
     int i = warp / hpc, pr = warp - i * hpc;
     int ti = -1, c = 0, rb = 0, ncb = 0, waited = -1;
     bool aborted = false;
@@ -594,7 +689,7 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
             rb = j - c * nrb;
             ncb = min(ch, nsb - c * ch);
         }
-        const int u0 = 2 * pr, nun = min(2, ncb - u0);
+        const int u0 = UT * pr, nun = min(UT, ncb - u0);
         if (nun > 0) {
             if (i != waited && !aborted) {
                 bool ok = true;
@@ -606,43 +701,65 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
                 }
                 waited = i;
             }
-            float y0 = 0.f, y1 = 0.f;
+            float y0[NM], y1[NM];
+#pragma unroll
+            for (int m = 0; m < NM; ++m) y0[m] = y1[m] = 0.f;
             if (!aborted) {
                 for (int uu = 0; uu < nun; ++uu) {
                     const int u = u0 + uu;
                     const uint32_t r0 = sbase + L.slots + (uint32_t)(i % NS) * SLOT + (uint32_t)(g * P.pitch + u * SPAN);
                     const uint32_t r1 = r0 + (uint32_t)(8 * P.pitch);
                     const int sbl = c * ch + u - sbA;             // the unit's super-block in the window
-                    const float4 xs = lds128f(sbase + L.tab4 + (uint32_t)(sbl * 4 + t) * 16);
-                    const uint32_t bb = bimg + (uint32_t)sbl * bstr;
-                    if constexpr (MASK == 1) {
-                        q4k_unit(r0, r1, t, sel4, bb, xs, K, y0, y1);
+                    if constexpr (NM == 1) {
+                        const float4 xs = lds128f(sbase + L.tab4 + (uint32_t)(sbl * 4 + t) * 16);
+                        const uint32_t bb = bimg + (uint32_t)sbl * bstr;
+                        if constexpr (MASK == 1) {
+                            q4k_unit(r0, r1, t, sel4, bb, xs, K, y0[0], y1[0]);
+                        } else {
+                            // rows start on 4-byte boundaries (pitch 16 ch), so the
+                            // unit is half-word aligned exactly when 210 u = 2 (mod 4)
+                            if ((SPAN * u) & 2) q6k_unit<true>(r0, r1, t, bb, xs, K, y0[0], y1[0]);
+                            else q6k_unit<false>(r0, r1, t, bb, xs, K, y0[0], y1[0]);
+                        }
                     } else {
-                        // rows start on 4-byte boundaries (pitch 16 ch), so the
-                        // unit is half-word aligned exactly when 210 u = 2 (mod 4)
-                        if ((SPAN * u) & 2) q6k_unit<true>(r0, r1, t, bb, xs, K, y0, y1);
-                        else q6k_unit<false>(r0, r1, t, bb, xs, K, y0, y1);
+                        static_assert(MASK == 2, "several x rows: Q6_K only");
+                        const uint32_t bb = bimg + (uint32_t)sbl * bstr, bs = bact ? imgrow : 0u;
+                        const uint32_t tb = sbase + L.tab4 + (uint32_t)(sbl * 4 + t) * 16;
+                        // one unit per take (U = 1): the unit's sums are the take's
+                        if ((SPAN * u) & 2) q6k_unit_m<true, NM>(r0, r1, t, bb, bs, tb, tabrow, sbase + L.zero, M, K, y0, y1);
+                        else q6k_unit_m<false, NM>(r0, r1, t, bb, bs, tb, tabrow, sbase + L.zero, M, K, y0, y1);
                     }
                 }
             }
-            y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 1);
-            y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, 2);
-            y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
-            y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, 2);
-            float* pu = part + ((i % NS) * hpc + pr) * 16;
-            if (t == 0) {
-                pu[g] = y0;
-                pu[g + 8] = y1;
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+                float a = y0[m], b = y1[m];
+                a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+                a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+                b += __shfl_xor_sync(0xFFFFFFFFu, b, 1);
+                b += __shfl_xor_sync(0xFFFFFFFFu, b, 2);
+                float* pu = part + (((i % NS) * hpc + pr) * NM + m) * 16;
+                if (t == 0) {
+                    pu[g] = a;
+                    pu[g + 8] = b;
+                }
             }
             __syncwarp();
             int last = 0;
             if (lane == 0) last = atom_add_acqrel_cta(&done[i], nun) + nun == ncb;
             if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-                // the item's sums, its pairs in column order
-                const float* pt = part + (i % NS) * hpc * 16;
-                float v = 0.f;
-                if (lane < 16)
-                    for (int k = 0; k < (ncb + 1) / 2; ++k) v += pt[k * 16 + lane];
+                // the item's sums, its pairs in column order: value e of this
+                // lane is (x row m, row r) = (idx / 16, idx % 16), idx = lane + 32 e
+                constexpr int NV = (16 * NM + 31) / 32;
+                const float* pt = part + (i % NS) * hpc * NM * 16;
+                float v[NV];
+#pragma unroll
+                for (int e = 0; e < NV; ++e) {
+                    const int idx = lane + 32 * e, m = idx >> 4, r = idx & 15;
+                    v[e] = 0.f;
+                    if (idx < 16 * M)
+                        for (int k = 0; k < (ncb + UT - 1) / UT; ++k) v[e] += pt[(k * NM + m) * 16 + r];
+                }
                 // the slot's next tile first (its reads of the slot are done)
                 if (i + NS < ntile && !aborted) {
                     __syncwarp();
@@ -650,26 +767,39 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
                     __syncwarp();
                     issue_tile(i + NS);
                 }
-                const int row = GV_ROWS * rb + lane;
                 if (P.nch == 1) {
-                    if (lane < 16 && row < P.rows) P.y[row] = seg_out(P.cap, v);
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int idx = lane + 32 * e, m = idx >> 4, row = GV_ROWS * rb + (idx & 15);
+                        if (idx < 16 * M && row < P.rows) P.y[(int64_t)m * P.ld_y + row] = seg_out(P.cap, v[e]);
+                    }
                 } else {
                     // publish the item's sums (the warp's stores, then one
                     // lane's acquire-release count: the release covers the
                     // stores the warp barrier ordered before it); the warp
                     // whose item completes the row block adds the chunks in
                     // order
-                    if (lane < 16) st_relaxed_gpu(P.part + (int64_t)(c * nrb + rb) * 16 + lane, v);
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int idx = lane + 32 * e, m = idx >> 4, r = idx & 15;
+                        if (idx < 16 * M) st_relaxed_gpu(P.part + ((int64_t)(c * nrb + rb) * NM + m) * 16 + r, v[e]);
+                    }
                     __syncwarp();
                     unsigned before = 0;
                     if (lane == 0) before = atom_inc_acqrel_gpu(P.cnt + rb, (unsigned)(P.nch - 1));
                     before = __shfl_sync(0xFFFFFFFFu, before, 0);
                     if (before == (unsigned)(P.nch - 1)) {
                         __syncwarp();                      // lane 0's acquire before every lane's loads
-                        float sum = 0.f;
-                        if (lane < 16)
-                            for (int cc = 0; cc < P.nch; ++cc) sum += ld_relaxed_gpu(P.part + (int64_t)(cc * nrb + rb) * 16 + lane);
-                        if (lane < 16 && row < P.rows) P.y[row] = seg_out(P.cap, sum);
+#pragma unroll
+                        for (int e = 0; e < NV; ++e) {
+                            const int idx = lane + 32 * e, m = idx >> 4, r = idx & 15, row = GV_ROWS * rb + r;
+                            if (idx < 16 * M) {
+                                float sum = 0.f;
+                                for (int cc = 0; cc < P.nch; ++cc)
+                                    sum += ld_relaxed_gpu(P.part + ((int64_t)(cc * nrb + rb) * NM + m) * 16 + r);
+                                if (row < P.rows) P.y[(int64_t)m * P.ld_y + row] = seg_out(P.cap, sum);
+                            }
+                        }
                     }
                 }
             }
@@ -693,22 +823,30 @@ void* gv_get(int mask) {
 
 }  // namespace
 
+// the instance for the format and x rows: <1,1>, <2,1>, <2,4>, <2,8>
+static void* gvw_get(int fmt, int nm) {
+    if (fmt == FMT_Q4_K) return reinterpret_cast<void*>(gvw_kernel<1, 1>);
+    return nm == 1 ? reinterpret_cast<void*>(gvw_kernel<2, 1>)
+         : nm == 4 ? reinterpret_cast<void*>(gvw_kernel<2, 4>)
+                   : reinterpret_cast<void*>(gvw_kernel<2, 8>);
+}
+
 cudaError_t gv_set_smem(int bytes) {
     for (int m : {1, 3}) {
         cudaError_t e = cudaFuncSetAttribute(gv_get(m), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
     }
-    for (void* f : {reinterpret_cast<void*>(gvw_kernel<1>), reinterpret_cast<void*>(gvw_kernel<2>)}) {
+    for (void* f : {gvw_get(FMT_Q4_K, 1), gvw_get(FMT_Q6_K, 1), gvw_get(FMT_Q6_K, 4), gvw_get(FMT_Q6_K, 8)}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
-size_t gvw_smem_bytes(int fmt, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch) {
-    (void)fmt;
-    return gvw_layout(nslots, slot_bytes, maxtiles, winsb, ch).total;
+size_t gvw_smem_bytes(int nm, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch) {
+    return gvw_layout(nslots, slot_bytes, maxtiles, winsb, ch, nm).total;
 }
+
 
 // The scratch sets of the column-chunked kernel: item sums and row-block
 // counters.  Device globals start at zero and every launch leaves each
@@ -727,7 +865,7 @@ cudaError_t gvw_scratch(unsigned** cnt, float** part) {
     return cudaSuccess;
 }
 
-cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaStream_t st) {
+cudaError_t gvw_launch(int fmt, int nm, const GvwParams& P, int grid, size_t smem, cudaStream_t st) {
     void* args[1] = {const_cast<GvwParams*>(&P)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -739,8 +877,7 @@ cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* f = fmt == FMT_Q4_K ? reinterpret_cast<void*>(gvw_kernel<1>) : reinterpret_cast<void*>(gvw_kernel<2>);
-    return cudaLaunchKernelExC(&cfg, f, args);
+    return cudaLaunchKernelExC(&cfg, gvw_get(fmt, nm), args);
 }
 
 cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaStream_t st) {

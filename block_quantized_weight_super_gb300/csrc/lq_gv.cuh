@@ -331,4 +331,80 @@ __device__ __forceinline__ void q6k_unit(uint32_t r0, uint32_t r1, int t, uint32
     y1 += v1;
 }
 
+// The same unit against NM x rows at once: x row m < M has its B slot at
+// bimg0 + m bstep and its table entry of the super-block and lane quad (four
+// floats: the scales of quarters 0..3, as xs of q6k_unit) at tab0 + m tstep;
+// rows m >= M read the zero slot (bstep = 0 with bimg0 the zero slot for
+// lanes holding no B values).  Each A fragment is built once and used by one MMA
+// per x row; a quarter's code words are loaded when it is reached, to keep
+// registers for the NM accumulators.  A row's arithmetic is q6k_unit's in
+// the same order (each quarter's four MMAs accumulate i = 0..3, the
+// quarters are added q = 0..3); v0[m], v1[m] are set to the row sums.
+template <bool ODD, int NM>
+__device__ __forceinline__ void q6k_unit_m(uint32_t r0, uint32_t r1, int t, uint32_t bimg0, uint32_t bstep,
+                                           uint32_t tab0, uint32_t tstep, uint32_t zero, int M, const GvK& K,
+                                           float (&v0)[NM], float (&v1)[NM]) {
+    const int h = t >> 1, s = t & 1;
+    const uint32_t sel = s ? 0x7531u : 0x6420u;
+    float ds0[4], ds1[4];
+    {
+        uint32_t c0[2], c1[2];
+        ldw<ODD>(r0 + 192 + 8 * h, c0);
+        ldw<ODD>(r1 + 192 + 8 * h, c1);
+        const uint32_t d0 = ODD ? lds32(r0 + 206) >> 16 : lds32(r0 + 208);
+        const uint32_t d1 = ODD ? lds32(r1 + 206) >> 16 : lds32(r1 + 208);
+        const uint32_t p0 = __byte_perm(c0[0], c0[1], sel), p1 = __byte_perm(c1[0], c1[1], sel);
+        const uint32_t a02 = hsub2_u32(lop_and_xor(p0, K.m8, K.x8), K.s8), a13 = hsub2_u32(lop_and_xor(p0 >> 8, K.m8, K.x8), K.s8);
+        const uint32_t b02 = hsub2_u32(lop_and_xor(p1, K.m8, K.x8), K.s8), b13 = hsub2_u32(lop_and_xor(p1 >> 8, K.m8, K.x8), K.s8);
+        ds0[0] = hmul_lo_lo(d0, a02, 0.0f);
+        ds0[2] = hmul_lo_hi(d0, a02, 0.0f);
+        ds0[1] = hmul_lo_lo(d0, a13, 0.0f);
+        ds0[3] = hmul_lo_hi(d0, a13, 0.0f);
+        ds1[0] = hmul_lo_lo(d1, b02, 0.0f);
+        ds1[2] = hmul_lo_hi(d1, b02, 0.0f);
+        ds1[1] = hmul_lo_lo(d1, b13, 0.0f);
+        ds1[3] = hmul_lo_hi(d1, b13, 0.0f);
+    }
+#pragma unroll
+    for (int m = 0; m < NM; ++m) v0[m] = v1[m] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        // quarter q: low codes from ql run 64h + 16s (q even) or 64h + 32 + 16s
+        // (q odd), high bits from qh run 32h + 16s
+        uint32_t L0[4], L1[4], H0[4], H1[4];
+        ldw<ODD>(r0 + 64 * h + 32 * (q & 1) + 16 * s, L0);
+        ldw<ODD>(r1 + 64 * h + 32 * (q & 1) + 16 * s, L1);
+        ldw<ODD>(r0 + 128 + 32 * h + 16 * s, H0);
+        ldw<ODD>(r1 + 128 + 32 * h + 16 * s, H1);
+        const bool hn = q >= 2;
+        const uint32_t ml = hn ? K.m4hi : K.m4lo, mh = hn ? K.m6hi : K.m6lo, sb = hn ? K.s6hi : K.s6lo;
+        float acc[NM][4];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t la0 = L0[i], la1 = L1[i];
+            const uint32_t lb0 = la0 >> 8, lb1 = la1 >> 8;
+            const uint32_t ha0 = (q & 1) ? H0[i] << 2 : H0[i] << 4, hb0 = (q & 1) ? H0[i] >> 6 : H0[i] >> 4;
+            const uint32_t ha1 = (q & 1) ? H1[i] << 2 : H1[i] << 4, hb1 = (q & 1) ? H1[i] >> 6 : H1[i] >> 4;
+            const uint32_t a0 = hsub2_u32(lop_and_or(la0, ml, lop_and_or(ha0, mh, K.magic)), sb);
+            const uint32_t a1 = hsub2_u32(lop_and_or(la1, ml, lop_and_or(ha1, mh, K.magic)), sb);
+            const uint32_t a2 = hsub2_u32(lop_and_or(lb0, ml, lop_and_or(hb0, mh, K.magic)), sb);
+            const uint32_t a3 = hsub2_u32(lop_and_or(lb1, ml, lop_and_or(hb1, mh, K.magic)), sb);
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+                const uint32_t ba = m < M ? bimg0 + m * bstep : zero;
+                const uint2 b = lds64(ba + 32 * q + 8 * i);
+                mma_h(acc[m], a0, a1, a2, a3, b.x, b.y);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+            const float sx = __uint_as_float(lds32((m < M ? tab0 + m * tstep : zero) + 4 * q));
+            v0[m] = fmaf(ds0[q], (acc[m][0] + acc[m][1]) * sx, v0[m]);
+            v1[m] = fmaf(ds1[q], (acc[m][2] + acc[m][3]) * sx, v1[m]);
+        }
+    }
+}
+
 }  // namespace lq

@@ -129,14 +129,15 @@ cudaError_t gv_launch(int mask, const GvParams& P, int grid, size_t smem, cudaSt
 // part[j][16], the counter cnt[rb] counts the items done (wrapping to 0), and
 // the CTA that completes the row block adds the chunks in order c = 0, 1, ...
 constexpr int GVW_SLOTS = 4;                 // scratch sets (one per stream in use)
-constexpr int GVW_MAX_PART = 1 << 17;        // floats of item sums per scratch set
+constexpr int GVW_MAX_PART = 1 << 18;        // floats of item sums per scratch set
 constexpr int GVW_MAX_RB = 1 << 13;          // row-block counters per scratch set
 constexpr int GVW_MAX_RB_PER_SM = 4;         // with nch > 1: fewer row blocks than this per SM
+constexpr int GVW_MAX_X = 8;                 // x rows of one launch (Q6_K; one for Q4_K)
 struct GvwParams {
     const uint8_t* w;
     float* y;
     const float* x;
-    float* part;             // nch > 1: [nch * nrb][16] item sums
+    float* part;             // nch > 1: [nch * nrb][NM][16] item sums
     unsigned* cnt;           // nch > 1: [nrb] items done (every entry 0 between launches)
     uint64_t timeout_ns;
     unsigned* status;
@@ -146,15 +147,17 @@ struct GvwParams {
     uint32_t slot_bytes;
     int32_t nslots, maxtiles;
     int32_t winsb;           // super-blocks of the widest CTA's column window
-    int32_t x16, xpre, act;  // xpre: GV_X_PLAIN or GV_X_ACT
+    int32_t x16, xpre, act;  // xpre: GV_X_PLAIN or GV_X_ACT (one x row)
+    int32_t nx;              // x rows (at most the instance's NM; several: x plain, no xout)
+    int64_t ld_x, ld_y;      // floats between x rows, between y rows
     const float* nw;         // unused (the RMS-norm needs whole rows)
     float eps;
     float* xout;
     float cap;
     int32_t cta_j[GV_MAX_CTA + 1];
 };
-cudaError_t gvw_launch(int fmt, const GvwParams& P, int grid, size_t smem, cudaStream_t st);
-size_t gvw_smem_bytes(int fmt, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch);
+cudaError_t gvw_launch(int fmt, int nm, const GvwParams& P, int grid, size_t smem, cudaStream_t st);
+size_t gvw_smem_bytes(int nm, int nslots, uint32_t slot_bytes, int maxtiles, int winsb, int ch);
 cudaError_t gvw_scratch(unsigned** cnt, float** part);   // the GVW_SLOTS scratch sets of the current device
 
 // quantized matvec kernel (lq_qmv_b{1,2,4,8}.cu); mask = block formats present

@@ -41,7 +41,9 @@
  *    multiple of 16 bytes, run on its column-chunked form (16-row x 7 or 8
  *    super-block items spread evenly over the SMs; a matrix with several
  *    chunks per row and at least 4 row blocks per SM stays on the CUDA-core
- *    kernel); Q4_K calls with batch >= 2 and Q8_0 calls with batch >= 3
+ *    kernel), and so do Q6_K calls of 3 to 8 x rows with more than 2048
+ *    columns (each weight fragment used by one MMA per x row); Q4_K calls
+ *    with batch >= 2 and Q8_0 calls with batch >= 3
  *    whose cols are a multiple of 512 (Q4_K) or 256 (Q8_0), with W and x
  *    16-byte aligned, run on the batched tensor-core kernel (exact bf16 /
  *    fp16 codes times x split into two pieces, fp32 sums); every other call

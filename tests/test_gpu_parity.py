@@ -134,6 +134,9 @@ def test_repeated_calls_reuse_plans(lq):
 #         (rows too wide for a tile, or Q6_K alone), weights 16-byte aligned
 #         with rows a multiple of 16 bytes (the column-chunked batch-1
 #         tensor-core kernel);
+#   "gvwm": the same kernel for a Q6_K matrix with several column chunks
+#         (more than 2048 columns) against 3 to 8 x rows (one unit per take:
+#         sums in another order than at batch 1);
 #   "cc": otherwise (the CUDA-core kernel).
 # The kernels sum in different orders, so only the oracle's bound relates
 # results of different kernels; calls on the same kernel give the same bits.
@@ -158,10 +161,12 @@ def _gv_path(fmts, cols, M, w_align=16):
 
 def _gvw_path(fmts, cols, M, w_align=16, rows=1):
     fmts = set(fmts)
-    if M != 1 or cols % 256 or len(fmts) != 1 or not fmts <= {Q4_K, Q6_K} or w_align % 16:
+    if not 1 <= M <= 8 or cols % 256 or len(fmts) != 1 or not fmts <= {Q4_K, Q6_K} or w_align % 16:
         return False
     fmt = next(iter(fmts))
     nch = -(-(cols // 256) // (7 if fmt == Q4_K else 8))
+    if M > 1 and (fmt != Q6_K or M < 3 or nch < 2):
+        return False
     if nch > 1 and -(-rows // 16) >= 4 * torch.cuda.get_device_properties(0).multi_processor_count:
         return False                 # many row blocks: the CUDA-core kernel
     return _row_bytes(fmt, cols) % 16 == 0
@@ -171,7 +176,7 @@ def _kernel(fmts, cols, M, w_align=16, rows=1):
     if _gv_path(fmts, cols, M, w_align):
         return "gv"
     if _gvw_path(fmts, cols, M, w_align, rows):
-        return "gvw"
+        return "gvw" if M == 1 else "gvwm"
     if len(set(fmts)) == 1 and _tensor_path(next(iter(fmts)), cols, M):
         return "tc"
     return "cc"
@@ -329,6 +334,37 @@ def test_gvw_rows_independent_of_partition(lq, fmt, cols):
         assert np.array_equal(host(y)[0], full[:n]), n
 
 
+@pytest.mark.parametrize("rows,cols,batch,xoff", [
+    (2560, 10240, 8, 0),    # the Gemma-3-4B down against 8 x rows
+    (2560, 10240, 3, 0),    # the 4-row instance with a row absent
+    (300, 10240, 6, 4),     # the 8-row instance with two rows absent; x not 16-byte aligned
+    (45, 4096, 5, 0),       # 2 chunks, a ragged row block
+])
+def test_gvw_several_x_rows(lq, rows, cols, batch, xoff):
+    """Q6_K against 3-8 x rows on the column-chunked kernel: every row against
+    the oracle, and each row equal bit for bit to the same x row in a call of
+    another width on the same kernel."""
+    assert _kernel({Q6_K}, cols, batch, rows=rows) == "gvwm"
+    g = synth.rng(rows + cols + batch)
+    W = synth.q6k(g, rows, cols)
+    X = synth.activations(g, batch, cols)
+    Wd = dev(W)
+    if xoff:
+        keep, xp = dev(X, offset_bytes=xoff)
+    else:
+        keep = xp = dev(X)
+    y = empty((batch, rows))
+    lq.lq_matvec(Q6_K, Wd, rows, cols, xp, y, batch)
+    ref, S = oracle.matvec(Q6_K, W, rows, cols, X, NTH)
+    assert_within(host(y), ref, oracle.matvec_bound(S), f"{rows}x{cols} b{batch}")
+    other = 3 if batch != 3 else 8
+    Xo = np.concatenate([X, synth.activations(g, max(0, other - batch), cols)])[:other]
+    yo = empty((other, rows))
+    lq.lq_matvec(Q6_K, Wd, rows, cols, dev(Xo), yo, other)
+    n = min(batch, other)
+    assert np.array_equal(host(yo)[:n], host(y)[:n])
+
+
 def test_gvw_streams(lq):
     """Calls on six streams at once: the column-chunked kernel has four
     scratch sets, each bound to the first stream that needs it (the default
@@ -423,6 +459,7 @@ def test_matvec_zero_rows_and_zero_x(lq):
     (Q6_K, 67, 2560, 1, 1.0, 4),       # the same on the plain-load kernel
     (Q6_K, 300, 10240, 1, 1.0, 0),     # column-chunked kernel: the cap after the chunk sum
     (Q6_K, 300, 10240, 1, 1.0, 4),     # the same with x not 16-byte aligned
+    (Q6_K, 300, 10240, 5, 1.0, 0),     # the same kernel against 5 x rows
     (Q4_K, 200, 2560, 1, 3000.0, 0),   # |y| >> cap: saturation
 ])
 def test_matvec_softcap(lq, fmt, rows, cols, batch, xscale, xoff):
