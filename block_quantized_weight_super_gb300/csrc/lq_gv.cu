@@ -471,10 +471,11 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gv_kernel(const __grid_constant
 
 // ---------------------------------------------------------------- column chunks
 // gvw_kernel: one plain matrix whose items are (column chunk, row block)
-// pieces (the parameter struct describes the numbering).  The structure is
-// gv_kernel's with two changes: a tile is an item (16 rows of ch
-// super-blocks, one bulk copy per row), and the CTA stages x only for the
-// column window of its chunks.
+// pieces (the parameter struct describes the numbering), against one x row
+// or (Q6_K) up to 8.  The structure is gv_kernel's with two changes: a tile
+// is an item (16 rows of ch super-blocks, one bulk copy per row), and the CTA
+// stages x only for the column window of its chunks.  Row sums of a row
+// block are added across CTAs in chunk order through the scratch set.
 
 // Shared memory of a gvw_kernel CTA: the tile slots, one mbarrier and two
 // counters per tile, the parameter area (the RMS-norm's scratch in
@@ -660,12 +661,12 @@ __global__ void __launch_bounds__(GV_NW * 32, 1) gvw_kernel(const __grid_constan
         gvw_images_m<MASK>(P, L, smem, sbA, nsbw, M, tid, warp, lane, issue_rest);
     __syncthreads();
 
-    // ---- the unit pairs v = 0, 1, ... of the CTA's tiles in order (hpc
-    // pairs per tile: pair v is units 2 (v % hpc) and 2 (v % hpc) + 1 of tile
-    // v / hpc; the last pair of a chunk with an odd unit count has one unit,
-    // and pairs past a ragged last chunk's end are skipped).  Warp w starts
-    // with pair w and then takes the next pair from a shared counter, so a
-    // warp held up (by a tile's completion) takes fewer.
+    // ---- the takes v = 0, 1, ... of the CTA's tiles in order, UT units each
+    // (pairs with one x row, single units with several; hpc takes per tile:
+    // take v is units UT (v % hpc) .. + UT - 1 of tile v / hpc; the last take
+    // of a chunk may be short, and takes past a ragged last chunk's end are
+    // skipped).  Warp w starts with take w and then takes the next from a
+    // shared counter, so a warp held up (by a tile's completion) takes fewer.
     const GvK K = gv_consts();
     const int g = lane >> 2, t = lane & 3;
     const bool bact = (g >> 1) == t;                       // lanes holding B values
