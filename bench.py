@@ -515,8 +515,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "33be94116df309764aa26c7dea19cc7f820f5e33b0f50b6acd6a17ced799a3b3",
-                  "bytes": 29_563_136,
+GATEUP_TRAFFIC = {"csrc_sha256": "8fb41abd9477569156a61e2a1b168d206511064f67c124fe4114ac55d5b8a4ce",
+                  "bytes": 29_563_904,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from
