@@ -515,8 +515,8 @@ class OracleLayers:
 
 # DRAM bytes (read + write) of one gate+up launch from an ncu capture, valid
 # while the sources of that kernel hash to the value they had when it was taken.
-GATEUP_TRAFFIC = {"csrc_sha256": "8fb41abd9477569156a61e2a1b168d206511064f67c124fe4114ac55d5b8a4ce",
-                  "bytes": 29_563_904,
+GATEUP_TRAFFIC = {"csrc_sha256": "722ebb852addff15d4313d0877a7fde740c31bf4365a4546da611af685a08e73",
+                  "bytes": 29_563_392,
                   "source": "profiles/gv_gate_up_q4k_gemma3.md (ncu dram bytes per launch, dram-only capture)"}
 
 # the sources the batch-1 gate+up launch is compiled from

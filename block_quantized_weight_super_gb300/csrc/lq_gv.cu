@@ -159,7 +159,10 @@ __device__ __forceinline__ void gv_load_nw(const GvParams& P, int nsb, int warp,
 
 constexpr uint32_t GV_RED_OFF = 384;      // in the parameter area: the warps' sums of squares
 constexpr uint32_t GV_NEXT_OFF = GV_RED_OFF + 4 * GV_NW;   // the unit counter
-constexpr int GV_DYN_PAIRS = 4 * GV_NW;   // unit pairs of a CTA from which they are handed out by the counter
+// unit pairs of a CTA from which they are handed out by the counter (the
+// layer's gate+up has 45 per CTA, QKV and O at most 15: 2 / 4 warps' worth
+// gave gate+up 11.28 / 11.52 us, QKV and O unchanged)
+constexpr int GV_DYN_PAIRS = 2 * GV_NW;
 // tiles requested before griddepcontrol.wait (the others of the ring once x's
 // loads are issued): 0 / 1 / 2 / 3 / 4 / 6 gave a Gemma-3-4B layer of
 // 36.4 / 35.3 / 34.5 / 34.9 / 35.1 / 35.5 us
